@@ -1,0 +1,194 @@
+"""Pins of the oracle's quantizers against what the pages and the mathematics fix.
+
+Hand-worked examples (tests/golden/quantizer_examples.json), the E4M3 format
+definition (tests/golden/e4m3_points.json and torch's float8_e4m3fn), the
+quantization error bound, exact reconstruction of constant groups, code ranges,
+and a float32 re-implementation of the pages' two listings run through torch.
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import kvq_oracle as O
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _gold(name):
+    with open(os.path.join(GOLD, name)) as f:
+        return json.load(f)
+
+
+def test_fl32_matches_ieee_float32_ops():
+    g = np.random.default_rng(1)
+    a = g.standard_normal(20000).astype(np.float32) * np.float32(7.0)
+    b = g.standard_normal(20000).astype(np.float32) + np.float32(0.01)
+    a64, b64 = a.astype(np.float64), b.astype(np.float64)
+    assert np.array_equal(O.fl32(a64 / b64), (a / b).astype(np.float64))
+    assert np.array_equal(O.fl32(a64 * b64), (a * b).astype(np.float64))
+    assert np.array_equal(O.fl32(a64 - b64), (a - b).astype(np.float64))
+    assert np.array_equal(O.fl32(a64 + b64), (a + b).astype(np.float64))
+
+
+@pytest.mark.parametrize("case", _gold("quantizer_examples.json")["sym"])
+def test_sym_hand_examples(case):
+    x = np.array(case["x"])
+    c, s = O.quant_sym(x, np.max(np.abs(x)), case["bits"])
+    assert float(s) == case["scale"]
+    assert c.tolist() == case["codes"]
+    assert O.dequant_sym(c, s).tolist() == case["deq"]
+
+
+@pytest.mark.parametrize("case", _gold("quantizer_examples.json")["asym"])
+def test_asym_hand_examples(case):
+    x = np.array(case["x"])
+    c, s, m = O.quant_asym(x, x.min(), x.max(), case["bits"])
+    assert float(s) == case["scale"] and float(m) == case["min"]
+    assert c.tolist() == case["codes"]
+    assert O.dequant_asym(c, s, m).tolist() == case["deq"]
+
+
+def _page_qint8_torch(x, axis):
+    """The first page's qint8 listing, in torch float32."""
+    s = (x.abs().amax() if axis is None else x.abs().amax(dim=axis, keepdim=True)) / 127.0
+    return torch.round(x / s).clamp(-127, 127) * s
+
+
+def _page_quant_dequant_torch(x, dim, bits):
+    """The fourth page's quant_dequant listing, in torch float32."""
+    qmax = 2 ** bits - 1
+    mn = x.amin(dim=dim, keepdim=True)
+    mx = x.amax(dim=dim, keepdim=True)
+    scale = (mx - mn).clamp(min=1e-8) / qmax
+    q = ((x - mn) / scale).round().clamp(0, qmax)
+    return q * scale + mn
+
+
+@pytest.mark.parametrize("axis", [None, 0, 1])
+def test_sym_equals_page_listing_in_fp32(axis):
+    torch.manual_seed(3)
+    x = torch.randn(256, 64)
+    x[:, [5, 9]] *= 20.0
+    ref = _page_qint8_torch(x, axis).double().numpy()
+    xn = x.double().numpy()
+    if axis is None:
+        c, s = O.quant_sym(xn, np.max(np.abs(xn)), 8)
+    else:
+        c, s = O.quant_sym(xn, np.max(np.abs(xn), axis=axis, keepdims=True), 8)
+    assert np.array_equal(O.dequant_sym(c, s), ref)
+
+
+@pytest.mark.parametrize("dim,bits", [(0, 4), (1, 4), (0, 2), (1, 8)])
+def test_asym_equals_page_listing_in_fp32(dim, bits):
+    torch.manual_seed(4)
+    x = torch.randn(512, 128)
+    x[:, [3, 17, 44, 91]] *= 60.0
+    ref = _page_quant_dequant_torch(x, dim, bits).double().numpy()
+    xn = x.double().numpy()
+    c, s, m = O.quant_asym(xn, xn.min(axis=dim, keepdims=True), xn.max(axis=dim, keepdims=True), bits)
+    assert np.array_equal(O.dequant_asym(c, s, m), ref)
+
+
+@pytest.mark.parametrize("bits", [2, 4, 8])
+def test_error_bound_and_code_ranges(bits):
+    g = np.random.default_rng(bits)
+    for trial in range(200):
+        n = int(g.integers(1, 70))
+        x = O.fl32(g.standard_normal(n) * 10.0 ** g.uniform(-3, 3) + g.uniform(-5, 5))
+        # asymmetric: |x - x^| <= s/2 (+ a few ulp of the operands), codes in [0, qmax]
+        c, s, m = O.quant_asym(x, x.min(), x.max(), bits)
+        xh = O.dequant_asym(c, s, m)
+        slack = 4 * np.spacing(np.float32(np.max(np.abs(x)) + s * O.asym_qmax(bits)))
+        assert np.all(np.abs(x - xh) <= s / 2 + slack)
+        assert c.min() >= 0 and c.max() <= O.asym_qmax(bits)
+        assert c[np.argmin(x)] == 0
+        if O.fl32(x.max() - x.min()) > O.FL32_1EM8:  # the range is not clamped
+            assert c[np.argmax(x)] == O.asym_qmax(bits)
+        # symmetric: |x - x^| <= s/2 (+ slack), codes in [-qmax, qmax], never -qmax-1
+        a = np.max(np.abs(x))
+        c, s = O.quant_sym(x, a, bits)
+        xh = O.dequant_sym(c, s)
+        slack = 4 * np.spacing(np.float32(a))
+        assert np.all(np.abs(x - xh) <= s / 2 + slack)
+        q = O.sym_qmax(bits)
+        assert c.min() >= -q and c.max() <= q
+        assert abs(c[np.argmax(np.abs(x))]) == q
+
+
+@pytest.mark.parametrize("bits", [2, 4, 8])
+def test_constant_groups(bits):
+    for v in [0.0, 1.0, -3.25, 1e-20, 12345.678]:
+        x = O.fl32(np.full(33, v))
+        c, s, m = O.quant_asym(x, x.min(), x.max(), bits)
+        assert np.all(c == 0) and np.array_equal(O.dequant_asym(c, s, m), x)
+        c, s = O.quant_sym(x, np.max(np.abs(x)), bits)
+        xh = O.dequant_sym(c, s)
+        if v == 0.0:
+            assert np.all(xh == 0.0)
+        else:  # 127*fl32(a/127) need not equal a: within one float32 ulp
+            assert np.all(np.abs(xh - x) <= np.spacing(np.float32(abs(v))))
+
+
+def test_e4m3_points():
+    d = _gold("e4m3_points.json")
+    for k, v in d["decode"].items():
+        got = O.e4m3_decode(int(k))
+        assert got == v and np.signbit(got) == np.signbit(v)
+    for b in d["nan_bytes"]:
+        assert np.isnan(O.e4m3_decode(b))
+    for y, byte in d["encode"]:
+        assert int(O.e4m3_encode(y)) == byte, (y, byte)
+
+
+def test_e4m3_table_against_torch_float8():
+    all_bytes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    t = all_bytes.view(torch.float8_e4m3fn).float().double().numpy()
+    mine = O.e4m3_decode_table()
+    nan = np.isnan(t)
+    assert np.array_equal(nan, np.isnan(mine))
+    assert np.array_equal(t[~nan], mine[~nan])
+
+
+def test_e4m3_encode_against_torch_below_saturation():
+    g = np.random.default_rng(7)
+    y = np.concatenate([
+        g.standard_normal(50000) * 10.0 ** g.uniform(-4, 2.6, 50000),
+        O.e4m3_decode_table()[:0x7E] * (1 + g.uniform(-0.07, 0.07, 0x7E)),
+    ])
+    y = O.fl32(y[np.abs(y) < 464.0])
+    ref = torch.from_numpy(y.astype(np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(O.e4m3_encode(y), ref.astype(np.int64))
+
+
+def test_e4m3_midpoints_ties_to_even_and_saturation():
+    pos = O.e4m3_decode_table()[:0x7F]
+    mids = (pos[:-1] + pos[1:]) / 2
+    enc = O.e4m3_encode(mids)
+    lo = np.arange(0x7E)
+    assert np.all(enc == np.where(lo % 2 == 0, lo, lo + 1))
+    assert np.all(O.e4m3_encode(-mids) == (enc | 0x80))
+    assert np.all(O.e4m3_encode([448.0, 463.9, 464.0, 1e9]) == 0x7E)
+    assert np.all(O.e4m3_encode([-448.0, -1e9]) == 0xFE)
+
+
+def test_e4m3_relative_error_in_normal_range():
+    # the first page: ~3 mantissa bits, <= 6.25% step error across binades
+    g = np.random.default_rng(9)
+    y = O.fl32(np.exp(g.uniform(np.log(2.0 ** -6), np.log(448.0), 100000)))
+    rel = np.abs(O.e4m3_decode(O.e4m3_encode(y)) - y) / y
+    assert rel.max() <= 2.0 ** -4
+
+
+def test_fp8_scale_roundtrip_and_zero_scale():
+    g = np.random.default_rng(11)
+    x = O.fl32(g.standard_normal(4096) * 30)
+    s = O.calibrate_absmax(x, 448.0)
+    assert s == float(np.float32(np.float32(np.max(np.abs(x))) / np.float32(448.0)))
+    b = O.quant_fp8(x, s)
+    xh = O.dequant_fp8(b, s)
+    assert np.all(np.abs(xh) <= 448.0 * s * (1 + 2 ** -23))
+    assert np.max(np.abs(xh - x) / np.maximum(np.abs(x), 2.0 ** -6 * s)) <= 2.0 ** -4 + 1e-6
+    assert np.all(O.quant_fp8(x, 0.0) == 0) and np.all(O.dequant_fp8(O.quant_fp8(x, 0.0), 0.0) == 0)
