@@ -1,0 +1,173 @@
+// Internal declarations shared by the libkvq translation units.
+//
+// KvqView is the resolved, by-value description of one cache (configuration,
+// page layout and caller pointers) that every kernel receives.  The helpers
+// below implement the bit-exact quantization steps of include/kvq.h with
+// explicit IEEE round-to-nearest intrinsics (no FMA contraction).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include "../../include/kvq.h"
+
+namespace kvq {
+
+struct KvqView {
+  // configuration
+  int Hq, Hkv, D, n_rep;
+  int kfmt, kmode, kaxis, kgroup;  // kgroup: G (PER_CHANNEL) or g (PER_TOKEN, resolved)
+  int vfmt, vmode, vaxis, vgroup;
+  int kbits, vbits;
+  int R, P;
+  int rope_pre;
+  float rope_theta;
+  int src_bf16;
+  // layout of one head block
+  int krow, vrow;                    // bytes per packed token row
+  int off_vc, off_vm, off_km;        // section offsets (K codes at 0)
+  int k_nmeta, v_nmeta;              // floats per group entry: 2 asym, 1 sym
+  int k_ng, v_ng;                    // PER_TOKEN groups per token
+  int head_bytes;
+  long long page_bytes;
+  // caller's cache
+  uint8_t* pages;
+  const int32_t* block_table;
+  int32_t* seq_lens;
+  void* k_win;
+  void* v_win;
+  const float* k_scale;
+  const float* v_scale;
+  int batch, max_pages, n_pages;
+  int32_t* status;
+};
+
+// Host: resolve a validated config + cache into a view (false when invalid).
+bool make_view(const kvq_config* cfg, const kvq_cache* cache, KvqView* out);
+
+// Host launchers (each returns KVQ_OK or KVQ_ERR_CUDA).
+kvq_status launch_append(const KvqView& v, const void* k_new, const void* v_new, int n_new,
+                         const int32_t* n_new_per_seq, cudaStream_t st);
+kvq_status launch_dequantize(const KvqView& v, int seq, int t0, int t1, float* k_out,
+                             float* v_out, cudaStream_t st);
+kvq_status launch_calibrate(const KvqView& v, const void* src, long long n_tokens, float qmax,
+                            float* scale_out, cudaStream_t st);
+size_t attention_workspace_bytes(const KvqView& v, int batch);
+kvq_status launch_attention(const KvqView& v, const void* q, float* out, float scale,
+                            void* ws, size_t ws_bytes, cudaStream_t st);
+
+// ------------------------------------------------------------------ device helpers
+
+__device__ __forceinline__ float load_src(const void* base, long long idx, int bf16) {
+  if (bf16) {
+    const unsigned short u = reinterpret_cast<const unsigned short*>(base)[idx];
+    return __uint_as_float(static_cast<unsigned>(u) << 16);
+  }
+  return reinterpret_cast<const float*>(base)[idx];
+}
+
+__device__ __forceinline__ void store_src(void* base, long long idx, float x, int bf16) {
+  if (bf16) {
+    // x already holds a bf16-exact value (it came from bf16 storage)
+    reinterpret_cast<unsigned short*>(base)[idx] =
+        static_cast<unsigned short>(__float_as_uint(x) >> 16);
+  } else {
+    reinterpret_cast<float*>(base)[idx] = x;
+  }
+}
+
+// Physical page of token t of sequence b, or nullptr (and a status bit) when the
+// block-table entry is out of range.
+__device__ __forceinline__ uint8_t* page_of(const KvqView& v, int b, int t) {
+  const int pid = v.block_table[(long long)b * v.max_pages + t / v.P];
+  if (pid < 0 || pid >= v.n_pages) {
+    atomicOr(v.status, KVQ_DEV_BAD_PAGE);
+    return nullptr;
+  }
+  return v.pages + (long long)pid * v.page_bytes;
+}
+
+__device__ __forceinline__ int n_quantized(int T, int R) { return R > 0 ? R * (T / R) : T; }
+
+// Unsigned code of channel c in a packed row of `bits`-bit codes.
+__device__ __forceinline__ unsigned get_code(const uint8_t* row, int c, int bits) {
+  if (bits == 8) return row[c];
+  const int bit = c * bits;
+  return (row[bit >> 3] >> (bit & 7)) & ((1u << bits) - 1u);
+}
+
+// Signed code value from the stored unsigned code (sym / asym encodings).
+__device__ __forceinline__ int signed_code(unsigned u, int bits, int mode) {
+  if (mode == KVQ_ASYM_MINMAX) return static_cast<int>(u);
+  if (bits == 8) return static_cast<int>(static_cast<int8_t>(u));
+  return static_cast<int>(u) - (1 << (bits - 1));
+}
+
+__device__ __forceinline__ unsigned stored_code(int c, int bits, int mode) {
+  if (mode == KVQ_ASYM_MINMAX) return static_cast<unsigned>(c);
+  if (bits == 8) return static_cast<unsigned>(c) & 0xFFu;
+  return static_cast<unsigned>(c + (1 << (bits - 1)));
+}
+
+__device__ __forceinline__ float fp8_e4m3_to_float(unsigned byte) {
+  const __half_raw h = __nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(byte), __NV_E4M3);
+  return __half2float(__half(h));
+}
+
+__device__ __forceinline__ unsigned float_to_fp8_e4m3(float y) {
+  return static_cast<unsigned>(__nv_cvt_float_to_fp8(y, __NV_SATFINITE, __NV_E4M3));
+}
+
+// ---- the exact quantization steps of include/kvq.h
+
+__device__ __forceinline__ int sym_qmax(int bits) { return (1 << (bits - 1)) - 1; }
+__device__ __forceinline__ int asym_qmax(int bits) { return (1 << bits) - 1; }
+
+__device__ __forceinline__ float sym_scale(float absmax, int bits) {
+  return __fdiv_rn(absmax, static_cast<float>(sym_qmax(bits)));
+}
+
+__device__ __forceinline__ int sym_code(float x, float s, int bits) {
+  if (s == 0.f) return 0;
+  const float q = static_cast<float>(sym_qmax(bits));
+  const float r = rintf(__fdiv_rn(x, s));
+  return static_cast<int>(fminf(fmaxf(r, -q), q));
+}
+
+__device__ __forceinline__ float asym_scale(float mn, float mx, int bits) {
+  const float d = fmaxf(__fsub_rn(mx, mn), 1e-8f);
+  return __fdiv_rn(d, static_cast<float>(asym_qmax(bits)));
+}
+
+__device__ __forceinline__ int asym_code(float x, float mn, float s, int bits) {
+  const float r = rintf(__fdiv_rn(__fsub_rn(x, mn), s));
+  return static_cast<int>(fminf(fmaxf(r, 0.f), static_cast<float>(asym_qmax(bits))));
+}
+
+__device__ __forceinline__ unsigned fp8_code(float x, float s) {
+  if (s == 0.f) return 0u;
+  return float_to_fp8_e4m3(__fdiv_rn(x, s));
+}
+
+__device__ __forceinline__ float dequant_sym(int c, float s) {
+  return __fmul_rn(static_cast<float>(c), s);
+}
+__device__ __forceinline__ float dequant_asym(int c, float s, float mn) {
+  return __fadd_rn(__fmul_rn(static_cast<float>(c), s), mn);
+}
+
+// ---- RoPE angle (turns) of position p for pair i, accurate for p < 2^24:
+// omega_i = theta^(-2i/D) / (2 pi) is held as a two-float hi + lo; p*hi is split
+// exactly with an FMA (TwoProduct), its integer part dropped, and the rest summed.
+__device__ __forceinline__ float rope_turns(int p, float w_hi, float w_lo) {
+  const float pf = static_cast<float>(p);
+  const float P = __fmul_rn(pf, w_hi);
+  const float E = fmaf(pf, w_hi, -P);
+  const float F = __fsub_rn(P, rintf(P));
+  return F + (E + pf * w_lo);
+}
+
+}  // namespace kvq

@@ -1,0 +1,162 @@
+"""Test helpers: build the same cache through the CUDA library and the oracle,
+and compare them (page bytes, window, lengths, dequantized values, attention)."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import kvq_inputs as W
+from oracle import kvq_oracle as O
+
+ATT_TOL = 1e-3  # relative L2 per (sequence, query head), against the oracle on the same dequantized values
+
+
+def to_c(cfg: O.Config):
+    import asymmetric_quantized_kv_gb300 as K
+    k, v = cfg.k, cfg.v
+    return K.make_config(cfg.num_q_heads, cfg.num_kv_heads, cfg.head_dim, (k.fmt, k.mode, k.axis, k.group),
+                         (v.fmt, v.mode, v.axis, v.group), cfg.residual, cfg.page_size, cfg.rope_pre,
+                         cfg.rope_theta, cfg.src_dtype)
+
+
+def torch_src(x: np.ndarray, cfg: O.Config, device="cuda"):
+    t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32))
+    if cfg.src_dtype == O.BF16:
+        t = t.to(torch.bfloat16)  # values are bf16-exact already: exact conversion
+    return t.to(device)
+
+
+class Case:
+    """Synthetic streams K[b][h], V[b][h] ([T_b, D] float32, exact in the source
+    dtype), per-head static scales, a GPU cache filled by chunked appends and
+    the oracle states."""
+
+    def __init__(self, cfg: O.Config, lens, seed=0, outliers=(3, 17), factor=30.0, chunking="random",
+                 permute_pages=True, extra_pages=1):
+        import asymmetric_quantized_kv_gb300 as K
+        self.cfg, self.lens, self.seed = cfg, list(lens), seed
+        Bn, H, D, P = len(lens), cfg.num_kv_heads, cfg.head_dim, cfg.page_size
+        bf = cfg.src_dtype == O.BF16
+        self.K = [[W.small_stream(seed * 1000 + b * 10 + h, int(lens[b]), D, outliers, factor, bf)
+                   for h in range(H)] for b in range(Bn)]
+        self.V = [[W.small_stream(seed * 1000 + 500 + b * 10 + h, int(lens[b]), D, (), 1.0, bf)
+                   for h in range(H)] for b in range(Bn)]
+        # static per-head scales over all sequences (oracle) and through the library
+        qk = 448.0 if cfg.k.fmt == O.FP8_E4M3 else float(O.sym_qmax(O.bits_of(cfg.k.fmt)))
+        qv = 448.0 if cfg.v.fmt == O.FP8_E4M3 else float(O.sym_qmax(O.bits_of(cfg.v.fmt)))
+        cat = lambda S, h: np.concatenate([S[b][h] for b in range(Bn)]) if sum(lens) else np.zeros((0, D))
+        self.k_scale = [O.calibrate_absmax(cat(self.K, h), qk) for h in range(H)]
+        self.v_scale = [O.calibrate_absmax(cat(self.V, h), qv) for h in range(H)]
+        self.maxp = max(1, (max(lens) + P - 1) // P + extra_pages)
+        n_pages = Bn * self.maxp
+        bt = np.arange(n_pages, dtype=np.int32)
+        if permute_pages:
+            bt = W.page_permutation(n_pages, seed + 17)
+        self.block_table = bt.reshape(Bn, self.maxp)
+        self.c_cfg = to_c(cfg)
+        self.cache = K.PagedKVCache(self.c_cfg, Bn, self.maxp, n_pages, self.block_table)
+        if sum(lens):
+            ks = torch_src(np.concatenate([np.stack([self.K[b][h] for h in range(H)], 1) for b in range(Bn)]), cfg)
+            vs = torch_src(np.concatenate([np.stack([self.V[b][h] for h in range(H)], 1) for b in range(Bn)]), cfg)
+            self.cache.calibrate(ks, vs, qk, qv)
+        self._append_all(chunking)
+        self.states = [[O.quantize_stream(cfg, self.K[b][h], self.V[b][h], self.k_scale[h], self.v_scale[h])
+                        for h in range(H)] for b in range(Bn)]
+
+    def _append_all(self, chunking):
+        cfg = self.cfg
+        Bn, H, D = len(self.lens), cfg.num_kv_heads, cfg.head_dim
+        g = np.random.default_rng(self.seed + 99)
+        done = [0] * Bn
+        while any(done[b] < self.lens[b] for b in range(Bn)):
+            if chunking == "all":
+                take = [self.lens[b] - done[b] for b in range(Bn)]
+            elif chunking == "one":
+                take = [min(1, self.lens[b] - done[b]) for b in range(Bn)]
+            else:
+                take = [min(int(g.integers(1, 3 * max(cfg.residual, 16))), self.lens[b] - done[b]) for b in range(Bn)]
+            n = max(take)
+            kn = np.zeros((Bn, n, H, D), np.float32)
+            vn = np.zeros((Bn, n, H, D), np.float32)
+            for b in range(Bn):
+                for h in range(H):
+                    kn[b, :take[b], h] = self.K[b][h][done[b]:done[b] + take[b]]
+                    vn[b, :take[b], h] = self.V[b][h][done[b]:done[b] + take[b]]
+            per = torch.tensor(take, dtype=torch.int32, device="cuda")
+            self.cache.append(torch_src(kn, cfg), torch_src(vn, cfg), per)
+            for b in range(Bn):
+                done[b] += take[b]
+        torch.cuda.synchronize()
+
+    # ---------------------------------------------------------------- comparisons
+    def oracle_pages(self):
+        L = O.layout(self.cfg)
+        n_pages = self.cache.n_pages
+        pages = np.zeros((n_pages, L["page"]), np.uint8)
+        defined = np.zeros_like(pages, dtype=bool)
+        for b in range(len(self.lens)):
+            for h in range(self.cfg.num_kv_heads):
+                O.write_head_pages(self.cfg, pages, defined, self.block_table, b, h, self.states[b][h])
+        return pages, defined
+
+    def check_pages(self):
+        pages, defined = self.oracle_pages()
+        gpu = self.cache.page_view().cpu().numpy()
+        bad = np.nonzero((gpu != pages) & defined)
+        assert bad[0].size == 0, f"{bad[0].size} page bytes differ, first at page {bad[0][0]} byte {bad[1][0]}"
+
+    def check_lengths_and_window(self):
+        assert self.cache.seq_lens.cpu().tolist() == self.lens
+        if self.cfg.residual:
+            kw = self.cache.k_win.float().cpu().numpy()
+            vw = self.cache.v_win.float().cpu().numpy()
+            for b, T in enumerate(self.lens):
+                for h in range(self.cfg.num_kv_heads):
+                    st = self.states[b][h]
+                    r = T - st.n_q
+                    assert np.array_equal(kw[b, :r, h], st.k_win.astype(np.float32))
+                    assert np.array_equal(vw[b, :r, h], st.v_win.astype(np.float32))
+
+    def check_scales(self):
+        ks = self.cache.k_scale.cpu().numpy().astype(np.float64)
+        vs = self.cache.v_scale.cpu().numpy().astype(np.float64)
+        assert np.array_equal(ks, np.array(self.k_scale)) and np.array_equal(vs, np.array(self.v_scale))
+
+    def check_dequantize(self):
+        for b, T in enumerate(self.lens):
+            if T == 0:
+                continue
+            k, v = self.cache.dequantize(b, 0, T)
+            k, v = k.cpu().numpy(), v.cpu().numpy()
+            for h in range(self.cfg.num_kv_heads):
+                ko, vo = O.dequantize_stream(self.cfg, self.states[b][h], self.k_scale[h], self.v_scale[h])
+                assert np.array_equal(k[:, h].astype(np.float64), ko), (b, h)
+                assert np.array_equal(v[:, h].astype(np.float64), vo), (b, h)
+
+    def queries(self, seed=5):
+        g = np.random.default_rng(seed)
+        q = g.standard_normal((len(self.lens), self.cfg.num_q_heads, self.cfg.head_dim)).astype(np.float32)
+        if self.cfg.src_dtype == O.BF16:
+            q = W.bf16_round(q)[1]
+        return q
+
+    def check_attention(self, q=None, scale=None, tol=ATT_TOL):
+        cfg = self.cfg
+        q = self.queries() if q is None else q
+        out = self.cache.attention(torch_src(q, cfg), softmax_scale=0.0 if scale is None else scale)
+        out = out.cpu().numpy().astype(np.float64)
+        worst = 0.0
+        for b in range(len(self.lens)):
+            for h in range(cfg.num_kv_heads):
+                heads = slice(h * cfg.n_rep, (h + 1) * cfg.n_rep)
+                ref = O.decode_head(cfg, self.states[b][h], q[b, heads].astype(np.float64), self.k_scale[h],
+                                    self.v_scale[h], scale)
+                got = out[b, heads]
+                if self.lens[b] == 0:
+                    assert np.all(got == 0)
+                    continue
+                err = np.linalg.norm(got - ref, axis=1) / np.maximum(np.linalg.norm(ref, axis=1), 1e-30)
+                worst = max(worst, float(err.max()))
+        assert worst <= tol, f"attention rel L2 {worst:.3e} > {tol}"
+        assert int(self.cache.status.item()) == 0
+        return worst

@@ -1,0 +1,115 @@
+"""Host-side checks of the C ABI (no GPU needed): the library builds, loads and
+exports every function include/kvq.h declares; validation and layout arithmetic
+agree with the oracle's independent reading of the documented layout; bad
+arguments are rejected before anything is launched."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from oracle import kvq_oracle as O
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def K():
+    import __graft_entry__
+    __graft_entry__.build()
+    import asymmetric_quantized_kv_gb300 as K
+    return K
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "kvq.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kvq_[a-z_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(K):
+    names = declared_functions()
+    assert len(names) >= 10
+    lib = ctypes.CDLL(K.binding.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(K):
+    for code in range(6):
+        assert K.status_string(code) not in ("", "unknown status")
+    assert K.status_string(99) == "unknown status"
+
+
+SPECS = [(O.INT2, O.ASYM, O.PER_CHANNEL, 32), (O.INT8, O.SYM, O.PER_CHANNEL, 64), (O.INT4, O.ASYM, O.PER_TOKEN, 0),
+         (O.INT4, O.SYM, O.PER_TOKEN, 32), (O.INT8, O.SYM, O.PER_TENSOR, 0), (O.FP8_E4M3, 0, O.PER_TENSOR, 0)]
+
+
+@pytest.mark.parametrize("D", [64, 128, 256])
+@pytest.mark.parametrize("P", [16, 64, 256])
+def test_layout_agrees_with_oracle(K, D, P):
+    for ks in SPECS:
+        for vs in SPECS:
+            if vs[2] == O.PER_CHANNEL:
+                continue
+            R = 64 if ks[2] == O.PER_CHANNEL else 0
+            if ks[2] == O.PER_CHANNEL and (P % ks[3] and ks[3] % P):
+                continue
+            cfg = O.Config(8, 2, D, O.QSpec(*ks), O.QSpec(*vs), R, P)
+            c = K.kvq_config(8, 2, D, K.kvq_qspec(*ks), K.kvq_qspec(*vs), R, P, 0, 1e4, 0)
+            assert K.kvq_validate(c) == 0
+            L = O.layout(cfg)
+            assert K.kvq_page_bytes(c) == L["page"]
+            assert K.kvq_head_block_bytes(c) == L["head"]
+            assert K.kvq_head_block_offsets(c) == [L["kc"], L["vc"], L["vm"], L["km"]]
+
+
+def _cfg(K, **kw):
+    base = dict(num_q_heads=32, num_kv_heads=8, head_dim=128, k=K.kvq_qspec(8, 0, 2, 64),
+                v=K.kvq_qspec(4, 1, 1, 0), residual=64, page_size=16, rope_pre=1, rope_theta=5e5, src_dtype=1)
+    base.update(kw)
+    return K.kvq_config(**base)
+
+
+def test_validation_rejects_bad_configs(K):
+    E, U = K.KVQ_ERR_INVALID_ARG, K.KVQ_ERR_UNSUPPORTED
+    assert K.kvq_validate(_cfg(K)) == 0
+    assert K.kvq_validate(_cfg(K, num_q_heads=30)) == E
+    assert K.kvq_validate(_cfg(K, head_dim=96)) == U
+    assert K.kvq_validate(_cfg(K, residual=60)) == E            # R % G != 0
+    assert K.kvq_validate(_cfg(K, residual=0)) == E             # per-channel keys need a window
+    assert K.kvq_validate(_cfg(K, page_size=24)) == E
+    assert K.kvq_validate(_cfg(K, k=K.kvq_qspec(3, 0, 2, 64))) == E
+    assert K.kvq_validate(_cfg(K, k=K.kvq_qspec(8, 0, 2, 40))) == E
+    assert K.kvq_validate(_cfg(K, v=K.kvq_qspec(4, 1, 2, 64))) == U   # per-channel values
+    assert K.kvq_validate(_cfg(K, v=K.kvq_qspec(9, 0, 1, 0))) == U    # FP8 is per-tensor only
+    assert K.kvq_validate(_cfg(K, v=K.kvq_qspec(4, 1, 0, 0))) == U    # asym per-tensor
+    assert K.kvq_validate(_cfg(K, v=K.kvq_qspec(4, 1, 1, 48))) == E   # group must divide D
+    assert K.kvq_validate(_cfg(K, rope_theta=0.0)) == E
+    assert K.kvq_validate(_cfg(K, src_dtype=3)) == E
+    assert K.kvq_page_bytes(_cfg(K, head_dim=96)) == 0
+    assert K.kvq_workspace_bytes(_cfg(K), 0, 100) == 0
+
+
+def test_entry_points_reject_bad_arguments_before_launch(K):
+    c = _cfg(K)
+    L = K.binding.LIB
+    cache = K.kvq_cache(None, None, None, None, None, None, None, 1, 1, 1, None)
+    by = ctypes.byref
+    assert L.kvq_quantize_append(by(c), by(cache), None, None, 1, None, None) == K.KVQ_ERR_INVALID_ARG
+    assert L.kvq_decode_attention(by(c), by(cache), None, None, 0.0, None, 0, None) == K.KVQ_ERR_INVALID_ARG
+    assert L.kvq_dequantize(by(c), by(cache), 0, 0, 1, None, None, None) == K.KVQ_ERR_INVALID_ARG
+    # a plausible-looking cache (fake, never dereferenced): the checks still fire first
+    fake = K.kvq_cache(4096, 4096, 4096, 4096, 4096, 4096, 4096, 2, 4, 8, 4096)
+    assert L.kvq_quantize_append(by(c), by(fake), None, None, 5, None, None) == K.KVQ_ERR_INVALID_ARG
+    assert L.kvq_quantize_append(by(c), by(fake), 4096, 4096, -1, None, None) == K.KVQ_ERR_INVALID_ARG
+    assert L.kvq_quantize_append(by(c), by(fake), 4096, 4096, 10 ** 6, None, None) == K.KVQ_ERR_CAPACITY
+    assert L.kvq_decode_attention(by(c), by(fake), 4096, 4096, 0.0, 4096, 10, None) == K.KVQ_ERR_WORKSPACE
+    assert L.kvq_decode_attention(by(c), by(fake), 4096, 4096, 0.0, 4097, 1 << 30, None) == K.KVQ_ERR_WORKSPACE
+    assert L.kvq_decode_attention(by(c), by(fake), 4096, 4096, -1.0, 4096, 1 << 30, None) == K.KVQ_ERR_INVALID_ARG
+    assert L.kvq_dequantize(by(c), by(fake), 2, 0, 1, 4096, 4096, None) == K.KVQ_ERR_INVALID_ARG
+    assert L.kvq_dequantize(by(c), by(fake), 0, 5, 1, 4096, 4096, None) == K.KVQ_ERR_INVALID_ARG
+    assert L.kvq_dequantize(by(c), by(fake), 0, 0, 65, 4096, 4096, None) == K.KVQ_ERR_CAPACITY
+    assert L.kvq_dequantize(by(c), by(fake), 0, 3, 3, None, None, None) == K.KVQ_OK  # empty range: no launch
+    assert L.kvq_calibrate_absmax(by(c), None, 10, 448.0, None, None) == K.KVQ_ERR_INVALID_ARG
+    assert L.kvq_calibrate_absmax(by(c), 4096, 10, 0.0, 4096, None) == K.KVQ_ERR_INVALID_ARG

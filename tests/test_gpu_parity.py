@@ -1,0 +1,96 @@
+"""CUDA path vs oracle on small cases that span several tiles and ragged tails.
+
+Bit-exact: page bytes (codes and scale/min metadata), window contents, lengths,
+static scales and kvq_dequantize.  Attention: relative L2 <= 1e-3 per
+(sequence, query head) against the oracle on the same dequantized values.
+"""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+from oracle import kvq_oracle as O  # noqa: E402
+
+if not torch.cuda.is_available():  # pragma: no cover
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+from kvq_testlib import Case  # noqa: E402
+
+Q = O.QSpec
+A, S = O.ASYM, O.SYM
+CH, TOK, TEN = O.PER_CHANNEL, O.PER_TOKEN, O.PER_TENSOR
+
+CASES = {
+    # KIVI-style 2-bit (the Llama-3.1-8B layer's formats), contiguous pages
+    "int2_kivi": (O.Config(8, 2, 128, Q(O.INT2, A, CH, 32), Q(O.INT2, A, TOK, 32), 128, 256, 0, 1e4, O.BF16),
+                  [0, 1, 127, 128, 129, 300, 1000]),
+    # INT8 per-channel pre-RoPE keys + INT4 per-token values in 16-token pages
+    "int8k_rope_int4v": (O.Config(8, 2, 128, Q(O.INT8, S, CH, 64), Q(O.INT4, A, TOK, 128), 64, 16, 1, 5e5, O.BF16),
+                         [1, 63, 64, 65, 700, 2100]),
+    # FP8 E4M3 with calibrated per-head scales, 8 query heads per kv-head
+    "fp8": (O.Config(16, 2, 128, Q(O.FP8_E4M3, S, TEN), Q(O.FP8_E4M3, S, TEN), 0, 256, 0, 1e4, O.BF16),
+            [1, 255, 256, 900]),
+    # per-tensor INT8 (the synthetic head's failing baseline), fp32 sources
+    "int8_tensor": (O.Config(1, 1, 128, Q(O.INT8, S, TEN), Q(O.INT8, S, TEN), 0, 256, 0, 1e4, O.F32), [4096]),
+    # per-channel K over one 4096-token group + per-token V, fp32
+    "int8_channel_4096": (O.Config(1, 1, 128, Q(O.INT8, S, CH, 4096), Q(O.INT8, S, TOK, 0), 4096, 4096, 0, 1e4,
+                                   O.F32), [4096]),
+    # asymmetric INT4 per-token keys, 64 query heads on one kv-head
+    "int4_token_64q": (O.Config(64, 1, 128, Q(O.INT4, A, TOK, 0), Q(O.INT4, A, TOK, 0), 0, 512, 0, 1e4, O.F32),
+                       [512]),
+    "int4_channel_64q": (O.Config(64, 1, 128, Q(O.INT4, A, CH, 512), Q(O.INT4, A, TOK, 0), 512, 512, 0, 1e4,
+                                  O.F32), [512]),
+    # other head sizes and mixed encodings
+    "d64_int4sym": (O.Config(4, 4, 64, Q(O.INT4, S, TOK, 32), Q(O.INT8, A, TOK, 16), 32, 32, 1, 1e4, O.F32),
+                    [5, 33, 64, 99]),
+    "d256_int8asym": (O.Config(6, 2, 256, Q(O.INT8, A, CH, 16), Q(O.INT2, S, TOK, 64), 48, 16, 0, 1e4, O.BF16),
+                      [47, 48, 49, 400]),
+}
+
+
+@pytest.fixture(scope="module", params=sorted(CASES))
+def case(request):
+    cfg, lens = CASES[request.param]
+    return Case(cfg, lens, seed=sorted(CASES).index(request.param))
+
+
+def test_pages_bit_exact(case):
+    case.check_pages()
+
+
+def test_lengths_window_scales(case):
+    case.check_lengths_and_window()
+    case.check_scales()
+
+
+def test_dequantize_bit_exact(case):
+    case.check_dequantize()
+
+
+def test_attention_within_tolerance(case):
+    case.check_attention()
+
+
+def test_attention_custom_scale(case):
+    case.check_attention(scale=0.05)
+
+
+@pytest.mark.parametrize("chunking", ["all", "one"])
+def test_chunking_invariance(chunking):
+    cfg, lens = CASES["int8k_rope_int4v"]
+    a = Case(cfg, lens, seed=3, chunking="random")
+    b = Case(cfg, lens, seed=3, chunking=chunking)
+    pa, pb = a.cache.page_view().cpu().numpy(), b.cache.page_view().cpu().numpy()
+    _, defined = a.oracle_pages()
+    assert np.array_equal(pa[defined], pb[defined])
+    ka, kb = a.cache.k_win.cpu().float().numpy(), b.cache.k_win.cpu().float().numpy()
+    for i, T in enumerate(lens):  # only the live window slots [0, T mod R) are defined
+        r = T % cfg.residual
+        assert np.array_equal(ka[i, :r], kb[i, :r])
+
+
+def test_empty_cache_outputs_zero():
+    cfg, _ = CASES["int2_kivi"]
+    c = Case(cfg, [0, 0], seed=1)
+    c.check_attention()
