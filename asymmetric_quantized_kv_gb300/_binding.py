@@ -20,6 +20,7 @@ KVQ_SYM_ABSMAX, KVQ_ASYM_MINMAX = 0, 1
 KVQ_PER_TENSOR, KVQ_PER_TOKEN, KVQ_PER_CHANNEL = 0, 1, 2
 KVQ_F32, KVQ_BF16 = 0, 1
 KVQ_DEV_BAD_PAGE, KVQ_DEV_OVERFLOW, KVQ_DEV_TIMEOUT, KVQ_DEV_BAD_LENGTH = 1, 2, 4, 8
+KVQ_NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
 
 
 class kvq_qspec(ctypes.Structure):
@@ -62,6 +63,8 @@ def _load():
                                           c_void_p, c_void_p]),
         "kvq_decode_attention": (c_int32, [P(kvq_config), P(kvq_cache), c_void_p, c_void_p, c_float,
                                            c_void_p, c_size_t, c_void_p]),
+        "kvq_decode_attention_noalloc": (c_int32, [P(kvq_config), P(kvq_cache), c_void_p, c_void_p, c_float,
+                                                   c_void_p]),
         "kvq_dequantize": (c_int32, [P(kvq_config), P(kvq_cache), c_int32, c_int32, c_int32, c_void_p,
                                      c_void_p, c_void_p]),
         "kvq_status_string": (ctypes.c_char_p, [c_int32]),
@@ -134,6 +137,14 @@ def kvq_decode_attention(cfg, cache: kvq_cache, q, out, softmax_scale, workspace
     _check("kvq_decode_attention",
            LIB.kvq_decode_attention(ctypes.byref(cfg), ctypes.byref(cache), _ptr(q), _ptr(out),
                                     float(softmax_scale), _ptr(workspace), nbytes, _stream(stream)))
+
+
+def kvq_decode_attention_noalloc(cfg, cache: kvq_cache, q, out, softmax_scale, stream=None):
+    """kvq_decode_attention with the library's own fixed scratch array instead of
+    a caller workspace, for callers that cannot allocate device memory."""
+    _check("kvq_decode_attention_noalloc",
+           LIB.kvq_decode_attention_noalloc(ctypes.byref(cfg), ctypes.byref(cache), _ptr(q), _ptr(out),
+                                            float(softmax_scale), _stream(stream)))
 
 
 def kvq_dequantize(cfg, cache: kvq_cache, seq, tok_begin, tok_end, k_out, v_out, stream=None):

@@ -202,6 +202,30 @@ kvq_status kvq_decode_attention(const kvq_config* cfg, const kvq_cache* cache, c
                                 float* out, float softmax_scale, void* workspace,
                                 size_t ws_bytes, void* stream);
 
+/* Size of the scratch array kvq_decode_attention_noalloc uses (32 MiB). */
+#define KVQ_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+
+/* kvq_decode_attention for callers that cannot allocate device memory; the
+ * pages have no counterpart to this entry point.  Examples: a plugin inside a
+ * serving process whose memory pool already owns the GPU's memory, or a
+ * latency-critical loop that must not call cudaMalloc (it can synchronise the
+ * device).  Arguments and results are those of kvq_decode_attention without
+ * the workspace: the split-K partials go to a KVQ_NOALLOC_SCRATCH_BYTES array
+ * inside the library, which every GPU that loads the library holds until the
+ * process exits.  It allocates nothing and calls no allocating routine.
+ * - Returns KVQ_ERR_CAPACITY (nothing launched) when the call would need more
+ *   than KVQ_NOALLOC_SCRATCH_BYTES, i.e. when
+ *   kvq_workspace_bytes(cfg, batch, max_pages_per_seq * page_size) exceeds it.
+ * - The first call on a device (the calling thread's current device, which
+ *   must be the cache's) looks up the array's device address; make that first
+ *   call before any stream capture.
+ * - All calls on a device share the one array: calls that overlap on the GPU
+ *   (other streams, other host threads) race and corrupt each other's results.
+ *   Calls ordered on one stream are safe; nothing needs clearing between them. */
+kvq_status kvq_decode_attention_noalloc(const kvq_config* cfg, const kvq_cache* cache,
+                                        const void* q, float* out, float softmax_scale,
+                                        void* stream);
+
 /* Dequantize tokens [tok_begin, tok_end) of sequence `seq` to fp32:
  * k_out, v_out: [tok_end - tok_begin][Hkv][D] device.  Quantized tokens use
  * the rules above (bit-exact); window tokens are the stored source values.
