@@ -265,12 +265,17 @@ __global__ void combine_kernel(KvqView v, float* ws, float* out) {
 size_t attention_workspace_bytes(const KvqView& v, int batch) {
   const int HB = (v.n_rep + kHB - 1) / kHB;
   const long long items = kTargetItems + 2LL * batch * v.Hkv * HB;
-  return plan_header_bytes(batch) + (size_t)items * kHB * (v.D + 2) * sizeof(float);
+  const size_t generic = plan_header_bytes(batch) + (size_t)items * kHB * (v.D + 2) * sizeof(float);
+  KvqView b = v;
+  b.batch = batch;
+  return fast_eligible(b) ? (generic > fast_workspace_bytes(v, batch) ? generic : fast_workspace_bytes(v, batch))
+                          : generic;
 }
 
 kvq_status launch_attention(const KvqView& v, const void* q, float* out, float scale, void* ws,
                             size_t ws_bytes, cudaStream_t st) {
   (void)ws_bytes;
+  if (fast_eligible(v)) return launch_fast(v, q, out, scale, ws, st);
   const size_t smem = sizeof(GenericSmem) + sizeof(int) * (v.batch + 1);
   static bool attr_set = false;
   if (!attr_set) {

@@ -1,12 +1,12 @@
 // Work plan shared by the split-K decode kernels and the combine.
 //
 // Every CTA derives the same plan from the device-side sequence lengths, so no
-// host synchronisation is needed: chunk size C (at least kMinChunk tokens, and
-// large enough that the quantized tokens of all sequences make at most about
-// kTargetItems chunks), and for each sequence b the item range
-// [pref[b], pref[b+1]) = (quantized chunks + 1 window item if the window is not
-// empty) x Hkv x head-blocks.  The first CTA stores the plan at the head of the
-// workspace for the combine kernel.
+// host synchronisation is needed: a chunk size C, and for each sequence b the
+// item range [pref[b], pref[b+1]) = (quantized chunks + 1 window item if the
+// window is not empty) x items per chunk.  The generic kernel's items are
+// (sequence, kv-head, head block, chunk); the tensor-core kernels' items are
+// (sequence, chunk) with all kv-heads.  The first CTA stores the plan at the
+// head of the workspace for the combine kernel.
 #pragma once
 
 #include "kvq_internal.cuh"
@@ -52,7 +52,11 @@ __device__ inline int seq_chunks(const KvqView& v, int T, int C) {
 }
 
 // Block-wide: pref[0..B] (shared, B+1 ints), *s_C, *s_items.  All threads call it.
-__device__ inline void plan_items(const KvqView& v, int HB, int* pref, int* s_C, int* s_items) {
+// Each chunk of a sequence counts `mult` items; C is a multiple of `align`, at
+// least `cmin`, and large enough that the quantized chunks number at most about
+// `target`.
+__device__ inline void plan_items_ex(const KvqView& v, int mult, int align, int target, int cmin,
+                                     int* pref, int* s_C, int* s_items) {
   __shared__ unsigned long long s_total;
   __shared__ int s_part[1024];
   const int B = v.batch;
@@ -62,15 +66,15 @@ __device__ inline void plan_items(const KvqView& v, int HB, int* pref, int* s_C,
   for (int b = threadIdx.x; b < B; b += blockDim.x) sum += (unsigned long long)seq_tokens(v, b);
   atomicAdd(&s_total, sum);
   __syncthreads();
-  const unsigned long long work = s_total * v.Hkv * HB;
-  long long C = (long long)((work + kTargetItems - 1) / kTargetItems);
-  C = (C + 15) / 16 * 16;
-  if (C < kMinChunk) C = kMinChunk;
+  const unsigned long long work = s_total * (unsigned long long)mult;
+  long long C = (long long)((work + target - 1) / target);
+  if (C < cmin) C = cmin;
+  C = (C + align - 1) / align * align;
   const int nt = blockDim.x;
   const int seg = (B + nt - 1) / nt;
   const int b0 = threadIdx.x * seg, b1 = min(B, b0 + seg);
   int local = 0;
-  for (int b = b0; b < b1; ++b) local += seq_chunks(v, seq_tokens(v, b), (int)C) * v.Hkv * HB;
+  for (int b = b0; b < b1; ++b) local += seq_chunks(v, seq_tokens(v, b), (int)C) * mult;
   s_part[threadIdx.x] = local;
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -87,10 +91,15 @@ __device__ inline void plan_items(const KvqView& v, int HB, int* pref, int* s_C,
   int run = s_part[threadIdx.x];
   for (int b = b0; b < b1; ++b) {
     pref[b] = run;
-    run += seq_chunks(v, seq_tokens(v, b), (int)C) * v.Hkv * HB;
+    run += seq_chunks(v, seq_tokens(v, b), (int)C) * mult;
   }
   if (threadIdx.x == 0) pref[B] = *s_items;
   __syncthreads();
+}
+
+// The generic kernel's plan: items are (sequence, kv-head, head block, chunk).
+__device__ inline void plan_items(const KvqView& v, int HB, int* pref, int* s_C, int* s_items) {
+  plan_items_ex(v, v.Hkv * HB, 16, kTargetItems, kMinChunk, pref, s_C, s_items);
 }
 
 __device__ inline void store_plan(const KvqView& v, float* ws, const int* pref, int C, int items) {

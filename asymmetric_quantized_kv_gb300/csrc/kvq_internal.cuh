@@ -56,6 +56,11 @@ kvq_status launch_dequantize(const KvqView& v, int seq, int t0, int t1, float* k
 kvq_status launch_calibrate(const KvqView& v, const void* src, long long n_tokens, float qmax,
                             float* scale_out, cudaStream_t st);
 size_t attention_workspace_bytes(const KvqView& v, int batch);
+// Tensor-core decode kernel for INT8 per-channel pre-RoPE keys + INT4 per-token values.
+bool fast_eligible(const KvqView& v);
+size_t fast_workspace_bytes(const KvqView& v, int batch);
+kvq_status launch_fast(const KvqView& v, const void* q, float* out, float scale, void* ws,
+                       cudaStream_t st);
 kvq_status launch_attention(const KvqView& v, const void* q, float* out, float scale,
                             void* ws, size_t ws_bytes, cudaStream_t st);
 

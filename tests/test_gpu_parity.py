@@ -41,6 +41,13 @@ CASES = {
                        [512]),
     "int4_channel_64q": (O.Config(64, 1, 128, Q(O.INT4, A, CH, 512), Q(O.INT4, A, TOK, 0), 512, 512, 0, 1e4,
                                   O.F32), [512]),
+    # the tensor-core kernel's formats: 8 kv-heads x 4 query heads, pre-RoPE INT8 keys, INT4 values
+    "fast_rope_i8i4_p16": (O.Config(32, 8, 128, Q(O.INT8, S, CH, 64), Q(O.INT4, A, TOK, 128), 64, 16, 1, 5e5,
+                                    O.BF16), [1, 63, 64, 65, 700, 2100, 3000, 777]),
+    "fast_rope_i8i4_p64": (O.Config(32, 8, 128, Q(O.INT8, S, CH, 64), Q(O.INT4, A, TOK, 128), 64, 64, 1, 5e5,
+                                    O.BF16), [5, 130, 1500]),
+    "fast_rope_i8i4_g128": (O.Config(32, 8, 128, Q(O.INT8, S, CH, 128), Q(O.INT4, A, TOK, 0), 128, 16, 1, 1e4,
+                                     O.BF16), [128, 129, 1000, 4100]),
     # other head sizes and mixed encodings
     "d64_int4sym": (O.Config(4, 4, 64, Q(O.INT4, S, TOK, 32), Q(O.INT8, A, TOK, 16), 32, 32, 1, 1e4, O.F32),
                     [5, 33, 64, 99]),
