@@ -9,24 +9,26 @@
 // Keys and Values Need Different Axes", section "What should I actually turn on
 // in production?", checklist.)
 //
-// One CTA per (flush block, kv-head, sequence).  CTA 0 of a sequence also owns
-// the window: it first quantizes the block that may read the old window, then
-// (after a barrier) writes the remaining new tokens into the window, so one
-// launch never reads and overwrites the same window slots out of order.
+// Two launches: the fold kernel, one CTA per (fold block, kv-head, sequence),
+// quantizes every window that fills (reading the old window and the new rows);
+// then one CTA per sequence writes the remaining new tokens into the window and
+// advances seq_lens, so window slots are never read and overwritten out of order.
 #include "kvq_internal.cuh"
 
 namespace kvq {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kSub = 32;        // tokens staged per sub-chunk
+constexpr int kSub = 16;        // tokens staged per sub-chunk
 constexpr int kUnitTok = 64;    // tokens per CTA when R == 0
 constexpr int kMaxD = 256;
 constexpr int kMaxGroups = 16;  // PER_TOKEN groups per token (D/g with g >= 16)
+constexpr int kStageMax = 64 * 1024;  // shared-memory staging of one fold block
 
 struct Src {
   const void* win;    // [B][R][Hkv][D]
   const void* fresh;  // [B][n_new][Hkv][D]
+  const void* staged; // the block's rows [count][D] in shared memory, or nullptr
 };
 
 struct TQ {  // one tensor's quantization parameters
@@ -35,11 +37,12 @@ struct TQ {  // one tensor's quantization parameters
 };
 
 struct AppendCtx {
-  int b, h, T0, wbase, n_stride;
+  int b, h, T0, wbase, n_stride, st_t0;
 };
 
 __device__ __forceinline__ float src_value(const KvqView& v, const Src& s, const AppendCtx& a,
                                            int t, int c) {
+  if (s.staged) return load_src(s.staged, (long long)(t - a.st_t0) * v.D + c, v.src_bf16);
   if (t < a.T0) {
     const long long i = (((long long)a.b * v.R + (t - a.wbase)) * v.Hkv + a.h) * v.D + c;
     return load_src(s.win, i, v.src_bf16);
@@ -49,27 +52,40 @@ __device__ __forceinline__ float src_value(const KvqView& v, const Src& s, const
 }
 
 struct Smem {
-  float xs[kSub][kMaxD];
+  float xs[kSub][kMaxD + 1];  // +1: a thread per row reads a column without bank conflicts
   uint32_t stage[kSub][kMaxD * 8 / 32];
   float gs[kSub][kMaxGroups];
+  float gr[kSub][kMaxGroups];  // 1 / scale, rounded to nearest
   float gm[kSub][kMaxGroups];
   float cmin[kThreads];
   float cmax[kThreads];
+  uint8_t* rowp[kSub];  // head block of each staged row (nullptr: bad page)
+  int rslot[kSub];      // its slot within the page
   float ch_s[kMaxD];
+  float ch_r[kMaxD];
   float ch_m[kMaxD];
 };
 
-// Pack the codes of rows [t0, t0+n) staged in sm.stage into the pages.
-__device__ void flush_stage(const KvqView& v, const AppendCtx& a, const TQ& q, Smem& sm, int t0,
-                            int n) {
-  const int wpr = q.row / 4;
-  for (int w = threadIdx.x; w < n * wpr; w += kThreads) {
-    const int r = w / wpr, k = w % wpr;
-    const int t = t0 + r;
+__device__ __forceinline__ int log2i(int x) { return __ffs(x) - 1; }  // x a power of two
+
+// Head-block address and page slot of each of the n rows of a sub-chunk, once.
+__device__ void load_rows(const KvqView& v, const AppendCtx& a, Smem& sm, int t0, int n) {
+  if (threadIdx.x < n) {
+    const int t = t0 + threadIdx.x;
     uint8_t* page = page_of(v, a.b, t);
-    if (!page) continue;
-    uint8_t* dst = page + (long long)a.h * v.head_bytes + q.off_codes + (t % v.P) * q.row;
-    reinterpret_cast<uint32_t*>(dst)[k] = sm.stage[r][k];
+    sm.rowp[threadIdx.x] = page ? page + (long long)a.h * v.head_bytes : nullptr;
+    sm.rslot[threadIdx.x] = t % v.P;
+  }
+}
+
+// Pack the codes of the n rows staged in sm.stage into the pages.
+__device__ void flush_stage(const KvqView& v, const TQ& q, Smem& sm, int n) {
+  const int wpr = q.row >> 2, lw = log2i(wpr);
+  for (int w = threadIdx.x; w < (n << lw); w += kThreads) {
+    const int r = w >> lw, k = w & (wpr - 1);
+    uint8_t* hb = sm.rowp[r];
+    if (!hb) continue;
+    reinterpret_cast<uint32_t*>(hb + q.off_codes + sm.rslot[r] * q.row)[k] = sm.stage[r][k];
   }
 }
 
@@ -79,69 +95,89 @@ __device__ __forceinline__ void stage_code(Smem& sm, int r, int c, int bits, uns
 }
 
 __device__ void clear_stage(Smem& sm, const TQ& q, int n) {
-  const int wpr = q.row / 4;
-  for (int w = threadIdx.x; w < n * wpr; w += kThreads) sm.stage[w / wpr][w % wpr] = 0u;
+  const int wpr = q.row >> 2, lw = log2i(wpr);
+  for (int w = threadIdx.x; w < (n << lw); w += kThreads) sm.stage[w >> lw][w & (wpr - 1)] = 0u;
 }
 
 // Tokens [t_begin, t_begin + count) of one tensor, quantized along a per-token,
-// per-tensor or FP8 axis.
+// per-tensor or FP8 axis.  D and the group sizes are powers of two.
 __device__ void quantize_rows(const KvqView& v, const Src& s, const AppendCtx& a, const TQ& q,
                               Smem& sm, int t_begin, int count) {
-  const int D = v.D;
+  const int D = v.D, lD = log2i(D);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int sub = 0; sub < count; sub += kSub) {
     const int n = min(kSub, count - sub);
     const int t0 = t_begin + sub;
-    for (int e = threadIdx.x; e < n * D; e += kThreads) sm.xs[e / D][e % D] = src_value(v, s, a, t0 + e / D, e % D);
+    for (int e = threadIdx.x; e < (n << lD); e += kThreads)
+      sm.xs[e >> lD][e & (D - 1)] = src_value(v, s, a, t0 + (e >> lD), e & (D - 1));
     clear_stage(sm, q, n);
+    load_rows(v, a, sm, t0, n);
     __syncthreads();
     if (q.axis == KVQ_PER_TOKEN) {
-      const int g = q.group;
-      for (int e = threadIdx.x; e < n * q.ng; e += kThreads) {
-        const int r = e / q.ng, grp = e % q.ng;
-        float mn = sm.xs[r][grp * g], mx = mn, am = fabsf(mn);
-        for (int c = grp * g + 1; c < (grp + 1) * g; ++c) {
-          const float x = sm.xs[r][c];
-          mn = fminf(mn, x);
-          mx = fmaxf(mx, x);
-          am = fmaxf(am, fabsf(x));
-        }
-        float sc;
-        if (q.mode == KVQ_ASYM_MINMAX) {
-          sc = asym_scale(mn, mx, q.bits);
-        } else {
-          sc = sym_scale(am, q.bits);
-          mn = 0.f;
-        }
-        sm.gs[r][grp] = sc;
-        sm.gm[r][grp] = mn;
-        uint8_t* page = page_of(v, a.b, t0 + r);
-        if (page) {
-          float* meta = reinterpret_cast<float*>(page + (long long)a.h * v.head_bytes + q.off_meta +
-                                                 ((t0 + r) % v.P) * q.ng * q.nmeta * 4);
-          meta[grp] = sc;
-          if (q.nmeta == 2) meta[q.ng + grp] = mn;
+      // one warp per row: lanes scan the group's channels, shuffles reduce
+      const int g = q.group, lg = log2i(g);
+      const int width = g < 32 ? g : 32;  // lanes sharing one group
+      for (int r = warp; r < n; r += kThreads / 32) {
+        for (int grp0 = 0; grp0 < q.ng; grp0 += 32 / width) {
+          const int grp = grp0 + lane / width;
+          float mn = INFINITY, mx = -INFINITY, am = 0.f;
+          if (grp < q.ng) {
+            for (int c = (grp << lg) + (lane & (width - 1)); c < ((grp + 1) << lg); c += width) {
+              const float x = sm.xs[r][c];
+              mn = fminf(mn, x);
+              mx = fmaxf(mx, x);
+              am = fmaxf(am, fabsf(x));
+            }
+          }
+          for (int o = width >> 1; o; o >>= 1) {
+            mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+            am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+          }
+          if ((lane & (width - 1)) == 0 && grp < q.ng) {
+            float sc;
+            if (q.mode == KVQ_ASYM_MINMAX) {
+              sc = asym_scale(mn, mx, q.bits);
+            } else {
+              sc = sym_scale(am, q.bits);
+              mn = 0.f;
+            }
+            sm.gs[r][grp] = sc;
+            sm.gr[r][grp] = sc > 0.f ? __frcp_rn(sc) : 0.f;
+            sm.gm[r][grp] = mn;
+            uint8_t* hb = sm.rowp[r];
+            if (hb) {
+              float* meta = reinterpret_cast<float*>(hb + q.off_meta + sm.rslot[r] * q.ng * q.nmeta * 4);
+              meta[grp] = sc;
+              if (q.nmeta == 2) meta[q.ng + grp] = mn;
+            }
+          }
         }
       }
       __syncthreads();
     }
-    for (int e = threadIdx.x; e < n * D; e += kThreads) {
-      const int r = e / D, c = e % D;
+    const int lg = q.axis == KVQ_PER_TOKEN ? log2i(q.group) : 0;
+    const float ss = q.axis == KVQ_PER_TENSOR || q.fmt == KVQ_FP8_E4M3 ? q.static_scale[a.h] : 0.f;
+    const float sr = ss > 0.f ? __frcp_rn(ss) : 0.f;
+    for (int e = threadIdx.x; e < (n << lD); e += kThreads) {
+      const int r = e >> lD, c = e & (D - 1);
       const float x = sm.xs[r][c];
       unsigned u;
       if (q.fmt == KVQ_FP8_E4M3) {
-        u = fp8_code(x, q.static_scale[a.h]);
+        u = fp8_code(x, ss);
       } else if (q.axis == KVQ_PER_TENSOR) {
-        u = stored_code(sym_code(x, q.static_scale[a.h], q.bits), q.bits, KVQ_SYM_ABSMAX);
+        u = stored_code(sym_code_r(x, ss, sr, q.bits), q.bits, KVQ_SYM_ABSMAX);
       } else {
-        const int grp = c / q.group;
-        const int code = q.mode == KVQ_ASYM_MINMAX ? asym_code(x, sm.gm[r][grp], sm.gs[r][grp], q.bits)
-                                                   : sym_code(x, sm.gs[r][grp], q.bits);
+        const int grp = c >> lg;
+        const int code = q.mode == KVQ_ASYM_MINMAX
+                             ? asym_code_r(x, sm.gm[r][grp], sm.gs[r][grp], sm.gr[r][grp], q.bits)
+                             : sym_code_r(x, sm.gs[r][grp], sm.gr[r][grp], q.bits);
         u = stored_code(code, q.bits, q.mode);
       }
       stage_code(sm, r, c, q.bits, u);
     }
     __syncthreads();
-    flush_stage(v, a, q, sm, t0, n);
+    flush_stage(v, q, sm, n);
     __syncthreads();
   }
 }
@@ -150,9 +186,9 @@ __device__ void quantize_rows(const KvqView& v, const Src& s, const AppendCtx& a
 // channel over groups of G tokens aligned to multiples of G.
 __device__ void quantize_key_channels(const KvqView& v, const Src& s, const AppendCtx& a,
                                       const TQ& q, Smem& sm, int t_begin, int count) {
-  const int D = v.D, G = q.group;
-  const int lanes = kThreads / D;
-  const int c = threadIdx.x % D, lane = threadIdx.x / D;
+  const int D = v.D, G = q.group, lD = log2i(D);
+  const int lanes = kThreads >> lD;
+  const int c = threadIdx.x & (D - 1), lane = threadIdx.x >> lD;
   for (int g0 = t_begin; g0 < t_begin + count; g0 += G) {
     float mn = INFINITY, mx = -INFINITY;
     for (int t = g0 + lane; t < g0 + G; t += lanes) {
@@ -176,6 +212,7 @@ __device__ void quantize_key_channels(const KvqView& v, const Src& s, const Appe
         mn = 0.f;
       }
       sm.ch_s[c] = sc;
+      sm.ch_r[c] = sc > 0.f ? __frcp_rn(sc) : 0.f;
       sm.ch_m[c] = mn;
       uint8_t* page = page_of(v, a.b, g0);
       if (page) {
@@ -191,16 +228,18 @@ __device__ void quantize_key_channels(const KvqView& v, const Src& s, const Appe
       const int n = min(kSub, G - sub);
       const int t0 = g0 + sub;
       clear_stage(sm, q, n);
+      load_rows(v, a, sm, t0, n);
       __syncthreads();
-      for (int e = threadIdx.x; e < n * D; e += kThreads) {
-        const int r = e / D, cc = e % D;
+      for (int e = threadIdx.x; e < (n << lD); e += kThreads) {
+        const int r = e >> lD, cc = e & (D - 1);
         const float x = src_value(v, s, a, t0 + r, cc);
-        const int code = q.mode == KVQ_ASYM_MINMAX ? asym_code(x, sm.ch_m[cc], sm.ch_s[cc], q.bits)
-                                                   : sym_code(x, sm.ch_s[cc], q.bits);
+        const int code = q.mode == KVQ_ASYM_MINMAX
+                             ? asym_code_r(x, sm.ch_m[cc], sm.ch_s[cc], sm.ch_r[cc], q.bits)
+                             : sym_code_r(x, sm.ch_s[cc], sm.ch_r[cc], q.bits);
         stage_code(sm, r, cc, q.bits, stored_code(code, q.bits, q.mode));
       }
       __syncthreads();
-      flush_stage(v, a, q, sm, t0, n);
+      flush_stage(v, q, sm, n);
       __syncthreads();
     }
   }
@@ -233,10 +272,37 @@ __device__ void quantize_block(const KvqView& v, const Src& ks, const Src& vs, c
   quantize_rows(v, vs, a, vq, sm, t_begin, count);
 }
 
+// Copy the source rows (window or new tokens) of tokens [t_begin, t_begin + count)
+// of one head into shared memory with 16-byte loads, K rows then V rows.
+__device__ void stage_block(const KvqView& v, const AppendCtx& a, const void* k_new, const void* v_new,
+                            int t_begin, int count, unsigned char* dst) {
+  const int row = v.D * (v.src_bf16 ? 2 : 4);
+  const int per_row = row / 16;
+  const int n = 2 * count * per_row;
+  for (int e = threadIdx.x; e < n; e += kThreads) {
+    const int tensor = e / (count * per_row);
+    const int rem = e % (count * per_row);
+    const int r = rem / per_row, k = rem % per_row;
+    const int t = t_begin + r;
+    const unsigned char* src;
+    if (t < a.T0) {
+      const long long i = (((long long)a.b * v.R + (t - a.wbase)) * v.Hkv + a.h) * row;
+      src = static_cast<const unsigned char*>(tensor ? v.v_win : v.k_win) + i;
+    } else {
+      const long long i = (((long long)a.b * a.n_stride + (t - a.T0)) * v.Hkv + a.h) * row;
+      src = static_cast<const unsigned char*>(tensor ? v_new : k_new) + i;
+    }
+    reinterpret_cast<uint4*>(dst + (long long)tensor * count * row + r * row)[k] =
+        reinterpret_cast<const uint4*>(src)[k];
+  }
+  __syncthreads();
+}
+
 __global__ void __launch_bounds__(kThreads) append_kernel(KvqView v, const void* k_new,
                                                            const void* v_new, int n_stride,
-                                                           const int32_t* n_per_seq) {
+                                                           const int32_t* n_per_seq, int stage_ok) {
   __shared__ Smem sm;
+  extern __shared__ __align__(16) unsigned char staged[];
   const int unit = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int T0 = v.seq_lens[b];
   const int n = n_per_seq ? n_per_seq[b] : n_stride;
@@ -252,22 +318,23 @@ __global__ void __launch_bounds__(kThreads) append_kernel(KvqView v, const void*
   a.h = h;
   a.T0 = T0;
   a.n_stride = n_stride;
-  const Src ks{v.k_win, k_new}, vs{v.v_win, v_new};
+  a.st_t0 = 0;
+  const Src ks{v.k_win, k_new, nullptr}, vs{v.v_win, v_new, nullptr};
   if (v.R > 0) {
     const int jb0 = T0 / v.R, jb1 = T1 / v.R;
     a.wbase = jb0 * v.R;
-    if (unit < jb1 - jb0) quantize_block(v, ks, vs, a, sm, (jb0 + unit) * v.R, v.R);
-    if (unit == 0) {
-      __syncthreads();
-      const int base = jb1 * v.R;
-      const int t_lo = max(base, T0);
-      const int D = v.D;
-      for (int e = threadIdx.x; e < (T1 - t_lo) * D; e += kThreads) {
-        const int t = t_lo + e / D, c = e % D;
-        const long long si = (((long long)b * n_stride + (t - T0)) * v.Hkv + h) * D + c;
-        const long long di = (((long long)b * v.R + (t - base)) * v.Hkv + h) * D + c;
-        store_src(v.k_win, di, load_src(k_new, si, v.src_bf16), v.src_bf16);
-        store_src(v.v_win, di, load_src(v_new, si, v.src_bf16), v.src_bf16);
+    if (unit < jb1 - jb0) {
+      const int tb = (jb0 + unit) * v.R;
+      if (stage_ok) {
+        // the whole R-token block fits in shared memory: one parallel pass of loads,
+        // then every quantizer pass reads shared memory
+        stage_block(v, a, k_new, v_new, tb, v.R, staged);
+        a.st_t0 = tb;
+        const int row = v.D * (v.src_bf16 ? 2 : 4);
+        const Src kss{v.k_win, k_new, staged}, vss{v.v_win, v_new, staged + (long long)v.R * row};
+        quantize_block(v, kss, vss, a, sm, tb, v.R);
+      } else {
+        quantize_block(v, ks, vs, a, sm, tb, v.R);
       }
     }
   } else {
@@ -277,13 +344,31 @@ __global__ void __launch_bounds__(kThreads) append_kernel(KvqView v, const void*
   }
 }
 
-__global__ void advance_lengths_kernel(KvqView v, int n_stride, const int32_t* n_per_seq) {
-  const int b = blockIdx.x * blockDim.x + threadIdx.x;
-  if (b >= v.batch) return;
+// After the folds: write each sequence's remaining new tokens into its window
+// (slots from the last fold boundary) and advance seq_lens.  One CTA per
+// sequence, so the CTA that updates seq_lens[b] is the only one that reads it.
+__global__ void __launch_bounds__(kThreads) window_lengths_kernel(KvqView v, const void* k_new,
+                                                                   const void* v_new, int n_stride,
+                                                                   const int32_t* n_per_seq) {
+  const int b = blockIdx.x;
   const int T0 = v.seq_lens[b];
   const int n = n_per_seq ? n_per_seq[b] : n_stride;
   if (n <= 0 || T0 < 0 || n > n_stride || (long long)T0 + n > (long long)v.max_pages * v.P) return;
-  v.seq_lens[b] = T0 + n;
+  const int T1 = T0 + n;
+  if (v.R > 0) {
+    const int base = (T1 / v.R) * v.R;
+    const int t_lo = max(base, T0);
+    const int row = v.Hkv * v.D;  // elements of one token (all heads)
+    for (int e = threadIdx.x; e < (T1 - t_lo) * row; e += kThreads) {
+      const int t = t_lo + e / row, c = e % row;
+      const long long si = ((long long)b * n_stride + (t - T0)) * row + c;
+      const long long di = ((long long)b * v.R + (t - base)) * row + c;
+      store_src(v.k_win, di, load_src(k_new, si, v.src_bf16), v.src_bf16);
+      store_src(v.v_win, di, load_src(v_new, si, v.src_bf16), v.src_bf16);
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) v.seq_lens[b] = T1;
 }
 
 // ------------------------------------------------------------------- dequantize
@@ -382,8 +467,20 @@ kvq_status launch_append(const KvqView& v, const void* k_new, const void* v_new,
                          const int32_t* n_new_per_seq, cudaStream_t st) {
   const int units = v.R > 0 ? n_new / v.R + 1 : (n_new + kUnitTok - 1) / kUnitTok;
   dim3 grid(units, v.Hkv, v.batch);
-  append_kernel<<<grid, kThreads, 0, st>>>(v, k_new, v_new, n_new, n_new_per_seq);
-  advance_lengths_kernel<<<(v.batch + 127) / 128, 128, 0, st>>>(v, n_new, n_new_per_seq);
+  const size_t stage_bytes = v.R > 0 ? 2ull * v.R * v.D * (v.src_bf16 ? 2 : 4) : 0;
+  const uintptr_t align_bits = reinterpret_cast<uintptr_t>(k_new) | reinterpret_cast<uintptr_t>(v_new) |
+                               reinterpret_cast<uintptr_t>(v.k_win) | reinterpret_cast<uintptr_t>(v.v_win);
+  const int stage_ok = stage_bytes > 0 && stage_bytes <= kStageMax && (align_bits & 15) == 0;
+  static bool attr_set = false;
+  if (stage_ok && !attr_set) {
+    if (cudaFuncSetAttribute(append_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kStageMax) !=
+        cudaSuccess)
+      return KVQ_ERR_CUDA;
+    attr_set = true;
+  }
+  append_kernel<<<grid, kThreads, stage_ok ? stage_bytes : 0, st>>>(v, k_new, v_new, n_new, n_new_per_seq,
+                                                                    stage_ok);
+  window_lengths_kernel<<<v.batch, kThreads, 0, st>>>(v, k_new, v_new, n_new, n_new_per_seq);
   return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }
 

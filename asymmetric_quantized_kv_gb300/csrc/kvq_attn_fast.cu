@@ -10,17 +10,18 @@
 // (cp.async.bulk, completion on an mbarrier, every wait bounded).
 //
 // Per 16-token tile and warp:
-//   QK: K codes -> fp32 (x per-channel scale) -> RoPE rotation by the token's
-//       absolute position (cos/sin from a per-tile table shared by the 8 warps)
-//       -> split into f16 hi + lo -> two mma.m16n8k16 per 16 channels with
-//       A = keys (16 tokens x 16 channels) and B = q (16 channels x 8 columns:
-//       4 query heads x {hi, lo} halves of q*scale*log2(e)).  The hi/lo split
-//       of both operands keeps the logits to ~2^-21 relative.
+//   QK: K codes -> fp32 (x per-channel scale, packed f32x2) -> RoPE rotation by
+//       the token's absolute position (cos/sin from a per-tile table shared by
+//       the 8 warps) -> split into f16 hi + lo -> two mma.m16n8k16 per 16
+//       channels with A = keys (16 tokens x 16 channels) and B = q (16 channels
+//       x 8 columns: 4 query heads x {hi, lo} halves of q*scale*log2(e)).  The
+//       hi/lo split of both operands keeps the logits to ~2^-21 relative.
 //   softmax: online in base 2, one running max per head with lazy rescaling
 //       (only when the max grows by more than 2^8).
 //   PV: A = V^T codes (16 channels x 16 tokens) formed with PRMT/LOP3 and one
 //       f16x2 fix-up as exact f16 integers, B = p * v_scale split hi/lo; the
 //       per-token minimum enters through a running sum of p * v_min.
+// Residual-window items use the same steps on the source-dtype rows.
 // Partials (max, sum, unnormalised output) per (item, query head) go to the
 // workspace; the combine kernel merges them.
 #include <math.h>
@@ -52,10 +53,19 @@ constexpr int kVM = kTile * 8;           // 128
 constexpr int kStageBytes = kKC + kVC + kVM;
 constexpr int kKMeta = kD * 4;           // per-channel scales of one key group
 
+// Shared-memory layouts are chosen so that every 64/128-bit load of a warp
+// meets no bank conflict within the quarter- or half-warp that the hardware
+// serves in one wavefront:
+//   trig: (cos, sin) per (token row, RoPE pair); 16-byte units (two pairs) of a
+//         row are XOR-swizzled by (2 * (unit / 8) + row % 2) % 8;
+//   kmeta: the 128 key scales of a group as 4 rows of 32, each row padded to
+//         36 floats (144 bytes), one row per lane quarter t;
+//   tokens: MMA row r holds tile token sig(r) = r ^ ((r >> 1) & 1), which
+//         spreads the value rows a half-warp reads over two bank offsets.
 struct __align__(128) SmemRI {
   uint8_t stage[kWarps][kStages][kStageBytes];
-  float kmeta[kWarps][2][kD];
-  float4 trig[2][kTile][32];  // per (token, pair pair): cos0, sin0, cos1, sin1; swizzled
+  float kmeta[kWarps][2][4][36];
+  float2 trig[2][kTile][64];
   uint64_t bar[kWarps][kStages];
   int valid[kWarps][kStages];
   float w_hi[kD / 2], w_lo[kD / 2];
@@ -66,22 +76,111 @@ struct FastItem {
   int b, t0, t1, window;
 };
 
-__device__ inline FastItem decode_fast_item(const KvqView& v, const int* pref, int C, int item) {
-  int lo = 0, hi = v.batch - 1;
+// Work plan of this kernel, at the head of the workspace:
+//   int C, NA, NB, pad; int prefA[B+1]; int prefB[B+1]; u64 counter
+// Items d < NA are the full C-token chunks of every sequence (prefA: per-sequence
+// prefix of counts); items d >= NA are the short ones (each sequence's last,
+// partial chunk and its residual window; prefB).  Long items come first, and
+// CTAs take items dynamically from the counter (zeroed by the host before each
+// call), so the last wave holds only short items.
+__host__ __device__ inline size_t fast_header_ints(int B) { return (size_t)2 * (B + 1) + 4; }
+__host__ __device__ inline size_t fast_counter_offset(int B) { return (fast_header_ints(B) * 4 + 7) & ~(size_t)7; }
+__host__ __device__ inline size_t fast_header_bytes(int B) { return (fast_counter_offset(B) + 8 + 255) / 256 * 256; }
+
+__device__ inline void fast_plan(const KvqView& v, int align, int* sA, int* sB, int* s_C, int* s_NA, int* s_NB) {
+  __shared__ unsigned long long s_total;
+  __shared__ int s_pa[kThreads], s_pb[kThreads];
+  const int B = v.batch;
+  if (threadIdx.x == 0) s_total = 0ull;
+  __syncthreads();
+  unsigned long long sum = 0;
+  for (int b = threadIdx.x; b < B; b += blockDim.x) sum += (unsigned long long)seq_tokens(v, b);
+  atomicAdd(&s_total, sum);
+  __syncthreads();
+  long long C = (long long)((s_total + kFastTarget - 1) / kFastTarget);
+  if (C < kFastMinChunk) C = kFastMinChunk;
+  C = (C + align - 1) / align * align;
+  const int seg = (B + kThreads - 1) / kThreads;
+  const int b0 = threadIdx.x * seg, b1 = min(B, b0 + seg);
+  int la = 0, lb = 0;
+  for (int b = b0; b < b1; ++b) {
+    const int T = seq_tokens(v, b), nq = n_quantized(T, v.R);
+    la += nq / (int)C;
+    lb += (nq % (int)C ? 1 : 0) + (T > nq ? 1 : 0);
+  }
+  s_pa[threadIdx.x] = la;
+  s_pb[threadIdx.x] = lb;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int ra = 0, rb = 0;
+    for (int k = 0; k < kThreads; ++k) {
+      const int xa = s_pa[k], xb = s_pb[k];
+      s_pa[k] = ra;
+      s_pb[k] = rb;
+      ra += xa;
+      rb += xb;
+    }
+    *s_NA = ra;
+    *s_NB = rb;
+    *s_C = (int)C;
+  }
+  __syncthreads();
+  int ra = s_pa[threadIdx.x], rb = s_pb[threadIdx.x];
+  for (int b = b0; b < b1; ++b) {
+    const int T = seq_tokens(v, b), nq = n_quantized(T, v.R);
+    sA[b] = ra;
+    sB[b] = rb;
+    ra += nq / (int)C;
+    rb += (nq % (int)C ? 1 : 0) + (T > nq ? 1 : 0);
+  }
+  if (threadIdx.x == 0) {
+    sA[B] = *s_NA;
+    sB[B] = *s_NB;
+  }
+  __syncthreads();
+}
+
+__device__ inline void store_fast_plan(const KvqView& v, float* ws, const int* sA, const int* sB, int C, int NA,
+                                       int NB) {
+  int* h = reinterpret_cast<int*>(ws);
+  if (threadIdx.x == 0) {
+    h[0] = C;
+    h[1] = NA;
+    h[2] = NB;
+  }
+  for (int b = threadIdx.x; b <= v.batch; b += blockDim.x) {
+    h[4 + b] = sA[b];
+    h[4 + v.batch + 1 + b] = sB[b];
+  }
+}
+
+// largest b with pref[b] <= x (pref[0] = 0, x < pref[B])
+__device__ inline int seq_of(const int* pref, int B, int x) {
+  int lo = 0, hi = B - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (pref[mid] <= item) lo = mid; else hi = mid - 1;
+    if (pref[mid] <= x) lo = mid; else hi = mid - 1;
   }
+  return lo;
+}
+
+__device__ inline FastItem decode_fast_item(const KvqView& v, const int* sA, const int* sB, int C, int NA,
+                                            int d) {
   FastItem it;
-  it.b = lo;
-  const int chunk = item - pref[lo];
-  const int T = seq_tokens(v, lo);
-  const int nq = n_quantized(T, v.R);
-  const int nqc = (nq + C - 1) / C;
-  if (chunk < nqc) {
+  if (d < NA) {
+    it.b = seq_of(sA, v.batch, d);
     it.window = 0;
-    it.t0 = chunk * C;
-    it.t1 = min(nq, it.t0 + C);
+    it.t0 = (d - sA[it.b]) * C;
+    it.t1 = it.t0 + C;
+    return it;
+  }
+  const int e = d - NA;
+  it.b = seq_of(sB, v.batch, e);
+  const int T = seq_tokens(v, it.b), nq = n_quantized(T, v.R);
+  if (e == sB[it.b] && nq % C) {
+    it.window = 0;
+    it.t0 = (nq / C) * C;
+    it.t1 = nq;
   } else {
     it.window = 1;
     it.t0 = nq;
@@ -100,23 +199,109 @@ __device__ __forceinline__ float2 rope_cs(int p, float w_hi, float w_lo) {
   return make_float2(c, s);
 }
 
-// Signed INT8 code j of word w as an exact float.
-__device__ __forceinline__ float i8_to_f32(uint32_t w_offset_binary, uint32_t j) {
-  const uint32_t x = prmt(w_offset_binary, 0x4B000000u, 0x7540u | j);
-  return __uint_as_float(x) - 8388736.f;  // 2^23 + 128
+// (lo, hi) halves of an f16x2 minus c, in fp32 (exact for the magic-number codes)
+__device__ __forceinline__ float2 h2_minus(uint32_t h2, float c) {
+  unsigned short h0, h1;
+  asm("mov.b32 {%0, %1}, %2;" : "=h"(h0), "=h"(h1) : "r"(h2));
+  float2 r;
+  asm("sub.rn.f32.f16 %0, %1, %2;" : "=f"(r.x) : "h"(h0), "f"(c));
+  asm("sub.rn.f32.f16 %0, %1, %2;" : "=f"(r.y) : "h"(h1), "f"(c));
+  return r;
+}
+
+__device__ __forceinline__ int sig(int x) { return x ^ ((x >> 1) & 1); }
+
+// Per-warp attention state of one item: PV accumulators (16-channel MMA tiles m,
+// rows g / g+8 = channels 16g + 2m / 16g + 2m + 1, columns head t hi / lo),
+// running max (log2 units), this lane's share of the softmax sum and of the
+// p * v_min sum.
+struct Acc {
+  float O[8][4];
+  float m_run, l_loc, mb;
+};
+
+// The RoPE table of one tile: entry (token d, pair p) = e^{i (tok0 + d) theta_p},
+// from the per-tile base Bp = e^{i tok0 theta_p} (re-seeded exactly every 16 tiles,
+// otherwise advanced by R16 = e^{i 16 theta_p}) times Td[j] = e^{i d theta_p}.
+__device__ __forceinline__ void rope_table(SmemRI& sm, uint32_t buf, int i, int tok0, int tp, int td,
+                                           const float2 (&Td)[4], float2 R16, float2& Bp) {
+  if ((i & 15) == 0) Bp = rope_cs(tok0, sm.w_hi[tp], sm.w_lo[tp]);
+  else Bp = cmul(Bp, R16);
+  const int u = tp >> 1;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int d = td + 4 * j;
+    const int key = (((u >> 3) << 1) | (d & 1)) & 7;
+    sm.trig[buf][d][((u ^ key) << 1) | (tp & 1)] = cmul(Bp, Td[j]);
+  }
+}
+
+// Rotate (k0, k1), (k2, k3) by the table's (cos, sin) of two pairs and split
+// each rotated pair into f16x2 hi and (hi - x).
+__device__ __forceinline__ void rotate_split(float k0, float k1, float k2, float k3, float4 cs, uint32_t& hi01,
+                                             uint32_t& nl01, uint32_t& hi23, uint32_t& nl23) {
+  const float r0 = k0 * cs.x - k1 * cs.y, r1 = k0 * cs.y + k1 * cs.x;
+  const float r2 = k2 * cs.z - k3 * cs.w, r3 = k2 * cs.w + k3 * cs.z;
+  split_hi_neglo(r0, r1, hi01, nl01);
+  split_hi_neglo(r2, r3, hi23, nl23);
+}
+
+// Online-softmax step for the two logits of this lane (tokens of MMA rows g and
+// g+8, head t), then the PV B operand: P' = p * pscale for k-slots 2t, 2t+1 and
+// 2t+8, 2t+9 of column g (head g/2, hi half for even g, lo half for odd g).
+__device__ __forceinline__ void softmax_step(Acc& A, float lg0, float lg1, float2 m0, float2 m1, int g, int t,
+                                             uint32_t& b01, uint32_t& b23) {
+  float mx = fmaxf(lg0, lg1);
+  mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+  mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+  mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+  const bool need = mx > A.m_run + kRescale;
+  if (__any_sync(0xffffffffu, need)) {
+    const float mn = need ? mx : A.m_run;
+    const float alpha = (A.m_run == -INFINITY) ? 0.f : ex2(A.m_run - mn);
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+      A.O[m][0] *= alpha; A.O[m][1] *= alpha; A.O[m][2] *= alpha; A.O[m][3] *= alpha;
+    }
+    A.l_loc *= alpha;
+    A.mb *= alpha;
+    A.m_run = mn;
+  }
+  float p0 = 0.f, p1 = 0.f;
+  if (A.m_run != -INFINITY) {
+    p0 = ex2(lg0 - A.m_run);
+    p1 = ex2(lg1 - A.m_run);
+  }
+  A.l_loc += p0 + p1;
+  A.mb += p0 * m0.y + p1 * m1.y;
+  const float pv0 = p0 * m0.x, pv1 = p1 * m1.x;
+  const int src0 = 4 * (2 * t) + (g >> 1), src1 = src0 + 4;
+  const float x0 = __shfl_sync(0xffffffffu, pv0, src0);
+  const float y0 = __shfl_sync(0xffffffffu, pv1, src0);
+  const float x1 = __shfl_sync(0xffffffffu, pv0, src1);
+  const float y1 = __shfl_sync(0xffffffffu, pv1, src1);
+  uint32_t hA, lA, hB, lB;
+  split_hi_lo(x0, x1, hA, lA);
+  split_hi_lo(y0, y1, hB, lB);
+  b01 = (g & 1) ? lA : hA;
+  b23 = (g & 1) ? lB : hB;
 }
 
 __global__ void __launch_bounds__(kThreads, 2)
     split_rope_i8i4_kernel(KvqView v, const void* q, float scale, float* ws) {
   extern __shared__ __align__(128) unsigned char dyn[];
   SmemRI& sm = *reinterpret_cast<SmemRI*>(dyn);
-  int* pref = reinterpret_cast<int*>(dyn + sizeof(SmemRI));
-  __shared__ int s_C, s_items;
+  int* prefA = reinterpret_cast<int*>(dyn + sizeof(SmemRI));
+  int* prefB = prefA + v.batch + 1;
+  __shared__ int s_C, s_NA, s_NB, s_next[2];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
-  const int G = v.kgroup;
-  plan_items_ex(v, 1, G, kFastTarget, kFastMinChunk, pref, &s_C, &s_items);
-  if (blockIdx.x == 0) store_plan(v, ws, pref, s_C, s_items);
+  const int G = v.kgroup;  // powers of two (checked on the host)
+  const int lgG = __ffs(G) - 1, lgP = __ffs(v.P) - 1;
+  fast_plan(v, G, prefA, prefB, &s_C, &s_NA, &s_NB);
+  if (blockIdx.x == 0) store_fast_plan(v, ws, prefA, prefB, s_C, s_NA, s_NB);
+  unsigned long long* counter =
+      reinterpret_cast<unsigned long long*>(reinterpret_cast<char*>(ws) + fast_counter_offset(v.batch));
   if (lane == 0) {
     for (int s = 0; s < kStages; ++s) mbar_init(&sm.bar[warp][s], 1);
     fence_mbar_init();
@@ -133,17 +318,23 @@ __global__ void __launch_bounds__(kThreads, 2)
   const float2 R16 = rope_cs(16, sm.w_hi[tp], sm.w_lo[tp]);
   float2 Bp = make_float2(1.f, 0.f);
 
-  const int C = s_C, n_items = s_items;
-  float* part = plan_partials(ws, v.batch);
+  const int C = s_C, NA = s_NA, n_items = s_NA + s_NB;
+  float* part = reinterpret_cast<float*>(reinterpret_cast<char*>(ws) + fast_header_bytes(v.batch));
   const float qscale = scale * kLog2e;
-  uint32_t load_seq = 0, cons_seq = 0;
-  uint32_t tc = 0;  // tiles processed by this CTA: selects the RoPE table buffer
   const int h = warp;
+  const int sg = sig(g);  // tile token of MMA row g (row g + 8: token sg + 8)
+  const long long head_off = (long long)h * v.head_bytes;
+  // this warp's ring: lane 0 loads at lstage, everyone consumes at cstage / cphase
+  int lstage = 0, cstage = 0;
+  uint32_t cphase = 0, n_loaded = 0, n_consumed = 0;
+  uint32_t tc = 0;  // tiles processed by this CTA: selects the RoPE table buffer
 
-  for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
-    const FastItem it = decode_fast_item(v, pref, C, item);
+  int item = blockIdx.x, npar = 0;
+  while (item < n_items) {
+    // the CTA's next item, fetched now and read after this item's tile barriers
+    if (threadIdx.x == 0) s_next[npar] = (int)gridDim.x + (int)atomicAdd(counter, 1ull);
+    const FastItem it = decode_fast_item(v, prefA, prefB, C, NA, item);
     const int ntiles = (it.t1 - it.t0 + kTile - 1) / kTile;
-    const int T = it.window ? it.t1 : 0;
 
     // B operand: q * scale * log2(e) for query head 4h + g/2, split hi (even g) / lo (odd g)
     uint32_t bq[8][2];
@@ -163,208 +354,128 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
     }
 
-    // prologue: this warp's first tile loads
-    auto issue = [&](int i) {
-      const int stage = load_seq % kStages;
-      ++load_seq;
-      const int tok = it.t0 + i * kTile;
-      uint64_t* bar = &sm.bar[warp][stage];
-      const int pid = v.block_table[(long long)it.b * v.max_pages + tok / v.P];
-      const bool ok = pid >= 0 && pid < v.n_pages;
-      sm.valid[warp][stage] = ok;
-      if (!ok) {
-        atomicOr(v.status, KVQ_DEV_BAD_PAGE);
-        mbar_arrive(bar);
-        return;
-      }
-      const uint8_t* hbk = v.pages + (long long)pid * v.page_bytes + (long long)h * v.head_bytes;
-      const int slot = tok % v.P;
-      const bool gstart = (tok % G) == 0;
-      mbar_arrive_expect_tx(bar, kStageBytes + (gstart ? kKMeta : 0));
-      uint8_t* dst = sm.stage[warp][stage];
-      if (v.P == kTile) {
-        bulk_g2s(dst, hbk, kStageBytes, bar);
-      } else {
-        bulk_g2s(dst, hbk + slot * kD, kKC, bar);
-        bulk_g2s(dst + kKC, hbk + v.off_vc + slot * (kD / 2), kVC, bar);
-        bulk_g2s(dst + kKC + kVC, hbk + v.off_vm + slot * 8, kVM, bar);
-      }
-      if (gstart) {
-        const int gslot = v.P >= G ? slot / G : 0;
-        bulk_g2s(sm.kmeta[warp][(tok / G) & 1], hbk + v.off_km + gslot * kKMeta, kKMeta, bar);
-      }
-    };
-    if (!it.window && lane == 0 && !sm.abort) {
-      for (int i = 0; i < min(kStages, ntiles); ++i) issue(i);
-    }
-    __syncwarp();
-
-    float O[8][4];
+    Acc A;
 #pragma unroll
-    for (int m = 0; m < 8; ++m) O[m][0] = O[m][1] = O[m][2] = O[m][3] = 0.f;
-    float m_run = -INFINITY, l_loc = 0.f, mb = 0.f;
+    for (int m = 0; m < 8; ++m) A.O[m][0] = A.O[m][1] = A.O[m][2] = A.O[m][3] = 0.f;
+    A.m_run = -INFINITY;
+    A.l_loc = 0.f;
+    A.mb = 0.f;
 
-    for (int i = 0; i < ntiles; ++i) {
-      const int tok0 = it.t0 + i * kTile;
-      // ---- RoPE table for this tile (all warps), then one CTA barrier
-      {
-        if ((i & 15) == 0) Bp = rope_cs(tok0, sm.w_hi[tp], sm.w_lo[tp]);
-        else Bp = cmul(Bp, R16);
-        float* tb = reinterpret_cast<float*>(&sm.trig[tc & 1][0][0]);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int d = td + 4 * j;
-          const float2 e = cmul(Bp, Td[j]);
-          const int unit = (tp >> 1) ^ (d & 7);
-          float* p = tb + (d * 32 + unit) * 4 + (tp & 1) * 2;
-          p[0] = e.x;
-          p[1] = e.y;
+    if (!it.window) {
+      // ======================= quantized chunk: tiles through the TMA ring
+      const int32_t* bt = v.block_table + (long long)it.b * v.max_pages;
+      auto issue = [&](int i, int pid) {
+        const int stage = lstage;
+        if (++lstage == kStages) lstage = 0;
+        ++n_loaded;
+        const int tok = it.t0 + i * kTile;
+        uint64_t* bar = &sm.bar[warp][stage];
+        const bool ok = pid >= 0 && pid < v.n_pages;
+        sm.valid[warp][stage] = ok;
+        if (!ok) {
+          atomicOr(v.status, KVQ_DEV_BAD_PAGE);
+          mbar_arrive(bar);
+          return;
         }
+        const uint8_t* hbk = v.pages + (long long)pid * v.page_bytes + head_off;
+        const int slot = tok & (v.P - 1);
+        const bool gstart = (tok & (G - 1)) == 0;
+        mbar_arrive_expect_tx(bar, kStageBytes + (gstart ? kKMeta : 0));
+        uint8_t* dst = sm.stage[warp][stage];
+        if (v.P == kTile) {
+          bulk_g2s(dst, hbk, kStageBytes, bar);
+        } else {
+          bulk_g2s(dst, hbk + slot * kD, kKC, bar);
+          bulk_g2s(dst + kKC, hbk + v.off_vc + slot * (kD / 2), kVC, bar);
+          bulk_g2s(dst + kKC + kVC, hbk + v.off_vm + slot * 8, kVM, bar);
+        }
+        if (gstart) {
+          const int gslot = v.P >= G ? (slot >> lgG) : 0;
+          const uint8_t* src = hbk + v.off_km + gslot * kKMeta;
+#pragma unroll
+          for (int r = 0; r < 4; ++r) bulk_g2s(sm.kmeta[warp][(tok >> lgG) & 1][r], src + 128 * r, 128, bar);
+        }
+      };
+      int pf = 0;  // lane 0: page id of the next tile to load, read one tile ahead
+      if (lane == 0 && !sm.abort) {
+        for (int i = 0; i < min(kStages, ntiles); ++i) issue(i, bt[(it.t0 + i * kTile) >> lgP]);
+        if (kStages < ntiles) pf = bt[(it.t0 + kStages * kTile) >> lgP];
       }
-      named_bar_sync(1, kThreads);
+      __syncwarp();
 
-      // ---- wait for this warp's tile
-      int stage = 0;
-      bool valid = true;
-      if (!it.window) {
-        stage = cons_seq % kStages;
-        const uint32_t parity = (cons_seq / kStages) & 1;
-        ++cons_seq;
+      for (int i = 0; i < ntiles; ++i) {
+        const int tok0 = it.t0 + i * kTile;
+        rope_table(sm, tc & 1, i, tok0, tp, td, Td, R16, Bp);
+        named_bar_sync(1, kThreads);
+
+        const int stage = cstage;
+        bool valid = false;
         if (!*reinterpret_cast<volatile int*>(&sm.abort)) {
-          if (!mbar_wait_bounded(&sm.bar[warp][stage], parity, kSpin)) {
+          if (!mbar_wait_bounded(&sm.bar[warp][stage], cphase, kSpin)) {
             atomicOr(v.status, KVQ_DEV_TIMEOUT);
             sm.abort = 1;
-            valid = false;
           } else {
             valid = sm.valid[warp][stage] != 0;
           }
-        } else {
-          valid = false;
         }
-      }
-      const uint8_t* buf = sm.stage[warp][stage];
-      // per-channel key scales of this tile's group (channels 32t .. 32t+31)
-      const float4* km = reinterpret_cast<const float4*>(&sm.kmeta[warp][(tok0 / G) & 1][32 * t]);
+        if (++cstage == kStages) {
+          cstage = 0;
+          cphase ^= 1u;
+        }
+        ++n_consumed;
+        const uint8_t* buf = sm.stage[warp][stage];
 
-      // ---- QK: rows g and g+8 of the tile, channels 32t .. 32t+31
-      float acc[4] = {0.f, 0.f, 0.f, 0.f}, accn[4] = {0.f, 0.f, 0.f, 0.f};
-      const float4* trow0 = &sm.trig[tc & 1][g][0];
-      const float4* trow1 = &sm.trig[tc & 1][g + 8][0];
-      if (!it.window) {
+        // ---- QK: MMA rows g / g+8 = tile tokens sg / sg+8, channels 32t .. 32t+31
+        const float4* km = reinterpret_cast<const float4*>(&sm.kmeta[warp][(tok0 >> lgG) & 1][t][0]);
+        const float4* trow0 = reinterpret_cast<const float4*>(&sm.trig[tc & 1][sg][0]);
+        const float4* trow1 = reinterpret_cast<const float4*>(&sm.trig[tc & 1][sg + 8][0]);
+        const int tkey = ((t << 1) | (sg & 1)) & 7;
         uint32_t kw[2][8];
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
-          const uint4* src = reinterpret_cast<const uint4*>(buf + (g + 8 * r) * kD + 32 * t);
-          const int rot = g & 1;
-          const uint4 a = src[rot], b = src[rot ^ 1];
-          const uint4 lo = rot ? b : a, hi = rot ? a : b;
+          const uint4* src = reinterpret_cast<const uint4*>(buf + (sg + 8 * r) * kD + 32 * t);
+          const uint4 lo = src[0], hi = src[1];
           kw[r][0] = lo.x ^ 0x80808080u; kw[r][1] = lo.y ^ 0x80808080u;
           kw[r][2] = lo.z ^ 0x80808080u; kw[r][3] = lo.w ^ 0x80808080u;
           kw[r][4] = hi.x ^ 0x80808080u; kw[r][5] = hi.y ^ 0x80808080u;
           kw[r][6] = hi.z ^ 0x80808080u; kw[r][7] = hi.w ^ 0x80808080u;
         }
+        float acc[4] = {0.f, 0.f, 0.f, 0.f}, accn[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int s = 0; s < 8; ++s) {
           uint32_t ahi[2][2], anl[2][2];
           const float4 ks = km[s];
 #pragma unroll
           for (int r = 0; r < 2; ++r) {
-            const float4 cs = (r ? trow1 : trow0)[(8 * t + s) ^ (g & 7)];
-            const float k0 = i8_to_f32(kw[r][s], 0) * ks.x;
-            const float k1 = i8_to_f32(kw[r][s], 1) * ks.y;
-            const float k2 = i8_to_f32(kw[r][s], 2) * ks.z;
-            const float k3 = i8_to_f32(kw[r][s], 3) * ks.w;
-            const float r0 = k0 * cs.x - k1 * cs.y, r1 = k0 * cs.y + k1 * cs.x;
-            const float r2 = k2 * cs.z - k3 * cs.w, r3 = k2 * cs.w + k3 * cs.z;
-            split_hi_neglo(r0, r1, ahi[r][0], anl[r][0]);
-            split_hi_neglo(r2, r3, ahi[r][1], anl[r][1]);
+            const float4 cs = (r ? trow1 : trow0)[(8 * t + s) ^ tkey];
+            const uint32_t w = kw[r][s];
+            // offset-binary bytes -> f16 1024 + u (u = code + 128) -> fp32 code -> code * scale
+            const float2 c01 = h2_minus(prmt(w, 0x64646464u, 0x4140u), 1152.f);
+            const float2 c23 = h2_minus(prmt(w, 0x64646464u, 0x4342u), 1152.f);
+            const float2 k01 = mul2(c01, make_float2(ks.x, ks.y));
+            const float2 k23 = mul2(c23, make_float2(ks.z, ks.w));
+            rotate_split(k01.x, k01.y, k23.x, k23.y, cs, ahi[r][0], anl[r][0], ahi[r][1], anl[r][1]);
           }
           mma_16816(acc, ahi[0][0], ahi[1][0], ahi[0][1], ahi[1][1], bq[s][0], bq[s][1]);
           mma_16816(accn, anl[0][0], anl[1][0], anl[0][1], anl[1][1], bq[s][0], bq[s][1]);
         }
-      } else {
-        // residual window: bf16/f32 keys straight from k_win
-#pragma unroll
-        for (int s = 0; s < 8; ++s) {
-          uint32_t ahi[2][2], anl[2][2];
-#pragma unroll
-          for (int r = 0; r < 2; ++r) {
-            const int tok = tok0 + g + 8 * r;
-            float k[4] = {0.f, 0.f, 0.f, 0.f};
-            if (tok < T) {
-              const long long wi = (((long long)it.b * v.R + (tok - it.t0)) * v.Hkv + h) * kD + 32 * t + 4 * s;
-#pragma unroll
-              for (int j = 0; j < 4; ++j) k[j] = load_src(v.k_win, wi + j, v.src_bf16);
-            }
-            const float4 cs = (r ? trow1 : trow0)[(8 * t + s) ^ (g & 7)];
-            const float r0 = k[0] * cs.x - k[1] * cs.y, r1 = k[0] * cs.y + k[1] * cs.x;
-            const float r2 = k[2] * cs.z - k[3] * cs.w, r3 = k[2] * cs.w + k[3] * cs.z;
-            split_hi_neglo(r0, r1, ahi[r][0], anl[r][0]);
-            split_hi_neglo(r2, r3, ahi[r][1], anl[r][1]);
-          }
-          mma_16816(acc, ahi[0][0], ahi[1][0], ahi[0][1], ahi[1][1], bq[s][0], bq[s][1]);
-          mma_16816(accn, anl[0][0], anl[1][0], anl[0][1], anl[1][1], bq[s][0], bq[s][1]);
-        }
-      }
-      float lg0 = acc[0] + acc[1] - accn[0] - accn[1];
-      float lg1 = acc[2] + acc[3] - accn[2] - accn[3];
-      const int last = it.window ? T : it.t1;
-      if (!valid || tok0 + g >= last) lg0 = -INFINITY;
-      if (!valid || tok0 + g + 8 >= last) lg1 = -INFINITY;
+        float lg0 = acc[0] + acc[1] - accn[0] - accn[1];
+        float lg1 = acc[2] + acc[3] - accn[2] - accn[3];
+        if (!valid) lg0 = lg1 = -INFINITY;
 
-      // ---- online softmax for head t (tokens g, g+8 in this lane)
-      float mx = fmaxf(lg0, lg1);
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-      const bool need = mx > m_run + kRescale;
-      if (__any_sync(0xffffffffu, need)) {
-        const float mn = need ? mx : m_run;
-        const float alpha = (m_run == -INFINITY) ? 0.f : ex2(m_run - mn);
-#pragma unroll
-        for (int m = 0; m < 8; ++m) {
-          O[m][0] *= alpha; O[m][1] *= alpha; O[m][2] *= alpha; O[m][3] *= alpha;
-        }
-        l_loc *= alpha;
-        mb *= alpha;
-        m_run = mn;
-      }
-      float p0 = 0.f, p1 = 0.f;
-      if (m_run != -INFINITY) {
-        p0 = ex2(lg0 - m_run);
-        p1 = ex2(lg1 - m_run);
-      }
-      l_loc += p0 + p1;
-      float pv0 = p0, pv1 = p1;
-      if (!it.window) {
-        const float2 m0 = valid ? reinterpret_cast<const float2*>(buf + kKC + kVC)[g] : make_float2(0.f, 0.f);
-        const float2 m1 = valid ? reinterpret_cast<const float2*>(buf + kKC + kVC)[g + 8] : make_float2(0.f, 0.f);
-        pv0 = p0 * m0.x;
-        pv1 = p1 * m1.x;
-        mb += p0 * m0.y + p1 * m1.y;
-      }
+        // ---- softmax and the PV B operand (P' = p * v_scale, v_min into A.mb)
+        const float2* vm = reinterpret_cast<const float2*>(buf + kKC + kVC);
+        const float2 m0 = valid ? vm[sg] : make_float2(0.f, 0.f);
+        const float2 m1 = valid ? vm[sg + 8] : make_float2(0.f, 0.f);
+        uint32_t b01, b23;
+        softmax_step(A, lg0, lg1, m0, m1, g, t, b01, b23);
 
-      // ---- P' to the PV B layout: tokens 2t, 2t+1 (b0b1) and 2t+8, 2t+9 (b2b3) of head g/2
-      const int src0 = 4 * (2 * t) + (g >> 1), src1 = src0 + 4;
-      const float x0 = __shfl_sync(0xffffffffu, pv0, src0);
-      const float y0 = __shfl_sync(0xffffffffu, pv1, src0);
-      const float x1 = __shfl_sync(0xffffffffu, pv0, src1);
-      const float y1 = __shfl_sync(0xffffffffu, pv1, src1);
-      uint32_t b01, b23;
-      {
-        uint32_t hA, lA, hB, lB;
-        split_hi_lo(x0, x1, hA, lA);
-        split_hi_lo(y0, y1, hB, lB);
-        b01 = (g & 1) ? lA : hA;
-        b23 = (g & 1) ? lB : hB;
-      }
-
-      // ---- PV: A = V^T (channel rows 16g + 2m (+1), tokens 2t, 2t+1, 2t+8, 2t+9)
-      if (!it.window) {
+        // ---- PV: A = V^T (channel rows 16g + 2m (+1); k-slots 2t, 2t+1, 2t+8, 2t+9 =
+        //      tokens sig(2t), sig(2t+1), +8), exact f16 codes
         uint2 vw[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          const int tok = 2 * t + (u & 1) + 8 * (u >> 1);
+          const int tok = sig(2 * t + (u & 1)) + 8 * (u >> 1);
           vw[u] = *reinterpret_cast<const uint2*>(buf + kKC + tok * (kD / 2) + 8 * g);
         }
 #pragma unroll
@@ -379,127 +490,226 @@ __global__ void __launch_bounds__(kThreads, 2)
             for (int sh = 0; sh < 2; ++sh) {
               const int m = 4 * w + 2 * hb + sh;
               const uint32_t ya = xa[hb] >> (8 * sh), yc = xc[hb] >> (8 * sh);
-              // 1024 + c -> c and 1024 + 16c -> c, both exact (tensor-core accumulation
-              // loses bits when an accumulator carries a large constant offset)
+              // 1024 + c -> c and 1024 + 16c -> c, both exact (an accumulator that
+              // carries a large constant offset loses bits in the tensor cores)
               const uint32_t lo_a = hsub2(and_or(ya, 0x000F000Fu, 0x64006400u), 0x64006400u);
               const uint32_t hi_a = hfma2(and_or(ya, 0x00F000F0u, 0x64006400u), 0x2C002C00u, 0xD400D400u);
               const uint32_t lo_c = hsub2(and_or(yc, 0x000F000Fu, 0x64006400u), 0x64006400u);
               const uint32_t hi_c = hfma2(and_or(yc, 0x00F000F0u, 0x64006400u), 0x2C002C00u, 0xD400D400u);
-              mma_16816(O[m], lo_a, hi_a, lo_c, hi_c, b01, b23);
+              mma_16816(A.O[m], lo_a, hi_a, lo_c, hi_c, b01, b23);
             }
           }
         }
-      } else {
-        // window values: f16 pairs (token 2t+u, 2t+1+u) per channel 16g + 2m (+1)
-        float vv[4][16];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int tok = tok0 + 2 * t + (u & 1) + 8 * (u >> 1);
-          const long long wi = (((long long)it.b * v.R + (tok - it.t0)) * v.Hkv + h) * kD + 16 * g;
-#pragma unroll
-          for (int c = 0; c < 16; ++c) vv[u][c] = tok < T ? load_src(v.v_win, wi + c, v.src_bf16) : 0.f;
-        }
-#pragma unroll
-        for (int m = 0; m < 8; ++m) {
-          const uint32_t a0 = pack_f16x2(vv[0][2 * m], vv[1][2 * m]);
-          const uint32_t a1 = pack_f16x2(vv[0][2 * m + 1], vv[1][2 * m + 1]);
-          const uint32_t a2 = pack_f16x2(vv[2][2 * m], vv[3][2 * m]);
-          const uint32_t a3 = pack_f16x2(vv[2][2 * m + 1], vv[3][2 * m + 1]);
-          mma_16816(O[m], a0, a1, a2, a3, b01, b23);
-        }
-      }
+        ++tc;
 
-      ++tc;
-      // ---- release the stage and refill it with tile i + kStages
-      if (!it.window) {
+        // ---- release the stage and refill it with tile i + kStages
         __syncwarp();
         if (lane == 0 && i + kStages < ntiles && !sm.abort) {
           fence_proxy_async();
-          issue(i + kStages);
+          issue(i + kStages, pf);
+          if (i + kStages + 1 < ntiles) pf = bt[(it.t0 + (i + kStages + 1) * kTile) >> lgP];
         }
         __syncwarp();
+      }
+    } else {
+      // ======================= residual window: source-dtype rows from k_win / v_win
+      const int T = it.t1;
+      const long long wrow = ((long long)it.b * v.R) * v.Hkv + h;  // (b, slot 0, h) row index
+      for (int i = 0; i < ntiles; ++i) {
+        const int tok0 = it.t0 + i * kTile;
+        rope_table(sm, tc & 1, i, tok0, tp, td, Td, R16, Bp);
+        named_bar_sync(1, kThreads);
+        const float4* trow0 = reinterpret_cast<const float4*>(&sm.trig[tc & 1][sg][0]);
+        const float4* trow1 = reinterpret_cast<const float4*>(&sm.trig[tc & 1][sg + 8][0]);
+        const int tkey = ((t << 1) | (sg & 1)) & 7;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f}, accn[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int s = 0; s < 8; ++s) {
+          uint32_t ahi[2][2], anl[2][2];
+#pragma unroll
+          for (int r = 0; r < 2; ++r) {
+            const int tok = tok0 + sg + 8 * r;
+            float k[4] = {0.f, 0.f, 0.f, 0.f};
+            if (tok < T) {
+              const long long wi = (wrow + (long long)(tok - it.t0) * v.Hkv) * kD + 32 * t + 4 * s;
+#pragma unroll
+              for (int j = 0; j < 4; ++j) k[j] = load_src(v.k_win, wi + j, v.src_bf16);
+            }
+            const float4 cs = (r ? trow1 : trow0)[(8 * t + s) ^ tkey];
+            rotate_split(k[0], k[1], k[2], k[3], cs, ahi[r][0], anl[r][0], ahi[r][1], anl[r][1]);
+          }
+          mma_16816(acc, ahi[0][0], ahi[1][0], ahi[0][1], ahi[1][1], bq[s][0], bq[s][1]);
+          mma_16816(accn, anl[0][0], anl[1][0], anl[0][1], anl[1][1], bq[s][0], bq[s][1]);
+        }
+        float lg0 = acc[0] + acc[1] - accn[0] - accn[1];
+        float lg1 = acc[2] + acc[3] - accn[2] - accn[3];
+        if (tok0 + sg >= T) lg0 = -INFINITY;
+        if (tok0 + sg + 8 >= T) lg1 = -INFINITY;
+        uint32_t b01, b23;
+        softmax_step(A, lg0, lg1, make_float2(1.f, 0.f), make_float2(1.f, 0.f), g, t, b01, b23);
+        // values as f16 pairs (k-slots 2t+u, 2t+1+u) per channel 16g + 2m (+1)
+        long long vi[4];
+        bool vok[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int tok = tok0 + sig(2 * t + (u & 1)) + 8 * (u >> 1);
+          vok[u] = tok < T;
+          vi[u] = (wrow + (long long)(tok - it.t0) * v.Hkv) * kD + 16 * g;
+        }
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+          float x[4][2];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            x[u][0] = vok[u] ? load_src(v.v_win, vi[u] + 2 * m, v.src_bf16) : 0.f;
+            x[u][1] = vok[u] ? load_src(v.v_win, vi[u] + 2 * m + 1, v.src_bf16) : 0.f;
+          }
+          mma_16816(A.O[m], pack_f16x2(x[0][0], x[1][0]), pack_f16x2(x[0][1], x[1][1]),
+                    pack_f16x2(x[2][0], x[3][0]), pack_f16x2(x[2][1], x[3][1]), b01, b23);
+        }
+        ++tc;
       }
     }
 
     // ---- epilogue: this warp's partial for query heads 4h .. 4h+3
 #pragma unroll
     for (int o = 4; o < 32; o <<= 1) {
-      l_loc += __shfl_xor_sync(0xffffffffu, l_loc, o);
-      mb += __shfl_xor_sync(0xffffffffu, mb, o);
+      A.l_loc += __shfl_xor_sync(0xffffffffu, A.l_loc, o);
+      A.mb += __shfl_xor_sync(0xffffffffu, A.mb, o);
     }
     const int hq = h * kNRep + t;
-    float* dst = part + ((long long)item * v.Hq + hq) * (kD + 2);
+    float* dst = part + ((long long)item * v.Hq + hq) * (kD + 4);
     if (g == 0) {
-      dst[0] = m_run;
-      dst[1] = l_loc;
+      dst[0] = A.m_run;
+      dst[1] = A.l_loc;
     }
 #pragma unroll
     for (int m = 0; m < 8; ++m) {
-      dst[2 + 16 * g + 2 * m] = (O[m][0] + O[m][1]) + mb;
-      dst[2 + 16 * g + 2 * m + 1] = (O[m][2] + O[m][3]) + mb;
+      const float2 o2 = make_float2((A.O[m][0] + A.O[m][1]) + A.mb, (A.O[m][2] + A.O[m][3]) + A.mb);
+      reinterpret_cast<float2*>(dst + 4 + 16 * g)[m] = o2;  // channels 16g + 2m, 16g + 2m + 1
     }
+    item = s_next[npar];
+    npar ^= 1;
   }
 
   // drain: wait (bounded) for loads that were issued but never consumed
   if (lane == 0) {
-    while (cons_seq < load_seq) {
-      const int stage = cons_seq % kStages;
-      const uint32_t parity = (cons_seq / kStages) & 1;
-      ++cons_seq;
-      mbar_wait_bounded(&sm.bar[warp][stage], parity, kSpin);
+    while (n_consumed < n_loaded) {
+      mbar_wait_bounded(&sm.bar[warp][cstage], cphase, kSpin);
+      if (++cstage == kStages) {
+        cstage = 0;
+        cphase ^= 1u;
+      }
+      ++n_consumed;
     }
   }
 }
 
-__global__ void combine_fast_kernel(KvqView v, float* ws, float* out) {
+// Merge the chunk partials of one (sequence, query head).  Records are
+// kRec = D + 4 floats (max, sum, 2 pad, output) so outputs are 16-byte aligned.
+// Weights 2^(m_i - M) are computed once into shared memory; then 8 chunk lanes x
+// 32 channel quads read the outputs with float4 loads and reduce through smem.
+constexpr int kRec = kD + 4;
+constexpr int kCombineThreads = 256;
+constexpr int kCombineCache = 2048;
+
+__global__ void __launch_bounds__(kCombineThreads) combine_fast_kernel(KvqView v, float* ws, float* out) {
+  __shared__ float wts[kCombineCache];
+  __shared__ float red[kCombineThreads / 32];
+  __shared__ float4 acc_s[8][kD / 4];
   const int hq = blockIdx.x, b = blockIdx.y;
-  const int D = v.D;
-  const int* pref = plan_prefix(ws);
-  const float* part = plan_partials(ws, v.batch);
-  const int i0 = pref[b], i1 = pref[b + 1];
+  const int* hdr = reinterpret_cast<const int*>(ws);
+  const int NA = hdr[1];
+  const int* pA = hdr + 4;
+  const int* pB = pA + v.batch + 1;
+  const float* part = reinterpret_cast<const float*>(reinterpret_cast<const char*>(ws) + fast_header_bytes(v.batch));
+  // this sequence's items: nA full chunks at pA[b].., then nB short items at NA + pB[b]..
+  const int nA = pA[b + 1] - pA[b], nB = pB[b + 1] - pB[b];
+  const int n = nA + nB;
+  const long long stride = (long long)v.Hq * kRec;
+  const float* baseA = part + ((long long)pA[b] * v.Hq + hq) * kRec;
+  const float* baseB = part + ((long long)(NA + pB[b]) * v.Hq + hq) * kRec;
+#define KVQ_REC(i) ((i) < nA ? baseA + (long long)(i) * stride : baseB + (long long)((i) - nA) * stride)
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   float M = -INFINITY;
-  for (int i = i0; i < i1; ++i) M = fmaxf(M, part[((long long)i * v.Hq + hq) * (D + 2)]);
+  for (int i = threadIdx.x; i < n; i += kCombineThreads) M = fmaxf(M, KVQ_REC(i)[0]);
+  for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  if (lane == 0) red[warp] = M;
+  __syncthreads();
+  M = red[0];
+  for (int w = 1; w < kCombineThreads / 32; ++w) M = fmaxf(M, red[w]);
+  __syncthreads();
   float L = 0.f;
-  for (int i = i0; i < i1; ++i) {
-    const float* p = part + ((long long)i * v.Hq + hq) * (D + 2);
-    L += p[0] == -INFINITY ? 0.f : p[1] * exp2f(p[0] - M);
+  for (int i = threadIdx.x; i < n; i += kCombineThreads) {
+    const float* r = KVQ_REC(i);
+    const float w = r[0] == -INFINITY ? 0.f : exp2f(r[0] - M);
+    if (i < kCombineCache) wts[i] = w;
+    L += r[1] * w;
   }
+  for (int o = 16; o; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+  if (lane == 0) red[warp] = L;
+  __syncthreads();
+  L = 0.f;
+  for (int w = 0; w < kCombineThreads / 32; ++w) L += red[w];
   const float invL = L > 0.f ? 1.f / L : 0.f;
-  for (int c = threadIdx.x; c < D; c += blockDim.x) {
-    float O = 0.f;
-    for (int i = i0; i < i1; ++i) {
-      const float* p = part + ((long long)i * v.Hq + hq) * (D + 2);
-      if (p[0] != -INFINITY) O += p[2 + c] * exp2f(p[0] - M);
+  // chunk lane j = warp (0..7), channel quad = lane (channels 4 lane .. 4 lane + 3)
+  float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int i = warp; i < n; i += 8) {
+    const float* r = KVQ_REC(i);
+    float w;
+    if (i < kCombineCache) {
+      w = wts[i];
+    } else {
+      w = r[0] == -INFINITY ? 0.f : exp2f(r[0] - M);
     }
-    out[((long long)b * v.Hq + hq) * D + c] = O * invL;
+    const float4 x = reinterpret_cast<const float4*>(r + 4)[lane];
+    o.x += x.x * w;
+    o.y += x.y * w;
+    o.z += x.z * w;
+    o.w += x.w * w;
+  }
+  acc_s[warp][lane] = o;
+  __syncthreads();
+  if (threadIdx.x < kD / 4) {
+    float4 r = acc_s[0][threadIdx.x];
+#pragma unroll
+    for (int j = 1; j < 8; ++j) {
+      const float4 x = acc_s[j][threadIdx.x];
+      r.x += x.x; r.y += x.y; r.z += x.z; r.w += x.w;
+    }
+    r.x *= invL; r.y *= invL; r.z *= invL; r.w *= invL;
+    reinterpret_cast<float4*>(out + ((long long)b * v.Hq + hq) * kD)[threadIdx.x] = r;
   }
 }
+#undef KVQ_REC
 
 }  // namespace
 
 bool fast_eligible(const KvqView& v) {
+  const bool pow2_g = v.kgroup > 0 && (v.kgroup & (v.kgroup - 1)) == 0;
+  const bool pow2_p = (v.P & (v.P - 1)) == 0;
   return v.D == kD && v.Hkv == kWarps && v.n_rep == kNRep && v.kfmt == KVQ_INT8 &&
          v.kmode == KVQ_SYM_ABSMAX && v.kaxis == KVQ_PER_CHANNEL && v.rope_pre == 1 &&
          v.vfmt == KVQ_INT4 && v.vmode == KVQ_ASYM_MINMAX && v.vaxis == KVQ_PER_TOKEN &&
-         v.vgroup == kD && v.kgroup % kTile == 0 && v.kgroup >= kTile * kStages && v.P % kTile == 0 &&
+         v.vgroup == kD && pow2_g && pow2_p && v.kgroup >= kTile * kStages && v.P >= kTile &&
          v.batch <= 4096;
 }
 
 size_t fast_workspace_bytes(const KvqView& v, int batch) {
   const long long items = kFastTarget + 2LL * batch;
-  return plan_header_bytes(batch) + (size_t)items * v.Hq * (v.D + 2) * sizeof(float);
+  return fast_header_bytes(batch) + (size_t)items * v.Hq * (v.D + 4) * sizeof(float);
 }
 
 kvq_status launch_fast(const KvqView& v, const void* q, float* out, float scale, void* ws,
                        cudaStream_t st) {
-  const size_t smem = sizeof(SmemRI) + sizeof(int) * (v.batch + 1);
+  const size_t smem = sizeof(SmemRI) + sizeof(int) * 2 * (v.batch + 1);
   static int occ_cache[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64) return KVQ_ERR_UNSUPPORTED;
   if (!occ_cache[dev]) {
     if (cudaFuncSetAttribute(split_rope_i8i4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)(sizeof(SmemRI) + sizeof(int) * 4097)) != cudaSuccess)
+                             (int)(sizeof(SmemRI) + sizeof(int) * 2 * 4097)) != cudaSuccess)
       return KVQ_ERR_CUDA;
     int occ = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, split_rope_i8i4_kernel, kThreads, smem) !=
@@ -508,8 +718,11 @@ kvq_status launch_fast(const KvqView& v, const void* q, float* out, float scale,
     occ_cache[dev] = occ > 0 ? occ : 1;
   }
   const int grid = num_sms() * occ_cache[dev];
+  // the dynamic item counter starts at zero on every call
+  if (cudaMemsetAsync(static_cast<char*>(ws) + fast_counter_offset(v.batch), 0, 8, st) != cudaSuccess)
+    return KVQ_ERR_CUDA;
   split_rope_i8i4_kernel<<<grid, kThreads, smem, st>>>(v, q, scale, static_cast<float*>(ws));
-  combine_fast_kernel<<<dim3(v.Hq, v.batch), 128, 0, st>>>(v, static_cast<float*>(ws), out);
+  combine_fast_kernel<<<dim3(v.Hq, v.batch), kCombineThreads, 0, st>>>(v, static_cast<float*>(ws), out);
   return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }
 

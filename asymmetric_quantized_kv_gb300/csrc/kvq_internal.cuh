@@ -152,6 +152,28 @@ __device__ __forceinline__ int asym_code(float x, float mn, float s, int bits) {
   return static_cast<int>(fminf(fmaxf(r, 0.f), static_cast<float>(asym_qmax(bits))));
 }
 
+// rint(fl32(x / s)) without a division per element: r = 1/s rounded to nearest,
+// so fl32(x * r) lies within 2^-23 (relative) of x / s, as does fl32(x / s).  The
+// two round to the same integer unless the product is near a half-integer; those
+// rare cases (and non-finite r) take the exact IEEE division.
+__device__ __forceinline__ float rint_quot(float x, float s, float r) {
+  const float q = __fmul_rn(x, r);
+  const float f = q - floorf(q);
+  if (!(fabsf(f - 0.5f) > 1.52587890625e-05f * fmaxf(1.f, fabsf(q)))) return rintf(__fdiv_rn(x, s));
+  return rintf(q);
+}
+
+__device__ __forceinline__ int sym_code_r(float x, float s, float r, int bits) {
+  if (s == 0.f) return 0;
+  const float q = static_cast<float>(sym_qmax(bits));
+  return static_cast<int>(fminf(fmaxf(rint_quot(x, s, r), -q), q));
+}
+
+__device__ __forceinline__ int asym_code_r(float x, float mn, float s, float r, int bits) {
+  const float c = rint_quot(__fsub_rn(x, mn), s, r);
+  return static_cast<int>(fminf(fmaxf(c, 0.f), static_cast<float>(asym_qmax(bits))));
+}
+
 __device__ __forceinline__ unsigned fp8_code(float x, float s) {
   if (s == 0.f) return 0u;
   return float_to_fp8_e4m3(__fdiv_rn(x, s));

@@ -51,8 +51,11 @@ LAUNCHES_APPEND = 2
 LAUNCHES_ATTENTION = 2
 
 
-def workload_spec(cid: int) -> dict:
+def workload_spec(cid: int, batch: int = 0) -> dict:
     w = W.WORKLOADS[cid]
+    if batch:  # the first `batch` sequences of the workload (smaller captures for ncu)
+        import dataclasses
+        w = dataclasses.replace(w, batch=min(batch, w.batch))
     if cid == 5:
         return dict(w=w, k=(INT8, SYM, CH, 64), v=(INT4, ASYM, TOK, 128), R=64, P=16, rope=1, theta=500000.0,
                     append=True, name="paged ragged 1K-64K (sum T ~1.0M), Hq32/Hkv8/D128, INT8 per-channel "
@@ -265,7 +268,7 @@ def build_cache(spec, device, extra_tokens, gen_seed=1):
     import asymmetric_quantized_kv_gb300 as K
     w = spec["w"]
     Bn, H, D, Hq = w.batch, w.num_kv_heads, w.head_dim, w.num_q_heads
-    lens = [int(x) for x in W.lengths(w)]
+    lens = [int(x) for x in W.lengths(W.WORKLOADS[w.cid])][:w.batch]
     P = spec["P"]
     cfg = K.make_config(Hq, H, D, spec["k"], spec["v"], spec["R"], P, spec["rope"], spec["theta"], BF16)
     need = [(T + extra_tokens + P - 1) // P for T in lens]
@@ -450,11 +453,12 @@ def main():
     ap.add_argument("--no-e2e", dest="e2e", action="store_false")
     ap.add_argument("--cpu-streams", type=int, default=16)
     ap.add_argument("--cpu-steps", type=int, default=8)
+    ap.add_argument("--batch", type=int, default=0, help="use only the first N sequences (profiling)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
-    spec = workload_spec(args.config)
+    spec = workload_spec(args.config, args.batch)
     w = spec["w"]
 
     if args.impl == "reference":

@@ -32,15 +32,18 @@ class Case:
     the oracle states."""
 
     def __init__(self, cfg: O.Config, lens, seed=0, outliers=(3, 17), factor=30.0, chunking="random",
-                 permute_pages=True, extra_pages=1):
+                 permute_pages=True, extra_pages=1, streams=None):
         import asymmetric_quantized_kv_gb300 as K
         self.cfg, self.lens, self.seed = cfg, list(lens), seed
         Bn, H, D, P = len(lens), cfg.num_kv_heads, cfg.head_dim, cfg.page_size
         bf = cfg.src_dtype == O.BF16
-        self.K = [[W.small_stream(seed * 1000 + b * 10 + h, int(lens[b]), D, outliers, factor, bf)
-                   for h in range(H)] for b in range(Bn)]
-        self.V = [[W.small_stream(seed * 1000 + 500 + b * 10 + h, int(lens[b]), D, (), 1.0, bf)
-                   for h in range(H)] for b in range(Bn)]
+        if streams is not None:  # caller-provided K[b][h], V[b][h] ([T_b, D], exact in the source dtype)
+            self.K, self.V = streams
+        else:
+            self.K = [[W.small_stream(seed * 1000 + b * 10 + h, int(lens[b]), D, outliers, factor, bf)
+                       for h in range(H)] for b in range(Bn)]
+            self.V = [[W.small_stream(seed * 1000 + 500 + b * 10 + h, int(lens[b]), D, (), 1.0, bf)
+                       for h in range(H)] for b in range(Bn)]
         # static per-head scales over all sequences (oracle) and through the library
         qk = 448.0 if cfg.k.fmt == O.FP8_E4M3 else float(O.sym_qmax(O.bits_of(cfg.k.fmt)))
         qv = 448.0 if cfg.v.fmt == O.FP8_E4M3 else float(O.sym_qmax(O.bits_of(cfg.v.fmt)))
