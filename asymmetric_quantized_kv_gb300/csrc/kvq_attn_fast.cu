@@ -10,17 +10,26 @@
 // (cp.async.bulk, completion on an mbarrier, every wait bounded).
 //
 // Per 16-token tile and warp:
-//   QK: K codes -> fp32 (x per-channel scale, packed f32x2) -> RoPE rotation by
-//       the token's absolute position (cos/sin from a per-tile table shared by
-//       the 8 warps) -> split into f16 hi + lo -> two mma.m16n8k16 per 16
-//       channels with A = keys (16 tokens x 16 channels) and B = q (16 channels
-//       x 8 columns: 4 query heads x {hi, lo} halves of q*scale*log2(e)).  The
-//       hi/lo split of both operands keeps the logits to ~2^-21 relative.
-//   softmax: online in base 2, one running max per head with lazy rescaling
-//       (only when the max grows by more than 2^8).
-//   PV: A = V^T codes (16 channels x 16 tokens) formed with PRMT/LOP3 and one
-//       f16x2 fix-up as exact f16 integers, B = p * v_scale split hi/lo; the
-//       per-token minimum enters through a running sum of p * v_min.
+//   QK: K codes -> fp32 (PRMT into the mantissa of 2^23, minus 2^23 + 128)
+//       -> x per-channel scale -> RoPE rotation by the token's
+//       absolute position -> split into f16 hi + (hi - x) -> two mma.m16n8k16
+//       per 16 channels with A = keys (16 tokens x 16 channels) and B = q (16
+//       channels x 8 columns: 4 query heads x {hi, lo} halves of
+//       q*scale*log2(e)).  The hi/lo split of both operands keeps the logits to
+//       ~2^-21 relative.  Scaling and rotation run as packed f32x2 arithmetic on
+//       the even channels (x0, x2) and odd channels (x1, x3) of two RoPE pairs.
+//   RoPE table: cos/sin of every (token, pair) of two tiles, built once per CTA
+//       into one of two shared buffers and handed between the 8 warps through
+//       full/empty mbarriers, so warps may drift by up to two tiles instead of
+//       meeting at a CTA barrier every tile.
+//   softmax: online in base 2, one running max per head, raised lazily (only
+//       when a logit exceeds it by more than 2^8; the common tile needs no
+//       cross-lane reduction).
+//   PV: A = V^T codes (16 channels x 16 tokens) as f16 subnormals c * 2^-24
+//       (high nibbles as 16c * 2^-24; two PRMT and four LOP per MMA), exact in
+//       the tensor cores; the power-of-two factors come out in the epilogue.
+//       B = p * v_scale split hi/lo; the per-token minimum enters through a
+//       running sum of p * v_min.
 // Residual-window items use the same steps on the source-dtype rows.
 // Partials (max, sum, unnormalised output) per (item, query head) go to the
 // workspace; the combine kernel merges them.
@@ -37,40 +46,52 @@ using namespace ptx;
 constexpr int kTile = 16;
 constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
-constexpr int kStages = 3;
+constexpr int kStages = 2;
 constexpr uint32_t kSpin = 1u << 20;  // polls per bounded mbarrier wait
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescale = 8.f;  // lazy rescale threshold in log2 units
+constexpr float kMinit = -1e30f;  // running max before the first logit (finite: no inf - inf)
+constexpr int kSuper = 2;    // tiles per RoPE table (one handoff between the warps per table)
+constexpr int kReseed = 16;  // RoPE table entries are recomputed exactly every kReseed tables
 constexpr int kFastTarget = 1536;
 constexpr int kFastMinChunk = 256;
 constexpr int kD = 128;
 constexpr int kNRep = 4;
 
-// Bytes per 16-token tile of one head: K codes, V codes, V meta (scale, min).
+// Bytes per 16-token tile of one head: K codes, V codes, V meta (scale, min);
+// a tile that starts a key group also carries the group's 128 key scales.
 constexpr int kKC = kTile * kD;          // 2048
 constexpr int kVC = kTile * kD / 2;      // 1024
 constexpr int kVM = kTile * 8;           // 128
 constexpr int kStageBytes = kKC + kVC + kVM;
 constexpr int kKMeta = kD * 4;           // per-channel scales of one key group
+constexpr int kStageAlloc = kStageBytes + kKMeta;
 
 // Shared-memory layouts are chosen so that every 64/128-bit load of a warp
 // meets no bank conflict within the quarter- or half-warp that the hardware
 // serves in one wavefront:
-//   trig: (cos, sin) per (token row, RoPE pair); 16-byte units (two pairs) of a
-//         row are XOR-swizzled by (2 * (unit / 8) + row % 2) % 8;
-//   kmeta: the 128 key scales of a group as 4 rows of 32, each row padded to
-//         36 floats (144 bytes), one row per lane quarter t;
+//   trig: per (token row, unit of two RoPE pairs A = 2u, B = 2u + 1) the float4
+//         (cos A, cos B, sin A, sin B); units are XOR-swizzled by
+//         (2 * (u / 8) + row % 2) % 8;
+//   kmeta: the 128 key scales of the current group as 4 rows of 32, each row
+//         padded to 36 floats, one row per lane quarter t; each quad of
+//         channels c..c+3 is stored as (s_c, s_c+2, s_c+1, s_c+3) so that the
+//         even and odd channels of two pairs are adjacent register pairs;
 //   tokens: MMA row r holds tile token sig(r) = r ^ ((r >> 1) & 1), which
 //         spreads the value rows a half-warp reads over two bank offsets.
 struct __align__(128) SmemRI {
-  uint8_t stage[kWarps][kStages][kStageBytes];
-  float kmeta[kWarps][2][4][36];
-  float2 trig[2][kTile][64];
+  uint8_t stage[kWarps][kStages][kStageAlloc];
+  float4 trig[2][kSuper * kTile][32];
+  uint2 bq[kWarps][8][32];  // q B fragments of the current item, per warp, step and lane
+  float4 rstep[32];         // (cos A, cos B, sin A, sin B) of kSuper * 16 theta per unit
+  float kmeta[kWarps][4][36];
   uint64_t bar[kWarps][kStages];
+  uint64_t tfull[2], tempty[2];
   int valid[kWarps][kStages];
   float w_hi[kD / 2], w_lo[kD / 2];
-  int abort;
 };
+static_assert(kStageAlloc % 16 == 0, "bulk-copy destinations must stay 16-byte aligned");
+static_assert(sizeof(SmemRI::stage) >= 2 * kThreads * sizeof(int), "plan scratch lives in the stage ring");
 
 struct FastItem {
   int b, t0, t1, window;
@@ -87,9 +108,12 @@ __host__ __device__ inline size_t fast_header_ints(int B) { return (size_t)2 * (
 __host__ __device__ inline size_t fast_counter_offset(int B) { return (fast_header_ints(B) * 4 + 7) & ~(size_t)7; }
 __host__ __device__ inline size_t fast_header_bytes(int B) { return (fast_counter_offset(B) + 8 + 255) / 256 * 256; }
 
-__device__ inline void fast_plan(const KvqView& v, int align, int* sA, int* sB, int* s_C, int* s_NA, int* s_NB) {
+// scratch: 2 * kThreads ints of shared memory that are free until the main loop
+__device__ inline void fast_plan(const KvqView& v, int align, int* sA, int* sB, int* s_C, int* s_NA, int* s_NB,
+                                 int* scratch) {
   __shared__ unsigned long long s_total;
-  __shared__ int s_pa[kThreads], s_pb[kThreads];
+  int* s_pa = scratch;
+  int* s_pb = scratch + kThreads;
   const int B = v.batch;
   if (threadIdx.x == 0) s_total = 0ull;
   __syncthreads();
@@ -189,9 +213,6 @@ __device__ inline FastItem decode_fast_item(const KvqView& v, const int* sA, con
   return it;
 }
 
-__device__ __forceinline__ float2 cmul(float2 a, float2 b) {
-  return make_float2(a.x * b.x - a.y * b.y, a.x * b.y + a.y * b.x);
-}
 
 __device__ __forceinline__ float2 rope_cs(int p, float w_hi, float w_lo) {
   float s, c;
@@ -199,20 +220,35 @@ __device__ __forceinline__ float2 rope_cs(int p, float w_hi, float w_lo) {
   return make_float2(c, s);
 }
 
-// (lo, hi) halves of an f16x2 minus c, in fp32 (exact for the magic-number codes)
-__device__ __forceinline__ float2 h2_minus(uint32_t h2, float c) {
-  unsigned short h0, h1;
-  asm("mov.b32 {%0, %1}, %2;" : "=h"(h0), "=h"(h1) : "r"(h2));
-  float2 r;
-  asm("sub.rn.f32.f16 %0, %1, %2;" : "=f"(r.x) : "h"(h0), "f"(c));
-  asm("sub.rn.f32.f16 %0, %1, %2;" : "=f"(r.y) : "h"(h1), "f"(c));
-  return r;
+// byte j of w placed in the low mantissa bits of 2^23: the float 2^23 + byte
+__device__ __forceinline__ float magic_f32(uint32_t w, int j) {
+  return __uint_as_float(prmt(w, 0x4B000000u, 0x7540u | j));
 }
+// (2^23 + 128, 2^23 + 128): 2^23 + u minus this is the signed code u - 128
+__device__ __forceinline__ float2 magic_bias() { return make_float2(8388736.f, 8388736.f); }
 
 __device__ __forceinline__ int sig(int x) { return x ^ ((x >> 1) & 1); }
 
+// Bounded wait on an mbarrier phase by every lane; a timeout raises the status
+// flag and this thread's `stalled` flag, after which it attempts no further wait
+// (the kernel then runs to completion on whatever the buffers hold).
+__device__ __forceinline__ void bounded_wait(uint64_t* bar, uint32_t parity, bool& stalled, int* status) {
+  if (stalled) return;
+  if (!mbar_wait_bounded(bar, parity, kSpin)) {
+    atomicOr(status, KVQ_DEV_TIMEOUT);
+    stalled = true;
+  }
+}
+
+// One arrival per warp, after every lane's shared-memory accesses are ordered
+// before it by the warp barrier.
+__device__ __forceinline__ void warp_arrive(uint64_t* bar) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+}
+
 // Per-warp attention state of one item: PV accumulators (16-channel MMA tiles m,
-// rows g / g+8 = channels 16g + 2m / 16g + 2m + 1, columns head t hi / lo),
+// rows g / g+8 = channels 16g + 2m / 16g + 2m + 1, columns head t hi / (hi - x)),
 // running max (log2 units), this lane's share of the softmax sum and of the
 // p * v_min sum.
 struct Acc {
@@ -220,45 +256,64 @@ struct Acc {
   float m_run, l_loc, mb;
 };
 
-// The RoPE table of one tile: entry (token d, pair p) = e^{i (tok0 + d) theta_p},
-// from the per-tile base Bp = e^{i tok0 theta_p} (re-seeded exactly every 16 tiles,
-// otherwise advanced by R16 = e^{i 16 theta_p}) times Td[j] = e^{i d theta_p}.
-__device__ __forceinline__ void rope_table(SmemRI& sm, uint32_t buf, int i, int tok0, int tp, int td,
-                                           const float2 (&Td)[4], float2 R16, float2& Bp) {
-  if ((i & 15) == 0) Bp = rope_cs(tok0, sm.w_hi[tp], sm.w_lo[tp]);
-  else Bp = cmul(Bp, R16);
-  const int u = tp >> 1;
+// RoPE table producer: thread (unit u = tid % 32, rows d0 + 8j, j < 2 * kSuper)
+// owns 2 * kSuper float4 entries per table, e^{i (tok0 + d) theta} for pairs 2u,
+// 2u + 1.  Entries are advanced table to table by e^{i 32 theta} (read back from
+// the thread's own slots of the previous table's buffer) and recomputed exactly
+// at an item's first table and every kReseed tables.
+
+__device__ __forceinline__ float4 trig_entry(const SmemRI& sm, int pos, int u) {
+  const float2 a = rope_cs(pos, sm.w_hi[2 * u], sm.w_lo[2 * u]);
+  const float2 b = rope_cs(pos, sm.w_hi[2 * u + 1], sm.w_lo[2 * u + 1]);
+  return make_float4(a.x, b.x, a.y, b.y);
+}
+
+__device__ __forceinline__ void trig_produce(SmemRI& sm, uint32_t buf, int ip, int tok0) {
+  const int u = threadIdx.x & 31, d0 = threadIdx.x >> 5;
+  const float4 r = sm.rstep[u];
+  const float2 rc = make_float2(r.x, r.y), rs = make_float2(r.z, r.w);
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const int d = td + 4 * j;
-    const int key = (((u >> 3) << 1) | (d & 1)) & 7;
-    sm.trig[buf][d][((u ^ key) << 1) | (tp & 1)] = cmul(Bp, Td[j]);
+  for (int j = 0; j < 2 * kSuper; ++j) {
+    const int d = d0 + 8 * j;
+    const int slot = u ^ ((((u >> 3) << 1) | (d & 1)) & 7);
+    float4 e;
+    if (ip % kReseed == 0) {
+      e = trig_entry(sm, tok0 + d, u);
+    } else {
+      const float4 p = sm.trig[buf ^ 1][d][slot];
+      const float2 c = make_float2(p.x, p.y), s = make_float2(p.z, p.w);
+      const float2 c2 = sub2(mul2(c, rc), mul2(s, rs));
+      const float2 s2 = fma2(c, rs, mul2(s, rc));
+      e = make_float4(c2.x, c2.y, s2.x, s2.y);
+    }
+    sm.trig[buf][d][slot] = e;
   }
 }
 
-// Rotate (k0, k1), (k2, k3) by the table's (cos, sin) of two pairs and split
-// each rotated pair into f16x2 hi and (hi - x).
-__device__ __forceinline__ void rotate_split(float k0, float k1, float k2, float k3, float4 cs, uint32_t& hi01,
-                                             uint32_t& nl01, uint32_t& hi23, uint32_t& nl23) {
-  const float r0 = k0 * cs.x - k1 * cs.y, r1 = k0 * cs.y + k1 * cs.x;
-  const float r2 = k2 * cs.z - k3 * cs.w, r3 = k2 * cs.w + k3 * cs.z;
-  split_hi_neglo(r0, r1, hi01, nl01);
-  split_hi_neglo(r2, r3, hi23, nl23);
+// Rotate two RoPE pairs held as even channels X = (x0, x2) and odd channels
+// Y = (x1, x3) by the table's float4 (cos A, cos B, sin A, sin B), then split
+// each rotated half into f16x2 hi and (hi - x): *0 = channels (0, 2), *1 = (1, 3).
+__device__ __forceinline__ void rot_split(float2 X, float2 Y, float4 cs, uint32_t& hi0, uint32_t& nl0,
+                                          uint32_t& hi1, uint32_t& nl1) {
+  const float2 C = make_float2(cs.x, cs.y), S = make_float2(cs.z, cs.w);
+  const float2 RA = sub2(mul2(X, C), mul2(Y, S));
+  const float2 RB = fma2(X, S, mul2(Y, C));
+  split_hi_neglo(RA.x, RA.y, hi0, nl0);
+  split_hi_neglo(RB.x, RB.y, hi1, nl1);
 }
 
 // Online-softmax step for the two logits of this lane (tokens of MMA rows g and
 // g+8, head t), then the PV B operand: P' = p * pscale for k-slots 2t, 2t+1 and
-// 2t+8, 2t+9 of column g (head g/2, hi half for even g, lo half for odd g).
+// 2t+8, 2t+9 of column g (head g/2, hi half for even g, (hi - x) for odd g).
 __device__ __forceinline__ void softmax_step(Acc& A, float lg0, float lg1, float2 m0, float2 m1, int g, int t,
                                              uint32_t& b01, uint32_t& b23) {
-  float mx = fmaxf(lg0, lg1);
-  mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-  mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-  mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-  const bool need = mx > A.m_run + kRescale;
-  if (__any_sync(0xffffffffu, need)) {
-    const float mn = need ? mx : A.m_run;
-    const float alpha = (A.m_run == -INFINITY) ? 0.f : ex2(A.m_run - mn);
+  if (__any_sync(0xffffffffu, fmaxf(lg0, lg1) > A.m_run + kRescale)) {
+    float mx = fmaxf(lg0, lg1);
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+    const float mn = fmaxf(A.m_run, mx);
+    const float alpha = ex2(A.m_run - mn);
 #pragma unroll
     for (int m = 0; m < 8; ++m) {
       A.O[m][0] *= alpha; A.O[m][1] *= alpha; A.O[m][2] *= alpha; A.O[m][3] *= alpha;
@@ -267,24 +322,20 @@ __device__ __forceinline__ void softmax_step(Acc& A, float lg0, float lg1, float
     A.mb *= alpha;
     A.m_run = mn;
   }
-  float p0 = 0.f, p1 = 0.f;
-  if (A.m_run != -INFINITY) {
-    p0 = ex2(lg0 - A.m_run);
-    p1 = ex2(lg1 - A.m_run);
-  }
+  const float p0 = ex2(lg0 - A.m_run), p1 = ex2(lg1 - A.m_run);
   A.l_loc += p0 + p1;
-  A.mb += p0 * m0.y + p1 * m1.y;
+  A.mb = fmaf(p1, m1.y, fmaf(p0, m0.y, A.mb));
   const float pv0 = p0 * m0.x, pv1 = p1 * m1.x;
   const int src0 = 4 * (2 * t) + (g >> 1), src1 = src0 + 4;
   const float x0 = __shfl_sync(0xffffffffu, pv0, src0);
   const float y0 = __shfl_sync(0xffffffffu, pv1, src0);
   const float x1 = __shfl_sync(0xffffffffu, pv0, src1);
   const float y1 = __shfl_sync(0xffffffffu, pv1, src1);
-  uint32_t hA, lA, hB, lB;
-  split_hi_lo(x0, x1, hA, lA);
-  split_hi_lo(y0, y1, hB, lB);
-  b01 = (g & 1) ? lA : hA;
-  b23 = (g & 1) ? lB : hB;
+  uint32_t hA, nA, hB, nB;
+  split_hi_neglo(x0, x1, hA, nA);
+  split_hi_neglo(y0, y1, hB, nB);
+  b01 = (g & 1) ? nA : hA;
+  b23 = (g & 1) ? nB : hB;
 }
 
 __global__ void __launch_bounds__(kThreads, 2)
@@ -298,46 +349,71 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int g = lane >> 2, t = lane & 3;
   const int G = v.kgroup;  // powers of two (checked on the host)
   const int lgG = __ffs(G) - 1, lgP = __ffs(v.P) - 1;
-  fast_plan(v, G, prefA, prefB, &s_C, &s_NA, &s_NB);
+  fast_plan(v, G, prefA, prefB, &s_C, &s_NA, &s_NB, reinterpret_cast<int*>(&sm.stage[0][0][0]));
   if (blockIdx.x == 0) store_fast_plan(v, ws, prefA, prefB, s_C, s_NA, s_NB);
   unsigned long long* counter =
       reinterpret_cast<unsigned long long*>(reinterpret_cast<char*>(ws) + fast_counter_offset(v.batch));
   if (lane == 0) {
     for (int s = 0; s < kStages; ++s) mbar_init(&sm.bar[warp][s], 1);
-    fence_mbar_init();
   }
+  if (threadIdx.x == 0) {
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&sm.tfull[b], kWarps);
+      mbar_init(&sm.tempty[b], kWarps);
+    }
+  }
+  if (lane == 0) fence_mbar_init();
   if (threadIdx.x < kD / 2) rope_split(v, threadIdx.x, &sm.w_hi[threadIdx.x], &sm.w_lo[threadIdx.x]);
-  if (threadIdx.x == 0) sm.abort = 0;
+  __syncthreads();
+  if (threadIdx.x < 32) sm.rstep[threadIdx.x] = trig_entry(sm, kSuper * kTile, threadIdx.x);
   __syncthreads();
 
-  // RoPE table producer role: pair tp, token offsets td + 4j within a tile.
-  const int tp = threadIdx.x & 63, td = threadIdx.x >> 6;
-  float2 Td[4];
-#pragma unroll
-  for (int j = 0; j < 4; ++j) Td[j] = rope_cs(td + 4 * j, sm.w_hi[tp], sm.w_lo[tp]);
-  const float2 R16 = rope_cs(16, sm.w_hi[tp], sm.w_lo[tp]);
-  float2 Bp = make_float2(1.f, 0.f);
 
   const int C = s_C, NA = s_NA, n_items = s_NA + s_NB;
   float* part = reinterpret_cast<float*>(reinterpret_cast<char*>(ws) + fast_header_bytes(v.batch));
   const float qscale = scale * kLog2e;
   const int h = warp;
   const int sg = sig(g);  // tile token of MMA row g (row g + 8: token sg + 8)
+  const int tkey = ((t << 1) | (sg & 1)) & 7;
   const long long head_off = (long long)h * v.head_bytes;
   // this warp's ring: lane 0 loads at lstage, everyone consumes at cstage / cphase
   int lstage = 0, cstage = 0;
   uint32_t cphase = 0, n_loaded = 0, n_consumed = 0;
-  uint32_t tc = 0;  // tiles processed by this CTA: selects the RoPE table buffer
+  bool stalled = false;  // set by a timed-out wait: no further waits
+  uint32_t tc = 0;  // RoPE tables used by this CTA: table tc in buffer tc & 1, its use tc >> 1
+
+  // produce CTA table tcp (item table ip, first token tok0) once the warps are
+  // done with the buffer's previous use
+  auto produce = [&](uint32_t tcp, int ip, int tok0) {
+    const uint32_t b = tcp & 1;
+    if (tcp >= 2) bounded_wait(&sm.tempty[b], ((tcp >> 1) - 1) & 1, stalled, v.status);
+    trig_produce(sm, b, ip, tok0);
+    warp_arrive(&sm.tfull[b]);
+  };
+  // before the K loop of item tile i: wait for its table and point at its rows
+  auto table_rows = [&](int i) {
+    if ((i & (kSuper - 1)) == 0) bounded_wait(&sm.tfull[tc & 1], (tc >> 1) & 1, stalled, v.status);
+    return &sm.trig[tc & 1][kTile * (i & (kSuper - 1)) + sg][0];
+  };
+  // after the K loop of item tile i: release the table after its last tile and
+  // produce the next one
+  auto table_done = [&](int i, int ntiles, int tok0) {
+    if ((i & (kSuper - 1)) == kSuper - 1 || i + 1 == ntiles) {
+      warp_arrive(&sm.tempty[tc & 1]);
+      if (i + 1 < ntiles) produce(tc + 1, (i + 1) / kSuper, tok0 + kTile);
+      ++tc;
+    }
+  };
 
   int item = blockIdx.x, npar = 0;
   while (item < n_items) {
-    // the CTA's next item, fetched now and read after this item's tile barriers
+    // the CTA's next item, fetched now and read after this item's closing barrier
     if (threadIdx.x == 0) s_next[npar] = (int)gridDim.x + (int)atomicAdd(counter, 1ull);
     const FastItem it = decode_fast_item(v, prefA, prefB, C, NA, item);
     const int ntiles = (it.t1 - it.t0 + kTile - 1) / kTile;
 
-    // B operand: q * scale * log2(e) for query head 4h + g/2, split hi (even g) / lo (odd g)
-    uint32_t bq[8][2];
+    // B operand: q * scale * log2(e) for query head 4h + g/2, split hi (even g) / lo (odd g);
+    // k-slots 2t, 2t+1 <- channels c, c+2 and 2t+8, 2t+9 <- c+1, c+3 (c = 32t + 4s)
     {
       const int hq = h * kNRep + (g >> 1);
       const long long qb = ((long long)it.b * v.Hq + hq) * kD + 32 * t;
@@ -346,21 +422,24 @@ __global__ void __launch_bounds__(kThreads, 2)
         float x[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) x[j] = load_src(q, qb + 4 * s + j, v.src_bf16) * qscale;
-        uint32_t h01, l01, h23, l23;
-        split_hi_lo(x[0], x[1], h01, l01);
-        split_hi_lo(x[2], x[3], h23, l23);
-        bq[s][0] = (g & 1) ? l01 : h01;
-        bq[s][1] = (g & 1) ? l23 : h23;
+        uint32_t h02, l02, h13, l13;
+        split_hi_lo(x[0], x[2], h02, l02);
+        split_hi_lo(x[1], x[3], h13, l13);
+        sm.bq[warp][s][lane] = make_uint2((g & 1) ? l02 : h02, (g & 1) ? l13 : h13);
       }
     }
+    __syncwarp();
+    const uint2* bqs = &sm.bq[warp][0][lane];  // step s at bqs[32 * s]
 
     Acc A;
 #pragma unroll
     for (int m = 0; m < 8; ++m) A.O[m][0] = A.O[m][1] = A.O[m][2] = A.O[m][3] = 0.f;
-    A.m_run = -INFINITY;
+    A.m_run = kMinit;
     A.l_loc = 0.f;
     A.mb = 0.f;
 
+    produce(tc, 0, it.t0);
+    const float4* trow0 = &sm.trig[0][sg][0];  // re-pointed per tile
     if (!it.window) {
       // ======================= quantized chunk: tiles through the TMA ring
       const int32_t* bt = v.block_table + (long long)it.b * v.max_pages;
@@ -378,26 +457,27 @@ __global__ void __launch_bounds__(kThreads, 2)
           return;
         }
         const uint8_t* hbk = v.pages + (long long)pid * v.page_bytes + head_off;
-        const int slot = tok & (v.P - 1);
         const bool gstart = (tok & (G - 1)) == 0;
-        mbar_arrive_expect_tx(bar, kStageBytes + (gstart ? kKMeta : 0));
+        const uint32_t bytes = kStageBytes + (gstart ? kKMeta : 0);
+        mbar_arrive_expect_tx(bar, bytes);
         uint8_t* dst = sm.stage[warp][stage];
         if (v.P == kTile) {
-          bulk_g2s(dst, hbk, kStageBytes, bar);
+          // the head's whole page section: codes, value meta, then the key scales
+          bulk_g2s(dst, hbk, bytes, bar);
         } else {
+          const int slot = tok & (v.P - 1);
           bulk_g2s(dst, hbk + slot * kD, kKC, bar);
           bulk_g2s(dst + kKC, hbk + v.off_vc + slot * (kD / 2), kVC, bar);
           bulk_g2s(dst + kKC + kVC, hbk + v.off_vm + slot * 8, kVM, bar);
-        }
-        if (gstart) {
-          const int gslot = v.P >= G ? (slot >> lgG) : 0;
-          const uint8_t* src = hbk + v.off_km + gslot * kKMeta;
-#pragma unroll
-          for (int r = 0; r < 4; ++r) bulk_g2s(sm.kmeta[warp][(tok >> lgG) & 1][r], src + 128 * r, 128, bar);
+          if (gstart) {
+            const int gslot = v.P >= G ? (slot >> lgG) : 0;
+            bulk_g2s(dst + kStageBytes, hbk + v.off_km + gslot * kKMeta, kKMeta, bar);
+          }
         }
       };
       int pf = 0;  // lane 0: page id of the next tile to load, read one tile ahead
-      if (lane == 0 && !sm.abort) {
+      if (lane == 0 && !stalled) {
+        fence_proxy_async();  // the ring's bytes were last written through the generic proxy
         for (int i = 0; i < min(kStages, ntiles); ++i) issue(i, bt[(it.t0 + i * kTile) >> lgP]);
         if (kStages < ntiles) pf = bt[(it.t0 + kStages * kTile) >> lgP];
       }
@@ -405,15 +485,12 @@ __global__ void __launch_bounds__(kThreads, 2)
 
       for (int i = 0; i < ntiles; ++i) {
         const int tok0 = it.t0 + i * kTile;
-        rope_table(sm, tc & 1, i, tok0, tp, td, Td, R16, Bp);
-        named_bar_sync(1, kThreads);
-
         const int stage = cstage;
         bool valid = false;
-        if (!*reinterpret_cast<volatile int*>(&sm.abort)) {
+        if (!stalled) {
           if (!mbar_wait_bounded(&sm.bar[warp][stage], cphase, kSpin)) {
             atomicOr(v.status, KVQ_DEV_TIMEOUT);
-            sm.abort = 1;
+            stalled = true;
           } else {
             valid = sm.valid[warp][stage] != 0;
           }
@@ -424,43 +501,53 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         ++n_consumed;
         const uint8_t* buf = sm.stage[warp][stage];
+        if (valid && (tok0 & (G - 1)) == 0) {
+          // new key group: its scales, quad (c, c+1, c+2, c+3) stored as (c, c+2, c+1, c+3)
+          const float4 raw = reinterpret_cast<const float4*>(buf + kStageBytes)[lane];
+          *reinterpret_cast<float4*>(&sm.kmeta[warp][lane >> 3][4 * (lane & 7)]) =
+              make_float4(raw.x, raw.z, raw.y, raw.w);
+          __syncwarp();
+        }
+        trow0 = table_rows(i);
+        const float4* trow1 = trow0 + 8 * 32;
 
         // ---- QK: MMA rows g / g+8 = tile tokens sg / sg+8, channels 32t .. 32t+31
-        const float4* km = reinterpret_cast<const float4*>(&sm.kmeta[warp][(tok0 >> lgG) & 1][t][0]);
-        const float4* trow0 = reinterpret_cast<const float4*>(&sm.trig[tc & 1][sg][0]);
-        const float4* trow1 = reinterpret_cast<const float4*>(&sm.trig[tc & 1][sg + 8][0]);
-        const int tkey = ((t << 1) | (sg & 1)) & 7;
-        uint32_t kw[2][8];
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          const uint4* src = reinterpret_cast<const uint4*>(buf + (sg + 8 * r) * kD + 32 * t);
-          const uint4 lo = src[0], hi = src[1];
-          kw[r][0] = lo.x ^ 0x80808080u; kw[r][1] = lo.y ^ 0x80808080u;
-          kw[r][2] = lo.z ^ 0x80808080u; kw[r][3] = lo.w ^ 0x80808080u;
-          kw[r][4] = hi.x ^ 0x80808080u; kw[r][5] = hi.y ^ 0x80808080u;
-          kw[r][6] = hi.z ^ 0x80808080u; kw[r][7] = hi.w ^ 0x80808080u;
-        }
+        const float4* km = reinterpret_cast<const float4*>(&sm.kmeta[warp][t][0]);
         float acc[4] = {0.f, 0.f, 0.f, 0.f}, accn[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int s = 0; s < 8; ++s) {
-          uint32_t ahi[2][2], anl[2][2];
-          const float4 ks = km[s];
+        for (int half = 0; half < 2; ++half) {
+          uint32_t kw[2][4];
 #pragma unroll
           for (int r = 0; r < 2; ++r) {
-            const float4 cs = (r ? trow1 : trow0)[(8 * t + s) ^ tkey];
-            const uint32_t w = kw[r][s];
-            // offset-binary bytes -> f16 1024 + u (u = code + 128) -> fp32 code -> code * scale
-            const float2 c01 = h2_minus(prmt(w, 0x64646464u, 0x4140u), 1152.f);
-            const float2 c23 = h2_minus(prmt(w, 0x64646464u, 0x4342u), 1152.f);
-            const float2 k01 = mul2(c01, make_float2(ks.x, ks.y));
-            const float2 k23 = mul2(c23, make_float2(ks.z, ks.w));
-            rotate_split(k01.x, k01.y, k23.x, k23.y, cs, ahi[r][0], anl[r][0], ahi[r][1], anl[r][1]);
+            const uint4 x = reinterpret_cast<const uint4*>(buf + (sg + 8 * r) * kD + 32 * t)[half];
+            kw[r][0] = x.x ^ 0x80808080u; kw[r][1] = x.y ^ 0x80808080u;
+            kw[r][2] = x.z ^ 0x80808080u; kw[r][3] = x.w ^ 0x80808080u;
           }
-          mma_16816(acc, ahi[0][0], ahi[1][0], ahi[0][1], ahi[1][1], bq[s][0], bq[s][1]);
-          mma_16816(accn, anl[0][0], anl[1][0], anl[0][1], anl[1][1], bq[s][0], bq[s][1]);
+#pragma unroll
+          for (int sq = 0; sq < 4; ++sq) {
+            const int s = 4 * half + sq;
+            uint32_t ahi[2][2], anl[2][2];
+            const float4 ks = km[s];
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+              const float4 cs = (r ? trow1 : trow0)[(8 * t + s) ^ tkey];
+              const uint32_t w = kw[r][sq];
+              // offset-binary byte u = code + 128 -> fp32 2^23 + u -> code -> code * scale
+              const float2 X = mul2(sub2(make_float2(magic_f32(w, 0), magic_f32(w, 2)), magic_bias()),
+                                    make_float2(ks.x, ks.y));
+              const float2 Y = mul2(sub2(make_float2(magic_f32(w, 1), magic_f32(w, 3)), magic_bias()),
+                                    make_float2(ks.z, ks.w));
+              rot_split(X, Y, cs, ahi[r][0], anl[r][0], ahi[r][1], anl[r][1]);
+            }
+            const uint2 bq = bqs[32 * s];
+            mma_16816(acc, ahi[0][0], ahi[1][0], ahi[0][1], ahi[1][1], bq.x, bq.y);
+            mma_16816(accn, anl[0][0], anl[1][0], anl[0][1], anl[1][1], bq.x, bq.y);
+          }
         }
-        float lg0 = acc[0] + acc[1] - accn[0] - accn[1];
-        float lg1 = acc[2] + acc[3] - accn[2] - accn[3];
+        table_done(i, ntiles, tok0);
+        const float2 d01 = sub2(make_float2(acc[0], acc[1]), make_float2(accn[0], accn[1]));
+        const float2 d23 = sub2(make_float2(acc[2], acc[3]), make_float2(accn[2], accn[3]));
+        float lg0 = d01.x + d01.y, lg1 = d23.x + d23.y;
         if (!valid) lg0 = lg1 = -INFINITY;
 
         // ---- softmax and the PV B operand (P' = p * v_scale, v_min into A.mb)
@@ -471,7 +558,8 @@ __global__ void __launch_bounds__(kThreads, 2)
         softmax_step(A, lg0, lg1, m0, m1, g, t, b01, b23);
 
         // ---- PV: A = V^T (channel rows 16g + 2m (+1); k-slots 2t, 2t+1, 2t+8, 2t+9 =
-        //      tokens sig(2t), sig(2t+1), +8), exact f16 codes
+        //      tokens sig(2t), sig(2t+1), +8) as f16 subnormals: low nibble c -> c * 2^-24
+        //      (rows g), high nibble -> 16c * 2^-24 (rows g+8)
         uint2 vw[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
@@ -480,31 +568,21 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
 #pragma unroll
         for (int w = 0; w < 2; ++w) {
-          const uint32_t a01 = w ? vw[0].y : vw[0].x, a1 = w ? vw[1].y : vw[1].x;
-          const uint32_t c01 = w ? vw[2].y : vw[2].x, c1 = w ? vw[3].y : vw[3].x;
-          const uint32_t xa[2] = {prmt(a01, a1, 0x5410u), prmt(a01, a1, 0x7632u)};
-          const uint32_t xc[2] = {prmt(c01, c1, 0x5410u), prmt(c01, c1, 0x7632u)};
+          const uint32_t a0 = w ? vw[0].y : vw[0].x, a1 = w ? vw[1].y : vw[1].x;
+          const uint32_t c0 = w ? vw[2].y : vw[2].x, c1 = w ? vw[3].y : vw[3].x;
 #pragma unroll
-          for (int hb = 0; hb < 2; ++hb) {
-#pragma unroll
-            for (int sh = 0; sh < 2; ++sh) {
-              const int m = 4 * w + 2 * hb + sh;
-              const uint32_t ya = xa[hb] >> (8 * sh), yc = xc[hb] >> (8 * sh);
-              // 1024 + c -> c and 1024 + 16c -> c, both exact (an accumulator that
-              // carries a large constant offset loses bits in the tensor cores)
-              const uint32_t lo_a = hsub2(and_or(ya, 0x000F000Fu, 0x64006400u), 0x64006400u);
-              const uint32_t hi_a = hfma2(and_or(ya, 0x00F000F0u, 0x64006400u), 0x2C002C00u, 0xD400D400u);
-              const uint32_t lo_c = hsub2(and_or(yc, 0x000F000Fu, 0x64006400u), 0x64006400u);
-              const uint32_t hi_c = hfma2(and_or(yc, 0x00F000F0u, 0x64006400u), 0x2C002C00u, 0xD400D400u);
-              mma_16816(A.O[m], lo_a, hi_a, lo_c, hi_c, b01, b23);
-            }
+          for (int j = 0; j < 4; ++j) {
+            // byte j of the two tokens' words into the low bytes of the two f16 halves
+            const uint32_t sel = 0x4400u + 0x1111u * j;
+            const uint32_t ya = prmt(a0, a1, sel), yc = prmt(c0, c1, sel);
+            mma_16816(A.O[4 * w + j], ya & 0x000F000Fu, ya & 0x00F000F0u, yc & 0x000F000Fu, yc & 0x00F000F0u,
+                      b01, b23);
           }
         }
-        ++tc;
 
         // ---- release the stage and refill it with tile i + kStages
         __syncwarp();
-        if (lane == 0 && i + kStages < ntiles && !sm.abort) {
+        if (lane == 0 && i + kStages < ntiles && !stalled) {
           fence_proxy_async();
           issue(i + kStages, pf);
           if (i + kStages + 1 < ntiles) pf = bt[(it.t0 + (i + kStages + 1) * kTile) >> lgP];
@@ -517,11 +595,8 @@ __global__ void __launch_bounds__(kThreads, 2)
       const long long wrow = ((long long)it.b * v.R) * v.Hkv + h;  // (b, slot 0, h) row index
       for (int i = 0; i < ntiles; ++i) {
         const int tok0 = it.t0 + i * kTile;
-        rope_table(sm, tc & 1, i, tok0, tp, td, Td, R16, Bp);
-        named_bar_sync(1, kThreads);
-        const float4* trow0 = reinterpret_cast<const float4*>(&sm.trig[tc & 1][sg][0]);
-        const float4* trow1 = reinterpret_cast<const float4*>(&sm.trig[tc & 1][sg + 8][0]);
-        const int tkey = ((t << 1) | (sg & 1)) & 7;
+        trow0 = table_rows(i);
+        const float4* trow1 = trow0 + 8 * 32;
         float acc[4] = {0.f, 0.f, 0.f, 0.f}, accn[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int s = 0; s < 8; ++s) {
@@ -536,11 +611,14 @@ __global__ void __launch_bounds__(kThreads, 2)
               for (int j = 0; j < 4; ++j) k[j] = load_src(v.k_win, wi + j, v.src_bf16);
             }
             const float4 cs = (r ? trow1 : trow0)[(8 * t + s) ^ tkey];
-            rotate_split(k[0], k[1], k[2], k[3], cs, ahi[r][0], anl[r][0], ahi[r][1], anl[r][1]);
+            rot_split(make_float2(k[0], k[2]), make_float2(k[1], k[3]), cs, ahi[r][0], anl[r][0], ahi[r][1],
+                      anl[r][1]);
           }
-          mma_16816(acc, ahi[0][0], ahi[1][0], ahi[0][1], ahi[1][1], bq[s][0], bq[s][1]);
-          mma_16816(accn, anl[0][0], anl[1][0], anl[0][1], anl[1][1], bq[s][0], bq[s][1]);
+          const uint2 bq = bqs[32 * s];
+          mma_16816(acc, ahi[0][0], ahi[1][0], ahi[0][1], ahi[1][1], bq.x, bq.y);
+          mma_16816(accn, anl[0][0], anl[1][0], anl[0][1], anl[1][1], bq.x, bq.y);
         }
+        table_done(i, ntiles, tok0);
         float lg0 = acc[0] + acc[1] - accn[0] - accn[1];
         float lg1 = acc[2] + acc[3] - accn[2] - accn[3];
         if (tok0 + sg >= T) lg0 = -INFINITY;
@@ -567,7 +645,6 @@ __global__ void __launch_bounds__(kThreads, 2)
           mma_16816(A.O[m], pack_f16x2(x[0][0], x[1][0]), pack_f16x2(x[0][1], x[1][1]),
                     pack_f16x2(x[2][0], x[3][0]), pack_f16x2(x[2][1], x[3][1]), b01, b23);
         }
-        ++tc;
       }
     }
 
@@ -577,6 +654,8 @@ __global__ void __launch_bounds__(kThreads, 2)
       A.l_loc += __shfl_xor_sync(0xffffffffu, A.l_loc, o);
       A.mb += __shfl_xor_sync(0xffffffffu, A.mb, o);
     }
+    // quantized values entered as c * 2^-24 (even channels) and 16c * 2^-24 (odd channels)
+    const float f_even = it.window ? 1.f : 16777216.f, f_odd = it.window ? 1.f : 1048576.f;
     const int hq = h * kNRep + t;
     float* dst = part + ((long long)item * v.Hq + hq) * (kD + 4);
     if (g == 0) {
@@ -585,9 +664,11 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
 #pragma unroll
     for (int m = 0; m < 8; ++m) {
-      const float2 o2 = make_float2((A.O[m][0] + A.O[m][1]) + A.mb, (A.O[m][2] + A.O[m][3]) + A.mb);
+      const float2 o2 = make_float2(fmaf(A.O[m][0] - A.O[m][1], f_even, A.mb),
+                                    fmaf(A.O[m][2] - A.O[m][3], f_odd, A.mb));
       reinterpret_cast<float2*>(dst + 4 + 16 * g)[m] = o2;  // channels 16g + 2m, 16g + 2m + 1
     }
+    named_bar_sync(1, kThreads);
     item = s_next[npar];
     npar ^= 1;
   }
@@ -692,7 +773,7 @@ bool fast_eligible(const KvqView& v) {
          v.kmode == KVQ_SYM_ABSMAX && v.kaxis == KVQ_PER_CHANNEL && v.rope_pre == 1 &&
          v.vfmt == KVQ_INT4 && v.vmode == KVQ_ASYM_MINMAX && v.vaxis == KVQ_PER_TOKEN &&
          v.vgroup == kD && pow2_g && pow2_p && v.kgroup >= kTile * kStages && v.P >= kTile &&
-         v.batch <= 4096;
+         (v.P != kTile || v.off_km == kStageBytes) && v.batch <= 4096;
 }
 
 size_t fast_workspace_bytes(const KvqView& v, int batch) {
