@@ -268,14 +268,15 @@ size_t attention_workspace_bytes(const KvqView& v, int batch) {
   const size_t generic = plan_header_bytes(batch) + (size_t)items * kHB * (v.D + 2) * sizeof(float);
   KvqView b = v;
   b.batch = batch;
-  return fast_eligible(b) ? (generic > fast_workspace_bytes(v, batch) ? generic : fast_workspace_bytes(v, batch))
-                          : generic;
+  const size_t split = fast_workspace_bytes(v, batch);  // layout of the tensor-core kernels
+  return (fast_eligible(b) || fp8_shape_eligible(b)) && split > generic ? split : generic;
 }
 
 kvq_status launch_attention(const KvqView& v, const void* q, float* out, float scale, void* ws,
                             size_t ws_bytes, cudaStream_t st) {
   (void)ws_bytes;
   if (fast_eligible(v)) return launch_fast(v, q, out, scale, ws, st);
+  if (fp8_eligible(v)) return launch_fp8(v, q, out, scale, ws, st);
   const size_t smem = sizeof(GenericSmem) + sizeof(int) * (v.batch + 1);
   static bool attr_set = false;
   if (!attr_set) {

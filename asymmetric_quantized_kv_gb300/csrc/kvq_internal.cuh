@@ -61,6 +61,10 @@ bool fast_eligible(const KvqView& v);
 size_t fast_workspace_bytes(const KvqView& v, int batch);
 kvq_status launch_fast(const KvqView& v, const void* q, float* out, float scale, void* ws,
                        cudaStream_t st);
+// Tensor-core decode kernel for FP8 E4M3 keys and values, 8 query heads per kv-head.
+bool fp8_shape_eligible(const KvqView& v);  // config only: sizes the workspace
+bool fp8_eligible(const KvqView& v);        // config, cache pointers and pool size
+kvq_status launch_fp8(const KvqView& v, const void* q, float* out, float scale, void* ws, cudaStream_t st);
 kvq_status launch_attention(const KvqView& v, const void* q, float* out, float scale,
                             void* ws, size_t ws_bytes, cudaStream_t st);
 

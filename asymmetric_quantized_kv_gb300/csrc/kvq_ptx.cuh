@@ -73,6 +73,27 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       : "memory");
 }
 
+// TMA tensor copy global -> shared::cta of one box of a 2-D tensor map at
+// element coordinates (x, y); completion counted in bytes on `bar`.  x must keep
+// the copy 16-byte aligned (x = 0 here); the destination is aligned to the
+// map's swizzle span.
+__device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+      "[%4];\n" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Two OCP E4M3 bytes (low byte -> low half) to f16x2; every E4M3 value is exact in f16.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(unsigned short x) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;\n" : "=r"(r) : "h"(x));
+  return r;
+}
+__device__ __forceinline__ unsigned short lo16(uint32_t x) { return static_cast<unsigned short>(x & 0xFFFFu); }
+__device__ __forceinline__ unsigned short hi16(uint32_t x) { return static_cast<unsigned short>(x >> 16); }
+
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t threads) {
   asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(threads) : "memory");
 }

@@ -31,6 +31,12 @@ CASES = {
     # FP8 E4M3 with calibrated per-head scales, 8 query heads per kv-head
     "fp8": (O.Config(16, 2, 128, Q(O.FP8_E4M3, S, TEN), Q(O.FP8_E4M3, S, TEN), 0, 256, 0, 1e4, O.BF16),
             [1, 255, 256, 900]),
+    # FP8 in 16-token pages (partial last tiles, permuted pages), fp32 sources
+    "fp8_p16_f32": (O.Config(16, 2, 128, Q(O.FP8_E4M3, S, TEN), Q(O.FP8_E4M3, S, TEN), 0, 16, 0, 1e4, O.F32),
+                    [1, 15, 16, 17, 300, 1000]),
+    # FP8 with the 70B layer's heads: 64 query heads on 8 kv-heads
+    "fp8_64q8kv": (O.Config(64, 8, 128, Q(O.FP8_E4M3, S, TEN), Q(O.FP8_E4M3, S, TEN), 0, 256, 0, 1e4, O.BF16),
+                   [700, 33]),
     # per-tensor INT8 (the synthetic head's failing baseline), fp32 sources
     "int8_tensor": (O.Config(1, 1, 128, Q(O.INT8, S, TEN), Q(O.INT8, S, TEN), 0, 256, 0, 1e4, O.F32), [4096]),
     # per-channel K over one 4096-token group + per-token V, fp32
