@@ -269,7 +269,7 @@ size_t attention_workspace_bytes(const KvqView& v, int batch) {
   KvqView b = v;
   b.batch = batch;
   const size_t split = fast_workspace_bytes(v, batch);  // layout of the tensor-core kernels
-  return (fast_eligible(b) || fp8_shape_eligible(b)) && split > generic ? split : generic;
+  return (fast_eligible(b) || fp8_shape_eligible(b) || int2_eligible(b)) && split > generic ? split : generic;
 }
 
 kvq_status launch_attention(const KvqView& v, const void* q, float* out, float scale, void* ws,
@@ -277,6 +277,7 @@ kvq_status launch_attention(const KvqView& v, const void* q, float* out, float s
   (void)ws_bytes;
   if (fast_eligible(v)) return launch_fast(v, q, out, scale, ws, st);
   if (fp8_eligible(v)) return launch_fp8(v, q, out, scale, ws, st);
+  if (int2_eligible(v)) return launch_int2(v, q, out, scale, ws, st);
   const size_t smem = sizeof(GenericSmem) + sizeof(int) * (v.batch + 1);
   static bool attr_set = false;
   if (!attr_set) {

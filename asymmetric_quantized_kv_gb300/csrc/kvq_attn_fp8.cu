@@ -70,6 +70,7 @@ __global__ void __launch_bounds__(kThreads8)
   __shared__ int s_C, s_NA, s_NB;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
+  const int lgP = __ffs(v.P) - 1;  // a power of two (checked on the host)
   fast_plan<kThreads8>(v, kTileT, prefA, prefB, &s_C, &s_NA, &s_NB, reinterpret_cast<int*>(&sm.kv[0][0][0][0]));
   if (blockIdx.x == 0) store_fast_plan(v, ws, prefA, prefB, s_C, s_NA, s_NB);
   unsigned long long* counter =
@@ -146,7 +147,7 @@ __global__ void __launch_bounds__(kThreads8)
         mbar_arrive(bar);
         return;
       }
-      const long long byte0 = (long long)pid * v.page_bytes + head_off + (long long)(tok % v.P) * kRowB;
+      const long long byte0 = (long long)pid * v.page_bytes + head_off + (long long)(tok & (v.P - 1)) * kRowB;
       const int yk = (int)(byte0 / kRowB), yv = yk + v.off_vc / kRowB;
       mbar_arrive_expect_tx(bar, 2 * kTileB);
       tma_load_2d(ring[stage][0], &tmap, 0, yk, bar);
@@ -155,8 +156,8 @@ __global__ void __launch_bounds__(kThreads8)
     int pf = 0;  // lane 0: page id of the next tile to load, read one tile ahead
     if (lane == 0 && !stalled) {
       fence_proxy_async();  // the ring's bytes were last written through the generic proxy
-      for (int i = 0; i < min(kStages8, ntiles); ++i) issue(i, bt[(it.t0 + i * kTileT) / v.P]);
-      if (kStages8 < ntiles) pf = bt[(it.t0 + kStages8 * kTileT) / v.P];
+      for (int i = 0; i < min(kStages8, ntiles); ++i) issue(i, bt[(it.t0 + i * kTileT) >> lgP]);
+      if (kStages8 < ntiles) pf = bt[(it.t0 + kStages8 * kTileT) >> lgP];
     }
     __syncwarp();
 
@@ -282,7 +283,7 @@ __global__ void __launch_bounds__(kThreads8)
       if (lane == 0 && i + kStages8 < ntiles && !stalled) {
         fence_proxy_async();
         issue(i + kStages8, pf);
-        if (i + kStages8 + 1 < ntiles) pf = bt[(it.t0 + (i + kStages8 + 1) * kTileT) / v.P];
+        if (i + kStages8 + 1 < ntiles) pf = bt[(it.t0 + (i + kStages8 + 1) * kTileT) >> lgP];
       }
       __syncwarp();
     }
@@ -345,7 +346,7 @@ long long pool_rows(const KvqView& v) { return (long long)v.n_pages * v.page_byt
 
 bool fp8_shape_eligible(const KvqView& v) {
   return v.D == kD && v.n_rep == kRep8 && v.kfmt == KVQ_FP8_E4M3 && v.vfmt == KVQ_FP8_E4M3 && v.R == 0 &&
-         v.P % kTileT == 0 && v.page_bytes % kRowB == 0 && v.head_bytes % kRowB == 0 && v.off_vc % kRowB == 0 &&
+         v.P >= kTileT && (v.P & (v.P - 1)) == 0 && v.page_bytes % kRowB == 0 && v.head_bytes % kRowB == 0 && v.off_vc % kRowB == 0 &&
          v.batch <= 4096;
 }
 

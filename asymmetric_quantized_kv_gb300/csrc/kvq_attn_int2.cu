@@ -1,0 +1,542 @@
+// Tensor-core split-K decode attention for 2-bit asymmetric keys quantized
+// per channel over token groups and 2-bit asymmetric values quantized per token
+// in 32-channel groups, head_dim 128, 4 query heads per kv-head, plus the bf16
+// residual window: the KIVI-style layer ("KIVI: A Tuning-Free Asymmetric 2bit
+// Quantization for KV Cache", section 3: keys per-channel, values per-token,
+// recent tokens kept in full precision).
+//
+// Work: a unit is (sequence, chunk of C tokens, kv-head); every warp takes units
+// from a global counter and streams its 16-token tiles through a private 3-stage
+// ring of TMA bulk copies (K codes, V codes, V scale/min rows; the key group's
+// scales and minima with the tile that starts the group).
+//
+// QK: with k = c * s + m per (group, channel), q.k = sum_c (q_c s_c) c + sum_c q_c m_c.
+//     A = the 2-bit codes, taken as f16 subnormals straight from the packed bytes
+//     (mask (3 << 2j) per f16 half: code * 4^j * 2^-24, exact); B = q * s / 4^j
+//     split hi/lo, rebuilt once per key group; the second sum is a per-group,
+//     per-head bias.
+// PV: with v = c * s_t + m_t per (token, 32-channel group), p.v = sum_t (p_t s_t) c
+//     + sum_t p_t m_t.  Lane row g holds byte 8G + g of every token (channels
+//     32G + 4g .. 32G + 4g + 3), so each 16-row MMA block stays inside one value
+//     group G and B = p * s_t(G) split hi/lo; the minima enter through running
+//     sums of p * m_t(G).
+#include <math.h>
+
+#include "kvq_ptx.cuh"
+#include "kvq_split_common.cuh"
+
+namespace kvq {
+namespace {
+
+using namespace ptx;
+
+constexpr int kTI = 16;
+constexpr int kWarpsI = 4;
+constexpr int kThreadsI = kWarpsI * 32;
+constexpr int kStagesI = 3;
+constexpr int kRepI = 4;
+constexpr int kRow2 = 32;                         // bytes of one token's 2-bit codes
+constexpr int kVMetaRow = 32;                     // (scale x 4, min x 4) fp32 per token
+constexpr int kKMeta2 = 2 * kD * 4;               // scales then minima of one key group (in the page)
+constexpr int kKMPad = 36;                        // floats per landed row of 32 key scales (or minima)
+constexpr int kOffV = kTI * kRow2;                // stage layout: K codes, V codes, V meta, K meta
+constexpr int kOffVM = kOffV + kTI * kRow2;
+constexpr int kOffKM = kOffVM + kTI * kVMetaRow;
+constexpr int kStageI = kOffKM + 8 * kKMPad * 4;  // key scales [4][36] then minima [4][36]
+constexpr uint32_t kSpinI = 1u << 20;
+constexpr float kLog2eI = 1.4426950408889634f;
+constexpr float kRescaleI = 8.f;
+constexpr float kMinitI = -1e30f;
+constexpr float kTwo24 = 16777216.f;
+
+struct __align__(128) SmemI2 {
+  uint8_t stage[kWarpsI][kStagesI][kStageI];
+  float4 qp[kWarpsI][8][32];  // per warp, step s, lane: q * qscale at the lane's 4 channels of step s
+  float pex[kWarpsI][2][32];  // p exchange: [token / 8][head * 8 + token % 8]
+  uint64_t bar[kWarpsI][kStagesI];
+  int valid[kWarpsI][kStagesI];
+};
+static_assert(kStageI % 16 == 0, "bulk-copy destinations stay 16-byte aligned");
+
+// Lane (g, t), step s: its four channels c0..c3 in k-slot order 2t, 2t+1, 2t+8,
+// 2t+9 are 32t + 16(s/4) + {j, 8+j, 4+j, 12+j} with j = s % 4: the code bit
+// fields (2j) of bytes 0/2 and 1/3 of the lane's word s/4.
+__device__ __forceinline__ int step_channel(int t, int s, int e) {
+  const int j = s & 3, base = 32 * t + 16 * (s >> 2);
+  return base + j + (e == 0 ? 0 : e == 1 ? 8 : e == 2 ? 4 : 12);
+}
+
+// 4 consecutive source-dtype values at element index i (16-byte aligned for fp32,
+// 8-byte aligned for bf16)
+__device__ __forceinline__ float4 load4_src(const void* base, long long i, int bf16) {
+  if (bf16) {
+    const uint2 u = *reinterpret_cast<const uint2*>(reinterpret_cast<const unsigned short*>(base) + i);
+    return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u), __uint_as_float(u.y << 16),
+                       __uint_as_float(u.y & 0xFFFF0000u));
+  }
+  return *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(base) + i);
+}
+
+// Per CTA: prefW[b] = number of sequences before b whose residual window is not
+// empty, *s_NW their total.  NT threads; scratch holds NT ints.
+template <int NT>
+__device__ inline void window_prefix(const KvqView& v, int* prefW, int* s_NW, int* scratch) {
+  const int B = v.batch;
+  const int seg = (B + NT - 1) / NT;
+  const int b0 = threadIdx.x * seg, b1 = min(B, b0 + seg);
+  int cnt = 0;
+  for (int b = b0; b < b1; ++b) {
+    const int T = seq_tokens(v, b);
+    cnt += T > n_quantized(T, v.R) ? 1 : 0;
+  }
+  scratch[threadIdx.x] = cnt;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int r = 0;
+    for (int k = 0; k < NT; ++k) {
+      const int x = scratch[k];
+      scratch[k] = r;
+      r += x;
+    }
+    *s_NW = r;
+  }
+  __syncthreads();
+  int r = scratch[threadIdx.x];
+  for (int b = b0; b < b1; ++b) {
+    prefW[b] = r;
+    const int T = seq_tokens(v, b);
+    r += T > n_quantized(T, v.R) ? 1 : 0;
+  }
+  if (threadIdx.x == 0) prefW[B] = *s_NW;
+  __syncthreads();
+}
+
+__device__ __forceinline__ void split_sel(float x0, float x1, bool lo, uint32_t& out) {
+  uint32_t hi, l;
+  split_hi_lo(x0, x1, hi, l);
+  out = lo ? l : hi;
+}
+
+__global__ void __launch_bounds__(kThreadsI, 3)
+    split_int2_kernel(KvqView v, const void* q, float scale, float* ws) {
+  extern __shared__ __align__(128) unsigned char dyn[];
+  SmemI2& sm = *reinterpret_cast<SmemI2*>(dyn);
+  int* prefA = reinterpret_cast<int*>(dyn + sizeof(SmemI2));
+  int* prefB = prefA + v.batch + 1;
+  int* prefW = prefB + v.batch + 1;
+  __shared__ int s_C, s_NA, s_NB, s_NW;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, t = lane & 3;
+  const bool odd = (g & 1) != 0;  // this lane's B columns carry lo halves
+  const int G = v.kgroup;  // powers of two (checked on the host)
+  const int lgP = __ffs(v.P) - 1, lgG = __ffs(G) - 1;
+  fast_plan<kThreadsI>(v, G, prefA, prefB, &s_C, &s_NA, &s_NB, reinterpret_cast<int*>(&sm.stage[0][0][0]));
+  window_prefix<kThreadsI>(v, prefW, &s_NW, reinterpret_cast<int*>(&sm.stage[0][0][0]));
+  if (blockIdx.x == 0) store_fast_plan(v, ws, prefA, prefB, s_C, s_NA, s_NB);
+  unsigned long long* counter =
+      reinterpret_cast<unsigned long long*>(reinterpret_cast<char*>(ws) + fast_counter_offset(v.batch));
+  if (lane == 0) {
+    for (int s = 0; s < kStagesI; ++s) mbar_init(&sm.bar[warp][s], 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  const int C = s_C, NA = s_NA, NW = s_NW;
+  // execution order: the residual-window units first (the slowest per token),
+  // then every unit of the plan in its long-first order, skipping the windows
+  const int n_units = (NW + s_NA + s_NB) * v.Hkv;
+  float* part = reinterpret_cast<float*>(reinterpret_cast<char*>(ws) + fast_header_bytes(v.batch));
+  int lstage = 0, cstage = 0;
+  uint32_t cphase = 0, n_loaded = 0, n_consumed = 0;
+  bool stalled = false;
+  const float qscale = scale * kLog2eI;
+
+  int unit = blockIdx.x * kWarpsI + warp;
+  const int unit_stride0 = gridDim.x * kWarpsI;
+  while (unit < n_units) {
+    unsigned long long nxt = 0;
+    if (lane == 0) nxt = atomicAdd(counter, 1ull);
+    int pair, h;
+    if (unit < NW * v.Hkv) {
+      const int w = unit / v.Hkv;
+      h = unit - w * v.Hkv;
+      const int b = seq_of(prefW, v.batch, w);
+      pair = NA + prefB[b] + (n_quantized(seq_tokens(v, b), v.R) % C ? 1 : 0);
+    } else {
+      const int u = unit - NW * v.Hkv;
+      pair = u / v.Hkv;
+      h = u - pair * v.Hkv;
+    }
+    const FastItem it = decode_fast_item(v, prefA, prefB, C, NA, pair);
+    if (it.window && unit >= NW * v.Hkv) {  // done in the first phase
+      unit = unit_stride0 + (int)__shfl_sync(0xffffffffu, (unsigned)nxt, 0);
+      continue;
+    }
+    const int ntiles = (it.t1 - it.t0 + kTI - 1) / kTI;
+
+    // q * scale * log2(e) / 4^(s % 4) of this lane's query head 4h + g/2 at its step
+    // channels (the power of two matches the code field's weight in the f16 subnormal)
+    {
+      const long long qb = ((long long)it.b * v.Hq + h * kRepI + (g >> 1)) * kD;
+      __syncwarp();
+#pragma unroll
+      for (int s = 0; s < 8; ++s) {
+        const float f = qscale / (float)(1 << (2 * (s & 3)));
+        float x[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) x[e] = load_src(q, qb + step_channel(t, s, e), v.src_bf16) * f;
+        sm.qp[warp][s][lane] = make_float4(x[0], x[1], x[2], x[3]);
+      }
+      __syncwarp();
+    }
+    const float4* qps = &sm.qp[warp][0][lane];  // step s at qps[32 * s]
+
+    // O[m]: rows g / g+8, columns 2t / 2t+1 = query head t hi / lo
+    float O[8][4];
+#pragma unroll
+    for (int m = 0; m < 8; ++m) O[m][0] = O[m][1] = O[m][2] = O[m][3] = 0.f;
+    float m_run = kMinitI, l_loc = 0.f;
+    float mb[4] = {0.f, 0.f, 0.f, 0.f};  // sum of p * v_min per value group (head t)
+    float* pe = &sm.pex[warp][0][0];
+
+    // softmax step for logits of tokens g, g+8 (head t); returns p
+    auto softmax = [&](float lg0, float lg1, float& p0, float& p1) {
+      if (__any_sync(0xffffffffu, fmaxf(lg0, lg1) > m_run + kRescaleI)) {
+        float mx = fmaxf(lg0, lg1);
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+        const float mn = fmaxf(m_run, mx);
+        const float alpha = ex2(m_run - mn);
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+          O[m][0] *= alpha; O[m][1] *= alpha; O[m][2] *= alpha; O[m][3] *= alpha;
+        }
+        l_loc *= alpha;
+#pragma unroll
+        for (int G4 = 0; G4 < 4; ++G4) mb[G4] *= alpha;
+        m_run = mn;
+      }
+      p0 = ex2(lg0 - m_run);
+      p1 = ex2(lg1 - m_run);
+      l_loc += p0 + p1;
+    };
+    // p of head g/2 at k-slots 2t, 2t+1 (x01) and 2t+8, 2t+9 (x89)
+    auto exchange = [&](float p0, float p1, float2& x01, float2& x89) {
+      __syncwarp();
+      pe[t * 8 + g] = p0;
+      pe[32 + t * 8 + g] = p1;
+      __syncwarp();
+      x01 = *reinterpret_cast<const float2*>(pe + (g >> 1) * 8 + 2 * t);
+      x89 = *reinterpret_cast<const float2*>(pe + 32 + (g >> 1) * 8 + 2 * t);
+    };
+
+    if (!it.window) {
+      // ======================= quantized chunk
+      const int32_t* bt = v.block_table + (long long)it.b * v.max_pages;
+      const long long head_off = (long long)h * v.head_bytes;
+      auto issue = [&](int i, int pid) {
+        const int stage = lstage;
+        if (++lstage == kStagesI) lstage = 0;
+        ++n_loaded;
+        const int tok = it.t0 + i * kTI;
+        uint64_t* bar = &sm.bar[warp][stage];
+        const bool ok = pid >= 0 && pid < v.n_pages;
+        sm.valid[warp][stage] = ok;
+        if (!ok) {
+          atomicOr(v.status, KVQ_DEV_BAD_PAGE);
+          mbar_arrive(bar);
+          return;
+        }
+        const uint8_t* hb = v.pages + (long long)pid * v.page_bytes + head_off;
+        const int slot = tok & (v.P - 1);
+        const bool gstart = (tok & (G - 1)) == 0;
+        mbar_arrive_expect_tx(bar, kOffKM + (gstart ? kKMeta2 : 0));
+        uint8_t* dst = sm.stage[warp][stage];
+        bulk_g2s(dst, hb + slot * kRow2, kTI * kRow2, bar);
+        bulk_g2s(dst + kOffV, hb + v.off_vc + slot * kRow2, kTI * kRow2, bar);
+        bulk_g2s(dst + kOffVM, hb + v.off_vm + slot * kVMetaRow, kTI * kVMetaRow, bar);
+        if (gstart) {
+          // the group's scales and minima as 8 rows of 32 floats, each padded to kKMPad so
+          // that the four lane quarters read distinct banks
+          const uint8_t* src = hb + v.off_km + (v.P >= G ? slot >> lgG : 0) * kKMeta2;
+#pragma unroll
+          for (int r = 0; r < 8; ++r) bulk_g2s(dst + kOffKM + r * kKMPad * 4, src + r * 128, 128, bar);
+        }
+      };
+      int pf = 0;
+      if (lane == 0 && !stalled) {
+        fence_proxy_async();
+        for (int i = 0; i < min(kStagesI, ntiles); ++i) issue(i, bt[(it.t0 + i * kTI) >> lgP]);
+        if (kStagesI < ntiles) pf = bt[(it.t0 + kStagesI * kTI) >> lgP];
+      }
+      __syncwarp();
+
+      uint32_t bk[8][2];  // QK B: q * s / 4^j of the current key group, hi (even g) / lo (odd g)
+      float bias = 0.f;   // sum_c q_c m_c of the current key group for query head t
+      for (int i = 0; i < ntiles; ++i) {
+        const int stage = cstage;
+        bool valid = false;
+        if (!stalled) {
+          if (!mbar_wait_bounded(&sm.bar[warp][stage], cphase, kSpinI)) {
+            atomicOr(v.status, KVQ_DEV_TIMEOUT);
+            stalled = true;
+          } else {
+            valid = sm.valid[warp][stage] != 0;
+          }
+        }
+        if (++cstage == kStagesI) {
+          cstage = 0;
+          cphase ^= 1u;
+        }
+        ++n_consumed;
+        const uint8_t* buf = sm.stage[warp][stage];
+        const int tok0 = it.t0 + i * kTI;
+
+        if ((tok0 & (G - 1)) == 0) {
+          // ---- new key group: B = q * s / 4^j and the bias sum_c q_c m_c
+          const float* ks = reinterpret_cast<const float*>(buf + kOffKM);  // [8][kKMPad]
+          float bl = 0.f;
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            float sc[16], mn[16];
+#pragma unroll
+            for (int k4 = 0; k4 < 4; ++k4) {
+              const float4 a = reinterpret_cast<const float4*>(ks + kKMPad * t + 16 * half)[k4];
+              const float4 b = reinterpret_cast<const float4*>(ks + kKMPad * (4 + t) + 16 * half)[k4];
+              sc[4 * k4] = a.x; sc[4 * k4 + 1] = a.y; sc[4 * k4 + 2] = a.z; sc[4 * k4 + 3] = a.w;
+              mn[4 * k4] = b.x; mn[4 * k4 + 1] = b.y; mn[4 * k4 + 2] = b.z; mn[4 * k4 + 3] = b.w;
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const int s = 4 * half + j;
+              // q / 4^j (staged so) at channels j, 8+j, 4+j, 12+j of the half
+              const float4 x = qps[32 * s];
+              split_sel(x.x * sc[j], x.y * sc[8 + j], odd, bk[s][0]);
+              split_sel(x.z * sc[4 + j], x.w * sc[12 + j], odd, bk[s][1]);
+              const float part = fmaf(x.x, mn[j], fmaf(x.y, mn[8 + j], fmaf(x.z, mn[4 + j], x.w * mn[12 + j])));
+              bl = fmaf(part, (float)(1 << (2 * j)), bl);  // undo the exact 4^-j
+            }
+          }
+          // lanes (g, t') of head g/2 hold disjoint channels: sum over t', then the
+          // logit lanes (head t) take it from lane 8t
+          bl += __shfl_xor_sync(0xffffffffu, bl, 1);
+          bl += __shfl_xor_sync(0xffffffffu, bl, 2);
+          bias = __shfl_sync(0xffffffffu, bl, 8 * t);
+        }
+
+        // ---- QK: rows g / g+8 = tokens g / g+8; codes as f16 subnormals
+        const uint2 w0 = *reinterpret_cast<const uint2*>(buf + g * kRow2 + 8 * t);
+        const uint2 w1 = *reinterpret_cast<const uint2*>(buf + (g + 8) * kRow2 + 8 * t);
+        const uint32_t u0[2] = {w0.x, w0.y}, u1[2] = {w1.x, w1.y};
+        const uint32_t s0[2] = {w0.x >> 8, w0.y >> 8}, s1[2] = {w1.x >> 8, w1.y >> 8};
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int s = 0; s < 8; ++s) {
+          const uint32_t msk = 0x00030003u << (2 * (s & 3));
+          const int wd = s >> 2;
+          mma_16816(acc, u0[wd] & msk, u1[wd] & msk, s0[wd] & msk, s1[wd] & msk, bk[s][0], bk[s][1]);
+        }
+        const int nvalid = valid ? min(kTI, it.t1 - tok0) : 0;
+        const float lg0 = g < nvalid ? fmaf(acc[0] + acc[1], kTwo24, bias) : -INFINITY;
+        const float lg1 = g + 8 < nvalid ? fmaf(acc[2] + acc[3], kTwo24, bias) : -INFINITY;
+        float p0, p1;
+        softmax(lg0, lg1, p0, p1);
+
+        // ---- value minima of tokens g, g+8 (head t) and scales of the B tokens
+        const float* vm = reinterpret_cast<const float*>(buf + kOffVM);
+        if (valid) {
+          const float4 n0 = reinterpret_cast<const float4*>(vm + g * 8)[1];
+          const float4 n1 = reinterpret_cast<const float4*>(vm + (g + 8) * 8)[1];
+          mb[0] = fmaf(p0, n0.x, fmaf(p1, n1.x, mb[0]));
+          mb[1] = fmaf(p0, n0.y, fmaf(p1, n1.y, mb[1]));
+          mb[2] = fmaf(p0, n0.z, fmaf(p1, n1.z, mb[2]));
+          mb[3] = fmaf(p0, n0.w, fmaf(p1, n1.w, mb[3]));
+        }
+        float2 x01, x89;
+        exchange(p0, p1, x01, x89);
+        const float4 sa = reinterpret_cast<const float4*>(vm + (2 * t) * 8)[0];
+        const float4 sb = reinterpret_cast<const float4*>(vm + (2 * t + 1) * 8)[0];
+        const float4 sc8 = reinterpret_cast<const float4*>(vm + (2 * t + 8) * 8)[0];
+        const float4 sd = reinterpret_cast<const float4*>(vm + (2 * t + 9) * 8)[0];
+        const float sA[4] = {sa.x, sa.y, sa.z, sa.w}, sB[4] = {sb.x, sb.y, sb.z, sb.w};
+        const float sC[4] = {sc8.x, sc8.y, sc8.z, sc8.w}, sD[4] = {sd.x, sd.y, sd.z, sd.w};
+
+        // ---- PV, value group G: byte 8G + g of tokens 2t, 2t+1 (ya) and 2t+8, 2t+9 (yc)
+        const uint8_t* vc = buf + kOffV;
+        const int gb = g & 3;
+        const uint32_t sel = gb * 0x0011u + (4 + gb) * 0x1100u;
+        const int woff = 4 * (g >> 2);
+#pragma unroll
+        for (int G4 = 0; G4 < 4; ++G4) {
+          uint32_t b01, b89;
+          split_sel(x01.x * sA[G4], x01.y * sB[G4], odd, b01);
+          split_sel(x89.x * sC[G4], x89.y * sD[G4], odd, b89);
+          const int off = 8 * G4 + woff;
+          const uint32_t wa = *reinterpret_cast<const uint32_t*>(vc + (2 * t) * kRow2 + off);
+          const uint32_t wb = *reinterpret_cast<const uint32_t*>(vc + (2 * t + 1) * kRow2 + off);
+          const uint32_t wc = *reinterpret_cast<const uint32_t*>(vc + (2 * t + 8) * kRow2 + off);
+          const uint32_t wd = *reinterpret_cast<const uint32_t*>(vc + (2 * t + 9) * kRow2 + off);
+          const uint32_t ya = prmt(wa, wb, sel), yc = prmt(wc, wd, sel);
+          // m-block 2G4: rows g / g+8 = channels 32G4 + 4g + 0 / + 1 (factors 1, 4)
+          mma_16816(O[2 * G4], ya & 0x00030003u, ya & 0x000C000Cu, yc & 0x00030003u, yc & 0x000C000Cu, b01, b89);
+          // m-block 2G4+1: channels 32G4 + 4g + 2 / + 3 (factors 16, 64)
+          mma_16816(O[2 * G4 + 1], ya & 0x00300030u, ya & 0x00C000C0u, yc & 0x00300030u, yc & 0x00C000C0u, b01,
+                    b89);
+        }
+
+        // ---- release the stage and refill it
+        __syncwarp();
+        if (lane == 0 && i + kStagesI < ntiles && !stalled) {
+          fence_proxy_async();
+          issue(i + kStagesI, pf);
+          if (i + kStagesI + 1 < ntiles) pf = bt[(it.t0 + (i + kStagesI + 1) * kTI) >> lgP];
+        }
+        __syncwarp();
+      }
+    } else {
+      // ======================= residual window: source-dtype rows from k_win / v_win
+      uint32_t bw[8][2];  // B = q (no group scale), hi / lo
+#pragma unroll
+      for (int s = 0; s < 8; ++s) {
+        const float4 x = qps[32 * s];
+        const float f = (float)(1 << (2 * (s & 3)));
+        split_sel(x.x * f, x.y * f, odd, bw[s][0]);
+        split_sel(x.z * f, x.w * f, odd, bw[s][1]);
+      }
+      const int T = it.t1;
+      const long long wrow = ((long long)it.b * v.R) * v.Hkv + h;
+      for (int i = 0; i < ntiles; ++i) {
+        const int tok0 = it.t0 + i * kTI;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f}, accn[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          // key rows of tokens g, g+8: channels 32t + 16 half .. + 15 (zero past the end)
+          float kw[2][16];
+#pragma unroll
+          for (int r = 0; r < 2; ++r) {
+            const int tok = tok0 + g + 8 * r;
+            const long long wi = (wrow + (long long)(tok - it.t0) * v.Hkv) * kD + 32 * t + 16 * half;
+#pragma unroll
+            for (int c4 = 0; c4 < 4; ++c4) {
+              const float4 x =
+                  tok < T ? load4_src(v.k_win, wi + 4 * c4, v.src_bf16) : make_float4(0.f, 0.f, 0.f, 0.f);
+              kw[r][4 * c4] = x.x; kw[r][4 * c4 + 1] = x.y; kw[r][4 * c4 + 2] = x.z; kw[r][4 * c4 + 3] = x.w;
+            }
+          }
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int s = 4 * half + j;
+            uint32_t ahi[2][2], anl[2][2];
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {  // channels j, 8+j | 4+j, 12+j of the half
+              split_hi_neglo(kw[r][j], kw[r][8 + j], ahi[r][0], anl[r][0]);
+              split_hi_neglo(kw[r][4 + j], kw[r][12 + j], ahi[r][1], anl[r][1]);
+            }
+            mma_16816(acc, ahi[0][0], ahi[1][0], ahi[0][1], ahi[1][1], bw[s][0], bw[s][1]);
+            mma_16816(accn, anl[0][0], anl[1][0], anl[0][1], anl[1][1], bw[s][0], bw[s][1]);
+          }
+        }
+        const float lg0 = tok0 + g < T ? (acc[0] + acc[1]) - (accn[0] + accn[1]) : -INFINITY;
+        const float lg1 = tok0 + g + 8 < T ? (acc[2] + acc[3]) - (accn[2] + accn[3]) : -INFINITY;
+        float p0, p1;
+        softmax(lg0, lg1, p0, p1);
+        float2 x01, x89;
+        exchange(p0, p1, x01, x89);
+        uint32_t b01, b89;
+        split_sel(x01.x, x01.y, odd, b01);
+        split_sel(x89.x, x89.y, odd, b89);
+        // values as f16, same row -> channel map as the quantized path (32G + 4g + k)
+        const int slots[4] = {2 * t, 2 * t + 1, 2 * t + 8, 2 * t + 9};
+#pragma unroll
+        for (int G4 = 0; G4 < 4; ++G4) {
+          float vv[4][4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int tok = tok0 + slots[u];
+            const long long wi = (wrow + (long long)(tok - it.t0) * v.Hkv) * kD + 32 * G4 + 4 * g;
+            const float4 x = tok < T ? load4_src(v.v_win, wi, v.src_bf16) : make_float4(0.f, 0.f, 0.f, 0.f);
+            vv[u][0] = x.x; vv[u][1] = x.y; vv[u][2] = x.z; vv[u][3] = x.w;
+          }
+#pragma unroll
+          for (int hb = 0; hb < 2; ++hb) {
+            const int k0 = 2 * hb;
+            mma_16816(O[2 * G4 + hb], pack_f16x2(vv[0][k0], vv[1][k0]), pack_f16x2(vv[0][k0 + 1], vv[1][k0 + 1]),
+                      pack_f16x2(vv[2][k0], vv[3][k0]), pack_f16x2(vv[2][k0 + 1], vv[3][k0 + 1]), b01, b89);
+          }
+        }
+      }
+    }
+
+    // ---- epilogue: partial record of query head 4h + t
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+      l_loc += __shfl_xor_sync(0xffffffffu, l_loc, o);
+#pragma unroll
+      for (int G4 = 0; G4 < 4; ++G4) mb[G4] += __shfl_xor_sync(0xffffffffu, mb[G4], o);
+    }
+    float* rec = part + ((long long)pair * v.Hq + h * kRepI + t) * (kD + 4);
+    if (g == 0) {
+      rec[0] = m_run;
+      rec[1] = l_loc;
+    }
+    // quantized codes entered as code * 4^k * 2^-24 (k = channel % 4)
+    const float f0 = it.window ? 1.f : kTwo24, f1 = it.window ? 1.f : kTwo24 / 4.f;
+    const float f2 = it.window ? 1.f : kTwo24 / 16.f, f3 = it.window ? 1.f : kTwo24 / 64.f;
+#pragma unroll
+    for (int G4 = 0; G4 < 4; ++G4) {
+      const float4 o4 = make_float4(fmaf(O[2 * G4][0] + O[2 * G4][1], f0, mb[G4]),
+                                    fmaf(O[2 * G4][2] + O[2 * G4][3], f1, mb[G4]),
+                                    fmaf(O[2 * G4 + 1][0] + O[2 * G4 + 1][1], f2, mb[G4]),
+                                    fmaf(O[2 * G4 + 1][2] + O[2 * G4 + 1][3], f3, mb[G4]));
+      *reinterpret_cast<float4*>(rec + 4 + 32 * G4 + 4 * g) = o4;
+    }
+    unit = unit_stride0 + (int)__shfl_sync(0xffffffffu, (unsigned)nxt, 0);
+  }
+
+  if (lane == 0) {
+    while (n_consumed < n_loaded) {
+      mbar_wait_bounded(&sm.bar[warp][cstage], cphase, kSpinI);
+      if (++cstage == kStagesI) {
+        cstage = 0;
+        cphase ^= 1u;
+      }
+      ++n_consumed;
+    }
+  }
+}
+
+}  // namespace
+
+bool int2_eligible(const KvqView& v) {
+  const bool pow2_g = v.kgroup > 0 && (v.kgroup & (v.kgroup - 1)) == 0;
+  return v.D == kD && v.n_rep == kRepI && v.kfmt == KVQ_INT2 && v.kmode == KVQ_ASYM_MINMAX &&
+         v.kaxis == KVQ_PER_CHANNEL && v.vfmt == KVQ_INT2 && v.vmode == KVQ_ASYM_MINMAX &&
+         v.vaxis == KVQ_PER_TOKEN && v.vgroup == 32 && v.rope_pre == 0 && pow2_g && v.kgroup >= kTI &&
+         v.P >= kTI && (v.P & (v.P - 1)) == 0 && v.batch <= 4096;
+}
+
+kvq_status launch_int2(const KvqView& v, const void* q, float* out, float scale, void* ws, cudaStream_t st) {
+  const size_t smem = sizeof(SmemI2) + sizeof(int) * 3 * (v.batch + 1);
+  static int occ_cache[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) return KVQ_ERR_UNSUPPORTED;
+  if (!occ_cache[dev]) {
+    if (cudaFuncSetAttribute(split_int2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)(sizeof(SmemI2) + sizeof(int) * 3 * 4097)) != cudaSuccess)
+      return KVQ_ERR_CUDA;
+    int occ = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, split_int2_kernel, kThreadsI, smem) != cudaSuccess)
+      return KVQ_ERR_CUDA;
+    occ_cache[dev] = occ > 0 ? occ : 1;
+  }
+  const int grid = num_sms() * occ_cache[dev];
+  if (cudaMemsetAsync(static_cast<char*>(ws) + fast_counter_offset(v.batch), 0, 8, st) != cudaSuccess)
+    return KVQ_ERR_CUDA;
+  split_int2_kernel<<<grid, kThreadsI, smem, st>>>(v, q, scale, static_cast<float*>(ws));
+  if (cudaGetLastError() != cudaSuccess) return KVQ_ERR_CUDA;
+  return launch_split_combine(v, static_cast<float*>(ws), out, st) == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+}
+
+}  // namespace kvq

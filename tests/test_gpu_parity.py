@@ -25,6 +25,12 @@ CASES = {
     # KIVI-style 2-bit (the Llama-3.1-8B layer's formats), contiguous pages
     "int2_kivi": (O.Config(8, 2, 128, Q(O.INT2, A, CH, 32), Q(O.INT2, A, TOK, 32), 128, 256, 0, 1e4, O.BF16),
                   [0, 1, 127, 128, 129, 300, 1000]),
+    # the same formats with the 8B layer's heads (32 query / 8 kv) in 16-token pages
+    "int2_kivi_p16": (O.Config(32, 8, 128, Q(O.INT2, A, CH, 32), Q(O.INT2, A, TOK, 32), 128, 16, 0, 1e4, O.BF16),
+                      [129, 1000, 2200]),
+    # 64-token key groups, fp32 sources
+    "int2_g64_f32": (O.Config(8, 2, 128, Q(O.INT2, A, CH, 64), Q(O.INT2, A, TOK, 32), 128, 64, 0, 1e4, O.F32),
+                     [63, 64, 65, 700]),
     # INT8 per-channel pre-RoPE keys + INT4 per-token values in 16-token pages
     "int8k_rope_int4v": (O.Config(8, 2, 128, Q(O.INT8, S, CH, 64), Q(O.INT4, A, TOK, 128), 64, 16, 1, 5e5, O.BF16),
                          [1, 63, 64, 65, 700, 2100]),
