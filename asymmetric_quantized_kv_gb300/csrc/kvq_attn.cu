@@ -269,7 +269,7 @@ size_t attention_workspace_bytes(const KvqView& v, int batch) {
   KvqView b = v;
   b.batch = batch;
   const size_t split = fast_workspace_bytes(v, batch);  // layout of the tensor-core kernels
-  return (fast_eligible(b) || fp8_shape_eligible(b) || int2_eligible(b)) && split > generic ? split : generic;
+  return (fast_eligible(b) || fp8_shape_eligible(b) || int2_shape_eligible(b)) && split > generic ? split : generic;
 }
 
 kvq_status launch_attention(const KvqView& v, const void* q, float* out, float scale, void* ws,

@@ -20,12 +20,11 @@
 //       B = p for the 8 query heads (one column each), once with the f16 hi
 //       part of p and once with the residual, into the same accumulators;
 //       v_scale multiplies the output once at the end.
-#include <cuda.h>
-#include <cudaTypedefs.h>
 #include <math.h>
 
 #include "kvq_ptx.cuh"
 #include "kvq_split_common.cuh"
+#include "kvq_tmap.h"
 
 namespace kvq {
 namespace {
@@ -327,19 +326,6 @@ __global__ void __launch_bounds__(kThreads8)
   }
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult res;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &res) ==
-            cudaSuccess &&
-        res == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
-  return fn;
-}
-
 long long pool_rows(const KvqView& v) { return (long long)v.n_pages * v.page_bytes / kRowB; }
 
 }  // namespace
@@ -352,7 +338,7 @@ bool fp8_shape_eligible(const KvqView& v) {
 
 bool fp8_eligible(const KvqView& v) {
   return fp8_shape_eligible(v) && (reinterpret_cast<uintptr_t>(v.pages) & 15) == 0 && pool_rows(v) > 0 &&
-         pool_rows(v) < (1LL << 31) && encode_fn() != nullptr;
+         pool_rows(v) < (1LL << 31) && tensor_map_encoder() != nullptr;
 }
 
 kvq_status launch_fp8(const KvqView& v, const void* q, float* out, float scale, void* ws, cudaStream_t st) {
@@ -362,7 +348,7 @@ kvq_status launch_fp8(const KvqView& v, const void* q, float* out, float scale, 
   const cuuint64_t strides[1] = {(cuuint64_t)kRowB};
   const cuuint32_t box[2] = {(cuuint32_t)kRowB, (cuuint32_t)kTileT};
   const cuuint32_t estr[2] = {1, 1};
-  if (encode_fn()(&tmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, v.pages, dims, strides, box, estr,
+  if (tensor_map_encoder()(&tmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, v.pages, dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return KVQ_ERR_UNSUPPORTED;

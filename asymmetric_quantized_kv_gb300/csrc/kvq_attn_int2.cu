@@ -7,8 +7,10 @@
 //
 // Work: a unit is (sequence, chunk of C tokens, kv-head); every warp takes units
 // from a global counter and streams its 16-token tiles through a private 3-stage
-// ring of TMA bulk copies (K codes, V codes, V scale/min rows; the key group's
-// scales and minima with the tile that starts the group).
+// ring.  One 5-D TMA tensor copy brings a tile's K codes, V codes and V scale/min
+// rows (three page sections with 32-byte rows); a tile that starts a key group
+// also brings the group's scales and minima with a 2-D tensor copy in 128-byte
+// swizzle, so the per-group reads meet no bank conflict.
 //
 // QK: with k = c * s + m per (group, channel), q.k = sum_c (q_c s_c) c + sum_c q_c m_c.
 //     A = the 2-bit codes, taken as f16 subnormals straight from the packed bytes
@@ -24,6 +26,7 @@
 
 #include "kvq_ptx.cuh"
 #include "kvq_split_common.cuh"
+#include "kvq_tmap.h"
 
 namespace kvq {
 namespace {
@@ -38,25 +41,28 @@ constexpr int kRepI = 4;
 constexpr int kRow2 = 32;                         // bytes of one token's 2-bit codes
 constexpr int kVMetaRow = 32;                     // (scale x 4, min x 4) fp32 per token
 constexpr int kKMeta2 = 2 * kD * 4;               // scales then minima of one key group (in the page)
-constexpr int kKMPad = 36;                        // floats per landed row of 32 key scales (or minima)
-constexpr int kOffV = kTI * kRow2;                // stage layout: K codes, V codes, V meta, K meta
+// stage layout (1024-byte aligned): key scales/minima as 8 swizzled rows of 128
+// bytes, then K codes, V codes and V meta rows of the tile ([3][16][32] bytes)
+constexpr int kOffKM = 0;
+constexpr int kOffK = kKMeta2;
+constexpr int kOffV = kOffK + kTI * kRow2;
 constexpr int kOffVM = kOffV + kTI * kRow2;
-constexpr int kOffKM = kOffVM + kTI * kVMetaRow;
-constexpr int kStageI = kOffKM + 8 * kKMPad * 4;  // key scales [4][36] then minima [4][36]
+constexpr int kTileBytesI = 3 * kTI * kRow2;
+constexpr int kStageI = 3072;
 constexpr uint32_t kSpinI = 1u << 20;
 constexpr float kLog2eI = 1.4426950408889634f;
 constexpr float kRescaleI = 8.f;
 constexpr float kMinitI = -1e30f;
 constexpr float kTwo24 = 16777216.f;
 
-struct __align__(128) SmemI2 {
+struct __align__(1024) SmemI2 {
   uint8_t stage[kWarpsI][kStagesI][kStageI];
   float4 qp[kWarpsI][8][32];  // per warp, step s, lane: q * qscale at the lane's 4 channels of step s
   float pex[kWarpsI][2][32];  // p exchange: [token / 8][head * 8 + token % 8]
   uint64_t bar[kWarpsI][kStagesI];
   int valid[kWarpsI][kStagesI];
 };
-static_assert(kStageI % 16 == 0, "bulk-copy destinations stay 16-byte aligned");
+static_assert(kStageI % 1024 == 0 && kOffVM + kTI * kVMetaRow <= kStageI, "stages stay 1024-byte aligned");
 
 // Lane (g, t), step s: its four channels c0..c3 in k-slot order 2t, 2t+1, 2t+8,
 // 2t+9 are 32t + 16(s/4) + {j, 8+j, 4+j, 12+j} with j = s % 4: the code bit
@@ -111,15 +117,19 @@ __device__ inline void window_prefix(const KvqView& v, int* prefW, int* s_NW, in
   __syncthreads();
 }
 
+// f16x2 hi part of (x0, x1), or (hi - x) for lanes that carry the residual
+// columns: a column pair then sums to hi - (hi - x) = x.
 __device__ __forceinline__ void split_sel(float x0, float x1, bool lo, uint32_t& out) {
-  uint32_t hi, l;
-  split_hi_lo(x0, x1, hi, l);
-  out = lo ? l : hi;
+  uint32_t hi, nl;
+  split_hi_neglo(x0, x1, hi, nl);
+  out = lo ? nl : hi;
 }
 
 __global__ void __launch_bounds__(kThreadsI, 3)
-    split_int2_kernel(KvqView v, const void* q, float scale, float* ws) {
-  extern __shared__ __align__(128) unsigned char dyn[];
+    split_int2_kernel(KvqView v, const void* q, float scale, float* ws, const __grid_constant__ CUtensorMap tmc,
+                      const __grid_constant__ CUtensorMap tmk) {
+  extern __shared__ unsigned char dyn_raw[];
+  unsigned char* dyn = dyn_raw + ((1024 - (smem_u32(dyn_raw) & 1023)) & 1023);  // 1024-byte aligned
   SmemI2& sm = *reinterpret_cast<SmemI2*>(dyn);
   int* prefA = reinterpret_cast<int*>(dyn + sizeof(SmemI2));
   int* prefB = prefA + v.batch + 1;
@@ -191,7 +201,7 @@ __global__ void __launch_bounds__(kThreadsI, 3)
     }
     const float4* qps = &sm.qp[warp][0][lane];  // step s at qps[32 * s]
 
-    // O[m]: rows g / g+8, columns 2t / 2t+1 = query head t hi / lo
+    // O[m]: rows g / g+8, columns 2t / 2t+1 = query head t hi / (hi - x)
     float O[8][4];
 #pragma unroll
     for (int m = 0; m < 8; ++m) O[m][0] = O[m][1] = O[m][2] = O[m][3] = 0.f;
@@ -248,20 +258,15 @@ __global__ void __launch_bounds__(kThreadsI, 3)
           mbar_arrive(bar);
           return;
         }
-        const uint8_t* hb = v.pages + (long long)pid * v.page_bytes + head_off;
         const int slot = tok & (v.P - 1);
         const bool gstart = (tok & (G - 1)) == 0;
-        mbar_arrive_expect_tx(bar, kOffKM + (gstart ? kKMeta2 : 0));
+        mbar_arrive_expect_tx(bar, kTileBytesI + (gstart ? kKMeta2 : 0));
         uint8_t* dst = sm.stage[warp][stage];
-        bulk_g2s(dst, hb + slot * kRow2, kTI * kRow2, bar);
-        bulk_g2s(dst + kOffV, hb + v.off_vc + slot * kRow2, kTI * kRow2, bar);
-        bulk_g2s(dst + kOffVM, hb + v.off_vm + slot * kVMetaRow, kTI * kVMetaRow, bar);
+        tma_load_5d(dst + kOffK, &tmc, 0, slot, 0, h, pid, bar);
         if (gstart) {
-          // the group's scales and minima as 8 rows of 32 floats, each padded to kKMPad so
-          // that the four lane quarters read distinct banks
-          const uint8_t* src = hb + v.off_km + (v.P >= G ? slot >> lgG : 0) * kKMeta2;
-#pragma unroll
-          for (int r = 0; r < 8; ++r) bulk_g2s(dst + kOffKM + r * kKMPad * 4, src + r * 128, 128, bar);
+          const long long byte0 = (long long)pid * v.page_bytes + head_off + v.off_km +
+                                  (long long)(v.P >= G ? slot >> lgG : 0) * kKMeta2;
+          tma_load_2d(dst + kOffKM, &tmk, 0, (int)(byte0 >> 7), bar);
         }
       };
       int pf = 0;
@@ -295,15 +300,18 @@ __global__ void __launch_bounds__(kThreadsI, 3)
 
         if ((tok0 & (G - 1)) == 0) {
           // ---- new key group: B = q * s / 4^j and the bias sum_c q_c m_c
-          const float* ks = reinterpret_cast<const float*>(buf + kOffKM);  // [8][kKMPad]
+          // rows r < 4: scales of channels 32r .., rows 4 + r: minima; 16-byte chunk c of row r
+          // sits at chunk c ^ r
+          const uint8_t* ks = buf + kOffKM;
           float bl = 0.f;
 #pragma unroll
           for (int half = 0; half < 2; ++half) {
             float sc[16], mn[16];
 #pragma unroll
             for (int k4 = 0; k4 < 4; ++k4) {
-              const float4 a = reinterpret_cast<const float4*>(ks + kKMPad * t + 16 * half)[k4];
-              const float4 b = reinterpret_cast<const float4*>(ks + kKMPad * (4 + t) + 16 * half)[k4];
+              const int c = 4 * half + k4;
+              const float4 a = *reinterpret_cast<const float4*>(ks + t * 128 + ((c ^ t) << 4));
+              const float4 b = *reinterpret_cast<const float4*>(ks + (4 + t) * 128 + ((c ^ (4 + t)) << 4));
               sc[4 * k4] = a.x; sc[4 * k4 + 1] = a.y; sc[4 * k4 + 2] = a.z; sc[4 * k4 + 3] = a.w;
               mn[4 * k4] = b.x; mn[4 * k4 + 1] = b.y; mn[4 * k4 + 2] = b.z; mn[4 * k4 + 3] = b.w;
             }
@@ -326,8 +334,8 @@ __global__ void __launch_bounds__(kThreadsI, 3)
         }
 
         // ---- QK: rows g / g+8 = tokens g / g+8; codes as f16 subnormals
-        const uint2 w0 = *reinterpret_cast<const uint2*>(buf + g * kRow2 + 8 * t);
-        const uint2 w1 = *reinterpret_cast<const uint2*>(buf + (g + 8) * kRow2 + 8 * t);
+        const uint2 w0 = *reinterpret_cast<const uint2*>(buf + kOffK + g * kRow2 + 8 * t);
+        const uint2 w1 = *reinterpret_cast<const uint2*>(buf + kOffK + (g + 8) * kRow2 + 8 * t);
         const uint32_t u0[2] = {w0.x, w0.y}, u1[2] = {w1.x, w1.y};
         const uint32_t s0[2] = {w0.x >> 8, w0.y >> 8}, s1[2] = {w1.x >> 8, w1.y >> 8};
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
@@ -338,8 +346,8 @@ __global__ void __launch_bounds__(kThreadsI, 3)
           mma_16816(acc, u0[wd] & msk, u1[wd] & msk, s0[wd] & msk, s1[wd] & msk, bk[s][0], bk[s][1]);
         }
         const int nvalid = valid ? min(kTI, it.t1 - tok0) : 0;
-        const float lg0 = g < nvalid ? fmaf(acc[0] + acc[1], kTwo24, bias) : -INFINITY;
-        const float lg1 = g + 8 < nvalid ? fmaf(acc[2] + acc[3], kTwo24, bias) : -INFINITY;
+        const float lg0 = g < nvalid ? fmaf(acc[0] - acc[1], kTwo24, bias) : -INFINITY;
+        const float lg1 = g + 8 < nvalid ? fmaf(acc[2] - acc[3], kTwo24, bias) : -INFINITY;
         float p0, p1;
         softmax(lg0, lg1, p0, p1);
 
@@ -437,8 +445,8 @@ __global__ void __launch_bounds__(kThreadsI, 3)
             mma_16816(accn, anl[0][0], anl[1][0], anl[0][1], anl[1][1], bw[s][0], bw[s][1]);
           }
         }
-        const float lg0 = tok0 + g < T ? (acc[0] + acc[1]) - (accn[0] + accn[1]) : -INFINITY;
-        const float lg1 = tok0 + g + 8 < T ? (acc[2] + acc[3]) - (accn[2] + accn[3]) : -INFINITY;
+        const float lg0 = tok0 + g < T ? (acc[0] - acc[1]) - (accn[0] - accn[1]) : -INFINITY;
+        const float lg1 = tok0 + g + 8 < T ? (acc[2] - acc[3]) - (accn[2] - accn[3]) : -INFINITY;
         float p0, p1;
         softmax(lg0, lg1, p0, p1);
         float2 x01, x89;
@@ -485,10 +493,10 @@ __global__ void __launch_bounds__(kThreadsI, 3)
     const float f2 = it.window ? 1.f : kTwo24 / 16.f, f3 = it.window ? 1.f : kTwo24 / 64.f;
 #pragma unroll
     for (int G4 = 0; G4 < 4; ++G4) {
-      const float4 o4 = make_float4(fmaf(O[2 * G4][0] + O[2 * G4][1], f0, mb[G4]),
-                                    fmaf(O[2 * G4][2] + O[2 * G4][3], f1, mb[G4]),
-                                    fmaf(O[2 * G4 + 1][0] + O[2 * G4 + 1][1], f2, mb[G4]),
-                                    fmaf(O[2 * G4 + 1][2] + O[2 * G4 + 1][3], f3, mb[G4]));
+      const float4 o4 = make_float4(fmaf(O[2 * G4][0] - O[2 * G4][1], f0, mb[G4]),
+                                    fmaf(O[2 * G4][2] - O[2 * G4][3], f1, mb[G4]),
+                                    fmaf(O[2 * G4 + 1][0] - O[2 * G4 + 1][1], f2, mb[G4]),
+                                    fmaf(O[2 * G4 + 1][2] - O[2 * G4 + 1][3], f3, mb[G4]));
       *reinterpret_cast<float4*>(rec + 4 + 32 * G4 + 4 * g) = o4;
     }
     unit = unit_stride0 + (int)__shfl_sync(0xffffffffu, (unsigned)nxt, 0);
@@ -508,23 +516,58 @@ __global__ void __launch_bounds__(kThreadsI, 3)
 
 }  // namespace
 
-bool int2_eligible(const KvqView& v) {
+long long int2_pool_rows(const KvqView& v) { return (long long)v.n_pages * v.page_bytes / 128; }
+
+bool int2_shape_eligible(const KvqView& v) {
   const bool pow2_g = v.kgroup > 0 && (v.kgroup & (v.kgroup - 1)) == 0;
-  return v.D == kD && v.n_rep == kRepI && v.kfmt == KVQ_INT2 && v.kmode == KVQ_ASYM_MINMAX &&
+  // the three per-token sections (K codes, V codes, V meta) share 32-byte rows at a
+  // uniform section stride, and every offset is a multiple of 128 bytes
+  return v.krow == kRow2 && v.vrow == kRow2 && v.v_ng * v.v_nmeta * 4 == kVMetaRow && v.off_vc == v.P * kRow2 &&
+         v.off_vm == 2 * v.P * kRow2 && v.off_km % 128 == 0 && v.head_bytes % 128 == 0 && v.page_bytes % 128 == 0 &&
+         v.D == kD && v.n_rep == kRepI && v.kfmt == KVQ_INT2 && v.kmode == KVQ_ASYM_MINMAX &&
          v.kaxis == KVQ_PER_CHANNEL && v.vfmt == KVQ_INT2 && v.vmode == KVQ_ASYM_MINMAX &&
          v.vaxis == KVQ_PER_TOKEN && v.vgroup == 32 && v.rope_pre == 0 && pow2_g && v.kgroup >= kTI &&
          v.P >= kTI && (v.P & (v.P - 1)) == 0 && v.batch <= 4096;
 }
 
+bool int2_eligible(const KvqView& v) {
+  return int2_shape_eligible(v) && (reinterpret_cast<uintptr_t>(v.pages) & 15) == 0 && int2_pool_rows(v) > 0 &&
+         int2_pool_rows(v) < (1LL << 31) && v.n_pages < (1 << 30) && tensor_map_encoder() != nullptr;
+}
+
 kvq_status launch_int2(const KvqView& v, const void* q, float* out, float scale, void* ws, cudaStream_t st) {
-  const size_t smem = sizeof(SmemI2) + sizeof(int) * 3 * (v.batch + 1);
+  // the per-token sections as a 5-D tensor (row bytes, slot, section, head, page), one tile per box
+  CUtensorMap tmc, tmk;
+  {
+    const cuuint64_t dims[5] = {(cuuint64_t)kRow2, (cuuint64_t)v.P, 3, (cuuint64_t)v.Hkv, (cuuint64_t)v.n_pages};
+    const cuuint64_t strides[4] = {(cuuint64_t)kRow2, (cuuint64_t)v.P * kRow2, (cuuint64_t)v.head_bytes,
+                                   (cuuint64_t)v.page_bytes};
+    const cuuint32_t box[5] = {(cuuint32_t)kRow2, (cuuint32_t)kTI, 3, 1, 1};
+    const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    if (tensor_map_encoder()(&tmc, CU_TENSOR_MAP_DATA_TYPE_UINT8, 5, v.pages, dims, strides, box, estr,
+                             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return KVQ_ERR_UNSUPPORTED;
+  }
+  {
+    // the pool as rows of 128 bytes: a key group's scales and minima are 8 rows
+    const cuuint64_t dims[2] = {128, (cuuint64_t)int2_pool_rows(v)};
+    const cuuint64_t strides[1] = {128};
+    const cuuint32_t box[2] = {128, 8};
+    const cuuint32_t estr[2] = {1, 1};
+    if (tensor_map_encoder()(&tmk, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, v.pages, dims, strides, box, estr,
+                             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return KVQ_ERR_UNSUPPORTED;
+  }
+  const size_t smem = sizeof(SmemI2) + 1024 + sizeof(int) * 3 * (v.batch + 1);
   static int occ_cache[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64) return KVQ_ERR_UNSUPPORTED;
   if (!occ_cache[dev]) {
     if (cudaFuncSetAttribute(split_int2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)(sizeof(SmemI2) + sizeof(int) * 3 * 4097)) != cudaSuccess)
+                             (int)(sizeof(SmemI2) + 1024 + sizeof(int) * 3 * 4097)) != cudaSuccess)
       return KVQ_ERR_CUDA;
     int occ = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, split_int2_kernel, kThreadsI, smem) != cudaSuccess)
@@ -534,7 +577,7 @@ kvq_status launch_int2(const KvqView& v, const void* q, float* out, float scale,
   const int grid = num_sms() * occ_cache[dev];
   if (cudaMemsetAsync(static_cast<char*>(ws) + fast_counter_offset(v.batch), 0, 8, st) != cudaSuccess)
     return KVQ_ERR_CUDA;
-  split_int2_kernel<<<grid, kThreadsI, smem, st>>>(v, q, scale, static_cast<float*>(ws));
+  split_int2_kernel<<<grid, kThreadsI, smem, st>>>(v, q, scale, static_cast<float*>(ws), tmc, tmk);
   if (cudaGetLastError() != cudaSuccess) return KVQ_ERR_CUDA;
   return launch_split_combine(v, static_cast<float*>(ws), out, st) == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }

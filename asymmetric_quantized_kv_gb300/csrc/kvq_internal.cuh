@@ -66,7 +66,8 @@ bool fp8_shape_eligible(const KvqView& v);  // config only: sizes the workspace
 bool fp8_eligible(const KvqView& v);        // config, cache pointers and pool size
 kvq_status launch_fp8(const KvqView& v, const void* q, float* out, float scale, void* ws, cudaStream_t st);
 // Tensor-core decode kernel for 2-bit asymmetric per-channel keys + per-token values (g = 32).
-bool int2_eligible(const KvqView& v);
+bool int2_shape_eligible(const KvqView& v);  // config only: sizes the workspace
+bool int2_eligible(const KvqView& v);        // config, cache pointers and pool size
 kvq_status launch_int2(const KvqView& v, const void* q, float* out, float scale, void* ws, cudaStream_t st);
 kvq_status launch_attention(const KvqView& v, const void* q, float* out, float scale,
                             void* ws, size_t ws_bytes, cudaStream_t st);
