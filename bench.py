@@ -281,11 +281,7 @@ def build_cache(spec, device, extra_tokens, gen_seed=1):
         bt[b, :need[b]] = perm[o:o + need[b]]
         o += need[b]
     cache = K.PagedKVCache(cfg, Bn, maxp, n_pages, bt, device=device)
-    scale = torch.ones(H, D, device=device)
-    for h in range(H):
-        ch, f = W.outliers(w, 0, h)
-        if len(ch):
-            scale[h, torch.as_tensor(ch, device=device)] = torch.as_tensor(f, device=device)
+    scale = W.torch_outlier_scale(w, device)
     g = torch.Generator(device=device)
     g.manual_seed(gen_seed)
     chunk = 4096 if Bn * H * D * 4096 * 2 < (1 << 31) else 1024
@@ -296,8 +292,7 @@ def build_cache(spec, device, extra_tokens, gen_seed=1):
         done = 0
         while done < max(lens):
             n = min(chunk, max(lens) - done)
-            kk = (torch.randn(Bn, n, H, D, generator=g, device=device) * scale).to(torch.bfloat16)
-            vv = torch.randn(Bn, n, H, D, generator=g, device=device).to(torch.bfloat16)
+            kk, vv = W.torch_kv_chunk(w, g, Bn, n, scale, device)
             kk = kk.transpose(0, 1).reshape(-1, H, D)
             vv = vv.transpose(0, 1).reshape(-1, H, D)
             tmp = torch.empty(H, device=device)
@@ -313,8 +308,7 @@ def build_cache(spec, device, extra_tokens, gen_seed=1):
     while done < max(lens):
         n = min(chunk, max(lens) - done)
         per = torch.tensor([max(0, min(n, T - done)) for T in lens], dtype=torch.int32, device=device)
-        kk = (torch.randn(Bn, n, H, D, generator=g, device=device) * scale).to(torch.bfloat16)
-        vv = torch.randn(Bn, n, H, D, generator=g, device=device).to(torch.bfloat16)
+        kk, vv = W.torch_kv_chunk(w, g, Bn, n, scale, device)
         cache.append(kk, vv, per)
         done += n
     torch.cuda.synchronize(device)

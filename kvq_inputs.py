@@ -177,3 +177,29 @@ def small_stream(seed: int, T: int, D: int, outlier_ch=(), factor=1.0, bf16=Fals
     if bf16:
         x = bf16_round(x)[1]
     return x
+
+
+# ---------------------------------------------------------------- device-side draws
+
+def torch_outlier_scale(w: Workload, device):
+    """[Hkv, D] float32 torch tensor: 1 except the K outlier channels of each
+    kv-head, which hold their factors (outliers() of sequence 0: the random
+    channels are per kv-head and shared by all sequences)."""
+    import torch
+    scale = torch.ones(w.num_kv_heads, w.head_dim, device=device)
+    for h in range(w.num_kv_heads):
+        ch, f = outliers(w, 0, h)
+        if len(ch):
+            scale[h, torch.as_tensor(ch, device=device)] = torch.as_tensor(f, device=device)
+    return scale
+
+
+def torch_kv_chunk(w: Workload, gen, batch: int, n: int, scale, device):
+    """The next n tokens of every stream as bf16 torch tensors [batch, n, Hkv, D]:
+    K ~ N(0,1) times the outlier scale, V ~ N(0,1), drawn from the seeded torch
+    generator `gen` (large workloads are generated on the device this way)."""
+    import torch
+    H, D = w.num_kv_heads, w.head_dim
+    k = (torch.randn(batch, n, H, D, generator=gen, device=device) * scale).to(torch.bfloat16)
+    v = torch.randn(batch, n, H, D, generator=gen, device=device).to(torch.bfloat16)
+    return k, v

@@ -163,3 +163,102 @@ class Case:
         assert worst <= tol, f"attention rel L2 {worst:.3e} > {tol}"
         assert int(self.cache.status.item()) == 0
         return worst
+
+
+class FullCase:
+    """A benchmark-sized workload (configs 3, 4, 5 of bench.py) filled through the
+    library from seeded device-side draws, exactly as bench.py fills it, with
+    host copies of the sampled (sequence, kv-head) source streams.  Static FP8
+    scales are fl32(absmax / 448) with the absmax taken by torch, so the oracle
+    and the library quantize with the same scale without the library computing it."""
+
+    def __init__(self, cid, samples, gen_seed=1):
+        import bench
+        import asymmetric_quantized_kv_gb300 as K
+        spec = bench.workload_spec(cid)
+        w = spec["w"]
+        self.spec, self.w = spec, w
+        Bn, H, D, Hq = w.batch, w.num_kv_heads, w.head_dim, w.num_q_heads
+        self.lens = [int(x) for x in W.lengths(w)]
+        P = spec["P"]
+        self.cfg = O.Config(Hq, H, D, O.QSpec(*spec["k"]), O.QSpec(*spec["v"]), spec["R"], P, spec["rope"],
+                            spec["theta"], O.BF16)
+        need = [(T + P - 1) // P for T in self.lens]
+        maxp, n_pages = max(need), sum(need)
+        perm = W.page_permutation(n_pages, 5)
+        bt = np.zeros((Bn, maxp), np.int32)
+        o = 0
+        for b in range(Bn):
+            bt[b, :need[b]] = perm[o:o + need[b]]
+            o += need[b]
+        self.cache = K.PagedKVCache(to_c(self.cfg), Bn, maxp, n_pages, bt)
+        dev = torch.device("cuda")
+        scale = W.torch_outlier_scale(w, dev)
+        g = torch.Generator(device=dev)
+        g.manual_seed(gen_seed)
+        chunk = 4096 if Bn * H * D * 4096 * 2 < (1 << 31) else 1024
+        T_max = max(self.lens)
+        self.k_scale = [0.0] * H
+        self.v_scale = [0.0] * H
+        if self.cfg.k.fmt == O.FP8_E4M3:
+            state = g.get_state()
+            kmax = torch.zeros(H, device=dev)
+            vmax = torch.zeros(H, device=dev)
+            done = 0
+            while done < T_max:
+                n = min(chunk, T_max - done)
+                kk, vv = W.torch_kv_chunk(w, g, Bn, n, scale, dev)
+                kmax = torch.maximum(kmax, kk.float().abs().amax(dim=(0, 1, 3)))
+                vmax = torch.maximum(vmax, vv.float().abs().amax(dim=(0, 1, 3)))
+                done += n
+            self.k_scale = [float(O.fl32(a / 448.0)) for a in kmax.double().cpu().tolist()]
+            self.v_scale = [float(O.fl32(a / 448.0)) for a in vmax.double().cpu().tolist()]
+            self.cache.k_scale.copy_(torch.tensor(self.k_scale, dtype=torch.float32))
+            self.cache.v_scale.copy_(torch.tensor(self.v_scale, dtype=torch.float32))
+            g.set_state(state)
+        self.samples = list(samples)
+        parts = {s: ([], []) for s in self.samples}
+        done = 0
+        while done < T_max:
+            n = min(chunk, T_max - done)
+            take = [max(0, min(n, T - done)) for T in self.lens]
+            kk, vv = W.torch_kv_chunk(w, g, Bn, n, scale, dev)
+            self.cache.append(kk, vv, torch.tensor(take, dtype=torch.int32, device=dev))
+            for (b, h) in self.samples:
+                if take[b]:
+                    parts[(b, h)][0].append(kk[b, :take[b], h].float().cpu().numpy())
+                    parts[(b, h)][1].append(vv[b, :take[b], h].float().cpu().numpy())
+            done += n
+        torch.cuda.synchronize()
+        self.streams = {s: (np.concatenate(k), np.concatenate(v)) for s, (k, v) in parts.items()}
+        self.q = torch.randn(Bn, Hq, D, generator=g, device=dev).to(torch.bfloat16)
+
+    def state(self, b, h):
+        K_, V_ = self.streams[(b, h)]
+        return O.quantize_stream(self.cfg, K_, V_, self.k_scale[h], self.v_scale[h])
+
+    def check_attention(self, tol=ATT_TOL):
+        out = self.cache.attention(self.q).cpu().numpy().astype(np.float64)
+        q = self.q.float().cpu().numpy().astype(np.float64)
+        n_rep = self.cfg.n_rep
+        worst = 0.0
+        for (b, h) in self.samples:
+            heads = slice(h * n_rep, (h + 1) * n_rep)
+            ref = O.decode_head(self.cfg, self.state(b, h), q[b, heads], self.k_scale[h], self.v_scale[h])
+            err = np.linalg.norm(out[b, heads] - ref, axis=1) / np.linalg.norm(ref, axis=1)
+            worst = max(worst, float(err.max()))
+        assert worst <= tol, f"attention rel L2 {worst:.3e} > {tol}"
+        assert int(self.cache.status.item()) == 0
+        return worst
+
+    def check_dequantize(self, span=2048):
+        """Bit-exact kvq_dequantize against the oracle on the first, a middle and
+        the last `span` tokens of each sampled stream."""
+        for (b, h) in self.samples:
+            T = self.lens[b]
+            ko, vo = O.dequantize_stream(self.cfg, self.state(b, h), self.k_scale[h], self.v_scale[h])
+            for t0 in sorted({0, max(0, T // 2 - span // 2), max(0, T - span)}):
+                t1 = min(T, t0 + span)
+                k, v = self.cache.dequantize(b, t0, t1)
+                assert np.array_equal(k[:, h].cpu().numpy().astype(np.float64), ko[t0:t1]), (b, h, t0)
+                assert np.array_equal(v[:, h].cpu().numpy().astype(np.float64), vo[t0:t1]), (b, h, t0)

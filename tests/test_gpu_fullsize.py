@@ -1,0 +1,33 @@
+"""Parity at the benchmark's full sizes, in the launch configuration bench.py
+times: the caches of configs 3, 4 and 5 are filled through the library from the
+same seeded device-side draws as the benchmark, and sampled (sequence, kv-head)
+streams are checked against the oracle: attention within 1e-3 relative L2 per
+query head, kvq_dequantize bit-exact on three token windows per stream."""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+import kvq_inputs as W  # noqa: E402
+
+if not torch.cuda.is_available():  # pragma: no cover
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+from kvq_testlib import FullCase  # noqa: E402
+
+
+def _samples(cid):
+    w = W.WORKLOADS[cid]
+    lens = W.lengths(w)
+    b_long, b_short = int(np.argmax(lens)), int(np.argmin(lens))
+    return [(b_long, 0), (b_short, w.num_kv_heads - 1), ((b_long + 1) % w.batch, 3)]
+
+
+@pytest.mark.parametrize("cid", [3, 4, 5])
+def test_fullsize_sampled_streams(cid):
+    case = FullCase(cid, _samples(cid))
+    case.check_attention()
+    case.check_dequantize()
+    del case
+    torch.cuda.empty_cache()
