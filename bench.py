@@ -45,10 +45,17 @@ SYM, ASYM = 0, 1
 TEN, TOK, CH = 0, 1, 2
 BF16 = 1
 
-# kernels this library launches per call (append: quantize + advance lengths;
+# kernels this library launches per call (append: fold + window/lengths;
 # attention: split-K + combine)
 LAUNCHES_APPEND = 2
 LAUNCHES_ATTENTION = 2
+
+# DRAM bytes (read + write) of one full-size split-kernel launch, from one ncu
+# capture of a smaller case of the same kernel scaled by algorithmic bytes
+# (profiles/split_rope_i8i4_paged_ragged_b16.md, split_fp8_70b_layer_b2.md,
+# split_int2_8b_layer_b8.md); to be re-captured whenever that kernel changes.
+SPLIT_TRAFFIC = {5: 1819.4e6, 4: 2268.8e6, 3: 573.0e6}
+SPLIT_KERNEL = {5: "split_rope_i8i4_kernel", 4: "split_fp8_kernel", 3: "split_int2_kernel"}
 
 
 def workload_spec(cid: int, batch: int = 0) -> dict:
@@ -507,7 +514,8 @@ def main():
                    "l2": "inputs (%.2f GB per step) larger than the 129 MB L2; no flush" % (att_bytes / 1e9)},
         "pct_of_hbm_peak": 100.0 * value / peak,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": None, "kernel": "kvq_decode_attention (split-K kernel + combine)",
+                     "traffic": SPLIT_TRAFFIC.get(args.config) if not args.batch else None,
+                     "kernel": f"kvq_decode_attention: {SPLIT_KERNEL[args.config]} + combine (timed together)",
                      "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)" if peak_kind == "measured"
                      else "fallback 6.8 TB/s", "us_per_launch": att_ms * 1e3,
                      "bytes_per_launch": att_bytes},
