@@ -210,6 +210,26 @@ def cpu_oracle_throughput(cid: int, n_streams: int, steps: int = 1):
                        f"{busy:.1f} s CPU, {wall:.1f} s wall")
 
 
+# ------------------------------------------------------------------ ranks
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The largest of every rank's x (the job's time is its slowest rank's);
+    identity for one rank.  `device`: where the process group's tensors live
+    (the GPU for NCCL, the CPU for gloo)."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(bytes_per_rank: float, world: int, elapsed_ms: float) -> float:
+    """Whole-job GB/s: every replica moves the same bytes in the slowest rank's time."""
+    return bytes_per_rank * world / (elapsed_ms / 1e3) / 1e9
+
+
 # ------------------------------------------------------------------ GPU leg
 
 class ClockSampler:
@@ -385,10 +405,7 @@ def run_gpu(args, spec, rank, world):
     torch.cuda.synchronize(device)
     elapsed_ms = ev0.elapsed_time(ev1)
     clock_info = clocks.stop()
-    if world > 1:
-        t = torch.tensor([elapsed_ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(elapsed_ms, world, device)
     att_ms = [a.elapsed_time(b) for a, b in att_ev]
     status = int(cache.status.item())
     # end to end through the public API: pinned host inputs in, result out, every step
@@ -432,12 +449,9 @@ def run_gpu(args, spec, rank, world):
         e1.record(stream)
         torch.cuda.synchronize(device)
         e_ms = e0.elapsed_time(e1)
-        if world > 1:
-            t = torch.tensor([e_ms], device=device)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e_ms = float(t.item())
+        e_ms = max_over_ranks(e_ms, world, device)
         h2d = dq.numel() * dq.element_size() + (2 * dk.numel() * dk.element_size() if do_append else 0)
-        e2e = {"value": e2e_bytes * world / (e_ms / 1e3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+        e2e = {"value": job_throughput(e2e_bytes, world, e_ms), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": out.numel() * out.element_size(), "ms_per_step": e_ms / steps}
     return dict(elapsed_ms=elapsed_ms, step_bytes=step_bytes, att_bytes=att_bytes, att_ms=att_ms,
                 clocks=clock_info, status=status, e2e=e2e, lens=cur)
@@ -498,8 +512,7 @@ def main():
         return
     steps = args.steps
     ms_per_step = r["elapsed_ms"] / steps
-    total_bytes = sum(r["step_bytes"]) * world
-    value = total_bytes / (r["elapsed_ms"] / 1e3) / 1e9
+    value = job_throughput(sum(r["step_bytes"]), world, r["elapsed_ms"])
     peak, peak_kind = load_peaks()
     att_ms = statistics.mean(r["att_ms"])
     att_bytes = statistics.mean(r["att_bytes"])
