@@ -10,7 +10,7 @@ namespace kvq {
 namespace {
 
 constexpr int kD = 128;
-constexpr int kFastTarget = 1536;
+constexpr int kFastTarget = 1024;
 constexpr int kFastMinChunk = 256;
 
 struct FastItem {
