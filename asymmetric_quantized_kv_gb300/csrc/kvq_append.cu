@@ -279,23 +279,216 @@ __device__ void stage_block(const KvqView& v, const AppendCtx& a, const void* k_
   const int row = v.D * (v.src_bf16 ? 2 : 4);
   const int per_row = row / 16;
   const int n = 2 * count * per_row;
-  for (int e = threadIdx.x; e < n; e += kThreads) {
-    const int tensor = e / (count * per_row);
-    const int rem = e % (count * per_row);
-    const int r = rem / per_row, k = rem % per_row;
-    const int t = t_begin + r;
-    const unsigned char* src;
-    if (t < a.T0) {
-      const long long i = (((long long)a.b * v.R + (t - a.wbase)) * v.Hkv + a.h) * row;
-      src = static_cast<const unsigned char*>(tensor ? v.v_win : v.k_win) + i;
-    } else {
-      const long long i = (((long long)a.b * a.n_stride + (t - a.T0)) * v.Hkv + a.h) * row;
-      src = static_cast<const unsigned char*>(tensor ? v_new : k_new) + i;
+  constexpr int kBatch = 8;  // loads in flight per thread before the shared-memory stores
+  for (int e0 = 0; e0 < n; e0 += kBatch * kThreads) {
+    uint4 val[kBatch];
+    int off[kBatch];
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      const int e = e0 + j * kThreads + threadIdx.x;
+      off[j] = -1;
+      if (e < n) {
+        const int tensor = e / (count * per_row);
+        const int rem = e - tensor * count * per_row;
+        const int r = rem / per_row, k = rem - r * per_row;
+        const int t = t_begin + r;
+        const unsigned char* src;
+        if (t < a.T0) {
+          const long long i = (((long long)a.b * v.R + (t - a.wbase)) * v.Hkv + a.h) * row;
+          src = static_cast<const unsigned char*>(tensor ? v.v_win : v.k_win) + i;
+        } else {
+          const long long i = (((long long)a.b * a.n_stride + (t - a.T0)) * v.Hkv + a.h) * row;
+          src = static_cast<const unsigned char*>(tensor ? v_new : k_new) + i;
+        }
+        val[j] = reinterpret_cast<const uint4*>(src)[k];
+        off[j] = tensor * count * row + r * row + 16 * k;
+      }
     }
-    reinterpret_cast<uint4*>(dst + (long long)tensor * count * row + r * row)[k] =
-        reinterpret_cast<const uint4*>(src)[k];
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j)
+      if (off[j] >= 0) *reinterpret_cast<uint4*>(dst + off[j]) = val[j];
   }
   __syncthreads();
+}
+
+// ---- parallel fold of one staged R-token block of one kv-head (R <= kMaxFold)
+//
+// The block's K rows then V rows sit in shared memory in the source dtype.  All
+// tokens are handled at once: page addresses first, then each key group's
+// per-channel scales, then every 32-bit code word by one thread (keys) or each
+// token row by one warp (values and per-token keys), packed in registers and
+// stored straight into the page.  Every scale and code comes from the same
+// helpers as the sub-chunk path, so the bytes are identical.
+constexpr int kMaxFold = 256;
+
+struct FoldSmem {
+  uint8_t* rowp[kMaxFold];  // head block of each token of the block (nullptr: bad page)
+  int rslot[kMaxFold];      // its slot within the page
+  float cmin[kThreads], cmax[kThreads];
+  float ch_s[kMaxD], ch_r[kMaxD], ch_m[kMaxD];
+};
+
+__device__ __forceinline__ float staged_value(const unsigned char* rows, int t, int c, int D, int bf16) {
+  return load_src(rows, (long long)t * D + c, bf16);
+}
+
+// Per-token (groups of q.group channels), per-tensor or FP8 rows: warp per token.
+__device__ void fold_rows(const KvqView& v, const TQ& q, const unsigned char* rows, FoldSmem& fs, int R) {
+  const int D = v.D, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int cpl = D >> 5;                         // channels per lane (2, 4 or 8)
+  const int lane_bits = cpl * q.bits;             // 8 .. 64
+  const float ss = (q.axis == KVQ_PER_TENSOR || q.fmt == KVQ_FP8_E4M3) ? q.static_scale[0] : 0.f;
+  const float sr = ss > 0.f ? __frcp_rn(ss) : 0.f;
+#pragma unroll 2
+  for (int t = warp; t < R; t += kThreads / 32) {
+    float x[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) x[i] = i < cpl ? staged_value(rows, t, lane * cpl + i, D, v.src_bf16) : 0.f;
+    float gs = ss, gr = sr, gm = 0.f;
+    if (q.axis == KVQ_PER_TOKEN && q.fmt != KVQ_FP8_E4M3) {
+      const int lpg = q.group / cpl;  // lanes per group (g >= 16 >= cpl)
+      float mn = INFINITY, mx = -INFINITY, am = 0.f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (i < cpl) {
+          mn = fminf(mn, x[i]);
+          mx = fmaxf(mx, x[i]);
+          am = fmaxf(am, fabsf(x[i]));
+        }
+      for (int o = 1; o < lpg && o < 32; o <<= 1) {
+        mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+      }
+      if (q.mode == KVQ_ASYM_MINMAX) {
+        gs = asym_scale(mn, mx, q.bits);
+        gm = mn;
+      } else {
+        gs = sym_scale(am, q.bits);
+      }
+      gr = gs > 0.f ? __frcp_rn(gs) : 0.f;
+      const int grp = (lane * cpl) / q.group;
+      uint8_t* hb = fs.rowp[t];
+      if (hb && (lane % lpg) == 0) {
+        float* meta = reinterpret_cast<float*>(hb + q.off_meta + fs.rslot[t] * q.ng * q.nmeta * 4);
+        meta[grp] = gs;
+        if (q.nmeta == 2) meta[q.ng + grp] = gm;
+      }
+    }
+    // this lane's codes, packed little-endian
+    unsigned long long bits = 0ull;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      if (i < cpl) {
+        unsigned u;
+        if (q.fmt == KVQ_FP8_E4M3) {
+          u = fp8_code(x[i], ss);
+        } else if (q.axis == KVQ_PER_TENSOR) {
+          u = stored_code(sym_code_r(x[i], ss, sr, q.bits), q.bits, KVQ_SYM_ABSMAX);
+        } else {
+          const int code = q.mode == KVQ_ASYM_MINMAX ? asym_code_r(x[i], gm, gs, gr, q.bits)
+                                                     : sym_code_r(x[i], gs, gr, q.bits);
+          u = stored_code(code, q.bits, q.mode);
+        }
+        bits |= (unsigned long long)u << (i * q.bits);
+      }
+    }
+    uint8_t* hb = fs.rowp[t];
+    uint32_t* dst = hb ? reinterpret_cast<uint32_t*>(hb + q.off_codes + fs.rslot[t] * q.row) : nullptr;
+    if (lane_bits >= 32) {
+      const int wpl = lane_bits >> 5;  // words per lane (1 or 2)
+      if (dst) {
+        dst[lane * wpl] = (uint32_t)bits;
+        if (wpl == 2) dst[lane * wpl + 1] = (uint32_t)(bits >> 32);
+      }
+    } else {
+      const int lpw = 32 / lane_bits;  // lanes per word (2 or 4)
+      uint32_t w = (uint32_t)bits << ((lane % lpw) * lane_bits);
+      for (int o = 1; o < lpw; o <<= 1) w |= __shfl_xor_sync(0xffffffffu, w, o);
+      if (dst && lane % lpw == 0) dst[lane / lpw] = w;
+    }
+  }
+}
+
+// Keys per channel over groups of G tokens of the block.
+__device__ void fold_key_channels(const KvqView& v, const TQ& q, const AppendCtx& a, const unsigned char* rows,
+                                  FoldSmem& fs, int tb, int R) {
+  const int D = v.D, G = q.group;
+  const int parts = kThreads / D;  // threads per channel for the scans (1, 2 or 4)
+  const int c = threadIdx.x % D, part = threadIdx.x / D;
+  const int cpw = 32 / q.bits, wpr = q.row >> 2;
+  for (int g0 = 0; g0 < R; g0 += G) {
+    float mn = INFINITY, mx = -INFINITY;
+    for (int t = g0 + part; t < g0 + G; t += parts) {
+      const float x = staged_value(rows, t, c, D, v.src_bf16);
+      mn = fminf(mn, x);
+      mx = fmaxf(mx, x);
+    }
+    fs.cmin[threadIdx.x] = mn;
+    fs.cmax[threadIdx.x] = mx;
+    __syncthreads();
+    if (threadIdx.x < D) {
+      for (int p = 1; p < parts; ++p) {
+        mn = fminf(mn, fs.cmin[p * D + c]);
+        mx = fmaxf(mx, fs.cmax[p * D + c]);
+      }
+      float sc;
+      if (q.mode == KVQ_ASYM_MINMAX) {
+        sc = asym_scale(mn, mx, q.bits);
+      } else {
+        sc = sym_scale(fmaxf(fabsf(mn), fabsf(mx)), q.bits);
+        mn = 0.f;
+      }
+      fs.ch_s[c] = sc;
+      fs.ch_r[c] = sc > 0.f ? __frcp_rn(sc) : 0.f;
+      fs.ch_m[c] = mn;
+      uint8_t* hb0 = fs.rowp[g0];  // head block of the page holding the group's first token
+      if (hb0) {
+        const int slot = ((tb + g0) % v.P) / G;
+        float* meta = reinterpret_cast<float*>(hb0 + q.off_meta + (long long)slot * D * q.nmeta * 4);
+        meta[c] = sc;
+        if (q.nmeta == 2) meta[D + c] = mn;
+      }
+    }
+    __syncthreads();
+    // one 32-bit code word per thread iteration
+    for (int w = threadIdx.x; w < G * wpr; w += kThreads) {
+      const int t = g0 + w / wpr, k = w % wpr;
+      uint32_t word = 0u;
+      for (int i = 0; i < cpw; ++i) {
+        const int cc = k * cpw + i;
+        const float x = staged_value(rows, t, cc, D, v.src_bf16);
+        const int code = q.mode == KVQ_ASYM_MINMAX ? asym_code_r(x, fs.ch_m[cc], fs.ch_s[cc], fs.ch_r[cc], q.bits)
+                                                   : sym_code_r(x, fs.ch_s[cc], fs.ch_r[cc], q.bits);
+        word |= stored_code(code, q.bits, q.mode) << (i * q.bits);
+      }
+      uint8_t* hb = fs.rowp[t];
+      if (hb) reinterpret_cast<uint32_t*>(hb + q.off_codes + fs.rslot[t] * q.row)[k] = word;
+    }
+    __syncthreads();
+  }
+}
+
+__device__ void fold_staged(const KvqView& v, const AppendCtx& a, const unsigned char* staged, int tb) {
+  __shared__ FoldSmem fs;
+  const int R = v.R;
+  if (threadIdx.x < R) {
+    const int t = tb + threadIdx.x;
+    uint8_t* page = page_of(v, a.b, t);
+    fs.rowp[threadIdx.x] = page ? page + (long long)a.h * v.head_bytes : nullptr;
+    fs.rslot[threadIdx.x] = t % v.P;
+  }
+  __syncthreads();
+  const int row = v.D * (v.src_bf16 ? 2 : 4);
+  TQ kq = key_q(v), vq = value_q(v);
+  kq.static_scale = v.k_scale + a.h;
+  vq.static_scale = v.v_scale + a.h;
+  if (kq.axis == KVQ_PER_CHANNEL) {
+    fold_key_channels(v, kq, a, staged, fs, tb, R);
+  } else {
+    fold_rows(v, kq, staged, fs, R);
+  }
+  fold_rows(v, vq, staged + (long long)R * row, fs, R);
 }
 
 __global__ void __launch_bounds__(kThreads) append_kernel(KvqView v, const void* k_new,
@@ -329,10 +522,14 @@ __global__ void __launch_bounds__(kThreads) append_kernel(KvqView v, const void*
         // the whole R-token block fits in shared memory: one parallel pass of loads,
         // then every quantizer pass reads shared memory
         stage_block(v, a, k_new, v_new, tb, v.R, staged);
-        a.st_t0 = tb;
-        const int row = v.D * (v.src_bf16 ? 2 : 4);
-        const Src kss{v.k_win, k_new, staged}, vss{v.v_win, v_new, staged + (long long)v.R * row};
-        quantize_block(v, kss, vss, a, sm, tb, v.R);
+        if (v.R <= kMaxFold) {
+          fold_staged(v, a, staged, tb);
+        } else {
+          a.st_t0 = tb;
+          const int row = v.D * (v.src_bf16 ? 2 : 4);
+          const Src kss{v.k_win, k_new, staged}, vss{v.v_win, v_new, staged + (long long)v.R * row};
+          quantize_block(v, kss, vss, a, sm, tb, v.R);
+        }
       } else {
         quantize_block(v, ks, vs, a, sm, tb, v.R);
       }
@@ -359,12 +556,29 @@ __global__ void __launch_bounds__(kThreads) window_lengths_kernel(KvqView v, con
     const int base = (T1 / v.R) * v.R;
     const int t_lo = max(base, T0);
     const int row = v.Hkv * v.D;  // elements of one token (all heads)
-    for (int e = threadIdx.x; e < (T1 - t_lo) * row; e += kThreads) {
-      const int t = t_lo + e / row, c = e % row;
-      const long long si = ((long long)b * n_stride + (t - T0)) * row + c;
-      const long long di = ((long long)b * v.R + (t - base)) * row + c;
-      store_src(v.k_win, di, load_src(k_new, si, v.src_bf16), v.src_bf16);
-      store_src(v.v_win, di, load_src(v_new, si, v.src_bf16), v.src_bf16);
+    const int esz = v.src_bf16 ? 2 : 4;
+    const uintptr_t al = reinterpret_cast<uintptr_t>(k_new) | reinterpret_cast<uintptr_t>(v_new) |
+                         reinterpret_cast<uintptr_t>(v.k_win) | reinterpret_cast<uintptr_t>(v.v_win);
+    if ((al & 15) == 0 && (row * esz) % 16 == 0) {
+      // 16-byte chunks: a token's row of all heads is contiguous in both tensors
+      const int cpr = row * esz / 16;
+      for (int e = threadIdx.x; e < (T1 - t_lo) * cpr; e += kThreads) {
+        const int t = t_lo + e / cpr, k = e % cpr;
+        const long long si = ((long long)b * n_stride + (t - T0)) * cpr + k;
+        const long long di = ((long long)b * v.R + (t - base)) * cpr + k;
+        const uint4 kx = reinterpret_cast<const uint4*>(k_new)[si];
+        const uint4 vx = reinterpret_cast<const uint4*>(v_new)[si];
+        reinterpret_cast<uint4*>(v.k_win)[di] = kx;
+        reinterpret_cast<uint4*>(v.v_win)[di] = vx;
+      }
+    } else {
+      for (int e = threadIdx.x; e < (T1 - t_lo) * row; e += kThreads) {
+        const int t = t_lo + e / row, c = e % row;
+        const long long si = ((long long)b * n_stride + (t - T0)) * row + c;
+        const long long di = ((long long)b * v.R + (t - base)) * row + c;
+        store_src(v.k_win, di, load_src(k_new, si, v.src_bf16), v.src_bf16);
+        store_src(v.v_win, di, load_src(v_new, si, v.src_bf16), v.src_bf16);
+      }
     }
   }
   __syncthreads();
