@@ -19,6 +19,7 @@ namespace kvq {
 namespace {
 
 constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
 constexpr int kSub = 16;        // tokens staged per sub-chunk
 constexpr int kUnitTok = 64;    // tokens per CTA when R == 0
 constexpr int kMaxD = 256;
@@ -273,24 +274,26 @@ __device__ void quantize_block(const KvqView& v, const Src& ks, const Src& vs, c
 }
 
 // Copy the source rows (window or new tokens) of tokens [t_begin, t_begin + count)
-// of one head into shared memory with 16-byte loads, K rows then V rows.
+// of one head into shared memory with 16-byte loads, K rows then V rows.  `between`
+// runs once, after the first batch of loads has been issued and before any of them
+// is consumed, so the global reads it makes overlap theirs.
+template <typename Between>
 __device__ void stage_block(const KvqView& v, const AppendCtx& a, const void* k_new, const void* v_new,
-                            int t_begin, int count, unsigned char* dst) {
+                            int t_begin, int count, unsigned char* dst, Between&& between) {
   const int row = v.D * (v.src_bf16 ? 2 : 4);
-  const int per_row = row / 16;
-  const int n = 2 * count * per_row;
+  const int lp = log2i(row >> 4);  // 16-byte pieces per row: 2^lp
+  const int per_tensor = count << lp;
+  const int n = 2 * per_tensor;
   constexpr int kBatch = 8;  // loads in flight per thread before the shared-memory stores
   for (int e0 = 0; e0 < n; e0 += kBatch * kThreads) {
     uint4 val[kBatch];
-    int off[kBatch];
 #pragma unroll
     for (int j = 0; j < kBatch; ++j) {
       const int e = e0 + j * kThreads + threadIdx.x;
-      off[j] = -1;
       if (e < n) {
-        const int tensor = e / (count * per_row);
-        const int rem = e - tensor * count * per_row;
-        const int r = rem / per_row, k = rem - r * per_row;
+        const int tensor = e >= per_tensor;
+        const int rem = tensor ? e - per_tensor : e;
+        const int r = rem >> lp, k = rem & ((1 << lp) - 1);
         const int t = t_begin + r;
         const unsigned char* src;
         if (t < a.T0) {
@@ -301,25 +304,31 @@ __device__ void stage_block(const KvqView& v, const AppendCtx& a, const void* k_
           src = static_cast<const unsigned char*>(tensor ? v_new : k_new) + i;
         }
         val[j] = reinterpret_cast<const uint4*>(src)[k];
-        off[j] = tensor * count * row + r * row + 16 * k;
       }
     }
+    if (e0 == 0) between();
 #pragma unroll
-    for (int j = 0; j < kBatch; ++j)
-      if (off[j] >= 0) *reinterpret_cast<uint4*>(dst + off[j]) = val[j];
+    for (int j = 0; j < kBatch; ++j) {
+      const int e = e0 + j * kThreads + threadIdx.x;
+      if (e < n) reinterpret_cast<uint4*>(dst)[e] = val[j];  // piece e sits at byte 16 e
+    }
   }
   __syncthreads();
 }
 
-// ---- parallel fold of one staged R-token block of one kv-head (R <= kMaxFold)
+// ---- parallel fold of one R-token block of one kv-head (R <= kMaxFold)
 //
-// The block's K rows then V rows sit in shared memory in the source dtype.  All
-// tokens are handled at once: page addresses first, then each key group's
-// per-channel scales, then every 32-bit code word by one thread (keys) or each
-// token row by one warp (values and per-token keys), packed in registers and
-// stored straight into the page.  Every scale and code comes from the same
-// helpers as the sub-chunk path, so the bytes are identical.
+// The block's K rows then V rows are staged in shared memory in the source dtype,
+// with the page address of every token looked up while the rows are in flight.
+// Per-channel keys: each key group's channel scales, then the code words, one
+// thread per word column with its channels' parameters in registers across the
+// group's tokens.  Rows (values, per-token keys, per-tensor and FP8 tensors):
+// D/16 lanes per token, 16 consecutive channels per lane, two batches of tokens
+// per warp in flight, each lane's codes packed into one aligned store.  Scales
+// and codes use the same arithmetic as the sub-chunk path, so the bytes are
+// identical.
 constexpr int kMaxFold = 256;
+constexpr int kCPL = 16;  // channels per lane in the row fold (every token group holds whole lanes)
 
 struct FoldSmem {
   uint8_t* rowp[kMaxFold];  // head block of each token of the block (nullptr: bad page)
@@ -332,98 +341,244 @@ __device__ __forceinline__ float staged_value(const unsigned char* rows, int t, 
   return load_src(rows, (long long)t * D + c, bf16);
 }
 
-// Per-token (groups of q.group channels), per-tensor or FP8 rows: warp per token.
-__device__ void fold_rows(const KvqView& v, const TQ& q, const unsigned char* rows, FoldSmem& fs, int R) {
-  const int D = v.D, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int cpl = D >> 5;                         // channels per lane (2, 4 or 8)
-  const int lane_bits = cpl * q.bits;             // 8 .. 64
-  const float ss = (q.axis == KVQ_PER_TENSOR || q.fmt == KVQ_FP8_E4M3) ? q.static_scale[0] : 0.f;
-  const float sr = ss > 0.f ? __frcp_rn(ss) : 0.f;
-#pragma unroll 2
-  for (int t = warp; t < R; t += kThreads / 32) {
-    float x[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) x[i] = i < cpl ? staged_value(rows, t, lane * cpl + i, D, v.src_bf16) : 0.f;
-    float gs = ss, gr = sr, gm = 0.f;
-    if (q.axis == KVQ_PER_TOKEN && q.fmt != KVQ_FP8_E4M3) {
-      const int lpg = q.group / cpl;  // lanes per group (g >= 16 >= cpl)
-      float mn = INFINITY, mx = -INFINITY, am = 0.f;
-#pragma unroll
-      for (int i = 0; i < 8; ++i)
-        if (i < cpl) {
-          mn = fminf(mn, x[i]);
-          mx = fmaxf(mx, x[i]);
-          am = fmaxf(am, fabsf(x[i]));
-        }
-      for (int o = 1; o < lpg && o < 32; o <<= 1) {
-        mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-        am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
-      }
-      if (q.mode == KVQ_ASYM_MINMAX) {
-        gs = asym_scale(mn, mx, q.bits);
-        gm = mn;
-      } else {
-        gs = sym_scale(am, q.bits);
-      }
-      gr = gs > 0.f ? __frcp_rn(gs) : 0.f;
-      const int grp = (lane * cpl) / q.group;
-      uint8_t* hb = fs.rowp[t];
-      if (hb && (lane % lpg) == 0) {
-        float* meta = reinterpret_cast<float*>(hb + q.off_meta + fs.rslot[t] * q.ng * q.nmeta * 4);
-        meta[grp] = gs;
-        if (q.nmeta == 2) meta[q.ng + grp] = gm;
-      }
-    }
-    // this lane's codes, packed little-endian
-    unsigned long long bits = 0ull;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      if (i < cpl) {
-        unsigned u;
-        if (q.fmt == KVQ_FP8_E4M3) {
-          u = fp8_code(x[i], ss);
-        } else if (q.axis == KVQ_PER_TENSOR) {
-          u = stored_code(sym_code_r(x[i], ss, sr, q.bits), q.bits, KVQ_SYM_ABSMAX);
-        } else {
-          const int code = q.mode == KVQ_ASYM_MINMAX ? asym_code_r(x[i], gm, gs, gr, q.bits)
-                                                     : sym_code_r(x[i], gs, gr, q.bits);
-          u = stored_code(code, q.bits, q.mode);
-        }
-        bits |= (unsigned long long)u << (i * q.bits);
-      }
-    }
-    uint8_t* hb = fs.rowp[t];
-    uint32_t* dst = hb ? reinterpret_cast<uint32_t*>(hb + q.off_codes + fs.rslot[t] * q.row) : nullptr;
-    if (lane_bits >= 32) {
-      const int wpl = lane_bits >> 5;  // words per lane (1 or 2)
-      if (dst) {
-        dst[lane * wpl] = (uint32_t)bits;
-        if (wpl == 2) dst[lane * wpl + 1] = (uint32_t)(bits >> 32);
-      }
+// N consecutive source values of staged row t from channel c0 (the address is a
+// multiple of N * 2 bytes for bf16, N * 4 for fp32).
+template <int N>
+__device__ __forceinline__ void load_chunk(const unsigned char* rows, int t, int c0, int D, int bf16,
+                                           float (&x)[N]) {
+  if (bf16) {
+    const unsigned char* p = rows + ((size_t)t * D + c0) * 2;
+    if constexpr (N == 4) {
+      const uint2 u = *reinterpret_cast<const uint2*>(p);
+      x[0] = __uint_as_float(u.x << 16);
+      x[1] = __uint_as_float(u.x & 0xffff0000u);
+      x[2] = __uint_as_float(u.y << 16);
+      x[3] = __uint_as_float(u.y & 0xffff0000u);
     } else {
-      const int lpw = 32 / lane_bits;  // lanes per word (2 or 4)
-      uint32_t w = (uint32_t)bits << ((lane % lpw) * lane_bits);
-      for (int o = 1; o < lpw; o <<= 1) w |= __shfl_xor_sync(0xffffffffu, w, o);
-      if (dst && lane % lpw == 0) dst[lane / lpw] = w;
+#pragma unroll
+      for (int j = 0; j < N / 8; ++j) {
+        const uint4 u = reinterpret_cast<const uint4*>(p)[j];
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          x[8 * j + 2 * i] = __uint_as_float(w[i] << 16);
+          x[8 * j + 2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+        }
+      }
+    }
+  } else {
+    const float4* p = reinterpret_cast<const float4*>(rows + ((size_t)t * D + c0) * 4);
+#pragma unroll
+    for (int j = 0; j < N / 4; ++j) {
+      const float4 f = p[j];
+      x[4 * j] = f.x;
+      x[4 * j + 1] = f.y;
+      x[4 * j + 2] = f.z;
+      x[4 * j + 3] = f.w;
     }
   }
 }
 
-// Keys per channel over groups of G tokens of the block.
-__device__ void fold_key_channels(const KvqView& v, const TQ& q, const AppendCtx& a, const unsigned char* rows,
-                                  FoldSmem& fs, int tb, int R) {
+// Stored codes of N elements with scales s, reciprocals r and minimums m: the
+// codes of sym_code_r / asym_code_r, with the exact-division check of rint_quot
+// taken once for the N elements (the near-half case is rare).
+template <int N>
+__device__ __forceinline__ void int_codes(const float (&x)[N], const float (&s)[N], const float (&r)[N],
+                                          const float (&m)[N], bool asym, int bits, unsigned (&u)[N]) {
+  float c[N];
+  bool any_near = false;
+#pragma unroll
+  for (int i = 0; i < N; ++i) {
+    const float q = __fmul_rn(asym ? __fsub_rn(x[i], m[i]) : x[i], r[i]);
+    c[i] = rintf(q);
+    any_near |= quot_near_half(q);
+  }
+  if (any_near) {
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+      const float y = asym ? __fsub_rn(x[i], m[i]) : x[i];
+      if (quot_near_half(__fmul_rn(y, r[i]))) c[i] = rint_div_exact(y, s[i]);
+    }
+  }
+  const float hi = static_cast<float>(asym ? asym_qmax(bits) : sym_qmax(bits));
+  const float lo = asym ? 0.f : -hi;
+  const int mode = asym ? KVQ_ASYM_MINMAX : KVQ_SYM_ABSMAX;
+#pragma unroll
+  for (int i = 0; i < N; ++i) {
+    const int code = (!asym && s[i] == 0.f) ? 0 : static_cast<int>(fminf(fmaxf(c[i], lo), hi));
+    u[i] = stored_code(code, bits, mode);
+  }
+}
+
+template <int N>
+__device__ __forceinline__ void tree_minmax(const float (&x)[N], float& mn, float& mx, float& am) {
+  float a[N / 2], b[N / 2], c[N / 2];
+#pragma unroll
+  for (int i = 0; i < N / 2; ++i) {
+    a[i] = fminf(x[i], x[i + N / 2]);
+    b[i] = fmaxf(x[i], x[i + N / 2]);
+    c[i] = fmaxf(fabsf(x[i]), fabsf(x[i + N / 2]));
+  }
+#pragma unroll
+  for (int w = N / 4; w >= 1; w >>= 1) {
+#pragma unroll
+    for (int i = 0; i < w; ++i) {
+      a[i] = fminf(a[i], a[i + w]);
+      b[i] = fmaxf(b[i], b[i + w]);
+      c[i] = fmaxf(c[i], c[i + w]);
+    }
+  }
+  mn = a[0];
+  mx = b[0];
+  am = c[0];
+}
+
+// Rows of one tensor with BITS-bit codes (8 for FP8).
+template <int BITS>
+__device__ __forceinline__ void fold_rows_t(const KvqView& v, const TQ& q, const unsigned char* rows,
+                                            FoldSmem& fs, int R) {
+  constexpr int kNB = 2;                   // token batches per warp in flight
+  constexpr int kWords = kCPL * BITS / 32;  // code words per lane: 1, 2 or 4
+  const int D = v.D, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int lpt = D / kCPL, tpw = 32 / lpt;  // lanes per token, tokens per warp batch
+  const int sub = lane % lpt, tok = lane / lpt;
+  const bool fp8 = q.fmt == KVQ_FP8_E4M3;
+  const bool stat = fp8 || q.axis == KVQ_PER_TENSOR;
+  const bool asym = !stat && q.mode == KVQ_ASYM_MINMAX;
+  const float ss = stat ? q.static_scale[0] : 0.f;
+  const float sr = ss > 0.f ? __frcp_rn(ss) : 0.f;
+  const int lpg = stat ? 1 : q.group / kCPL;  // lanes per group (group = lpg * 16 channels)
+  const int step = kNB * tpw;
+#pragma unroll 1
+  for (int t0 = warp * step; t0 < R; t0 += kWarps * step) {
+    float x[kNB][kCPL];
+    int tt[kNB];
+#pragma unroll
+    for (int b = 0; b < kNB; ++b) {
+      tt[b] = t0 + b * tpw + tok;
+      if (tt[b] < R) {
+        load_chunk<kCPL>(rows, tt[b], sub * kCPL, D, v.src_bf16, x[b]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < kCPL; ++i) x[b][i] = 0.f;
+      }
+    }
+    float gs[kNB], gr[kNB], gm[kNB];
+    if (stat) {
+#pragma unroll
+      for (int b = 0; b < kNB; ++b) {
+        gs[b] = ss;
+        gr[b] = sr;
+        gm[b] = 0.f;
+      }
+    } else {
+      float mn[kNB], mx[kNB], am[kNB];
+#pragma unroll
+      for (int b = 0; b < kNB; ++b) tree_minmax<kCPL>(x[b], mn[b], mx[b], am[b]);
+      for (int o = 1; o < lpg; o <<= 1) {
+#pragma unroll
+        for (int b = 0; b < kNB; ++b) {
+          mn[b] = fminf(mn[b], __shfl_xor_sync(0xffffffffu, mn[b], o));
+          mx[b] = fmaxf(mx[b], __shfl_xor_sync(0xffffffffu, mx[b], o));
+          am[b] = fmaxf(am[b], __shfl_xor_sync(0xffffffffu, am[b], o));
+        }
+      }
+#pragma unroll
+      for (int b = 0; b < kNB; ++b) {
+        if (asym) {
+          gs[b] = asym_scale(mn[b], mx[b], BITS);
+          gm[b] = mn[b];
+        } else {
+          gs[b] = sym_scale(am[b], BITS);
+          gm[b] = 0.f;
+        }
+        gr[b] = gs[b] > 0.f ? __frcp_rn(gs[b]) : 0.f;
+      }
+    }
+#pragma unroll
+    for (int b = 0; b < kNB; ++b) {
+      const int t = tt[b];
+      uint8_t* hb = t < R ? fs.rowp[t] : nullptr;
+      if (hb) {
+        const int slot = fs.rslot[t];
+        if (!stat && sub % lpg == 0) {
+          float* meta = reinterpret_cast<float*>(hb + q.off_meta + slot * q.ng * q.nmeta * 4);
+          meta[sub / lpg] = gs[b];
+          if (q.nmeta == 2) meta[q.ng + sub / lpg] = gm[b];
+        }
+        unsigned u[kCPL];
+        if (fp8) {
+#pragma unroll
+          for (int i = 0; i < kCPL; ++i) u[i] = fp8_code(x[b][i], ss);
+        } else {
+          float s[kCPL], r[kCPL], m[kCPL];
+#pragma unroll
+          for (int i = 0; i < kCPL; ++i) {
+            s[i] = gs[b];
+            r[i] = gr[b];
+            m[i] = gm[b];
+          }
+          int_codes<kCPL>(x[b], s, r, m, asym, BITS, u);
+        }
+        uint32_t w[kWords];
+#pragma unroll
+        for (int j = 0; j < kWords; ++j) w[j] = 0u;
+#pragma unroll
+        for (int i = 0; i < kCPL; ++i) w[(i * BITS) >> 5] |= u[i] << ((i * BITS) & 31);
+        uint8_t* dst = hb + q.off_codes + slot * q.row + sub * (kWords * 4);
+        if constexpr (kWords == 1) {
+          *reinterpret_cast<uint32_t*>(dst) = w[0];
+        } else if constexpr (kWords == 2) {
+          *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
+        } else {
+          *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void fold_rows(const KvqView& v, const TQ& q, const unsigned char* rows, FoldSmem& fs,
+                                          int R) {
+  if (q.bits == 2) {
+    fold_rows_t<2>(v, q, rows, fs, R);
+  } else if (q.bits == 4) {
+    fold_rows_t<4>(v, q, rows, fs, R);
+  } else {
+    fold_rows_t<8>(v, q, rows, fs, R);
+  }
+}
+
+// Keys per channel over groups of G tokens of the block, BITS-bit codes.
+template <int BITS>
+__device__ __forceinline__ void fold_key_channels_t(const KvqView& v, const TQ& q, const unsigned char* rows,
+                                                    FoldSmem& fs, int tb, int R) {
+  constexpr int kCPW = 32 / BITS;  // channels per code word
   const int D = v.D, G = q.group;
   const int parts = kThreads / D;  // threads per channel for the scans (1, 2 or 4)
   const int c = threadIdx.x % D, part = threadIdx.x / D;
-  const int cpw = 32 / q.bits, wpr = q.row >> 2;
+  const int wpr = D / kCPW;                     // code words per row
+  const int k = threadIdx.x % wpr, tl = threadIdx.x / wpr, ntl = kThreads / wpr;
+  const bool asym = q.mode == KVQ_ASYM_MINMAX;
   for (int g0 = 0; g0 < R; g0 += G) {
-    float mn = INFINITY, mx = -INFINITY;
-    for (int t = g0 + part; t < g0 + G; t += parts) {
-      const float x = staged_value(rows, t, c, D, v.src_bf16);
-      mn = fminf(mn, x);
-      mx = fmaxf(mx, x);
+    // min and max of channel c over the group's tokens, two chains per thread
+    float mn0 = INFINITY, mx0 = -INFINITY, mn1 = INFINITY, mx1 = -INFINITY;
+    int t = g0 + part;
+#pragma unroll 4
+    for (; t + parts < g0 + G; t += 2 * parts) {
+      const float x0 = staged_value(rows, t, c, D, v.src_bf16);
+      const float x1 = staged_value(rows, t + parts, c, D, v.src_bf16);
+      mn0 = fminf(mn0, x0);
+      mx0 = fmaxf(mx0, x0);
+      mn1 = fminf(mn1, x1);
+      mx1 = fmaxf(mx1, x1);
     }
+    if (t < g0 + G) {
+      const float x0 = staged_value(rows, t, c, D, v.src_bf16);
+      mn0 = fminf(mn0, x0);
+      mx0 = fmaxf(mx0, x0);
+    }
+    float mn = fminf(mn0, mn1), mx = fmaxf(mx0, mx1);
     fs.cmin[threadIdx.x] = mn;
     fs.cmax[threadIdx.x] = mx;
     __syncthreads();
@@ -433,10 +588,10 @@ __device__ void fold_key_channels(const KvqView& v, const TQ& q, const AppendCtx
         mx = fmaxf(mx, fs.cmax[p * D + c]);
       }
       float sc;
-      if (q.mode == KVQ_ASYM_MINMAX) {
-        sc = asym_scale(mn, mx, q.bits);
+      if (asym) {
+        sc = asym_scale(mn, mx, BITS);
       } else {
-        sc = sym_scale(fmaxf(fabsf(mn), fabsf(mx)), q.bits);
+        sc = sym_scale(fmaxf(fabsf(mn), fabsf(mx)), BITS);
         mn = 0.f;
       }
       fs.ch_s[c] = sc;
@@ -451,44 +606,62 @@ __device__ void fold_key_channels(const KvqView& v, const TQ& q, const AppendCtx
       }
     }
     __syncthreads();
-    // one 32-bit code word per thread iteration
-    for (int w = threadIdx.x; w < G * wpr; w += kThreads) {
-      const int t = g0 + w / wpr, k = w % wpr;
-      uint32_t word = 0u;
-      for (int i = 0; i < cpw; ++i) {
-        const int cc = k * cpw + i;
-        const float x = staged_value(rows, t, cc, D, v.src_bf16);
-        const int code = q.mode == KVQ_ASYM_MINMAX ? asym_code_r(x, fs.ch_m[cc], fs.ch_s[cc], fs.ch_r[cc], q.bits)
-                                                   : sym_code_r(x, fs.ch_s[cc], fs.ch_r[cc], q.bits);
-        word |= stored_code(code, q.bits, q.mode) << (i * q.bits);
-      }
-      uint8_t* hb = fs.rowp[t];
-      if (hb) reinterpret_cast<uint32_t*>(hb + q.off_codes + fs.rslot[t] * q.row)[k] = word;
+    // word column k (channels k * kCPW ..) of the group's tokens tl, tl + ntl, ...
+    float cs[kCPW], cr[kCPW], cm[kCPW];
+#pragma unroll
+    for (int i = 0; i < kCPW; i += 4) {
+      const float4 a4 = *reinterpret_cast<const float4*>(&fs.ch_s[k * kCPW + i]);
+      const float4 b4 = *reinterpret_cast<const float4*>(&fs.ch_r[k * kCPW + i]);
+      const float4 c4 = *reinterpret_cast<const float4*>(&fs.ch_m[k * kCPW + i]);
+      cs[i] = a4.x; cs[i + 1] = a4.y; cs[i + 2] = a4.z; cs[i + 3] = a4.w;
+      cr[i] = b4.x; cr[i + 1] = b4.y; cr[i + 2] = b4.z; cr[i + 3] = b4.w;
+      cm[i] = c4.x; cm[i + 1] = c4.y; cm[i + 2] = c4.z; cm[i + 3] = c4.w;
+    }
+#pragma unroll 2
+    for (int tt = g0 + tl; tt < g0 + G; tt += ntl) {
+      float x[kCPW];
+      load_chunk<kCPW>(rows, tt, k * kCPW, D, v.src_bf16, x);
+      unsigned u[kCPW];
+      int_codes<kCPW>(x, cs, cr, cm, asym, BITS, u);
+      uint32_t w = 0u;
+#pragma unroll
+      for (int i = 0; i < kCPW; ++i) w |= u[i] << (i * BITS);
+      uint8_t* hb = fs.rowp[tt];
+      if (hb) reinterpret_cast<uint32_t*>(hb + q.off_codes + fs.rslot[tt] * q.row)[k] = w;
     }
     __syncthreads();
   }
 }
 
-__device__ void fold_staged(const KvqView& v, const AppendCtx& a, const unsigned char* staged, int tb) {
+// Stage the block, look up its pages meanwhile, then fold keys and values.
+__device__ __forceinline__ void fold_block(const KvqView& v, const AppendCtx& a, const void* k_new,
+                                           const void* v_new, int tb, unsigned char* staged) {
   __shared__ FoldSmem fs;
   const int R = v.R;
-  if (threadIdx.x < R) {
-    const int t = tb + threadIdx.x;
-    uint8_t* page = page_of(v, a.b, t);
-    fs.rowp[threadIdx.x] = page ? page + (long long)a.h * v.head_bytes : nullptr;
-    fs.rslot[threadIdx.x] = t % v.P;
-  }
-  __syncthreads();
+  stage_block(v, a, k_new, v_new, tb, R, staged, [&] {
+    if (threadIdx.x < R) {
+      const int t = tb + threadIdx.x;
+      uint8_t* page = page_of(v, a.b, t);
+      fs.rowp[threadIdx.x] = page ? page + (long long)a.h * v.head_bytes : nullptr;
+      fs.rslot[threadIdx.x] = t % v.P;
+    }
+  });
   const int row = v.D * (v.src_bf16 ? 2 : 4);
   TQ kq = key_q(v), vq = value_q(v);
   kq.static_scale = v.k_scale + a.h;
   vq.static_scale = v.v_scale + a.h;
   if (kq.axis == KVQ_PER_CHANNEL) {
-    fold_key_channels(v, kq, a, staged, fs, tb, R);
-  } else {
-    fold_rows(v, kq, staged, fs, R);
+    if (kq.bits == 2) {
+      fold_key_channels_t<2>(v, kq, staged, fs, tb, R);
+    } else if (kq.bits == 4) {
+      fold_key_channels_t<4>(v, kq, staged, fs, tb, R);
+    } else {
+      fold_key_channels_t<8>(v, kq, staged, fs, tb, R);
+    }
   }
-  fold_rows(v, vq, staged + (long long)R * row, fs, R);
+#pragma unroll 1
+  for (int tensor = kq.axis == KVQ_PER_CHANNEL ? 1 : 0; tensor < 2; ++tensor)
+    fold_rows(v, tensor ? vq : kq, staged + (long long)tensor * R * row, fs, R);
 }
 
 __global__ void __launch_bounds__(kThreads) append_kernel(KvqView v, const void* k_new,
@@ -521,10 +694,10 @@ __global__ void __launch_bounds__(kThreads) append_kernel(KvqView v, const void*
       if (stage_ok) {
         // the whole R-token block fits in shared memory: one parallel pass of loads,
         // then every quantizer pass reads shared memory
-        stage_block(v, a, k_new, v_new, tb, v.R, staged);
         if (v.R <= kMaxFold) {
-          fold_staged(v, a, staged, tb);
+          fold_block(v, a, k_new, v_new, tb, staged);
         } else {
+          stage_block(v, a, k_new, v_new, tb, v.R, staged, [] {});
           a.st_t0 = tb;
           const int row = v.D * (v.src_bf16 ? 2 : 4);
           const Src kss{v.k_win, k_new, staged}, vss{v.v_win, v_new, staged + (long long)v.R * row};

@@ -337,17 +337,18 @@ __global__ void __launch_bounds__(kThreads, 2)
         const uint32_t bytes = kStageBytes + (gstart ? kKMeta : 0);
         mbar_arrive_expect_tx(bar, bytes);
         uint8_t* dst = sm.stage[warp][stage];
+        const uint64_t pol = l2_evict_first();
         if (v.P == kTile) {
           // the head's whole page section: codes, value meta, then the key scales
-          bulk_g2s(dst, hbk, bytes, bar);
+          bulk_g2s_hint(dst, hbk, bytes, bar, pol);
         } else {
           const int slot = tok & (v.P - 1);
-          bulk_g2s(dst, hbk + slot * kD, kKC, bar);
-          bulk_g2s(dst + kKC, hbk + v.off_vc + slot * (kD / 2), kVC, bar);
-          bulk_g2s(dst + kKC + kVC, hbk + v.off_vm + slot * 8, kVM, bar);
+          bulk_g2s_hint(dst, hbk + slot * kD, kKC, bar, pol);
+          bulk_g2s_hint(dst + kKC, hbk + v.off_vc + slot * (kD / 2), kVC, bar, pol);
+          bulk_g2s_hint(dst + kKC + kVC, hbk + v.off_vm + slot * 8, kVM, bar, pol);
           if (gstart) {
             const int gslot = v.P >= G ? (slot >> lgG) : 0;
-            bulk_g2s(dst + kStageBytes, hbk + v.off_km + gslot * kKMeta, kKMeta, bar);
+            bulk_g2s_hint(dst + kStageBytes, hbk + v.off_km + gslot * kKMeta, kKMeta, bar, pol);
           }
         }
       };

@@ -149,8 +149,9 @@ __global__ void __launch_bounds__(kThreads8)
       const long long byte0 = (long long)pid * v.page_bytes + head_off + (long long)(tok & (v.P - 1)) * kRowB;
       const int yk = (int)(byte0 / kRowB), yv = yk + v.off_vc / kRowB;
       mbar_arrive_expect_tx(bar, 2 * kTileB);
-      tma_load_2d(ring[stage][0], &tmap, 0, yk, bar);
-      tma_load_2d(ring[stage][1], &tmap, 0, yv, bar);
+      const uint64_t pol = l2_evict_first();
+      tma_load_2d_hint(ring[stage][0], &tmap, 0, yk, bar, pol);
+      tma_load_2d_hint(ring[stage][1], &tmap, 0, yv, bar, pol);
     };
     int pf = 0;  // lane 0: page id of the next tile to load, read one tile ahead
     if (lane == 0 && !stalled) {

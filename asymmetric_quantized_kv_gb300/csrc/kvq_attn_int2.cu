@@ -262,11 +262,12 @@ __global__ void __launch_bounds__(kThreadsI, 3)
         const bool gstart = (tok & (G - 1)) == 0;
         mbar_arrive_expect_tx(bar, kTileBytesI + (gstart ? kKMeta2 : 0));
         uint8_t* dst = sm.stage[warp][stage];
-        tma_load_5d(dst + kOffK, &tmc, 0, slot, 0, h, pid, bar);
+        const uint64_t pol = l2_evict_first();
+        tma_load_5d_hint(dst + kOffK, &tmc, 0, slot, 0, h, pid, bar, pol);
         if (gstart) {
           const long long byte0 = (long long)pid * v.page_bytes + head_off + v.off_km +
                                   (long long)(v.P >= G ? slot >> lgG : 0) * kKMeta2;
-          tma_load_2d(dst + kOffKM, &tmk, 0, (int)(byte0 >> 7), bar);
+          tma_load_2d_hint(dst + kOffKM, &tmk, 0, (int)(byte0 >> 7), bar, pol);
         }
       };
       int pf = 0;

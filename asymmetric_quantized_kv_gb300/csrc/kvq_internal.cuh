@@ -164,10 +164,20 @@ __device__ __forceinline__ int asym_code(float x, float mn, float s, int bits) {
 // so fl32(x * r) lies within 2^-23 (relative) of x / s, as does fl32(x / s).  The
 // two round to the same integer unless the product is near a half-integer; those
 // rare cases (and non-finite r) take the exact IEEE division.
+// The exact path, kept out of line: it is rare, and inlining the IEEE division at
+// every quantizer call site would bloat the code a short kernel has to fetch.
+static __device__ __noinline__ float rint_div_exact(float x, float s) { return rintf(__fdiv_rn(x, s)); }
+
+// True when the product q = fl32(x * r) may round to another integer than x / s
+// (near a half-integer, or not a number).
+__device__ __forceinline__ bool quot_near_half(float q) {
+  const float f = q - floorf(q);
+  return !(fabsf(f - 0.5f) > 1.52587890625e-05f * fmaxf(1.f, fabsf(q)));
+}
+
 __device__ __forceinline__ float rint_quot(float x, float s, float r) {
   const float q = __fmul_rn(x, r);
-  const float f = q - floorf(q);
-  if (!(fabsf(f - 0.5f) > 1.52587890625e-05f * fmaxf(1.f, fabsf(q)))) return rintf(__fdiv_rn(x, s));
+  if (quot_near_half(q)) return rint_div_exact(x, s);
   return rintf(q);
 }
 
