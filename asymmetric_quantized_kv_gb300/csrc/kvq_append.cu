@@ -273,10 +273,19 @@ __device__ void quantize_block(const KvqView& v, const Src& ks, const Src& vs, c
   quantize_rows(v, vs, a, vq, sm, t_begin, count);
 }
 
+// 16-byte global -> shared copy that completes asynchronously (cp.async, sm_80+);
+// cp.async.wait_all makes the thread's copies visible to itself.
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc) {
+  const unsigned d = static_cast<unsigned>(__cvta_generic_to_shared(smem_dst));
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(d), "l"(gsrc) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
+
 // Copy the source rows (window or new tokens) of tokens [t_begin, t_begin + count)
-// of one head into shared memory with 16-byte loads, K rows then V rows.  `between`
-// runs once, after the first batch of loads has been issued and before any of them
-// is consumed, so the global reads it makes overlap theirs.
+// of one head into shared memory as 16-byte asynchronous copies, K rows then V
+// rows.  `between` runs while the copies are in flight, so the global reads it
+// makes overlap theirs.  The loop stays rolled: a launch runs this code once, so
+// its size, not its instruction count, sets its cost.
 template <typename Between>
 __device__ void stage_block(const KvqView& v, const AppendCtx& a, const void* k_new, const void* v_new,
                             int t_begin, int count, unsigned char* dst, Between&& between) {
@@ -284,35 +293,24 @@ __device__ void stage_block(const KvqView& v, const AppendCtx& a, const void* k_
   const int lp = log2i(row >> 4);  // 16-byte pieces per row: 2^lp
   const int per_tensor = count << lp;
   const int n = 2 * per_tensor;
-  constexpr int kBatch = 8;  // loads in flight per thread before the shared-memory stores
-  for (int e0 = 0; e0 < n; e0 += kBatch * kThreads) {
-    uint4 val[kBatch];
-#pragma unroll
-    for (int j = 0; j < kBatch; ++j) {
-      const int e = e0 + j * kThreads + threadIdx.x;
-      if (e < n) {
-        const int tensor = e >= per_tensor;
-        const int rem = tensor ? e - per_tensor : e;
-        const int r = rem >> lp, k = rem & ((1 << lp) - 1);
-        const int t = t_begin + r;
-        const unsigned char* src;
-        if (t < a.T0) {
-          const long long i = (((long long)a.b * v.R + (t - a.wbase)) * v.Hkv + a.h) * row;
-          src = static_cast<const unsigned char*>(tensor ? v.v_win : v.k_win) + i;
-        } else {
-          const long long i = (((long long)a.b * a.n_stride + (t - a.T0)) * v.Hkv + a.h) * row;
-          src = static_cast<const unsigned char*>(tensor ? v_new : k_new) + i;
-        }
-        val[j] = reinterpret_cast<const uint4*>(src)[k];
-      }
+#pragma unroll 1
+  for (int e = threadIdx.x; e < n; e += kThreads) {
+    const int tensor = e >= per_tensor;
+    const int rem = tensor ? e - per_tensor : e;
+    const int r = rem >> lp, k = rem & ((1 << lp) - 1);
+    const int t = t_begin + r;
+    const unsigned char* src;
+    if (t < a.T0) {
+      const long long i = (((long long)a.b * v.R + (t - a.wbase)) * v.Hkv + a.h) * row;
+      src = static_cast<const unsigned char*>(tensor ? v.v_win : v.k_win) + i;
+    } else {
+      const long long i = (((long long)a.b * a.n_stride + (t - a.T0)) * v.Hkv + a.h) * row;
+      src = static_cast<const unsigned char*>(tensor ? v_new : k_new) + i;
     }
-    if (e0 == 0) between();
-#pragma unroll
-    for (int j = 0; j < kBatch; ++j) {
-      const int e = e0 + j * kThreads + threadIdx.x;
-      if (e < n) reinterpret_cast<uint4*>(dst)[e] = val[j];  // piece e sits at byte 16 e
-    }
+    cp_async16(dst + 16 * e, src + 16 * k);  // piece e of the block sits at byte 16 e
   }
+  between();
+  cp_async_wait_all();
   __syncthreads();
 }
 
@@ -323,10 +321,10 @@ __device__ void stage_block(const KvqView& v, const AppendCtx& a, const void* k_
 // Per-channel keys: each key group's channel scales, then the code words, one
 // thread per word column with its channels' parameters in registers across the
 // group's tokens.  Rows (values, per-token keys, per-tensor and FP8 tensors):
-// D/16 lanes per token, 16 consecutive channels per lane, two batches of tokens
-// per warp in flight, each lane's codes packed into one aligned store.  Scales
-// and codes use the same arithmetic as the sub-chunk path, so the bytes are
-// identical.
+// D/16 lanes per token, 16 consecutive channels per lane, one code word at a time.
+// A launch runs this code about once, from cold instruction caches, so loops stay
+// rolled.  Scales and codes follow the rules of the sub-chunk path exactly, so the
+// bytes are identical.
 constexpr int kMaxFold = 256;
 constexpr int kCPL = 16;  // channels per lane in the row fold (every token group holds whole lanes)
 
@@ -337,17 +335,22 @@ struct FoldSmem {
   float ch_s[kMaxD], ch_r[kMaxD], ch_m[kMaxD];
 };
 
-__device__ __forceinline__ float staged_value(const unsigned char* rows, int t, int c, int D, int bf16) {
-  return load_src(rows, (long long)t * D + c, bf16);
+template <bool BF16>
+__device__ __forceinline__ float staged_value(const unsigned char* rows, int t, int c, int D) {
+  if constexpr (BF16) {
+    const unsigned short u = reinterpret_cast<const unsigned short*>(rows)[t * D + c];
+    return __uint_as_float(static_cast<unsigned>(u) << 16);
+  } else {
+    return reinterpret_cast<const float*>(rows)[t * D + c];
+  }
 }
 
 // N consecutive source values of staged row t from channel c0 (the address is a
 // multiple of N * 2 bytes for bf16, N * 4 for fp32).
-template <int N>
-__device__ __forceinline__ void load_chunk(const unsigned char* rows, int t, int c0, int D, int bf16,
-                                           float (&x)[N]) {
-  if (bf16) {
-    const unsigned char* p = rows + ((size_t)t * D + c0) * 2;
+template <int N, bool BF16>
+__device__ __forceinline__ void load_chunk(const unsigned char* rows, int t, int c0, int D, float (&x)[N]) {
+  if constexpr (BF16) {
+    const unsigned char* p = rows + (t * D + c0) * 2;
     if constexpr (N == 4) {
       const uint2 u = *reinterpret_cast<const uint2*>(p);
       x[0] = __uint_as_float(u.x << 16);
@@ -367,7 +370,7 @@ __device__ __forceinline__ void load_chunk(const unsigned char* rows, int t, int
       }
     }
   } else {
-    const float4* p = reinterpret_cast<const float4*>(rows + ((size_t)t * D + c0) * 4);
+    const float4* p = reinterpret_cast<const float4*>(rows + (t * D + c0) * 4);
 #pragma unroll
     for (int j = 0; j < N / 4; ++j) {
       const float4 f = p[j];
@@ -379,35 +382,37 @@ __device__ __forceinline__ void load_chunk(const unsigned char* rows, int t, int
   }
 }
 
-// Stored codes of N elements with scales s, reciprocals r and minimums m: the
-// codes of sym_code_r / asym_code_r, with the exact-division check of rint_quot
-// taken once for the N elements (the near-half case is rare).
-template <int N>
-__device__ __forceinline__ void int_codes(const float (&x)[N], const float (&s)[N], const float (&r)[N],
-                                          const float (&m)[N], bool asym, int bits, unsigned (&u)[N]) {
-  float c[N];
-  bool any_near = false;
-#pragma unroll
-  for (int i = 0; i < N; ++i) {
-    const float q = __fmul_rn(asym ? __fsub_rn(x[i], m[i]) : x[i], r[i]);
-    c[i] = rintf(q);
-    any_near |= quot_near_half(q);
-  }
-  if (any_near) {
-#pragma unroll
-    for (int i = 0; i < N; ++i) {
-      const float y = asym ? __fsub_rn(x[i], m[i]) : x[i];
-      if (quot_near_half(__fmul_rn(y, r[i]))) c[i] = rint_div_exact(y, s[i]);
-    }
-  }
-  const float hi = static_cast<float>(asym ? asym_qmax(bits) : sym_qmax(bits));
+// rint(fl32(y * r)) with r = fl32(1 / s) equals rint(fl32(y / s)) unless a
+// half-integer lies between the two: both are within 3 * 2^-24 |y / s| of the exact
+// quotient.  A product farther than kNearHalf |q| (over five times that distance) from
+// every half-integer is therefore safe; a nearer one, or one that is not a finite
+// number, takes the exact rule.  Besides the band's own width, bf16 sources put x / s
+// exactly on a half-integer fairly often (about 0.4% of the codes of normal data).
+constexpr float kNearHalf = 9.5367431640625e-07f;  // 2^-20
+
+// One code word: the BITS-bit stored codes of N elements with scales s,
+// reciprocals r and minimums m, equal to those of sym_code_r / asym_code_r.  The
+// quotient comes from the reciprocal; the few elements within kNearHalf |q| of a
+// half-integer (or not finite) take the IEEE division, inline, so a warp pays for
+// it only at the element positions where one of its lanes needs it.
+template <int N, int BITS>
+__device__ __forceinline__ uint32_t pack_codes(const float (&x)[N], const float (&s)[N], const float (&r)[N],
+                                               const float (&m)[N], bool asym) {
+  const float hi = static_cast<float>(asym ? (1 << BITS) - 1 : (1 << (BITS - 1)) - 1);
   const float lo = asym ? 0.f : -hi;
-  const int mode = asym ? KVQ_ASYM_MINMAX : KVQ_SYM_ABSMAX;
+  const unsigned off = (asym || BITS == 8) ? 0u : (1u << (BITS - 1));  // offset binary for sym INT2 / INT4
+  uint32_t w = 0u;
 #pragma unroll
   for (int i = 0; i < N; ++i) {
-    const int code = (!asym && s[i] == 0.f) ? 0 : static_cast<int>(fminf(fmaxf(c[i], lo), hi));
-    u[i] = stored_code(code, bits, mode);
+    const float y = asym ? __fsub_rn(x[i], m[i]) : x[i];
+    const float q = __fmul_rn(y, r[i]);
+    float c = rintf(q);
+    if (!(fabsf(__fsub_rn(fabsf(__fsub_rn(q, c)), 0.5f)) > __fmul_rn(kNearHalf, fabsf(q))))
+      c = rintf(__fdiv_rn(y, s[i]));
+    const int code = (!asym && s[i] == 0.f) ? 0 : static_cast<int>(fminf(fmaxf(c, lo), hi));
+    w |= ((static_cast<unsigned>(code) + off) & ((1u << BITS) - 1u)) << (i * BITS);
   }
+  return w;
 }
 
 template <int N>
@@ -434,13 +439,13 @@ __device__ __forceinline__ void tree_minmax(const float (&x)[N], float& mn, floa
 }
 
 // Rows of one tensor with BITS-bit codes (8 for FP8).
-template <int BITS>
+template <int BITS, bool BF16>
 __device__ __forceinline__ void fold_rows_t(const KvqView& v, const TQ& q, const unsigned char* rows,
                                             FoldSmem& fs, int R) {
-  constexpr int kNB = 2;                   // token batches per warp in flight
-  constexpr int kWords = kCPL * BITS / 32;  // code words per lane: 1, 2 or 4
+  constexpr int kCPW = 32 / BITS;       // codes per word
+  constexpr int kWords = kCPL / kCPW;   // words per lane: 1, 2 or 4
   const int D = v.D, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int lpt = D / kCPL, tpw = 32 / lpt;  // lanes per token, tokens per warp batch
+  const int lpt = D / kCPL, tpw = 32 / lpt;  // lanes per token, tokens per warp
   const int sub = lane % lpt, tok = lane / lpt;
   const bool fp8 = q.fmt == KVQ_FP8_E4M3;
   const bool stat = fp8 || q.axis == KVQ_PER_TENSOR;
@@ -448,133 +453,105 @@ __device__ __forceinline__ void fold_rows_t(const KvqView& v, const TQ& q, const
   const float ss = stat ? q.static_scale[0] : 0.f;
   const float sr = ss > 0.f ? __frcp_rn(ss) : 0.f;
   const int lpg = stat ? 1 : q.group / kCPL;  // lanes per group (group = lpg * 16 channels)
-  const int step = kNB * tpw;
 #pragma unroll 1
-  for (int t0 = warp * step; t0 < R; t0 += kWarps * step) {
-    float x[kNB][kCPL];
-    int tt[kNB];
-#pragma unroll
-    for (int b = 0; b < kNB; ++b) {
-      tt[b] = t0 + b * tpw + tok;
-      if (tt[b] < R) {
-        load_chunk<kCPL>(rows, tt[b], sub * kCPL, D, v.src_bf16, x[b]);
+  for (int t0 = warp * tpw; t0 < R; t0 += kWarps * tpw) {
+    const int t = t0 + tok;
+    const bool ok = t < R;
+    float gs = ss, gr = sr, gm = 0.f;
+    if (!stat) {
+      float x[kCPL];
+      if (ok) {
+        load_chunk<kCPL, BF16>(rows, t, sub * kCPL, D, x);
       } else {
 #pragma unroll
-        for (int i = 0; i < kCPL; ++i) x[b][i] = 0.f;
+        for (int i = 0; i < kCPL; ++i) x[i] = 0.f;
       }
-    }
-    float gs[kNB], gr[kNB], gm[kNB];
-    if (stat) {
-#pragma unroll
-      for (int b = 0; b < kNB; ++b) {
-        gs[b] = ss;
-        gr[b] = sr;
-        gm[b] = 0.f;
-      }
-    } else {
-      float mn[kNB], mx[kNB], am[kNB];
-#pragma unroll
-      for (int b = 0; b < kNB; ++b) tree_minmax<kCPL>(x[b], mn[b], mx[b], am[b]);
+      float mn, mx, am;
+      tree_minmax<kCPL>(x, mn, mx, am);
       for (int o = 1; o < lpg; o <<= 1) {
-#pragma unroll
-        for (int b = 0; b < kNB; ++b) {
-          mn[b] = fminf(mn[b], __shfl_xor_sync(0xffffffffu, mn[b], o));
-          mx[b] = fmaxf(mx[b], __shfl_xor_sync(0xffffffffu, mx[b], o));
-          am[b] = fmaxf(am[b], __shfl_xor_sync(0xffffffffu, am[b], o));
-        }
+        mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
       }
-#pragma unroll
-      for (int b = 0; b < kNB; ++b) {
-        if (asym) {
-          gs[b] = asym_scale(mn[b], mx[b], BITS);
-          gm[b] = mn[b];
-        } else {
-          gs[b] = sym_scale(am[b], BITS);
-          gm[b] = 0.f;
-        }
-        gr[b] = gs[b] > 0.f ? __frcp_rn(gs[b]) : 0.f;
+      if (asym) {
+        gs = asym_scale(mn, mx, BITS);
+        gm = mn;
+      } else {
+        gs = sym_scale(am, BITS);
       }
+      gr = gs > 0.f ? __frcp_rn(gs) : 0.f;
     }
+    uint8_t* hb = ok ? fs.rowp[t] : nullptr;
+    if (!hb) continue;
+    const int slot = fs.rslot[t];
+    if (!stat && sub % lpg == 0) {
+      float* meta = reinterpret_cast<float*>(hb + q.off_meta + slot * q.ng * q.nmeta * 4);
+      meta[sub / lpg] = gs;
+      if (q.nmeta == 2) meta[q.ng + sub / lpg] = gm;
+    }
+    uint32_t* dst = reinterpret_cast<uint32_t*>(hb + q.off_codes + slot * q.row) + sub * kWords;
+    float sc[kCPW], r[kCPW], m[kCPW];
 #pragma unroll
-    for (int b = 0; b < kNB; ++b) {
-      const int t = tt[b];
-      uint8_t* hb = t < R ? fs.rowp[t] : nullptr;
-      if (hb) {
-        const int slot = fs.rslot[t];
-        if (!stat && sub % lpg == 0) {
-          float* meta = reinterpret_cast<float*>(hb + q.off_meta + slot * q.ng * q.nmeta * 4);
-          meta[sub / lpg] = gs[b];
-          if (q.nmeta == 2) meta[q.ng + sub / lpg] = gm[b];
-        }
-        unsigned u[kCPL];
-        if (fp8) {
+    for (int i = 0; i < kCPW; ++i) {
+      sc[i] = gs;
+      r[i] = gr;
+      m[i] = gm;
+    }
+#pragma unroll 1
+    for (int j = 0; j < kWords; ++j) {
+      const int c0 = sub * kCPL + j * kCPW;
+      float x[kCPW];
+      load_chunk<kCPW, BF16>(rows, t, c0, D, x);
+      uint32_t w = 0u;
+      if (fp8) {
 #pragma unroll
-          for (int i = 0; i < kCPL; ++i) u[i] = fp8_code(x[b][i], ss);
-        } else {
-          float s[kCPL], r[kCPL], m[kCPL];
-#pragma unroll
-          for (int i = 0; i < kCPL; ++i) {
-            s[i] = gs[b];
-            r[i] = gr[b];
-            m[i] = gm[b];
-          }
-          int_codes<kCPL>(x[b], s, r, m, asym, BITS, u);
-        }
-        uint32_t w[kWords];
-#pragma unroll
-        for (int j = 0; j < kWords; ++j) w[j] = 0u;
-#pragma unroll
-        for (int i = 0; i < kCPL; ++i) w[(i * BITS) >> 5] |= u[i] << ((i * BITS) & 31);
-        uint8_t* dst = hb + q.off_codes + slot * q.row + sub * (kWords * 4);
-        if constexpr (kWords == 1) {
-          *reinterpret_cast<uint32_t*>(dst) = w[0];
-        } else if constexpr (kWords == 2) {
-          *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
-        } else {
-          *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
-        }
+        for (int i = 0; i < kCPW; ++i) w |= fp8_code(x[i], ss) << (8 * i);
+      } else {
+        w = pack_codes<kCPW, BITS>(x, sc, r, m, asym);
       }
+      dst[j] = w;
     }
   }
 }
 
+template <bool BF16>
 __device__ __forceinline__ void fold_rows(const KvqView& v, const TQ& q, const unsigned char* rows, FoldSmem& fs,
                                           int R) {
   if (q.bits == 2) {
-    fold_rows_t<2>(v, q, rows, fs, R);
+    fold_rows_t<2, BF16>(v, q, rows, fs, R);
   } else if (q.bits == 4) {
-    fold_rows_t<4>(v, q, rows, fs, R);
+    fold_rows_t<4, BF16>(v, q, rows, fs, R);
   } else {
-    fold_rows_t<8>(v, q, rows, fs, R);
+    fold_rows_t<8, BF16>(v, q, rows, fs, R);
   }
 }
 
 // Keys per channel over groups of G tokens of the block, BITS-bit codes.
-template <int BITS>
+template <int BITS, bool BF16>
 __device__ __forceinline__ void fold_key_channels_t(const KvqView& v, const TQ& q, const unsigned char* rows,
                                                     FoldSmem& fs, int tb, int R) {
   constexpr int kCPW = 32 / BITS;  // channels per code word
   const int D = v.D, G = q.group;
   const int parts = kThreads / D;  // threads per channel for the scans (1, 2 or 4)
   const int c = threadIdx.x % D, part = threadIdx.x / D;
-  const int wpr = D / kCPW;                     // code words per row
+  const int wpr = D / kCPW;        // code words per row
   const int k = threadIdx.x % wpr, tl = threadIdx.x / wpr, ntl = kThreads / wpr;
   const bool asym = q.mode == KVQ_ASYM_MINMAX;
+#pragma unroll 1
   for (int g0 = 0; g0 < R; g0 += G) {
     // min and max of channel c over the group's tokens, two chains per thread
     float mn0 = INFINITY, mx0 = -INFINITY, mn1 = INFINITY, mx1 = -INFINITY;
     int t = g0 + part;
-#pragma unroll 4
+#pragma unroll 2
     for (; t + parts < g0 + G; t += 2 * parts) {
-      const float x0 = staged_value(rows, t, c, D, v.src_bf16);
-      const float x1 = staged_value(rows, t + parts, c, D, v.src_bf16);
+      const float x0 = staged_value<BF16>(rows, t, c, D), x1 = staged_value<BF16>(rows, t + parts, c, D);
       mn0 = fminf(mn0, x0);
       mx0 = fmaxf(mx0, x0);
       mn1 = fminf(mn1, x1);
       mx1 = fmaxf(mx1, x1);
     }
     if (t < g0 + G) {
-      const float x0 = staged_value(rows, t, c, D, v.src_bf16);
+      const float x0 = staged_value<BF16>(rows, t, c, D);
       mn0 = fminf(mn0, x0);
       mx0 = fmaxf(mx0, x0);
     }
@@ -610,22 +587,18 @@ __device__ __forceinline__ void fold_key_channels_t(const KvqView& v, const TQ& 
     float cs[kCPW], cr[kCPW], cm[kCPW];
 #pragma unroll
     for (int i = 0; i < kCPW; i += 4) {
-      const float4 a4 = *reinterpret_cast<const float4*>(&fs.ch_s[k * kCPW + i]);
-      const float4 b4 = *reinterpret_cast<const float4*>(&fs.ch_r[k * kCPW + i]);
-      const float4 c4 = *reinterpret_cast<const float4*>(&fs.ch_m[k * kCPW + i]);
-      cs[i] = a4.x; cs[i + 1] = a4.y; cs[i + 2] = a4.z; cs[i + 3] = a4.w;
-      cr[i] = b4.x; cr[i + 1] = b4.y; cr[i + 2] = b4.z; cr[i + 3] = b4.w;
-      cm[i] = c4.x; cm[i + 1] = c4.y; cm[i + 2] = c4.z; cm[i + 3] = c4.w;
+      const float4 s4 = *reinterpret_cast<const float4*>(&fs.ch_s[k * kCPW + i]);
+      const float4 r4 = *reinterpret_cast<const float4*>(&fs.ch_r[k * kCPW + i]);
+      const float4 m4 = *reinterpret_cast<const float4*>(&fs.ch_m[k * kCPW + i]);
+      cs[i] = s4.x; cs[i + 1] = s4.y; cs[i + 2] = s4.z; cs[i + 3] = s4.w;
+      cr[i] = r4.x; cr[i + 1] = r4.y; cr[i + 2] = r4.z; cr[i + 3] = r4.w;
+      cm[i] = m4.x; cm[i + 1] = m4.y; cm[i + 2] = m4.z; cm[i + 3] = m4.w;
     }
-#pragma unroll 2
+#pragma unroll 1
     for (int tt = g0 + tl; tt < g0 + G; tt += ntl) {
       float x[kCPW];
-      load_chunk<kCPW>(rows, tt, k * kCPW, D, v.src_bf16, x);
-      unsigned u[kCPW];
-      int_codes<kCPW>(x, cs, cr, cm, asym, BITS, u);
-      uint32_t w = 0u;
-#pragma unroll
-      for (int i = 0; i < kCPW; ++i) w |= u[i] << (i * BITS);
+      load_chunk<kCPW, BF16>(rows, tt, k * kCPW, D, x);
+      const uint32_t w = pack_codes<kCPW, BITS>(x, cs, cr, cm, asym);
       uint8_t* hb = fs.rowp[tt];
       if (hb) reinterpret_cast<uint32_t*>(hb + q.off_codes + fs.rslot[tt] * q.row)[k] = w;
     }
@@ -634,9 +607,9 @@ __device__ __forceinline__ void fold_key_channels_t(const KvqView& v, const TQ& 
 }
 
 // Stage the block, look up its pages meanwhile, then fold keys and values.
+template <bool BF16>
 __device__ __forceinline__ void fold_block(const KvqView& v, const AppendCtx& a, const void* k_new,
-                                           const void* v_new, int tb, unsigned char* staged) {
-  __shared__ FoldSmem fs;
+                                           const void* v_new, int tb, unsigned char* staged, FoldSmem& fs) {
   const int R = v.R;
   stage_block(v, a, k_new, v_new, tb, R, staged, [&] {
     if (threadIdx.x < R) {
@@ -646,22 +619,22 @@ __device__ __forceinline__ void fold_block(const KvqView& v, const AppendCtx& a,
       fs.rslot[threadIdx.x] = t % v.P;
     }
   });
-  const int row = v.D * (v.src_bf16 ? 2 : 4);
+  const int row = v.D * (BF16 ? 2 : 4);
   TQ kq = key_q(v), vq = value_q(v);
   kq.static_scale = v.k_scale + a.h;
   vq.static_scale = v.v_scale + a.h;
   if (kq.axis == KVQ_PER_CHANNEL) {
     if (kq.bits == 2) {
-      fold_key_channels_t<2>(v, kq, staged, fs, tb, R);
+      fold_key_channels_t<2, BF16>(v, kq, staged, fs, tb, R);
     } else if (kq.bits == 4) {
-      fold_key_channels_t<4>(v, kq, staged, fs, tb, R);
+      fold_key_channels_t<4, BF16>(v, kq, staged, fs, tb, R);
     } else {
-      fold_key_channels_t<8>(v, kq, staged, fs, tb, R);
+      fold_key_channels_t<8, BF16>(v, kq, staged, fs, tb, R);
     }
   }
 #pragma unroll 1
   for (int tensor = kq.axis == KVQ_PER_CHANNEL ? 1 : 0; tensor < 2; ++tensor)
-    fold_rows(v, tensor ? vq : kq, staged + (long long)tensor * R * row, fs, R);
+    fold_rows<BF16>(v, tensor ? vq : kq, staged + tensor * R * row, fs, R);
 }
 
 __global__ void __launch_bounds__(kThreads) append_kernel(KvqView v, const void* k_new,
@@ -695,7 +668,12 @@ __global__ void __launch_bounds__(kThreads) append_kernel(KvqView v, const void*
         // the whole R-token block fits in shared memory: one parallel pass of loads,
         // then every quantizer pass reads shared memory
         if (v.R <= kMaxFold) {
-          fold_block(v, a, k_new, v_new, tb, staged);
+          __shared__ FoldSmem fs;
+          if (v.src_bf16) {
+            fold_block<true>(v, a, k_new, v_new, tb, staged, fs);
+          } else {
+            fold_block<false>(v, a, k_new, v_new, tb, staged, fs);
+          }
         } else {
           stage_block(v, a, k_new, v_new, tb, v.R, staged, [] {});
           a.st_t0 = tb;
