@@ -227,6 +227,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int lgG = __ffs(G) - 1, lgP = __ffs(v.P) - 1;
   fast_plan<kThreads>(v, G, prefA, prefB, &s_C, &s_NA, &s_NB, reinterpret_cast<int*>(&sm.stage[0][0][0]));
   if (blockIdx.x == 0) store_fast_plan(v, ws, prefA, prefB, s_C, s_NA, s_NB);
+  grid_dep_launch();  // the combine kernel may be scheduled; it waits for this grid to complete
   unsigned long long* counter =
       reinterpret_cast<unsigned long long*>(reinterpret_cast<char*>(ws) + fast_counter_offset(v.batch));
   if (lane == 0) {

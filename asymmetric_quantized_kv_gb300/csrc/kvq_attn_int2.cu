@@ -143,6 +143,7 @@ __global__ void __launch_bounds__(kThreadsI, 3)
   fast_plan<kThreadsI>(v, G, prefA, prefB, &s_C, &s_NA, &s_NB, reinterpret_cast<int*>(&sm.stage[0][0][0]));
   window_prefix<kThreadsI>(v, prefW, &s_NW, reinterpret_cast<int*>(&sm.stage[0][0][0]));
   if (blockIdx.x == 0) store_fast_plan(v, ws, prefA, prefB, s_C, s_NA, s_NB);
+  grid_dep_launch();  // the combine kernel may be scheduled; it waits for this grid to complete
   unsigned long long* counter =
       reinterpret_cast<unsigned long long*>(reinterpret_cast<char*>(ws) + fast_counter_offset(v.batch));
   if (lane == 0) {

@@ -144,6 +144,13 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(unsigned short x) {
 __device__ __forceinline__ unsigned short lo16(uint32_t x) { return static_cast<unsigned short>(x & 0xFFFFu); }
 __device__ __forceinline__ unsigned short hi16(uint32_t x) { return static_cast<unsigned short>(x >> 16); }
 
+// Programmatic dependent launch (sm_90+).  grid_dep_wait blocks until the grids
+// this one depends on have completed and their writes are visible (it returns at
+// once when the kernel was launched without the attribute); grid_dep_launch lets
+// the dependent grid's CTAs be scheduled before this grid completes.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory"); }
+
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t threads) {
   asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(threads) : "memory");
 }

@@ -5,6 +5,7 @@
 #pragma once
 
 #include "kvq_attn_plan.cuh"
+#include "kvq_ptx.cuh"
 
 namespace kvq {
 namespace {
@@ -138,16 +139,21 @@ __device__ inline FastItem decode_fast_item(const KvqView& v, const int* sA, con
 
 // Merge the chunk partials of one (sequence, query head).  Records are
 // kRec = D + 4 floats (max, sum, 2 pad, output) so outputs are 16-byte aligned.
-// Weights 2^(m_i - M) are computed once into shared memory; then 8 chunk lanes x
-// 32 channel quads read the outputs with float4 loads and reduce through smem.
+// Four warps take every fourth record; a warp loads a batch of up to
+// kCombineBatch records at once (lane = channel quad, float4 loads) and merges
+// them online into its running max, sum and output, so one round of loads covers
+// a typical sequence.  The warps then merge through shared memory.  Launched as a
+// programmatic dependent of the split kernel: it waits for that grid to complete
+// before reading the workspace.
 constexpr int kRec = kD + 4;
-constexpr int kCombineThreads = 256;
-constexpr int kCombineCache = 2048;
+constexpr int kCombineWarps = 4;
+constexpr int kCombineThreads = kCombineWarps * 32;
+constexpr int kCombineBatch = 8;
 
 __global__ void __launch_bounds__(kCombineThreads) combine_fast_kernel(KvqView v, float* ws, float* out) {
-  __shared__ float wts[kCombineCache];
-  __shared__ float red[kCombineThreads / 32];
-  __shared__ float4 acc_s[8][kD / 4];
+  __shared__ float4 o_s[kCombineWarps][kD / 4];
+  __shared__ float m_s[kCombineWarps], l_s[kCombineWarps];
+  ptx::grid_dep_wait();
   const int hq = blockIdx.x, b = blockIdx.y;
   const int* hdr = reinterpret_cast<const int*>(ws);
   const int NA = hdr[1];
@@ -160,69 +166,89 @@ __global__ void __launch_bounds__(kCombineThreads) combine_fast_kernel(KvqView v
   const long long stride = (long long)v.Hq * kRec;
   const float* baseA = part + ((long long)pA[b] * v.Hq + hq) * kRec;
   const float* baseB = part + ((long long)(NA + pB[b]) * v.Hq + hq) * kRec;
-#define KVQ_REC(i) ((i) < nA ? baseA + (long long)(i) * stride : baseB + (long long)((i) - nA) * stride)
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  float M = -INFINITY;
-  for (int i = threadIdx.x; i < n; i += kCombineThreads) M = fmaxf(M, KVQ_REC(i)[0]);
-  for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-  if (lane == 0) red[warp] = M;
-  __syncthreads();
-  M = red[0];
-  for (int w = 1; w < kCombineThreads / 32; ++w) M = fmaxf(M, red[w]);
-  __syncthreads();
-  float L = 0.f;
-  for (int i = threadIdx.x; i < n; i += kCombineThreads) {
-    const float* r = KVQ_REC(i);
-    const float w = r[0] == -INFINITY ? 0.f : exp2f(r[0] - M);
-    if (i < kCombineCache) wts[i] = w;
-    L += r[1] * w;
-  }
-  for (int o = 16; o; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
-  if (lane == 0) red[warp] = L;
-  __syncthreads();
-  L = 0.f;
-  for (int w = 0; w < kCombineThreads / 32; ++w) L += red[w];
-  const float invL = L > 0.f ? 1.f / L : 0.f;
-  // chunk lane j = warp (0..7), channel quad = lane (channels 4 lane .. 4 lane + 3)
+  float m = -INFINITY, l = 0.f;
   float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int i = warp; i < n; i += 8) {
-    const float* r = KVQ_REC(i);
-    float w;
-    if (i < kCombineCache) {
-      w = wts[i];
-    } else {
-      w = r[0] == -INFINITY ? 0.f : exp2f(r[0] - M);
-    }
-    const float4 x = reinterpret_cast<const float4*>(r + 4)[lane];
-    o.x += x.x * w;
-    o.y += x.y * w;
-    o.z += x.z * w;
-    o.w += x.w * w;
-  }
-  acc_s[warp][lane] = o;
-  __syncthreads();
-  if (threadIdx.x < kD / 4) {
-    float4 r = acc_s[0][threadIdx.x];
+  for (int i0 = warp; i0 < n; i0 += kCombineWarps * kCombineBatch) {
+    float rm[kCombineBatch], rl[kCombineBatch];
+    float4 x[kCombineBatch];
 #pragma unroll
-    for (int j = 1; j < 8; ++j) {
-      const float4 x = acc_s[j][threadIdx.x];
-      r.x += x.x; r.y += x.y; r.z += x.z; r.w += x.w;
+    for (int j = 0; j < kCombineBatch; ++j) {
+      const int i = i0 + j * kCombineWarps;
+      rm[j] = -INFINITY;
+      rl[j] = 0.f;
+      x[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (i < n) {
+        const float* r = i < nA ? baseA + (long long)i * stride : baseB + (long long)(i - nA) * stride;
+        rm[j] = r[0];
+        rl[j] = r[1];
+        x[j] = reinterpret_cast<const float4*>(r + 4)[lane];
+      }
     }
+    float mn = m;
+#pragma unroll
+    for (int j = 0; j < kCombineBatch; ++j) mn = fmaxf(mn, rm[j]);
+    if (mn != -INFINITY) {  // warp-uniform: every lane read the same records
+      const float a = exp2f(m - mn);  // 0 while nothing has been merged
+      l *= a;
+      o.x *= a; o.y *= a; o.z *= a; o.w *= a;
+#pragma unroll
+      for (int j = 0; j < kCombineBatch; ++j) {
+        const float w = rm[j] == -INFINITY ? 0.f : exp2f(rm[j] - mn);
+        l = fmaf(rl[j], w, l);
+        o.x = fmaf(x[j].x, w, o.x); o.y = fmaf(x[j].y, w, o.y);
+        o.z = fmaf(x[j].z, w, o.z); o.w = fmaf(x[j].w, w, o.w);
+      }
+      m = mn;
+    }
+  }
+  if (lane == 0) {
+    m_s[warp] = m;
+    l_s[warp] = l;
+  }
+  o_s[warp][lane] = o;
+  __syncthreads();
+  if (warp == 0) {
+    float M = m_s[0];
+#pragma unroll
+    for (int w = 1; w < kCombineWarps; ++w) M = fmaxf(M, m_s[w]);
+    float L = 0.f;
+    float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < kCombineWarps; ++w) {
+        const float a = m_s[w] == -INFINITY ? 0.f : exp2f(m_s[w] - M);
+        const float4 x = o_s[w][lane];
+        L = fmaf(l_s[w], a, L);
+        r.x = fmaf(x.x, a, r.x); r.y = fmaf(x.y, a, r.y); r.z = fmaf(x.z, a, r.z); r.w = fmaf(x.w, a, r.w);
+      }
+    }
+    const float invL = L > 0.f ? 1.f / L : 0.f;
     r.x *= invL; r.y *= invL; r.z *= invL; r.w *= invL;
-    reinterpret_cast<float4*>(out + ((long long)b * v.Hq + hq) * kD)[threadIdx.x] = r;
+    reinterpret_cast<float4*>(out + ((long long)b * v.Hq + hq) * kD)[lane] = r;
   }
 }
-#undef KVQ_REC
 
 inline size_t split_workspace_bytes(const KvqView& v, int batch) {
   const long long items = kFastTarget + 2LL * batch;
   return fast_header_bytes(batch) + (size_t)items * v.Hq * (v.D + 4) * sizeof(float);
 }
 
-// Partials -> out: one CTA per (query head, sequence).
+// Partials -> out: one CTA per (query head, sequence), launched as a programmatic
+// dependent of the split kernel just before it in the stream, so its CTAs are
+// scheduled as the split kernel's CTAs retire.
 inline cudaError_t launch_split_combine(const KvqView& v, float* ws, float* out, cudaStream_t st) {
-  combine_fast_kernel<<<dim3(v.Hq, v.batch), kCombineThreads, 0, st>>>(v, ws, out);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(v.Hq, v.batch);
+  cfg.blockDim = dim3(kCombineThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, combine_fast_kernel, v, ws, out);
 }
 
 }  // namespace
