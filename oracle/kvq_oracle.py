@@ -26,6 +26,12 @@ Everything here is the plain definition, written for a reader to check by eye:
   cache?" (E4M3 saturates at +-448, ~3 mantissa bits).  The encoder below is
   written from the OCP E4M3FN format definition (bias 7, subnormal step 2^-9,
   no infinities, 0x7F/0xFF NaN): round to nearest, ties to even, saturate.
+  FP8 E5M2 (the same page and section: saturates at +-57344, 2 mantissa bits)
+  is written from its format definition (bias 15, subnormal step 2^-16,
+  exponent 31 for infinities and NaN): round to nearest, ties to even,
+  saturating at 57344; an uncalibrated cache uses the unit scale (the same page,
+  section "Why do per-tensor scales waste bits on the K cache?", failure mode
+  1), which the static-scale path covers with scale 1.
 * Axes: K per channel over G-token groups, V per token ("Why Keys Are More
   Sensitive Than Values in INT8 KV Cache Quantization", section "Outlier
   Distribution in Key Channels"; fourth page, "What should I actually turn on
@@ -49,13 +55,14 @@ from dataclasses import dataclass
 
 import numpy as np
 
-INT2, INT4, INT8, FP8_E4M3 = 2, 4, 8, 9
+INT2, INT4, INT8, FP8_E4M3, FP8_E5M2 = 2, 4, 8, 9, 10
 SYM, ASYM = 0, 1
 PER_TENSOR, PER_TOKEN, PER_CHANNEL = 0, 1, 2
 F32, BF16 = 0, 1
 
 FL32_1EM8 = float(np.float32(1e-8))
 E4M3_MAX = 448.0
+E5M2_MAX = 57344.0
 
 
 def fl32(x):
@@ -65,8 +72,12 @@ def fl32(x):
 
 # ----------------------------------------------------------------------------- formats
 
+def is_fp8(fmt: int) -> bool:
+    return fmt in (FP8_E4M3, FP8_E5M2)
+
+
 def bits_of(fmt: int) -> int:
-    return 8 if fmt == FP8_E4M3 else int(fmt)
+    return 8 if is_fp8(fmt) else int(fmt)
 
 
 def sym_qmax(bits: int) -> int:
@@ -122,6 +133,64 @@ def e4m3_decode(byte) -> np.ndarray:
     return _E4M3[np.asarray(byte, dtype=np.int64)]
 
 
+def e5m2_decode_table() -> np.ndarray:
+    """Value of every E5M2 byte (+-inf for 0x7C/0xFC, NaN for 0x7D..0x7F and
+    0xFD..0xFF)."""
+    t = np.empty(256, dtype=np.float64)
+    for byte in range(256):
+        sign = -1.0 if byte & 0x80 else 1.0
+        e = (byte >> 2) & 0x1F
+        m = byte & 0x3
+        if e == 0x1F:
+            t[byte] = sign * np.inf if m == 0 else np.nan
+        elif e == 0:
+            t[byte] = sign * m * 2.0 ** -16
+        else:
+            t[byte] = sign * (1.0 + m / 4.0) * 2.0 ** (e - 15)
+    return t
+
+
+_E5M2 = e5m2_decode_table()
+_E5M2_POS = _E5M2[:0x7C]  # bytes 0x00..0x7B: every finite non-negative value, increasing
+
+
+def e5m2_encode(y) -> np.ndarray:
+    """Encode float values to E5M2 bytes: nearest value, ties to the even
+    mantissa (the even byte), magnitudes >= 57344 saturate to 57344 (0x7B)."""
+    y = np.asarray(y, dtype=np.float64)
+    a = np.abs(y)
+    sat = a >= E5M2_MAX
+    ac = np.where(sat | np.isnan(y), 0.0, a)
+    idx = np.searchsorted(_E5M2_POS, ac, side="right") - 1  # _E5M2_POS[idx] <= a
+    idx = np.clip(idx, 0, 0x7A)
+    lo = _E5M2_POS[idx]
+    hi = _E5M2_POS[idx + 1]
+    dlo = ac - lo
+    dhi = hi - ac
+    up = (dhi < dlo) | ((dhi == dlo) & (idx % 2 == 1))
+    mag = np.where(up, idx + 1, idx)
+    mag = np.where(sat, 0x7B, mag)
+    out = mag.astype(np.int64) | np.where(np.signbit(y), 0x80, 0)
+    out = np.where(np.isnan(y), 0x7F, out)
+    return out.astype(np.int64)
+
+
+def e5m2_decode(byte) -> np.ndarray:
+    return _E5M2[np.asarray(byte, dtype=np.int64)]
+
+
+def fp8_max(fmt: int) -> float:
+    return E5M2_MAX if fmt == FP8_E5M2 else E4M3_MAX
+
+
+def fp8_encode(y, fmt: int) -> np.ndarray:
+    return e5m2_encode(y) if fmt == FP8_E5M2 else e4m3_encode(y)
+
+
+def fp8_decode(byte, fmt: int) -> np.ndarray:
+    return e5m2_decode(byte) if fmt == FP8_E5M2 else e4m3_decode(byte)
+
+
 # ------------------------------------------------------------------------- quantizers
 
 def quant_sym(x, absmax, bits: int):
@@ -157,17 +226,17 @@ def dequant_asym(c, s, mn):
     return fl32(fl32(np.asarray(c, dtype=np.float64) * s) + mn)
 
 
-def quant_fp8(x, scale):
-    """FP8 E4M3 bytes of x/scale (scale 0 gives byte 0)."""
+def quant_fp8(x, scale, fmt: int = FP8_E4M3):
+    """FP8 bytes (E4M3 or E5M2) of x/scale (scale 0 gives byte 0)."""
     scale = np.asarray(scale, dtype=np.float64)
     with np.errstate(divide="ignore", invalid="ignore"):
         y = fl32(np.asarray(x, dtype=np.float64) / scale)
-    b = e4m3_encode(np.where(scale == 0.0, 0.0, y))
+    b = fp8_encode(np.where(scale == 0.0, 0.0, y), fmt)
     return np.where(scale == 0.0, 0, b).astype(np.int64)
 
 
-def dequant_fp8(byte, scale):
-    return fl32(e4m3_decode(byte) * np.asarray(scale, dtype=np.float64))
+def dequant_fp8(byte, scale, fmt: int = FP8_E4M3):
+    return fl32(fp8_decode(byte, fmt) * np.asarray(scale, dtype=np.float64))
 
 
 def calibrate_absmax(x, qmax: float) -> float:
@@ -209,7 +278,7 @@ def _tok_group(spec: QSpec, D: int) -> int:
 
 
 def _n_meta(spec: QSpec) -> int:
-    return 2 if (spec.mode == ASYM and spec.fmt != FP8_E4M3) else 1
+    return 2 if (spec.mode == ASYM and not is_fp8(spec.fmt)) else 1
 
 
 def _align16(n: int) -> int:
@@ -245,8 +314,8 @@ def _quant_tokens(x, spec: QSpec, static_scale, D):
 
     Returns (codes [n, D], scales [n, ng] or None, mins [n, ng] or None)."""
     bits = bits_of(spec.fmt)
-    if spec.fmt == FP8_E4M3:
-        return quant_fp8(x, static_scale), None, None
+    if is_fp8(spec.fmt):
+        return quant_fp8(x, static_scale, spec.fmt), None, None
     if spec.axis == PER_TENSOR:
         # static symmetric scale: the same rounding rule as quant_sym, with s given
         s = np.float64(static_scale)
@@ -359,8 +428,8 @@ class StreamCache:
 
 
 def _dequant_tokens(c, s, m, spec: QSpec, static_scale, D):
-    if spec.fmt == FP8_E4M3:
-        return dequant_fp8(c, static_scale)
+    if is_fp8(spec.fmt):
+        return dequant_fp8(c, static_scale, spec.fmt)
     if spec.axis == PER_TENSOR:
         return dequant_sym(c, np.float64(static_scale))
     g = _tok_group(spec, D)
@@ -468,7 +537,7 @@ def _code_bytes(c, spec: QSpec):
     """Unsigned stored code values from signed codes."""
     bits = bits_of(spec.fmt)
     c = np.asarray(c, dtype=np.int64)
-    if spec.fmt == FP8_E4M3 or spec.mode == ASYM:
+    if is_fp8(spec.fmt) or spec.mode == ASYM:
         return c
     if bits == 8:
         return c & 0xFF

@@ -182,6 +182,71 @@ def test_e4m3_relative_error_in_normal_range():
     assert rel.max() <= 2.0 ** -4
 
 
+def test_e5m2_table_is_the_top_byte_of_ieee_half():
+    # E5M2 shares IEEE binary16's sign, exponent field and bias; its two mantissa
+    # bits are the top two of binary16's ten, so byte b is the half with bits b << 8
+    halves = (np.arange(256, dtype=np.uint16) << 8).view(np.float16).astype(np.float64)
+    mine = O.e5m2_decode_table()
+    nan = np.isnan(halves)
+    assert np.array_equal(nan, np.isnan(mine))
+    assert np.array_equal(halves[~nan], mine[~nan])
+    assert O.e5m2_decode(0x7B) == O.E5M2_MAX == 57344.0  # the first page: E5M2 saturates at +-57344
+    assert O.e5m2_decode(0x01) == 2.0 ** -16 and O.e5m2_decode(0x04) == 2.0 ** -14
+
+
+def test_e5m2_encode_is_nearest_with_ties_to_even_over_all_halves():
+    # every finite half below saturation, against a brute-force nearest search
+    h = np.arange(0, 0x7C00, dtype=np.uint16).view(np.float16).astype(np.float64)
+    h = h[h < O.E5M2_MAX]
+    pos = O.e5m2_decode_table()[:0x7C]
+    d = np.abs(h[:, None] - pos[None, :])
+    best = d.min(axis=1, keepdims=True)
+    cand = d == best
+    # ties: the even byte (even mantissa)
+    want = np.where(cand.sum(1) > 1, np.argmax(cand & (np.arange(0x7C) % 2 == 0)[None, :], axis=1),
+                    np.argmax(cand, axis=1))
+    assert np.array_equal(O.e5m2_encode(h), want)
+    assert np.array_equal(O.e5m2_encode(-h[h > 0]), want[h > 0] | 0x80)
+
+
+def test_e5m2_midpoints_saturation_and_torch():
+    pos = O.e5m2_decode_table()[:0x7C]
+    mids = (pos[:-1] + pos[1:]) / 2
+    lo = np.arange(0x7B)
+    assert np.all(O.e5m2_encode(mids) == np.where(lo % 2 == 0, lo, lo + 1))
+    assert np.all(O.e5m2_encode([57344.0, 61439.0, 61440.0, 1e9]) == 0x7B)
+    assert np.all(O.e5m2_encode([-57344.0, -1e9]) == 0xFB)
+    all_bytes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    t = all_bytes.view(torch.float8_e5m2).float().double().numpy()
+    nan = np.isnan(t)
+    assert np.array_equal(nan, np.isnan(O.e5m2_decode_table()))
+    assert np.array_equal(t[~nan], O.e5m2_decode_table()[~nan])
+    g = np.random.default_rng(13)
+    y = O.fl32(g.standard_normal(50000) * 10.0 ** g.uniform(-5, 4.6, 50000))
+    y = y[np.abs(y) < 57344.0]
+    ref = torch.from_numpy(y.astype(np.float32)).to(torch.float8_e5m2).view(torch.uint8).numpy()
+    assert np.array_equal(O.e5m2_encode(y), ref.astype(np.int64))
+
+
+def test_e5m2_relative_error_in_normal_range():
+    # the first page: E5M2 has only 2 mantissa bits: <= 12.5% step error
+    g = np.random.default_rng(10)
+    y = O.fl32(np.exp(g.uniform(np.log(2.0 ** -14), np.log(57344.0), 100000)))
+    rel = np.abs(O.e5m2_decode(O.e5m2_encode(y)) - y) / y
+    assert rel.max() <= 2.0 ** -3
+    assert rel.max() > 2.0 ** -4  # coarser than E4M3
+
+
+def test_fp8_formats_quantize_with_their_own_tables():
+    g = np.random.default_rng(12)
+    x = O.fl32(g.standard_normal(4096) * 30)
+    for fmt, qmax, dec in ((O.FP8_E4M3, 448.0, O.e4m3_decode), (O.FP8_E5M2, 57344.0, O.e5m2_decode)):
+        s = O.calibrate_absmax(x, qmax)
+        b = O.quant_fp8(x, s, fmt)
+        assert np.array_equal(O.dequant_fp8(b, s, fmt), O.fl32(dec(b) * s))
+        assert np.array_equal(b, O.fp8_encode(O.fl32(x / s), fmt))
+
+
 def test_fp8_scale_roundtrip_and_zero_scale():
     g = np.random.default_rng(11)
     x = O.fl32(g.standard_normal(4096) * 30)

@@ -184,6 +184,54 @@ def test_attention_kl_falls_with_bits():
         assert ov >= 0.95
 
 
+# ------------------------------------------- FP8 formats, calibrated and unit scales
+
+def fp8_head(seed, T=2048, reach=1000.0):
+    """A synthetic head for the FP8 comparison ("FP8 KV Cache Quantization: Why
+    Keys Break Before Values", section "Why do per-tensor scales waste bits on
+    the K cache?", failure mode 1): N(0,1) keys whose channels 3, 17, 44 and 91
+    are scaled by reach / 3 (so they reach about +-reach), N(0,1) values and 8
+    queries N(0, 0.05^2); all bf16."""
+    K = W.small_stream(seed, T, 128).astype(np.float64)
+    K[:, [3, 17, 44, 91]] *= reach / 3.0
+    K = W.bf16_round(K.astype(np.float32))[1].astype(np.float64)
+    V = W.small_stream(seed + 50, T, 128, bf16=True).astype(np.float64)
+    q = W.bf16_round(np.random.default_rng(seed).standard_normal((8, 128)).astype(np.float32) * 0.05)[1]
+    return K, V, q.astype(np.float64)
+
+
+FP8_SCHEMES = (("E4M3, unit scale", O.FP8_E4M3, None), ("E5M2, unit scale", O.FP8_E5M2, None),
+               ("E4M3, calibrated", O.FP8_E4M3, 448.0), ("E5M2, calibrated", O.FP8_E5M2, 57344.0))
+
+
+def fp8_errors(reach, seeds=(0, 1, 2)):
+    """Mean relative L2 attention error of each FP8 key scheme (values kept
+    exact) against float64 attention over the bf16 keys."""
+    out = {}
+    for seed in seeds:
+        K, V, q = fp8_head(seed, reach=reach)
+        ref = O.attention(q, K, V)
+        for name, fmt, qmax in FP8_SCHEMES:
+            s = 1.0 if qmax is None else O.calibrate_absmax(K, qmax)
+            Kq = O.dequant_fp8(O.quant_fp8(K, s, fmt), s, fmt)
+            e = np.linalg.norm(O.attention(q, Kq, V) - ref, axis=1) / np.linalg.norm(ref, axis=1)
+            out.setdefault(name, []).append(e.mean())
+    return {k: float(np.mean(v)) for k, v in out.items()}
+
+
+def test_unit_scale_clipping_is_worse_than_coarse_e5m2():
+    e = fp8_errors(1000.0)
+    assert e["E4M3, unit scale"] > 2.0 * e["E5M2, unit scale"], e  # clipping deletes the channel
+    assert e["E5M2, unit scale"] > e["E4M3, calibrated"], e
+    assert e["E4M3, calibrated"] < e["E5M2, calibrated"], e  # 3 mantissa bits beat 2 once nothing clips
+
+
+def test_unit_scale_costs_little_in_range():
+    e = fp8_errors(250.0)  # below 448: nothing clips; calibration only moves values to finer binades
+    assert e["E4M3, unit scale"] <= 1.3 * e["E4M3, calibrated"], e
+    assert e["E4M3, unit scale"] < 0.1 * fp8_errors(1000.0)["E4M3, unit scale"], e
+
+
 # --------------------------------------------------------------------- the tables
 
 def test_study_tables():
@@ -204,3 +252,7 @@ def test_study_tables():
                             ("INT8 per-channel", O.QSpec(O.INT8, O.SYM, O.PER_CHANNEL, g))):
             r = np.array([_agreement(cid, s, h, 4096, spec, theta) for s, h in HEADS[cid]])
             print(f"  workload {cid} {label:18s} {r[:, 0].mean():9.3g} {r[:, 1].mean():6.3f} {r[:, 2].mean():6.3f}")
+    print("FP8 keys, attention rel L2 error (values exact), keys reaching ~250 / ~1000:")
+    lo, hi = fp8_errors(250.0), fp8_errors(1000.0)
+    for name, _, _ in FP8_SCHEMES:
+        print(f"  {name:18s} {lo[name]:.4f} / {hi[name]:.4f}")
