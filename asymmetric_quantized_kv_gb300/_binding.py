@@ -15,7 +15,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libkvq.so")
 
 KVQ_OK, KVQ_ERR_INVALID_ARG, KVQ_ERR_UNSUPPORTED, KVQ_ERR_CUDA, KVQ_ERR_CAPACITY, KVQ_ERR_WORKSPACE = range(6)
-KVQ_INT2, KVQ_INT4, KVQ_INT8, KVQ_FP8_E4M3 = 2, 4, 8, 9
+KVQ_INT2, KVQ_INT4, KVQ_INT8, KVQ_FP8_E4M3, KVQ_FP8_E5M2 = 2, 4, 8, 9, 10
 KVQ_SYM_ABSMAX, KVQ_ASYM_MINMAX = 0, 1
 KVQ_PER_TENSOR, KVQ_PER_TOKEN, KVQ_PER_CHANNEL = 0, 1, 2
 KVQ_F32, KVQ_BF16 = 0, 1

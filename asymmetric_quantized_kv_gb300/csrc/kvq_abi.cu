@@ -8,16 +8,17 @@
 
 namespace {
 
-inline int bits_of(int fmt) { return fmt == KVQ_FP8_E4M3 ? 8 : fmt; }
+inline bool fmt_is_fp8(int fmt) { return fmt == KVQ_FP8_E4M3 || fmt == KVQ_FP8_E5M2; }
+inline int bits_of(int fmt) { return fmt_is_fp8(fmt) ? 8 : fmt; }
 inline bool fmt_ok(int fmt) {
-  return fmt == KVQ_INT2 || fmt == KVQ_INT4 || fmt == KVQ_INT8 || fmt == KVQ_FP8_E4M3;
+  return fmt == KVQ_INT2 || fmt == KVQ_INT4 || fmt == KVQ_INT8 || fmt_is_fp8(fmt);
 }
 inline size_t align16(size_t n) { return (n + 15) & ~size_t(15); }
 
 int tok_group(const kvq_qspec& s, int D) { return s.group ? s.group : D; }
 
 int n_meta(const kvq_qspec& s) {
-  return (s.mode == KVQ_ASYM_MINMAX && s.fmt != KVQ_FP8_E4M3) ? 2 : 1;
+  return (s.mode == KVQ_ASYM_MINMAX && !fmt_is_fp8(s.fmt)) ? 2 : 1;
 }
 
 kvq_status check_spec(const kvq_qspec& s, int D, bool is_key) {
@@ -25,7 +26,7 @@ kvq_status check_spec(const kvq_qspec& s, int D, bool is_key) {
   if (s.mode != KVQ_SYM_ABSMAX && s.mode != KVQ_ASYM_MINMAX) return KVQ_ERR_INVALID_ARG;
   if (s.axis != KVQ_PER_TENSOR && s.axis != KVQ_PER_TOKEN && s.axis != KVQ_PER_CHANNEL)
     return KVQ_ERR_INVALID_ARG;
-  if (s.fmt == KVQ_FP8_E4M3) return s.axis == KVQ_PER_TENSOR ? KVQ_OK : KVQ_ERR_UNSUPPORTED;
+  if (fmt_is_fp8(s.fmt)) return s.axis == KVQ_PER_TENSOR ? KVQ_OK : KVQ_ERR_UNSUPPORTED;
   if (s.axis == KVQ_PER_TENSOR) return s.mode == KVQ_SYM_ABSMAX ? KVQ_OK : KVQ_ERR_UNSUPPORTED;
   if (s.axis == KVQ_PER_CHANNEL) {
     if (!is_key) return KVQ_ERR_UNSUPPORTED;
@@ -88,12 +89,12 @@ bool make_view(const kvq_config* c, const kvq_cache* k, KvqView* v) {
   v->D = c->head_dim;
   v->n_rep = c->num_q_heads / c->num_kv_heads;
   v->kfmt = c->k.fmt;
-  v->kmode = c->k.fmt == KVQ_FP8_E4M3 ? KVQ_SYM_ABSMAX : c->k.mode;
+  v->kmode = fmt_is_fp8(c->k.fmt) ? KVQ_SYM_ABSMAX : c->k.mode;
   v->kaxis = c->k.axis;
   v->kgroup = c->k.axis == KVQ_PER_CHANNEL ? c->k.group
               : c->k.axis == KVQ_PER_TOKEN ? tok_group(c->k, c->head_dim) : 0;
   v->vfmt = c->v.fmt;
-  v->vmode = c->v.fmt == KVQ_FP8_E4M3 ? KVQ_SYM_ABSMAX : c->v.mode;
+  v->vmode = fmt_is_fp8(c->v.fmt) ? KVQ_SYM_ABSMAX : c->v.mode;
   v->vaxis = c->v.axis;
   v->vgroup = c->v.axis == KVQ_PER_TOKEN ? tok_group(c->v, c->head_dim) : 0;
   v->kbits = bits_of(c->k.fmt);

@@ -158,14 +158,14 @@ __device__ void quantize_rows(const KvqView& v, const Src& s, const AppendCtx& a
       __syncthreads();
     }
     const int lg = q.axis == KVQ_PER_TOKEN ? log2i(q.group) : 0;
-    const float ss = q.axis == KVQ_PER_TENSOR || q.fmt == KVQ_FP8_E4M3 ? q.static_scale[a.h] : 0.f;
+    const float ss = q.axis == KVQ_PER_TENSOR || is_fp8(q.fmt) ? q.static_scale[a.h] : 0.f;
     const float sr = ss > 0.f ? __frcp_rn(ss) : 0.f;
     for (int e = threadIdx.x; e < (n << lD); e += kThreads) {
       const int r = e >> lD, c = e & (D - 1);
       const float x = sm.xs[r][c];
       unsigned u;
-      if (q.fmt == KVQ_FP8_E4M3) {
-        u = fp8_code(x, ss);
+      if (is_fp8(q.fmt)) {
+        u = fp8_code(x, ss, q.fmt);
       } else if (q.axis == KVQ_PER_TENSOR) {
         u = stored_code(sym_code_r(x, ss, sr, q.bits), q.bits, KVQ_SYM_ABSMAX);
       } else {
@@ -447,7 +447,7 @@ __device__ __forceinline__ void fold_rows_t(const KvqView& v, const TQ& q, const
   const int D = v.D, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int lpt = D / kCPL, tpw = 32 / lpt;  // lanes per token, tokens per warp
   const int sub = lane % lpt, tok = lane / lpt;
-  const bool fp8 = q.fmt == KVQ_FP8_E4M3;
+  const bool fp8 = is_fp8(q.fmt);
   const bool stat = fp8 || q.axis == KVQ_PER_TENSOR;
   const bool asym = !stat && q.mode == KVQ_ASYM_MINMAX;
   const float ss = stat ? q.static_scale[0] : 0.f;
@@ -505,7 +505,7 @@ __device__ __forceinline__ void fold_rows_t(const KvqView& v, const TQ& q, const
       uint32_t w = 0u;
       if (fp8) {
 #pragma unroll
-        for (int i = 0; i < kCPW; ++i) w |= fp8_code(x[i], ss) << (8 * i);
+        for (int i = 0; i < kCPW; ++i) w |= fp8_code(x[i], ss, q.fmt) << (8 * i);
       } else {
         w = pack_codes<kCPW, BITS>(x, sc, r, m, asym);
       }
@@ -755,8 +755,8 @@ __global__ void dequantize_kernel(KvqView v, int seq, int t0, float* k_out, floa
         const uint8_t* hb = page + (long long)h * v.head_bytes;
         const int slot = t % v.P;
         const unsigned ku = get_code(hb + slot * v.krow, c, v.kbits);
-        if (v.kfmt == KVQ_FP8_E4M3) {
-          kx = __fmul_rn(fp8_e4m3_to_float(ku), v.k_scale[h]);
+        if (is_fp8(v.kfmt)) {
+          kx = __fmul_rn(fp8_to_float(ku, v.kfmt), v.k_scale[h]);
         } else if (v.kaxis == KVQ_PER_TENSOR) {
           kx = dequant_sym(signed_code(ku, v.kbits, KVQ_SYM_ABSMAX), v.k_scale[h]);
         } else {
@@ -780,8 +780,8 @@ __global__ void dequantize_kernel(KvqView v, int seq, int t0, float* k_out, floa
           kx = v.kmode == KVQ_ASYM_MINMAX ? dequant_asym(code, s, mn) : dequant_sym(code, s);
         }
         const unsigned vu = get_code(hb + v.off_vc + slot * v.vrow, c, v.vbits);
-        if (v.vfmt == KVQ_FP8_E4M3) {
-          vx = __fmul_rn(fp8_e4m3_to_float(vu), v.v_scale[h]);
+        if (is_fp8(v.vfmt)) {
+          vx = __fmul_rn(fp8_to_float(vu, v.vfmt), v.v_scale[h]);
         } else if (v.vaxis == KVQ_PER_TENSOR) {
           vx = dequant_sym(signed_code(vu, v.vbits, KVQ_SYM_ABSMAX), v.v_scale[h]);
         } else {

@@ -34,7 +34,7 @@ struct TileKeys {
 
 __device__ __forceinline__ float deq_key(const KvqView& v, const TileKeys& tk, int h, int c) {
   const unsigned u = get_code(tk.hb + tk.slot * v.krow, c, v.kbits);
-  if (v.kfmt == KVQ_FP8_E4M3) return __fmul_rn(fp8_e4m3_to_float(u), v.k_scale[h]);
+  if (is_fp8(v.kfmt)) return __fmul_rn(fp8_to_float(u, v.kfmt), v.k_scale[h]);
   if (v.kaxis == KVQ_PER_TENSOR) return dequant_sym(signed_code(u, v.kbits, KVQ_SYM_ABSMAX), v.k_scale[h]);
   const int code = signed_code(u, v.kbits, v.kmode);
   float s, mn = 0.f;
@@ -51,7 +51,7 @@ __device__ __forceinline__ float deq_key(const KvqView& v, const TileKeys& tk, i
 
 __device__ __forceinline__ float deq_value(const KvqView& v, const uint8_t* hb, int slot, int h, int c) {
   const unsigned u = get_code(hb + v.off_vc + slot * v.vrow, c, v.vbits);
-  if (v.vfmt == KVQ_FP8_E4M3) return __fmul_rn(fp8_e4m3_to_float(u), v.v_scale[h]);
+  if (is_fp8(v.vfmt)) return __fmul_rn(fp8_to_float(u, v.vfmt), v.v_scale[h]);
   if (v.vaxis == KVQ_PER_TENSOR) return dequant_sym(signed_code(u, v.vbits, KVQ_SYM_ABSMAX), v.v_scale[h]);
   const float* meta = reinterpret_cast<const float*>(hb + v.off_vm + slot * v.v_ng * v.v_nmeta * 4);
   const int grp = c / v.vgroup;

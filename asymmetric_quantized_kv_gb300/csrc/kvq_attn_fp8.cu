@@ -1,4 +1,4 @@
-// Tensor-core split-K decode attention for FP8 E4M3 keys and values with
+// Tensor-core split-K decode attention for FP8 E4M3 (or E5M2) keys and values with
 // per-head static scales (k_scale, v_scale), head_dim 128, 8 query heads per
 // kv-head, no residual window: the 70B-shaped decode layer of the FP8 scheme
 // ("Quantized KV Cache" / vLLM documentation, section "FP8 E4M3 with
@@ -11,7 +11,7 @@
 // so the warps never wait on one another.
 //
 // Per 16-token tile and warp:
-//   QK: K bytes -> f16 with cvt.e4m3x2 (exact), A = keys (16 tokens x 16
+//   QK: K bytes -> f16 with cvt.e4m3x2 / cvt.e5m2x2 (exact), A = keys (16 tokens x 16
 //       channels), B = q * k_scale * softmax_scale * log2(e) split hi/lo, two
 //       8-column blocks (4 query heads x {hi, lo} each).  K needs no split: its
 //       f16 values are exact.
@@ -58,6 +58,7 @@ __device__ __forceinline__ const uint4* swz_row(const uint8_t* tile, int row) {
   return reinterpret_cast<const uint4*>(tile + row * kRowB);
 }
 
+template <bool kE5M2>
 __global__ void __launch_bounds__(kThreads8)
     split_fp8_kernel(KvqView v, const void* q, float scale, float* ws, const __grid_constant__ CUtensorMap tmap) {
   extern __shared__ unsigned char dyn_raw[];
@@ -192,8 +193,8 @@ __global__ void __launch_bounds__(kThreads8)
         for (int j = 0; j < 4; ++j) {
           const int s = 4 * hh + j;
           const uint4 b = sm.bq[warp][s][lane];
-          const uint32_t a0 = e4m3x2_to_f16x2(lo16(w0[j])), a2 = e4m3x2_to_f16x2(hi16(w0[j]));
-          const uint32_t a1 = e4m3x2_to_f16x2(lo16(w1[j])), a3 = e4m3x2_to_f16x2(hi16(w1[j]));
+          const uint32_t a0 = fp8x2_to_f16x2<kE5M2>(lo16(w0[j])), a2 = fp8x2_to_f16x2<kE5M2>(hi16(w0[j]));
+          const uint32_t a1 = fp8x2_to_f16x2<kE5M2>(lo16(w1[j])), a3 = fp8x2_to_f16x2<kE5M2>(hi16(w1[j]));
           mma_16816(acc[0], a0, a1, a2, a3, b.x, b.y);
           mma_16816(acc[1], a0, a1, a2, a3, b.z, b.w);
         }
@@ -273,8 +274,8 @@ __global__ void __launch_bounds__(kThreads8)
         // bytes 2(m%2), 2(m%2)+1 of word m/2 of the two tokens: (ch even: tok A, tok B, ch odd: tok A, tok B)
         const uint32_t sel = (m & 1) ? 0x7362u : 0x5140u;
         const uint32_t ya = prmt(wa[m >> 1], wb[m >> 1], sel), yc = prmt(wc[m >> 1], wd[m >> 1], sel);
-        const uint32_t a0 = e4m3x2_to_f16x2(lo16(ya)), a1 = e4m3x2_to_f16x2(hi16(ya));
-        const uint32_t a2 = e4m3x2_to_f16x2(lo16(yc)), a3 = e4m3x2_to_f16x2(hi16(yc));
+        const uint32_t a0 = fp8x2_to_f16x2<kE5M2>(lo16(ya)), a1 = fp8x2_to_f16x2<kE5M2>(hi16(ya));
+        const uint32_t a2 = fp8x2_to_f16x2<kE5M2>(lo16(yc)), a3 = fp8x2_to_f16x2<kE5M2>(hi16(yc));
         mma_16816(O[m], a0, a1, a2, a3, b0h, b1h);
         mma_16816(O[m], a0, a1, a2, a3, b0l, b1l);
       }
@@ -333,7 +334,8 @@ long long pool_rows(const KvqView& v) { return (long long)v.n_pages * v.page_byt
 }  // namespace
 
 bool fp8_shape_eligible(const KvqView& v) {
-  return v.D == kD && v.n_rep == kRep8 && v.kfmt == KVQ_FP8_E4M3 && v.vfmt == KVQ_FP8_E4M3 && v.R == 0 &&
+  return v.D == kD && v.n_rep == kRep8 && (v.kfmt == KVQ_FP8_E4M3 || v.kfmt == KVQ_FP8_E5M2) &&
+         v.vfmt == v.kfmt && v.R == 0 &&
          v.P >= kTileT && (v.P & (v.P - 1)) == 0 && v.page_bytes % kRowB == 0 && v.head_bytes % kRowB == 0 && v.off_vc % kRowB == 0 &&
          v.batch <= 4096;
 }
@@ -355,23 +357,27 @@ kvq_status launch_fp8(const KvqView& v, const void* q, float* out, float scale, 
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return KVQ_ERR_UNSUPPORTED;
   const size_t smem = sizeof(SmemF8) + 1024 + sizeof(int) * 2 * (v.batch + 1);
-  static int occ_cache[64] = {0};
+  const bool e5m2 = v.kfmt == KVQ_FP8_E5M2;
+  void (*kern)(KvqView, const void*, float, float*, const CUtensorMap) =
+      e5m2 ? split_fp8_kernel<true> : split_fp8_kernel<false>;
+  static int occ_cache[2][64] = {{0}};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64) return KVQ_ERR_UNSUPPORTED;
-  if (!occ_cache[dev]) {
-    if (cudaFuncSetAttribute(split_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  int& occ_dev = occ_cache[e5m2 ? 1 : 0][dev];
+  if (!occ_dev) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)(sizeof(SmemF8) + 1024 + sizeof(int) * 2 * 4097)) != cudaSuccess)
       return KVQ_ERR_CUDA;
     int occ = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, split_fp8_kernel, kThreads8, smem) != cudaSuccess)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kThreads8, smem) != cudaSuccess)
       return KVQ_ERR_CUDA;
-    occ_cache[dev] = occ > 0 ? occ : 1;
+    occ_dev = occ > 0 ? occ : 1;
   }
-  const int grid = num_sms() * occ_cache[dev];
+  const int grid = num_sms() * occ_dev;
   if (cudaMemsetAsync(static_cast<char*>(ws) + fast_counter_offset(v.batch), 0, 8, st) != cudaSuccess)
     return KVQ_ERR_CUDA;
-  split_fp8_kernel<<<grid, kThreads8, smem, st>>>(v, q, scale, static_cast<float*>(ws), tmap);
+  kern<<<grid, kThreads8, smem, st>>>(v, q, scale, static_cast<float*>(ws), tmap);
   if (cudaGetLastError() != cudaSuccess) return KVQ_ERR_CUDA;
   return launch_split_combine(v, static_cast<float*>(ws), out, st) == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }

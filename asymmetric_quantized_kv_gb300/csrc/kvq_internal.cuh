@@ -125,13 +125,19 @@ __device__ __forceinline__ unsigned stored_code(int c, int bits, int mode) {
   return static_cast<unsigned>(c + (1 << (bits - 1)));
 }
 
-__device__ __forceinline__ float fp8_e4m3_to_float(unsigned byte) {
-  const __half_raw h = __nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(byte), __NV_E4M3);
+__device__ __forceinline__ bool is_fp8(int fmt) { return fmt == KVQ_FP8_E4M3 || fmt == KVQ_FP8_E5M2; }
+
+// Value of an FP8 byte of format fmt (E4M3 or E5M2); exact in f16 and fp32.
+__device__ __forceinline__ float fp8_to_float(unsigned byte, int fmt) {
+  const __half_raw h = __nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(byte),
+                                               fmt == KVQ_FP8_E5M2 ? __NV_E5M2 : __NV_E4M3);
   return __half2float(__half(h));
 }
 
-__device__ __forceinline__ unsigned float_to_fp8_e4m3(float y) {
-  return static_cast<unsigned>(__nv_cvt_float_to_fp8(y, __NV_SATFINITE, __NV_E4M3));
+// FP8 byte of y: nearest value, ties to even, saturating at the format's maximum.
+__device__ __forceinline__ unsigned float_to_fp8(float y, int fmt) {
+  return static_cast<unsigned>(
+      __nv_cvt_float_to_fp8(y, __NV_SATFINITE, fmt == KVQ_FP8_E5M2 ? __NV_E5M2 : __NV_E4M3));
 }
 
 // ---- the exact quantization steps of include/kvq.h
@@ -192,9 +198,9 @@ __device__ __forceinline__ int asym_code_r(float x, float mn, float s, float r, 
   return static_cast<int>(fminf(fmaxf(c, 0.f), static_cast<float>(asym_qmax(bits))));
 }
 
-__device__ __forceinline__ unsigned fp8_code(float x, float s) {
+__device__ __forceinline__ unsigned fp8_code(float x, float s, int fmt) {
   if (s == 0.f) return 0u;
-  return float_to_fp8_e4m3(__fdiv_rn(x, s));
+  return float_to_fp8(__fdiv_rn(x, s), fmt);
 }
 
 __device__ __forceinline__ float dequant_sym(int c, float s) {

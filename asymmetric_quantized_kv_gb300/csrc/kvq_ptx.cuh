@@ -141,6 +141,17 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(unsigned short x) {
   asm("cvt.rn.f16x2.e4m3x2 %0, %1;\n" : "=r"(r) : "h"(x));
   return r;
 }
+// Two E5M2 bytes (low byte -> low half) to f16x2; E5M2 is a subset of f16, so
+// the conversion is exact.
+__device__ __forceinline__ uint32_t e5m2x2_to_f16x2(unsigned short x) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.e5m2x2 %0, %1;\n" : "=r"(r) : "h"(x));
+  return r;
+}
+template <bool E5M2>
+__device__ __forceinline__ uint32_t fp8x2_to_f16x2(unsigned short x) {
+  return E5M2 ? e5m2x2_to_f16x2(x) : e4m3x2_to_f16x2(x);
+}
 __device__ __forceinline__ unsigned short lo16(uint32_t x) { return static_cast<unsigned short>(x & 0xFFFFu); }
 __device__ __forceinline__ unsigned short hi16(uint32_t x) { return static_cast<unsigned short>(x >> 16); }
 

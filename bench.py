@@ -40,7 +40,9 @@ sys.path.insert(0, ROOT)
 import kvq_inputs as W  # noqa: E402
 
 METRIC = "quantized-KV decode attention: KV bytes GB/s (% of HBM peak), µs/step"
-INT2, INT4, INT8, FP8 = 2, 4, 8, 9
+INT2, INT4, INT8, FP8, FP8_E5M2 = 2, 4, 8, 9, 10
+FP8_MAX = {FP8: 448.0, FP8_E5M2: 57344.0}  # calibration qmax of each FP8 format
+FP8_FORMATS = {"e4m3": FP8, "e5m2": FP8_E5M2}
 SYM, ASYM = 0, 1
 TEN, TOK, CH = 0, 1, 2
 BF16 = 1
@@ -58,7 +60,7 @@ SPLIT_TRAFFIC = {5: 1791.3e6, 4: 2193.4e6, 3: 557.3e6}
 SPLIT_KERNEL = {5: "split_rope_i8i4_kernel", 4: "split_fp8_kernel", 3: "split_int2_kernel"}
 
 
-def workload_spec(cid: int, batch: int = 0) -> dict:
+def workload_spec(cid: int, batch: int = 0, fp8: str = "e4m3") -> dict:
     w = W.WORKLOADS[cid]
     if batch:  # the first `batch` sequences of the workload (smaller captures for ncu)
         import dataclasses
@@ -73,16 +75,21 @@ def workload_spec(cid: int, batch: int = 0) -> dict:
                     append=False, name="Llama-3.1-8B decode layer, B16, 32768 quantized + 127 window tokens, "
                                        "Hq32/Hkv8/D128, KIVI 2-bit K per-channel (G32) + V per-token (g32)")
     if cid == 4:
-        return dict(w=w, k=(FP8, SYM, TEN, 0), v=(FP8, SYM, TEN, 0), R=0, P=256, rope=0, theta=1e4, append=False,
-                    name="Llama-3.1-70B decode layer, B8, 131072 tokens, Hq64/Hkv8/D128, FP8 E4M3 K/V with "
-                         "per-head absmax/448 scales")
+        f = FP8_FORMATS[fp8]
+        return dict(w=w, k=(f, SYM, TEN, 0), v=(f, SYM, TEN, 0), R=0, P=256, rope=0, theta=1e4, append=False,
+                    name=f"Llama-3.1-70B decode layer, B8, 131072 tokens, Hq64/Hkv8/D128, FP8 {fp8.upper()} K/V "
+                         f"with per-head absmax/{FP8_MAX[f]:g} scales")
     raise SystemExit(f"unknown --config {cid}")
 
 
 # ------------------------------------------------------------------ byte accounting
 
+def _is_fp8(fmt):
+    return fmt in FP8_MAX
+
+
 def _bits(fmt):
-    return 8 if fmt == FP8 else fmt
+    return 8 if _is_fp8(fmt) else fmt
 
 
 def quantized_bytes(spec, n: int) -> int:
@@ -90,8 +97,8 @@ def quantized_bytes(spec, n: int) -> int:
     D = spec["w"].head_dim
     kf, kmode, kaxis, kg = spec["k"]
     vf, vmode, vaxis, vg = spec["v"]
-    nmk = 2 if kmode == ASYM and kf != FP8 else 1
-    nmv = 2 if vmode == ASYM and vf != FP8 else 1
+    nmk = 2 if kmode == ASYM and not _is_fp8(kf) else 1
+    nmv = 2 if vmode == ASYM and not _is_fp8(vf) else 1
     total = n * D * (_bits(kf) + _bits(vf)) // 8
     if kaxis == CH:
         total += (n // kg) * D * 4 * nmk
@@ -145,16 +152,16 @@ def append_bytes(spec, lens_before) -> int:
 def _oracle_worker(job):
     """Time the oracle's decode (dequantize + RoPE + attention) on one sampled
     (sequence, kv-head) stream; one BLAS thread per worker process."""
-    cid, b, h, T, steps = job
+    cid, b, h, T, steps, fp8 = job
     from oracle import kvq_oracle as O
-    spec = workload_spec(cid)
+    spec = workload_spec(cid, 0, fp8)
     w = spec["w"]
     cfg = O.Config(w.num_q_heads, w.num_kv_heads, w.head_dim, O.QSpec(*spec["k"]), O.QSpec(*spec["v"]),
                    spec["R"], spec["P"], spec["rope"], spec["theta"], O.BF16 if w.src_dtype == "bf16" else O.F32)
     K = W.kv_block(w, b, h, W.KIND_K, 0, T)
     V = W.kv_block(w, b, h, W.KIND_V, 0, T)
-    ks = O.calibrate_absmax(K, 448.0) if spec["k"][0] == FP8 else 0.0
-    vs = O.calibrate_absmax(V, 448.0) if spec["v"][0] == FP8 else 0.0
+    ks = O.calibrate_absmax(K, FP8_MAX[spec["k"][0]]) if _is_fp8(spec["k"][0]) else 0.0
+    vs = O.calibrate_absmax(V, FP8_MAX[spec["v"][0]]) if _is_fp8(spec["v"][0]) else 0.0
     st = O.quantize_stream(cfg, K, V, ks, vs)
     q = W.queries(w, 0)[b % w.batch, h * cfg.n_rep:(h + 1) * cfg.n_rep].astype(np.float64)
     t0 = time.perf_counter()
@@ -163,19 +170,19 @@ def _oracle_worker(job):
     return time.perf_counter() - t0
 
 
-def cpu_oracle_throughput(cid: int, n_streams: int, steps: int = 1):
+def cpu_oracle_throughput(cid: int, n_streams: int, steps: int = 1, fp8: str = "e4m3"):
     """Oracle GB/s on a bounded sample of the workload's streams, timed in a
     spawned process pool (one BLAS thread per process)."""
     import multiprocessing as mp
-    spec = workload_spec(cid)
+    spec = workload_spec(cid, 0, fp8)
     w = spec["w"]
     lens = W.lengths(w)
     g = np.random.default_rng(1234)
     picks = [(int(g.integers(0, w.batch)), int(g.integers(0, w.num_kv_heads))) for _ in range(n_streams)]
     if cid == 4:  # 131072-token streams: a prefix keeps the sample bounded
-        jobs = [(cid, b, h, 16384, steps) for b, h in picks]
+        jobs = [(cid, b, h, 16384, steps, fp8) for b, h in picks]
     else:
-        jobs = [(cid, b, h, int(lens[b]), steps) for b, h in picks]
+        jobs = [(cid, b, h, int(lens[b]), steps, fp8) for b, h in picks]
     try:
         cores = len(os.sched_getaffinity(0))
     except AttributeError:
@@ -312,7 +319,7 @@ def build_cache(spec, device, extra_tokens, gen_seed=1):
     g = torch.Generator(device=device)
     g.manual_seed(gen_seed)
     chunk = 4096 if Bn * H * D * 4096 * 2 < (1 << 31) else 1024
-    if spec["k"][0] == FP8:  # calibrate on the whole source, then append it (same draws)
+    if _is_fp8(spec["k"][0]):  # calibrate on the whole source, then append it (same draws)
         state = g.get_state()
         kmax = torch.zeros(H, device=device)
         vmax = torch.zeros(H, device=device)
@@ -323,9 +330,9 @@ def build_cache(spec, device, extra_tokens, gen_seed=1):
             kk = kk.transpose(0, 1).reshape(-1, H, D)
             vv = vv.transpose(0, 1).reshape(-1, H, D)
             tmp = torch.empty(H, device=device)
-            K.kvq_calibrate_absmax(cfg, kk.contiguous(), kk.shape[0], 448.0, tmp)
+            K.kvq_calibrate_absmax(cfg, kk.contiguous(), kk.shape[0], FP8_MAX[spec["k"][0]], tmp)
             kmax = torch.maximum(kmax, tmp)
-            K.kvq_calibrate_absmax(cfg, vv.contiguous(), vv.shape[0], 448.0, tmp)
+            K.kvq_calibrate_absmax(cfg, vv.contiguous(), vv.shape[0], FP8_MAX[spec["v"][0]], tmp)
             vmax = torch.maximum(vmax, tmp)
             done += n
         cache.k_scale.copy_(kmax)
@@ -469,11 +476,12 @@ def main():
     ap.add_argument("--cpu-streams", type=int, default=16)
     ap.add_argument("--cpu-steps", type=int, default=8)
     ap.add_argument("--batch", type=int, default=0, help="use only the first N sequences (profiling)")
+    ap.add_argument("--fp8", default="e4m3", choices=sorted(FP8_FORMATS), help="FP8 format of --config 4")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
-    spec = workload_spec(args.config, args.batch)
+    spec = workload_spec(args.config, args.batch, args.fp8)
     w = spec["w"]
 
     if args.impl == "reference":
@@ -484,7 +492,7 @@ def main():
         for _ in range(args.warmup):
             pass  # the oracle has no warm state to build
         for _ in range(args.steps):
-            detail = cpu_oracle_throughput(args.config, n_streams=max(2, args.cpu_streams // 4))
+            detail = cpu_oracle_throughput(args.config, n_streams=max(2, args.cpu_streams // 4), fp8=args.fp8)
             per_step.append(detail["value"])
         val = statistics.median(per_step)
         detail["value"] = val
@@ -498,7 +506,7 @@ def main():
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_oracle_throughput(args.config, n_streams=args.cpu_streams, steps=args.cpu_steps)
+        cpu = cpu_oracle_throughput(args.config, n_streams=args.cpu_streams, steps=args.cpu_steps, fp8=args.fp8)
 
     import torch
     if world > 1:
@@ -527,7 +535,7 @@ def main():
                    "l2": "inputs (%.2f GB per step) larger than the 129 MB L2; no flush" % (att_bytes / 1e9)},
         "pct_of_hbm_peak": 100.0 * value / peak,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": SPLIT_TRAFFIC.get(args.config) if not args.batch else None,
+                     "traffic": SPLIT_TRAFFIC.get(args.config) if not args.batch and args.fp8 == "e4m3" else None,
                      "kernel": f"kvq_decode_attention: {SPLIT_KERNEL[args.config]} + combine (timed together)",
                      "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)" if peak_kind == "measured"
                      else "fallback 6.8 TB/s", "us_per_launch": att_ms * 1e3,

@@ -24,8 +24,11 @@
  *     by an angle that depends on the absolute position (fourth page, section
  *     "Where does RoPE break this?").
  *   - FP8 E4M3 with calibrated per-head k_scale / v_scale, saturating at
- *     +-448 (first page, section "Why do per-tensor scales waste bits on the
- *     K cache?").
+ *     +-448, and FP8 E5M2, saturating at +-57344 with 2 mantissa bits (first
+ *     page, section "Why do per-tensor scales waste bits on the K cache?").
+ *     A cache without calibrated scales holds 1.0 in k_scale / v_scale (the
+ *     unit scale of that section's first failure mode): raw magnitudes are
+ *     then clipped at the format's maximum.
  *
  * Conventions for every entry point
  *   - All tensor pointers are DEVICE pointers unless stated otherwise; the
@@ -51,6 +54,8 @@
  *   FP8 E4M3:   s = k_scale[h] (or v_scale[h]); y = x/s; byte = E4M3FN
  *               encoding of y, round-to-nearest-even, saturating to +-448
  *               (byte 0 when s == 0); x^ = decode(byte)*s.
+ *   FP8 E5M2:   the same with the E5M2 encoding (bias 15, 2 mantissa bits,
+ *               subnormal step 2^-16), saturating to +-57344.
  *   rint() is round-half-to-even.
  *
  * Axes (kvq_qspec.axis):
@@ -83,7 +88,7 @@
  * Codes are packed along D: channel c's code occupies bits (c*b) % 8 ..
  * of byte (c*b)/8 of the token's row (little-endian bit order).  Code values:
  * sym INT8 two's complement; sym INT2/INT4 offset binary c + 2^(b-1);
- * asym unsigned 0..2^b-1; FP8 the raw E4M3 byte.
+ * asym unsigned 0..2^b-1; FP8 the raw E4M3 or E5M2 byte.
  *
  * Residual window buffers k_win / v_win: [batch][R][num_kv_heads][head_dim]
  * in the source dtype; window slot j of sequence b holds token n_q + j.
@@ -109,7 +114,7 @@ typedef enum {
   KVQ_ERR_WORKSPACE = 5    /* workspace missing, too small or misaligned    */
 } kvq_status;
 
-typedef enum { KVQ_INT2 = 2, KVQ_INT4 = 4, KVQ_INT8 = 8, KVQ_FP8_E4M3 = 9 } kvq_format;
+typedef enum { KVQ_INT2 = 2, KVQ_INT4 = 4, KVQ_INT8 = 8, KVQ_FP8_E4M3 = 9, KVQ_FP8_E5M2 = 10 } kvq_format;
 typedef enum { KVQ_SYM_ABSMAX = 0, KVQ_ASYM_MINMAX = 1 } kvq_mode; /* ignored for FP8 */
 typedef enum { KVQ_PER_TENSOR = 0, KVQ_PER_TOKEN = 1, KVQ_PER_CHANNEL = 2 } kvq_axis;
 typedef enum { KVQ_F32 = 0, KVQ_BF16 = 1 } kvq_dtype; /* source, window and q dtype */
@@ -172,7 +177,8 @@ size_t kvq_workspace_bytes(const kvq_config* cfg, int32_t batch, int32_t max_seq
 
 /* Static per-head scale: scale_out[h] = (max over the n_tokens x D values of
  * head h of |src|) / qmax, fp32; 0 when all are 0.  src: [n_tokens][Hkv][D]
- * device, src dtype.  qmax: 448 for FP8 E4M3, 2^(b-1)-1 for sym INT-b.
+ * device, src dtype.  qmax: 448 for FP8 E4M3, 57344 for FP8 E5M2, 2^(b-1)-1
+ * for sym INT-b.
  * scale_out: [Hkv] device fp32, overwritten (also used as the reduction
  * buffer, so it must not alias src). */
 kvq_status kvq_calibrate_absmax(const kvq_config* cfg, const void* src, int64_t n_tokens,

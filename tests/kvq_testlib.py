@@ -32,7 +32,7 @@ class Case:
     the oracle states."""
 
     def __init__(self, cfg: O.Config, lens, seed=0, outliers=(3, 17), factor=30.0, chunking="random",
-                 permute_pages=True, extra_pages=1, streams=None):
+                 permute_pages=True, extra_pages=1, streams=None, static_scales=None):
         import asymmetric_quantized_kv_gb300 as K
         self.cfg, self.lens, self.seed = cfg, list(lens), seed
         Bn, H, D, P = len(lens), cfg.num_kv_heads, cfg.head_dim, cfg.page_size
@@ -45,8 +45,8 @@ class Case:
             self.V = [[W.small_stream(seed * 1000 + 500 + b * 10 + h, int(lens[b]), D, (), 1.0, bf)
                        for h in range(H)] for b in range(Bn)]
         # static per-head scales over all sequences (oracle) and through the library
-        qk = 448.0 if cfg.k.fmt == O.FP8_E4M3 else float(O.sym_qmax(O.bits_of(cfg.k.fmt)))
-        qv = 448.0 if cfg.v.fmt == O.FP8_E4M3 else float(O.sym_qmax(O.bits_of(cfg.v.fmt)))
+        qk = O.fp8_max(cfg.k.fmt) if O.is_fp8(cfg.k.fmt) else float(O.sym_qmax(O.bits_of(cfg.k.fmt)))
+        qv = O.fp8_max(cfg.v.fmt) if O.is_fp8(cfg.v.fmt) else float(O.sym_qmax(O.bits_of(cfg.v.fmt)))
         cat = lambda S, h: np.concatenate([S[b][h] for b in range(Bn)]) if sum(lens) else np.zeros((0, D))
         self.k_scale = [O.calibrate_absmax(cat(self.K, h), qk) for h in range(H)]
         self.v_scale = [O.calibrate_absmax(cat(self.V, h), qv) for h in range(H)]
@@ -58,7 +58,12 @@ class Case:
         self.block_table = bt.reshape(Bn, self.maxp)
         self.c_cfg = to_c(cfg)
         self.cache = K.PagedKVCache(self.c_cfg, Bn, self.maxp, n_pages, self.block_table)
-        if sum(lens):
+        if static_scales is not None:  # given per-head scales (e.g. the uncalibrated unit scale)
+            self.k_scale = [float(O.fl32(x)) for x in static_scales[0]]
+            self.v_scale = [float(O.fl32(x)) for x in static_scales[1]]
+            self.cache.k_scale.copy_(torch.tensor(self.k_scale, dtype=torch.float32))
+            self.cache.v_scale.copy_(torch.tensor(self.v_scale, dtype=torch.float32))
+        elif sum(lens):
             ks = torch_src(np.concatenate([np.stack([self.K[b][h] for h in range(H)], 1) for b in range(Bn)]), cfg)
             vs = torch_src(np.concatenate([np.stack([self.V[b][h] for h in range(H)], 1) for b in range(Bn)]), cfg)
             self.cache.calibrate(ks, vs, qk, qv)
@@ -169,13 +174,14 @@ class FullCase:
     """A benchmark-sized workload (configs 3, 4, 5 of bench.py) filled through the
     library from seeded device-side draws, exactly as bench.py fills it, with
     host copies of the sampled (sequence, kv-head) source streams.  Static FP8
-    scales are fl32(absmax / 448) with the absmax taken by torch, so the oracle
-    and the library quantize with the same scale without the library computing it."""
+    scales are fl32(absmax / qmax) (qmax 448 for E4M3, 57344 for E5M2) with the
+    absmax taken by torch, so the oracle and the library quantize with the same
+    scale without the library computing it."""
 
-    def __init__(self, cid, samples, gen_seed=1):
+    def __init__(self, cid, samples, gen_seed=1, fp8="e4m3"):
         import bench
         import asymmetric_quantized_kv_gb300 as K
-        spec = bench.workload_spec(cid)
+        spec = bench.workload_spec(cid, 0, fp8)
         w = spec["w"]
         self.spec, self.w = spec, w
         Bn, H, D, Hq = w.batch, w.num_kv_heads, w.head_dim, w.num_q_heads
@@ -200,7 +206,8 @@ class FullCase:
         T_max = max(self.lens)
         self.k_scale = [0.0] * H
         self.v_scale = [0.0] * H
-        if self.cfg.k.fmt == O.FP8_E4M3:
+        if O.is_fp8(self.cfg.k.fmt):
+            qmax = O.fp8_max(self.cfg.k.fmt)
             state = g.get_state()
             kmax = torch.zeros(H, device=dev)
             vmax = torch.zeros(H, device=dev)
@@ -211,8 +218,8 @@ class FullCase:
                 kmax = torch.maximum(kmax, kk.float().abs().amax(dim=(0, 1, 3)))
                 vmax = torch.maximum(vmax, vv.float().abs().amax(dim=(0, 1, 3)))
                 done += n
-            self.k_scale = [float(O.fl32(a / 448.0)) for a in kmax.double().cpu().tolist()]
-            self.v_scale = [float(O.fl32(a / 448.0)) for a in vmax.double().cpu().tolist()]
+            self.k_scale = [float(O.fl32(a / qmax)) for a in kmax.double().cpu().tolist()]
+            self.v_scale = [float(O.fl32(a / qmax)) for a in vmax.double().cpu().tolist()]
             self.cache.k_scale.copy_(torch.tensor(self.k_scale, dtype=torch.float32))
             self.cache.v_scale.copy_(torch.tensor(self.v_scale, dtype=torch.float32))
             g.set_state(state)

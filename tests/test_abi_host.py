@@ -42,7 +42,8 @@ def test_status_strings(K):
 
 
 SPECS = [(O.INT2, O.ASYM, O.PER_CHANNEL, 32), (O.INT8, O.SYM, O.PER_CHANNEL, 64), (O.INT4, O.ASYM, O.PER_TOKEN, 0),
-         (O.INT4, O.SYM, O.PER_TOKEN, 32), (O.INT8, O.SYM, O.PER_TENSOR, 0), (O.FP8_E4M3, 0, O.PER_TENSOR, 0)]
+         (O.INT4, O.SYM, O.PER_TOKEN, 32), (O.INT8, O.SYM, O.PER_TENSOR, 0), (O.FP8_E4M3, 0, O.PER_TENSOR, 0),
+         (O.FP8_E5M2, 0, O.PER_TENSOR, 0)]
 
 
 @pytest.mark.parametrize("D", [64, 128, 256])

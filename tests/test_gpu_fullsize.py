@@ -24,9 +24,10 @@ def _samples(cid):
     return [(b_long, 0), (b_short, w.num_kv_heads - 1), ((b_long + 1) % w.batch, 3)]
 
 
-@pytest.mark.parametrize("cid", [3, 4, 5])
-def test_fullsize_sampled_streams(cid):
-    case = FullCase(cid, _samples(cid))
+@pytest.mark.parametrize("cid,fp8", [(3, "e4m3"), (4, "e4m3"), (4, "e5m2"), (5, "e4m3")])
+def test_fullsize_sampled_streams(cid, fp8):
+    """(config 4 also in FP8 E5M2: the 70B layer with absmax/57344 scales)"""
+    case = FullCase(cid, _samples(cid), fp8=fp8)
     case.check_attention()
     case.check_dequantize()
     del case

@@ -43,6 +43,14 @@ CASES = {
     # FP8 with the 70B layer's heads: 64 query heads on 8 kv-heads
     "fp8_64q8kv": (O.Config(64, 8, 128, Q(O.FP8_E4M3, S, TEN), Q(O.FP8_E4M3, S, TEN), 0, 256, 0, 1e4, O.BF16),
                    [700, 33]),
+    # FP8 E5M2 (2 mantissa bits, saturating at 57344) through the tensor-core kernel
+    "fp8_e5m2": (O.Config(16, 2, 128, Q(O.FP8_E5M2, S, TEN), Q(O.FP8_E5M2, S, TEN), 0, 256, 0, 1e4, O.BF16),
+                 [1, 255, 256, 900]),
+    "fp8_e5m2_p16_f32": (O.Config(16, 2, 128, Q(O.FP8_E5M2, S, TEN), Q(O.FP8_E5M2, S, TEN), 0, 16, 0, 1e4, O.F32),
+                         [1, 15, 16, 17, 300, 1000]),
+    # E4M3 keys with E5M2 values, 4 query heads per kv-head (the generic kernel)
+    "fp8_mixed": (O.Config(8, 2, 128, Q(O.FP8_E4M3, S, TEN), Q(O.FP8_E5M2, S, TEN), 0, 64, 0, 1e4, O.BF16),
+                  [5, 64, 333]),
     # per-tensor INT8 (the synthetic head's failing baseline), fp32 sources
     "int8_tensor": (O.Config(1, 1, 128, Q(O.INT8, S, TEN), Q(O.INT8, S, TEN), 0, 256, 0, 1e4, O.F32), [4096]),
     # per-channel K over one 4096-token group + per-token V, fp32
