@@ -32,6 +32,12 @@ Everything here is the plain definition, written for a reader to check by eye:
   saturating at 57344; an uncalibrated cache uses the unit scale (the same page,
   section "Why do per-tensor scales waste bits on the K cache?", failure mode
   1), which the static-scale path covers with scale 1.
+* fp16 scale/min storage (optional): the scale is stored rounded up to the next
+  binary16 value and the minimum rounded down, and the codes are computed from
+  the stored values, so the +-s/2 error bound of the fp32 rule still holds.
+  Reading: the asymmetric range is taken from the stored (rounded-down) minimum,
+  d = max(mx - mn16, 1e-8), so the top code never clips.  Values beyond the
+  binary16 range saturate (scale 65504, minimum -65504).
 * Axes: K per channel over G-token groups, V per token ("Why Keys Are More
   Sensitive Than Values in INT8 KV Cache Quantization", section "Outlier
   Distribution in Key Channels"; fourth page, "What should I actually turn on
@@ -58,7 +64,7 @@ import numpy as np
 INT2, INT4, INT8, FP8_E4M3, FP8_E5M2 = 2, 4, 8, 9, 10
 SYM, ASYM = 0, 1
 PER_TENSOR, PER_TOKEN, PER_CHANNEL = 0, 1, 2
-F32, BF16 = 0, 1
+F32, BF16, F16 = 0, 1, 2  # source dtypes; F16 also names fp16 scale/min storage
 
 FL32_1EM8 = float(np.float32(1e-8))
 E4M3_MAX = 448.0
@@ -206,6 +212,52 @@ def quant_sym(x, absmax, bits: int):
     return c.astype(np.int64), s
 
 
+F16_MAX = 65504.0
+
+
+def f16_up(x) -> np.ndarray:
+    """Smallest binary16 value >= x (as float64), saturating at +-65504."""
+    x = np.asarray(x, dtype=np.float64)
+    h = np.clip(x, -F16_MAX, F16_MAX).astype(np.float16)  # nearest
+    with np.errstate(over="ignore"):  # stepping past 65504 gives inf, saturated below
+        h = np.where(h.astype(np.float64) < x, np.nextafter(h, np.float16(np.inf)), h)
+    return np.minimum(h.astype(np.float64), F16_MAX)
+
+
+def f16_down(x) -> np.ndarray:
+    """Largest binary16 value <= x (as float64), saturating at +-65504."""
+    x = np.asarray(x, dtype=np.float64)
+    h = np.clip(x, -F16_MAX, F16_MAX).astype(np.float16)
+    with np.errstate(over="ignore"):
+        h = np.where(h.astype(np.float64) > x, np.nextafter(h, np.float16(-np.inf)), h)
+    return np.maximum(h.astype(np.float64), -F16_MAX)
+
+
+def quant_sym16(x, absmax, bits: int):
+    """Symmetric INT-b with the scale stored as binary16 rounded up:
+    s = f16_up(fl32(a / qmax)), c = clamp(rint(fl32(x / s)), -qmax, qmax)."""
+    qmax = sym_qmax(bits)
+    s = f16_up(fl32(np.asarray(absmax, dtype=np.float64) / qmax))
+    with np.errstate(divide="ignore", invalid="ignore"):
+        y = fl32(np.asarray(x, dtype=np.float64) / s)
+    c = np.clip(np.rint(y), -qmax, qmax)
+    c = np.where(s == 0.0, 0.0, c)
+    return c.astype(np.int64), s
+
+
+def quant_asym16(x, mn, mx, bits: int):
+    """Asymmetric INT-b with binary16 storage: mn16 = f16_down(mn),
+    d = max(fl32(mx - mn16), 1e-8f), s = f16_up(fl32(d / qmax)),
+    c = clamp(rint(fl32(fl32(x - mn16) / s)), 0, qmax).  Returns (codes, s, mn16)."""
+    qmax = asym_qmax(bits)
+    mn16 = f16_down(np.asarray(mn, dtype=np.float64))
+    d = np.maximum(fl32(np.asarray(mx, dtype=np.float64) - mn16), FL32_1EM8)
+    s = f16_up(fl32(d / qmax))
+    t = fl32(np.asarray(x, dtype=np.float64) - mn16)
+    c = np.clip(np.rint(fl32(t / s)), 0, qmax)
+    return c.astype(np.int64), s, mn16
+
+
 def dequant_sym(c, s):
     return fl32(np.asarray(c, dtype=np.float64) * s)
 
@@ -267,6 +319,7 @@ class Config:
     rope_pre: int = 0
     rope_theta: float = 10000.0
     src_dtype: int = F32
+    meta_dtype: int = F32  # stored scales / minima: F32 or F16
 
     @property
     def n_rep(self) -> int:
@@ -279,6 +332,11 @@ def _tok_group(spec: QSpec, D: int) -> int:
 
 def _n_meta(spec: QSpec) -> int:
     return 2 if (spec.mode == ASYM and not is_fp8(spec.fmt)) else 1
+
+
+def meta_bytes(cfg: Config) -> int:
+    """Bytes of one stored scale or minimum."""
+    return 2 if cfg.meta_dtype == F16 else 4
 
 
 def _align16(n: int) -> int:
@@ -294,12 +352,13 @@ def layout(cfg: Config) -> dict:
     kc = 0
     vc = _align16(kc + P * krow)
     vm = _align16(vc + P * vrow)
-    vm_bytes = P * (D // _tok_group(cfg.v, D)) * _n_meta(cfg.v) * 4 if cfg.v.axis == PER_TOKEN else 0
+    mb = meta_bytes(cfg)
+    vm_bytes = P * (D // _tok_group(cfg.v, D)) * _n_meta(cfg.v) * mb if cfg.v.axis == PER_TOKEN else 0
     km = _align16(vm + vm_bytes)
     if cfg.k.axis == PER_CHANNEL:
-        km_bytes = max(1, P // cfg.k.group) * D * _n_meta(cfg.k) * 4
+        km_bytes = max(1, P // cfg.k.group) * D * _n_meta(cfg.k) * mb
     elif cfg.k.axis == PER_TOKEN:
-        km_bytes = P * (D // _tok_group(cfg.k, D)) * _n_meta(cfg.k) * 4
+        km_bytes = P * (D // _tok_group(cfg.k, D)) * _n_meta(cfg.k) * mb
     else:
         km_bytes = 0
     head = _align16(km + km_bytes)
@@ -309,7 +368,7 @@ def layout(cfg: Config) -> dict:
 
 # -------------------------------------------------------------- one (seq, kv-head) stream
 
-def _quant_tokens(x, spec: QSpec, static_scale, D):
+def _quant_tokens(x, spec: QSpec, static_scale, D, meta16=False):
     """Quantize rows x [n, D] along a per-token / per-tensor / FP8 axis.
 
     Returns (codes [n, D], scales [n, ng] or None, mins [n, ng] or None)."""
@@ -329,15 +388,15 @@ def _quant_tokens(x, spec: QSpec, static_scale, D):
     xg = x.reshape(n, D // g, g)
     if spec.mode == SYM:
         a = np.max(np.abs(xg), axis=2, keepdims=True)
-        c, s = quant_sym(xg, a, bits)
+        c, s = (quant_sym16 if meta16 else quant_sym)(xg, a, bits)
         return c.reshape(n, D), s[..., 0], None
     mn = np.min(xg, axis=2, keepdims=True)
     mx = np.max(xg, axis=2, keepdims=True)
-    c, s, m = quant_asym(xg, mn, mx, bits)
+    c, s, m = (quant_asym16 if meta16 else quant_asym)(xg, mn, mx, bits)
     return c.reshape(n, D), s[..., 0], m[..., 0]
 
 
-def _quant_k_channel(x, spec: QSpec):
+def _quant_k_channel(x, spec: QSpec, meta16=False):
     """Per-channel K over groups of G consecutive tokens: x [n, D], n % G == 0.
 
     Returns (codes [n, D], scales [n/G, D], mins [n/G, D] or None)."""
@@ -347,11 +406,11 @@ def _quant_k_channel(x, spec: QSpec):
     xg = x.reshape(n // G, G, D)
     if spec.mode == SYM:
         a = np.max(np.abs(xg), axis=1, keepdims=True)
-        c, s = quant_sym(xg, a, bits)
+        c, s = (quant_sym16 if meta16 else quant_sym)(xg, a, bits)
         return c.reshape(n, D), s[:, 0, :], None
     mn = np.min(xg, axis=1, keepdims=True)
     mx = np.max(xg, axis=1, keepdims=True)
-    c, s, m = quant_asym(xg, mn, mx, bits)
+    c, s, m = (quant_asym16 if meta16 else quant_asym)(xg, mn, mx, bits)
     return c.reshape(n, D), s[:, 0, :], m[:, 0, :]
 
 
@@ -381,11 +440,12 @@ def quantize_stream(cfg: Config, K, V, k_scale=0.0, v_scale=0.0) -> HeadState:
     V = np.asarray(V, dtype=np.float64)
     T, D = K.shape
     nq = n_quantized(T, cfg.residual)
+    m16 = cfg.meta_dtype == F16
     if cfg.k.axis == PER_CHANNEL:
-        kc, ks, km = _quant_k_channel(K[:nq], cfg.k)
+        kc, ks, km = _quant_k_channel(K[:nq], cfg.k, m16)
     else:
-        kc, ks, km = _quant_tokens(K[:nq], cfg.k, k_scale, D)
-    vc, vs, vm = _quant_tokens(V[:nq], cfg.v, v_scale, D)
+        kc, ks, km = _quant_tokens(K[:nq], cfg.k, k_scale, D, m16)
+    vc, vs, vm = _quant_tokens(V[:nq], cfg.v, v_scale, D, m16)
     return HeadState(T, nq, kc, ks, km, vc, vs, vm, K[nq:].copy(), V[nq:].copy())
 
 
@@ -569,7 +629,8 @@ def write_head_pages(cfg: Config, pages: np.ndarray, defined: np.ndarray, block_
     kb, vb = bits_of(cfg.k.fmt), bits_of(cfg.v.fmt)
     kpack = pack_rows(_code_bytes(st.kc, cfg.k), kb) if st.n_q else np.zeros((0, L["krow"]), np.uint8)
     vpack = pack_rows(_code_bytes(st.vc, cfg.v), vb) if st.n_q else np.zeros((0, L["vrow"]), np.uint8)
-    f32 = lambda a: np.asarray(a, dtype=np.float32).view(np.uint8)
+    mb = meta_bytes(cfg)
+    f32 = lambda a: np.asarray(a, dtype=np.float16 if mb == 2 else np.float32).view(np.uint8)
 
     def put(page, off, data):
         base = h * L["head"] + off
@@ -584,11 +645,11 @@ def write_head_pages(cfg: Config, pages: np.ndarray, defined: np.ndarray, block_
         if cfg.v.axis == PER_TOKEN:
             ng = D // _tok_group(cfg.v, D)
             row = [st.vs[t]] + ([st.vm[t]] if _n_meta(cfg.v) == 2 else [])
-            put(page, L["vm"] + slot * ng * _n_meta(cfg.v) * 4, f32(np.concatenate(row)))
+            put(page, L["vm"] + slot * ng * _n_meta(cfg.v) * mb, f32(np.concatenate(row)))
         if cfg.k.axis == PER_TOKEN:
             ng = D // _tok_group(cfg.k, D)
             row = [st.ks[t]] + ([st.km[t]] if _n_meta(cfg.k) == 2 else [])
-            put(page, L["km"] + slot * ng * _n_meta(cfg.k) * 4, f32(np.concatenate(row)))
+            put(page, L["km"] + slot * ng * _n_meta(cfg.k) * mb, f32(np.concatenate(row)))
     if cfg.k.axis == PER_CHANNEL:
         G = cfg.k.group
         for j in range(st.n_q // G):
@@ -596,7 +657,7 @@ def write_head_pages(cfg: Config, pages: np.ndarray, defined: np.ndarray, block_
             page = int(block_table[b][t0 // P])
             slot = (t0 % P) // G
             row = [st.ks[j]] + ([st.km[j]] if _n_meta(cfg.k) == 2 else [])
-            put(page, L["km"] + slot * D * _n_meta(cfg.k) * 4, f32(np.concatenate(row)))
+            put(page, L["km"] + slot * D * _n_meta(cfg.k) * mb, f32(np.concatenate(row)))
 
 
 def kv_bytes_per_token(n_layers: int, n_kv_heads: int, head_dim: int, dtype_bytes: float) -> float:

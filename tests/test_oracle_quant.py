@@ -12,6 +12,7 @@ import numpy as np
 import pytest
 import torch
 
+import kvq_inputs as W
 from oracle import kvq_oracle as O
 
 GOLD = os.path.join(os.path.dirname(__file__), "golden")
@@ -245,6 +246,83 @@ def test_fp8_formats_quantize_with_their_own_tables():
         b = O.quant_fp8(x, s, fmt)
         assert np.array_equal(O.dequant_fp8(b, s, fmt), O.fl32(dec(b) * s))
         assert np.array_equal(b, O.fp8_encode(O.fl32(x / s), fmt))
+
+
+# ---------------------------------------------------------- fp16 scale/min storage
+
+_HALVES = np.unique(np.arange(0, 0x10000, dtype=np.uint16).view(np.float16).astype(np.float64))
+_HALVES = _HALVES[np.isfinite(_HALVES)]  # every finite binary16 value, increasing
+
+
+def test_f16_directed_rounding_against_every_half():
+    g = np.random.default_rng(21)
+    x = np.concatenate([g.standard_normal(20000) * 10.0 ** g.uniform(-9, 4.9, 20000),
+                        _HALVES[::97], [0.0, -0.0, 65504.0, -65504.0, 6.0e-8, 3.0e-8]])
+    x = O.fl32(x)
+    x = x[np.abs(x) <= 65504.0]  # beyond: saturation, checked below
+    up = _HALVES[np.searchsorted(_HALVES, x, side="left")]
+    down = _HALVES[np.searchsorted(_HALVES, x, side="right") - 1]
+    assert np.array_equal(O.f16_up(x), up)
+    assert np.array_equal(O.f16_down(x), down)
+    assert np.all(O.f16_up([7e4, 1e9]) == 65504.0) and np.all(O.f16_down([-7e4, -1e9]) == -65504.0)
+
+
+@pytest.mark.parametrize("bits", [2, 4, 8])
+def test_fp16_meta_keeps_the_half_step_bound(bits):
+    g = np.random.default_rng(22 + bits)
+    for trial in range(200):
+        scale = 10.0 ** g.uniform(-3, 3)
+        x = O.fl32(g.standard_normal(64) * scale + g.uniform(-3, 3) * scale)
+        mn, mx = x.min(), x.max()
+        c, s, m = O.quant_asym16(x, mn, mx, bits)
+        c32, s32, _ = O.quant_asym(x, mn, mx, bits)
+        assert s == O.f16_up(s) and m == O.f16_down(m) and m <= mn and s >= s32 * (1 - 2.0 ** -23)
+        assert c.min() >= 0 and c.max() <= O.asym_qmax(bits)
+        err = np.abs(O.dequant_asym(c, s, m) - x)
+        assert np.all(err <= s / 2 * (1 + 2.0 ** -20) + 4 * np.spacing(np.float32(np.abs(x).max())))
+        a = np.max(np.abs(x))
+        c, s = O.quant_sym16(x, a, bits)
+        assert s == O.f16_up(s) and s >= float(O.fl32(a / O.sym_qmax(bits)))
+        assert np.abs(c).max() <= O.sym_qmax(bits)
+        err = np.abs(O.dequant_sym(c, s) - x)
+        assert np.all(err <= s / 2 * (1 + 2.0 ** -20) + 4 * np.spacing(np.float32(a)))
+
+
+def test_fp16_meta_zero_and_constant_groups():
+    z = np.zeros(16)
+    c, s = O.quant_sym16(z, 0.0, 4)
+    assert s == 0.0 and np.all(c == 0)
+    x = np.full(16, 3.25)  # a binary16 value: the minimum is stored exactly
+    c, s, m = O.quant_asym16(x, x.min(), x.max(), 4)
+    assert np.all(c == 0) and m == 3.25 and np.all(O.dequant_asym(c, s, m) == x)
+
+
+def test_fp16_meta_halves_the_metadata_of_the_2bit_layer():
+    # the 8B layer's formats: 2-bit codes (32 B K + 32 B V per token and kv-head), key
+    # scale+min per (32-token group, channel), value scale+min per (token, 32-channel group)
+    base = dict(num_q_heads=32, num_kv_heads=8, head_dim=128, k=O.QSpec(O.INT2, O.ASYM, O.PER_CHANNEL, 32),
+                v=O.QSpec(O.INT2, O.ASYM, O.PER_TOKEN, 32), residual=128, page_size=256)
+    L32, L16 = O.layout(O.Config(**base)), O.layout(O.Config(meta_dtype=O.F16, **base))
+    per_tok = lambda L: (L["head"] - 0) / 256
+    assert per_tok(L32) == 64 + 32 + 32 and per_tok(L16) == 64 + 16 + 16
+    # 16 sequences x 8 kv-heads x 32768 quantized tokens, + 127 bf16 window rows of K and V, + q/out
+    nq = 16 * 8 * 32768
+    extra = 16 * 8 * 127 * 128 * 2 * 2 + 16 * 32 * 128 * (2 + 4)
+    assert round((nq * per_tok(L32) + extra) / 1e6, 1) == 545.6
+    assert round((nq * per_tok(L16) + extra) / 1e6, 1) == 411.4
+
+
+def test_fp16_meta_chunking_invariance():
+    cfg = O.Config(4, 1, 64, O.QSpec(O.INT4, O.ASYM, O.PER_CHANNEL, 16), O.QSpec(O.INT2, O.SYM, O.PER_TOKEN, 32),
+                   residual=32, page_size=16, meta_dtype=O.F16)
+    K = W.small_stream(31, 200, 64, (3, 9), 40.0)
+    V = W.small_stream(32, 200, 64)
+    sc = O.StreamCache(cfg)
+    for a, b in ((0, 1), (1, 40), (40, 41), (41, 200)):
+        sc.append(K[a:b], V[a:b])
+    st, ref = sc.state(), O.quantize_stream(cfg, K, V)
+    for f in ("kc", "ks", "km", "vc", "vs"):
+        assert np.array_equal(getattr(st, f), getattr(ref, f)), f
 
 
 def test_fp8_scale_roundtrip_and_zero_scale():
