@@ -18,7 +18,7 @@ KVQ_OK, KVQ_ERR_INVALID_ARG, KVQ_ERR_UNSUPPORTED, KVQ_ERR_CUDA, KVQ_ERR_CAPACITY
 KVQ_INT2, KVQ_INT4, KVQ_INT8, KVQ_FP8_E4M3, KVQ_FP8_E5M2 = 2, 4, 8, 9, 10
 KVQ_SYM_ABSMAX, KVQ_ASYM_MINMAX = 0, 1
 KVQ_PER_TENSOR, KVQ_PER_TOKEN, KVQ_PER_CHANNEL = 0, 1, 2
-KVQ_F32, KVQ_BF16 = 0, 1
+KVQ_F32, KVQ_BF16, KVQ_F16 = 0, 1, 2
 KVQ_DEV_BAD_PAGE, KVQ_DEV_OVERFLOW, KVQ_DEV_TIMEOUT, KVQ_DEV_BAD_LENGTH = 1, 2, 4, 8
 KVQ_NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
 
@@ -30,7 +30,8 @@ class kvq_qspec(ctypes.Structure):
 class kvq_config(ctypes.Structure):
     _fields_ = [("num_q_heads", c_int32), ("num_kv_heads", c_int32), ("head_dim", c_int32),
                 ("k", kvq_qspec), ("v", kvq_qspec), ("residual", c_int32), ("page_size", c_int32),
-                ("rope_pre", c_int32), ("rope_theta", c_float), ("src_dtype", c_int32)]
+                ("rope_pre", c_int32), ("rope_theta", c_float), ("src_dtype", c_int32),
+                ("meta_dtype", c_int32)]
 
 
 class kvq_cache(ctypes.Structure):

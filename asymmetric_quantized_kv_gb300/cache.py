@@ -10,10 +10,10 @@ from . import _binding as B
 
 
 def make_config(num_q_heads, num_kv_heads, head_dim, k, v, residual, page_size, rope_pre=0,
-                rope_theta=10000.0, src_dtype=B.KVQ_F32) -> B.kvq_config:
-    """k, v: (fmt, mode, axis, group) tuples."""
+                rope_theta=10000.0, src_dtype=B.KVQ_F32, meta_dtype=B.KVQ_F32) -> B.kvq_config:
+    """k, v: (fmt, mode, axis, group) tuples; meta_dtype: stored scales / minima (F32 or F16)."""
     cfg = B.kvq_config(num_q_heads, num_kv_heads, head_dim, B.kvq_qspec(*k), B.kvq_qspec(*v), residual,
-                       page_size, rope_pre, rope_theta, src_dtype)
+                       page_size, rope_pre, rope_theta, src_dtype, meta_dtype)
     code = B.kvq_validate(cfg)
     if code != B.KVQ_OK:
         raise B.KvqError("kvq_validate", code)

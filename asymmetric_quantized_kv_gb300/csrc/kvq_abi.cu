@@ -45,20 +45,21 @@ struct Layout {
 bool layout_of(const kvq_config* c, Layout* L) {
   if (kvq_validate(c) != KVQ_OK) return false;
   const size_t D = c->head_dim, P = c->page_size;
+  const size_t mb = c->meta_dtype == KVQ_F16 ? 2 : 4;  // bytes per stored scale / minimum
   L->krow = D * bits_of(c->k.fmt) / 8;
   L->vrow = D * bits_of(c->v.fmt) / 8;
   L->kc = 0;
   L->vc = align16(L->kc + P * L->krow);
   L->vm = align16(L->vc + P * L->vrow);
   size_t vm_bytes = 0;
-  if (c->v.axis == KVQ_PER_TOKEN) vm_bytes = P * (D / tok_group(c->v, D)) * n_meta(c->v) * 4;
+  if (c->v.axis == KVQ_PER_TOKEN) vm_bytes = P * (D / tok_group(c->v, D)) * n_meta(c->v) * mb;
   L->km = align16(L->vm + vm_bytes);
   size_t km_bytes = 0;
   if (c->k.axis == KVQ_PER_CHANNEL) {
     const size_t G = c->k.group;
-    km_bytes = (P >= G ? P / G : 1) * D * n_meta(c->k) * 4;
+    km_bytes = (P >= G ? P / G : 1) * D * n_meta(c->k) * mb;
   } else if (c->k.axis == KVQ_PER_TOKEN) {
-    km_bytes = P * (D / tok_group(c->k, D)) * n_meta(c->k) * 4;
+    km_bytes = P * (D / tok_group(c->k, D)) * n_meta(c->k) * mb;
   }
   L->head = align16(L->km + km_bytes);
   L->page = L->head * c->num_kv_heads;
@@ -109,6 +110,8 @@ bool make_view(const kvq_config* c, const kvq_cache* k, KvqView* v) {
   v->off_vc = (int)L.vc;
   v->off_vm = (int)L.vm;
   v->off_km = (int)L.km;
+  v->meta16 = c->meta_dtype == KVQ_F16;
+  v->mb = v->meta16 ? 2 : 4;
   v->k_nmeta = n_meta(c->k);
   v->v_nmeta = n_meta(c->v);
   v->k_ng = c->k.axis == KVQ_PER_TOKEN ? c->head_dim / v->kgroup : 0;
@@ -156,6 +159,7 @@ kvq_status kvq_validate(const kvq_config* c) {
   if (c->rope_pre != 0 && c->rope_pre != 1) return KVQ_ERR_INVALID_ARG;
   if (c->rope_pre && !(c->rope_theta > 1.0f && isfinite(c->rope_theta))) return KVQ_ERR_INVALID_ARG;
   if (c->src_dtype != KVQ_F32 && c->src_dtype != KVQ_BF16) return KVQ_ERR_INVALID_ARG;
+  if (c->meta_dtype != KVQ_F32 && c->meta_dtype != KVQ_F16) return KVQ_ERR_INVALID_ARG;
   return KVQ_OK;
 }
 

@@ -136,21 +136,16 @@ __device__ void quantize_rows(const KvqView& v, const Src& s, const AppendCtx& a
             am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
           }
           if ((lane & (width - 1)) == 0 && grp < q.ng) {
-            float sc;
-            if (q.mode == KVQ_ASYM_MINMAX) {
-              sc = asym_scale(mn, mx, q.bits);
-            } else {
-              sc = sym_scale(am, q.bits);
-              mn = 0.f;
-            }
+            float sc, gm;
+            group_scale(mn, mx, am, q.mode == KVQ_ASYM_MINMAX, q.bits, v.meta16, sc, gm);
             sm.gs[r][grp] = sc;
             sm.gr[r][grp] = sc > 0.f ? __frcp_rn(sc) : 0.f;
-            sm.gm[r][grp] = mn;
+            sm.gm[r][grp] = gm;
             uint8_t* hb = sm.rowp[r];
             if (hb) {
-              float* meta = reinterpret_cast<float*>(hb + q.off_meta + sm.rslot[r] * q.ng * q.nmeta * 4);
-              meta[grp] = sc;
-              if (q.nmeta == 2) meta[q.ng + grp] = mn;
+              uint8_t* meta = hb + q.off_meta + sm.rslot[r] * q.ng * q.nmeta * v.mb;
+              store_meta(meta, grp, sc, v.meta16);
+              if (q.nmeta == 2) store_meta(meta, q.ng + grp, gm, v.meta16);
             }
           }
         }
@@ -206,22 +201,16 @@ __device__ void quantize_key_channels(const KvqView& v, const Src& s, const Appe
         mx = fmaxf(mx, sm.cmax[l * D + c]);
       }
       float sc;
-      if (q.mode == KVQ_ASYM_MINMAX) {
-        sc = asym_scale(mn, mx, q.bits);
-      } else {
-        sc = sym_scale(fmaxf(fabsf(mn), fabsf(mx)), q.bits);
-        mn = 0.f;
-      }
+      group_scale(mn, mx, fmaxf(fabsf(mn), fabsf(mx)), q.mode == KVQ_ASYM_MINMAX, q.bits, v.meta16, sc, mn);
       sm.ch_s[c] = sc;
       sm.ch_r[c] = sc > 0.f ? __frcp_rn(sc) : 0.f;
       sm.ch_m[c] = mn;
       uint8_t* page = page_of(v, a.b, g0);
       if (page) {
         const int slot = (g0 % v.P) / G;
-        float* meta = reinterpret_cast<float*>(page + (long long)a.h * v.head_bytes + q.off_meta +
-                                               (long long)slot * D * q.nmeta * 4);
-        meta[c] = sc;
-        if (q.nmeta == 2) meta[D + c] = mn;
+        uint8_t* meta = page + (long long)a.h * v.head_bytes + q.off_meta + (long long)slot * D * q.nmeta * v.mb;
+        store_meta(meta, c, sc, v.meta16);
+        if (q.nmeta == 2) store_meta(meta, D + c, mn, v.meta16);
       }
     }
     __syncthreads();
@@ -473,21 +462,16 @@ __device__ __forceinline__ void fold_rows_t(const KvqView& v, const TQ& q, const
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
         am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
       }
-      if (asym) {
-        gs = asym_scale(mn, mx, BITS);
-        gm = mn;
-      } else {
-        gs = sym_scale(am, BITS);
-      }
+      group_scale(mn, mx, am, asym, BITS, v.meta16, gs, gm);
       gr = gs > 0.f ? __frcp_rn(gs) : 0.f;
     }
     uint8_t* hb = ok ? fs.rowp[t] : nullptr;
     if (!hb) continue;
     const int slot = fs.rslot[t];
     if (!stat && sub % lpg == 0) {
-      float* meta = reinterpret_cast<float*>(hb + q.off_meta + slot * q.ng * q.nmeta * 4);
-      meta[sub / lpg] = gs;
-      if (q.nmeta == 2) meta[q.ng + sub / lpg] = gm;
+      uint8_t* meta = hb + q.off_meta + slot * q.ng * q.nmeta * v.mb;
+      store_meta(meta, sub / lpg, gs, v.meta16);
+      if (q.nmeta == 2) store_meta(meta, q.ng + sub / lpg, gm, v.meta16);
     }
     uint32_t* dst = reinterpret_cast<uint32_t*>(hb + q.off_codes + slot * q.row) + sub * kWords;
     float sc[kCPW], r[kCPW], m[kCPW];
@@ -565,21 +549,16 @@ __device__ __forceinline__ void fold_key_channels_t(const KvqView& v, const TQ& 
         mx = fmaxf(mx, fs.cmax[p * D + c]);
       }
       float sc;
-      if (asym) {
-        sc = asym_scale(mn, mx, BITS);
-      } else {
-        sc = sym_scale(fmaxf(fabsf(mn), fabsf(mx)), BITS);
-        mn = 0.f;
-      }
+      group_scale(mn, mx, fmaxf(fabsf(mn), fabsf(mx)), asym, BITS, v.meta16, sc, mn);
       fs.ch_s[c] = sc;
       fs.ch_r[c] = sc > 0.f ? __frcp_rn(sc) : 0.f;
       fs.ch_m[c] = mn;
       uint8_t* hb0 = fs.rowp[g0];  // head block of the page holding the group's first token
       if (hb0) {
         const int slot = ((tb + g0) % v.P) / G;
-        float* meta = reinterpret_cast<float*>(hb0 + q.off_meta + (long long)slot * D * q.nmeta * 4);
-        meta[c] = sc;
-        if (q.nmeta == 2) meta[D + c] = mn;
+        uint8_t* meta = hb0 + q.off_meta + (long long)slot * D * q.nmeta * v.mb;
+        store_meta(meta, c, sc, v.meta16);
+        if (q.nmeta == 2) store_meta(meta, D + c, mn, v.meta16);
       }
     }
     __syncthreads();
@@ -760,21 +739,21 @@ __global__ void dequantize_kernel(KvqView v, int seq, int t0, float* k_out, floa
         } else if (v.kaxis == KVQ_PER_TENSOR) {
           kx = dequant_sym(signed_code(ku, v.kbits, KVQ_SYM_ABSMAX), v.k_scale[h]);
         } else {
-          const float* meta;
+          const uint8_t* meta;
           float s, mn = 0.f;
           if (v.kaxis == KVQ_PER_TOKEN) {
-            meta = reinterpret_cast<const float*>(hb + v.off_km + slot * v.k_ng * v.k_nmeta * 4);
+            meta = hb + v.off_km + slot * v.k_ng * v.k_nmeta * v.mb;
             const int grp = c / v.kgroup;
-            s = meta[grp];
-            if (v.k_nmeta == 2) mn = meta[v.k_ng + grp];
+            s = load_meta(meta, grp, v.meta16);
+            if (v.k_nmeta == 2) mn = load_meta(meta, v.k_ng + grp, v.meta16);
           } else {
             const int g0 = (t / v.kgroup) * v.kgroup;
             const uint8_t* gp = page_of(v, seq, g0);
-            meta = gp ? reinterpret_cast<const float*>(gp + (long long)h * v.head_bytes + v.off_km +
-                                                       (long long)((g0 % v.P) / v.kgroup) * v.D * v.k_nmeta * 4)
+            meta = gp ? gp + (long long)h * v.head_bytes + v.off_km +
+                            (long long)((g0 % v.P) / v.kgroup) * v.D * v.k_nmeta * v.mb
                       : nullptr;
-            s = meta ? meta[c] : 0.f;
-            if (meta && v.k_nmeta == 2) mn = meta[v.D + c];
+            s = meta ? load_meta(meta, c, v.meta16) : 0.f;
+            if (meta && v.k_nmeta == 2) mn = load_meta(meta, v.D + c, v.meta16);
           }
           const int code = signed_code(ku, v.kbits, v.kmode);
           kx = v.kmode == KVQ_ASYM_MINMAX ? dequant_asym(code, s, mn) : dequant_sym(code, s);
@@ -785,11 +764,12 @@ __global__ void dequantize_kernel(KvqView v, int seq, int t0, float* k_out, floa
         } else if (v.vaxis == KVQ_PER_TENSOR) {
           vx = dequant_sym(signed_code(vu, v.vbits, KVQ_SYM_ABSMAX), v.v_scale[h]);
         } else {
-          const float* meta = reinterpret_cast<const float*>(hb + v.off_vm + slot * v.v_ng * v.v_nmeta * 4);
+          const uint8_t* meta = hb + v.off_vm + slot * v.v_ng * v.v_nmeta * v.mb;
           const int grp = c / v.vgroup;
           const int code = signed_code(vu, v.vbits, v.vmode);
-          vx = v.vmode == KVQ_ASYM_MINMAX ? dequant_asym(code, meta[grp], meta[v.v_ng + grp])
-                                          : dequant_sym(code, meta[grp]);
+          const float vs = load_meta(meta, grp, v.meta16);
+          vx = v.vmode == KVQ_ASYM_MINMAX ? dequant_asym(code, vs, load_meta(meta, v.v_ng + grp, v.meta16))
+                                          : dequant_sym(code, vs);
         }
       }
     }

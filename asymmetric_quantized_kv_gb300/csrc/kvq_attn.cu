@@ -28,7 +28,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 struct TileKeys {
   const uint8_t* hb;     // head block of the token's page (quantized tokens)
-  const float* kmeta;    // PER_CHANNEL: group meta; PER_TOKEN: token meta
+  const uint8_t* kmeta;  // PER_CHANNEL: group meta; PER_TOKEN: token meta (fp32 or binary16 entries)
   int slot;
 };
 
@@ -40,11 +40,11 @@ __device__ __forceinline__ float deq_key(const KvqView& v, const TileKeys& tk, i
   float s, mn = 0.f;
   if (v.kaxis == KVQ_PER_TOKEN) {
     const int grp = c / v.kgroup;
-    s = tk.kmeta[grp];
-    if (v.k_nmeta == 2) mn = tk.kmeta[v.k_ng + grp];
+    s = load_meta(tk.kmeta, grp, v.meta16);
+    if (v.k_nmeta == 2) mn = load_meta(tk.kmeta, v.k_ng + grp, v.meta16);
   } else {
-    s = tk.kmeta[c];
-    if (v.k_nmeta == 2) mn = tk.kmeta[v.D + c];
+    s = load_meta(tk.kmeta, c, v.meta16);
+    if (v.k_nmeta == 2) mn = load_meta(tk.kmeta, v.D + c, v.meta16);
   }
   return v.kmode == KVQ_ASYM_MINMAX ? dequant_asym(code, s, mn) : dequant_sym(code, s);
 }
@@ -53,11 +53,12 @@ __device__ __forceinline__ float deq_value(const KvqView& v, const uint8_t* hb, 
   const unsigned u = get_code(hb + v.off_vc + slot * v.vrow, c, v.vbits);
   if (is_fp8(v.vfmt)) return __fmul_rn(fp8_to_float(u, v.vfmt), v.v_scale[h]);
   if (v.vaxis == KVQ_PER_TENSOR) return dequant_sym(signed_code(u, v.vbits, KVQ_SYM_ABSMAX), v.v_scale[h]);
-  const float* meta = reinterpret_cast<const float*>(hb + v.off_vm + slot * v.v_ng * v.v_nmeta * 4);
+  const uint8_t* meta = hb + v.off_vm + slot * v.v_ng * v.v_nmeta * v.mb;
   const int grp = c / v.vgroup;
   const int code = signed_code(u, v.vbits, v.vmode);
-  return v.vmode == KVQ_ASYM_MINMAX ? dequant_asym(code, meta[grp], meta[v.v_ng + grp])
-                                    : dequant_sym(code, meta[grp]);
+  const float s = load_meta(meta, grp, v.meta16);
+  return v.vmode == KVQ_ASYM_MINMAX ? dequant_asym(code, s, load_meta(meta, v.v_ng + grp, v.meta16))
+                                    : dequant_sym(code, s);
 }
 
 __device__ __forceinline__ float warp_max(float x) {
@@ -130,14 +131,14 @@ __global__ void __launch_bounds__(kThreads) split_generic_kernel(KvqView v, cons
           tk.hb = page + (long long)it.kvh * v.head_bytes;
           tk.slot = t % v.P;
           if (v.kaxis == KVQ_PER_TOKEN) {
-            tk.kmeta = reinterpret_cast<const float*>(tk.hb + v.off_km + tk.slot * v.k_ng * v.k_nmeta * 4);
+            tk.kmeta = tk.hb + v.off_km + tk.slot * v.k_ng * v.k_nmeta * v.mb;
           } else if (v.kaxis == KVQ_PER_CHANNEL) {
             const int g0 = (t / v.kgroup) * v.kgroup;
             const uint8_t* gp = page_of(v, it.b, g0);
             valid = gp != nullptr;
             if (valid)
-              tk.kmeta = reinterpret_cast<const float*>(gp + (long long)it.kvh * v.head_bytes + v.off_km +
-                                                        (long long)((g0 % v.P) / v.kgroup) * D * v.k_nmeta * 4);
+              tk.kmeta = gp + (long long)it.kvh * v.head_bytes + v.off_km +
+                         (long long)((g0 % v.P) / v.kgroup) * D * v.k_nmeta * v.mb;
           }
         }
       } else if (valid) {

@@ -570,7 +570,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 bool fast_eligible(const KvqView& v) {
   const bool pow2_g = v.kgroup > 0 && (v.kgroup & (v.kgroup - 1)) == 0;
   const bool pow2_p = (v.P & (v.P - 1)) == 0;
-  return v.D == kD && v.Hkv == kWarps && v.n_rep == kNRep && v.kfmt == KVQ_INT8 &&
+  return !v.meta16 && v.D == kD && v.Hkv == kWarps && v.n_rep == kNRep && v.kfmt == KVQ_INT8 &&
          v.kmode == KVQ_SYM_ABSMAX && v.kaxis == KVQ_PER_CHANNEL && v.rope_pre == 1 &&
          v.vfmt == KVQ_INT4 && v.vmode == KVQ_ASYM_MINMAX && v.vaxis == KVQ_PER_TOKEN &&
          v.vgroup == kD && pow2_g && pow2_p && v.kgroup >= kTile * kStages && v.P >= kTile &&

@@ -524,7 +524,8 @@ bool int2_shape_eligible(const KvqView& v) {
   const bool pow2_g = v.kgroup > 0 && (v.kgroup & (v.kgroup - 1)) == 0;
   // the three per-token sections (K codes, V codes, V meta) share 32-byte rows at a
   // uniform section stride, and every offset is a multiple of 128 bytes
-  return v.krow == kRow2 && v.vrow == kRow2 && v.v_ng * v.v_nmeta * 4 == kVMetaRow && v.off_vc == v.P * kRow2 &&
+  return !v.meta16 && v.krow == kRow2 && v.vrow == kRow2 && v.v_ng * v.v_nmeta * 4 == kVMetaRow &&
+         v.off_vc == v.P * kRow2 &&
          v.off_vm == 2 * v.P * kRow2 && v.off_km % 128 == 0 && v.head_bytes % 128 == 0 && v.page_bytes % 128 == 0 &&
          v.D == kD && v.n_rep == kRepI && v.kfmt == KVQ_INT2 && v.kmode == KVQ_ASYM_MINMAX &&
          v.kaxis == KVQ_PER_CHANNEL && v.vfmt == KVQ_INT2 && v.vmode == KVQ_ASYM_MINMAX &&

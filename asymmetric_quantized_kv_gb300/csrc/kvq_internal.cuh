@@ -29,7 +29,8 @@ struct KvqView {
   // layout of one head block
   int krow, vrow;                    // bytes per packed token row
   int off_vc, off_vm, off_km;        // section offsets (K codes at 0)
-  int k_nmeta, v_nmeta;              // floats per group entry: 2 asym, 1 sym
+  int k_nmeta, v_nmeta;              // values per group entry: 2 asym (scale, min), 1 sym
+  int meta16, mb;                    // stored scales / minima binary16 (mb = 2 bytes) or fp32 (4)
   int k_ng, v_ng;                    // PER_TOKEN groups per token
   int head_bytes;
   long long page_bytes;
@@ -201,6 +202,41 @@ __device__ __forceinline__ int asym_code_r(float x, float mn, float s, float r, 
 __device__ __forceinline__ unsigned fp8_code(float x, float s, int fmt) {
   if (s == 0.f) return 0u;
   return float_to_fp8(__fdiv_rn(x, s), fmt);
+}
+
+// ---- binary16 storage of scales and minima (meta_dtype KVQ_F16): the scale
+// rounded up, the minimum rounded down, saturating at +-65504
+__device__ __forceinline__ float f16_up(float x) { return fminf(__half2float(__float2half_ru(x)), 65504.f); }
+__device__ __forceinline__ float f16_down(float x) { return fmaxf(__half2float(__float2half_rd(x)), -65504.f); }
+
+__device__ __forceinline__ float load_meta(const uint8_t* p, int i, int m16) {
+  return m16 ? __half2float(reinterpret_cast<const __half*>(p)[i]) : reinterpret_cast<const float*>(p)[i];
+}
+__device__ __forceinline__ void store_meta(uint8_t* p, int i, float x, int m16) {
+  if (m16) {
+    reinterpret_cast<__half*>(p)[i] = __float2half_rn(x);  // x is a binary16 value already
+  } else {
+    reinterpret_cast<float*>(p)[i] = x;
+  }
+}
+
+// Scale s and minimum m of one group as stored (include/kvq.h): from the group's
+// min / max (asym) or absmax (sym), fp32 or binary16 storage.
+__device__ __forceinline__ void group_scale(float mn, float mx, float amax, bool asym, int bits, int m16,
+                                            float& s, float& m) {
+  if (asym) {
+    if (m16) {
+      m = f16_down(mn);
+      s = f16_up(__fdiv_rn(fmaxf(__fsub_rn(mx, m), 1e-8f), static_cast<float>(asym_qmax(bits))));
+    } else {
+      s = asym_scale(mn, mx, bits);
+      m = mn;
+    }
+  } else {
+    s = sym_scale(amax, bits);
+    if (m16) s = f16_up(s);
+    m = 0.f;
+  }
 }
 
 __device__ __forceinline__ float dequant_sym(int c, float s) {

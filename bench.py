@@ -12,7 +12,10 @@ log-uniform in [1024, 65536) tokens (seeded), 32 query / 8 KV heads, head_dim
 (64-token groups) stored pre-RoPE (theta 500000, rotated after dequantization),
 INT4 asymmetric per-token values, a 64-token bf16 residual window.
 --config 3 (Llama-3.1-8B-shaped, 2-bit KIVI-style, 32K) and --config 4
-(Llama-3.1-70B-shaped, FP8 E4M3, 128K) time the decode call alone.
+(Llama-3.1-70B-shaped, FP8 E4M3, or E5M2 with --fp8 e5m2, 128K) time the
+decode call alone.  Defaults: 20 warm-up and 200 timed steps; every decode call
+is also bracketed by events, and roofline.us_per_launch (mean) and
+us_per_launch_median come from those.
 
 value = algorithmic bytes per step (packed codes + scale/min metadata + window
 + q + out, plus the append's reads and writes) / device time per step, in
@@ -207,7 +210,7 @@ def cpu_oracle_throughput(cid: int, n_streams: int, steps: int = 1, fp8: str = "
     # bytes of the sampled streams, as one attention call would move them (per kv-head share)
     src = 2 if w.src_dtype == "bf16" else 4
     nbytes = 0
-    for (_, b, h, T, _) in jobs:  # the stream's KV bytes plus its query heads' q and out
+    for (_, b, h, T, _, _) in jobs:  # the stream's KV bytes plus its query heads' q and out
         nbytes += (head_bytes(spec, T) + (w.num_q_heads // w.num_kv_heads) * w.head_dim * (src + 4)) * steps
     busy = sum(times)
     return dict(value=nbytes / (busy / procs) / 1e9, unit="GB/s", cores=procs, kind="oracle",
@@ -467,8 +470,8 @@ def run_gpu(args, spec, rank, world):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", type=int, default=5, choices=[3, 4, 5])
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -539,6 +542,7 @@ def main():
                      "kernel": f"kvq_decode_attention: {SPLIT_KERNEL[args.config]} + combine (timed together)",
                      "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)" if peak_kind == "measured"
                      else "fallback 6.8 TB/s", "us_per_launch": att_ms * 1e3,
+                     "us_per_launch_median": statistics.median(r["att_ms"]) * 1e3,
                      "bytes_per_launch": att_bytes},
         "cpu_baseline": cpu,
         "e2e": r["e2e"],

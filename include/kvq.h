@@ -57,6 +57,13 @@
  *   FP8 E5M2:   the same with the E5M2 encoding (bias 15, 2 mantissa bits,
  *               subnormal step 2^-16), saturating to +-57344.
  *   rint() is round-half-to-even.
+ *   fp16 scale/min storage (meta_dtype = KVQ_F16; the pages leave the dtype of
+ *   the metadata open): the scale is stored rounded up to a binary16 value and
+ *   the minimum rounded down, and the codes use the stored values:
+ *     sym:  s = f16_up(a/qmax);
+ *     asym: m = f16_down(mn); d = max(mx-m, 1e-8f); s = f16_up(d/qmax);
+ *           c = clamp(rint((x-m)/s), 0, qmax); x^ = (c*s) + m;
+ *   so |x - x^| <= s/2 still holds.  f16_up / f16_down saturate at +-65504.
  *
  * Axes (kvq_qspec.axis):
  *   PER_CHANNEL (K only): one group per (channel, block of `group` tokens),
@@ -80,11 +87,12 @@
  * Each head block holds, each section starting on a 16-byte boundary:
  *   K codes  [P][D*bk/8]   bk = bits (8 for FP8)
  *   V codes  [P][D*bv/8]
- *   V meta   [P][ {D/gv scales} {D/gv mins (asym only)} ]  fp32, PER_TOKEN V
- *   K meta   PER_CHANNEL: [max(1, P/G)][ {D scales} {D mins (asym)} ] fp32;
+ *   V meta   [P][ {D/gv scales} {D/gv mins (asym only)} ]  PER_TOKEN V
+ *   K meta   PER_CHANNEL: [max(1, P/G)][ {D scales} {D mins (asym)} ];
  *            key group j is stored in the page holding token j*G, in slot
  *            (j*G % P) / G;
- *            PER_TOKEN:   [P][ {D/gk scales} {D/gk mins (asym)} ] fp32
+ *            PER_TOKEN:   [P][ {D/gk scales} {D/gk mins (asym)} ]
+ *            (scales and minima: fp32, or binary16 with meta_dtype = KVQ_F16)
  * Codes are packed along D: channel c's code occupies bits (c*b) % 8 ..
  * of byte (c*b)/8 of the token's row (little-endian bit order).  Code values:
  * sym INT8 two's complement; sym INT2/INT4 offset binary c + 2^(b-1);
@@ -117,7 +125,8 @@ typedef enum {
 typedef enum { KVQ_INT2 = 2, KVQ_INT4 = 4, KVQ_INT8 = 8, KVQ_FP8_E4M3 = 9, KVQ_FP8_E5M2 = 10 } kvq_format;
 typedef enum { KVQ_SYM_ABSMAX = 0, KVQ_ASYM_MINMAX = 1 } kvq_mode; /* ignored for FP8 */
 typedef enum { KVQ_PER_TENSOR = 0, KVQ_PER_TOKEN = 1, KVQ_PER_CHANNEL = 2 } kvq_axis;
-typedef enum { KVQ_F32 = 0, KVQ_BF16 = 1 } kvq_dtype; /* source, window and q dtype */
+typedef enum { KVQ_F32 = 0, KVQ_BF16 = 1, KVQ_F16 = 2 } kvq_dtype; /* source/window/q: F32, BF16;
+                                                                 stored scales/minima: F32, F16 */
 
 /* Device-side status bits (OR-ed into *kvq_cache.status). */
 #define KVQ_DEV_BAD_PAGE 0x1      /* block-table entry outside [0, n_pages)          */
@@ -142,6 +151,7 @@ typedef struct {
   int32_t rope_pre;     /* 1: the cache holds pre-RoPE keys, rotated after dequant */
   float rope_theta;     /* RoPE base; angle of pair i at position p = p*theta^(-2i/D) */
   int32_t src_dtype;    /* kvq_dtype of appended K/V, the window and q            */
+  int32_t meta_dtype;   /* stored scales / minima: KVQ_F32 (0) or KVQ_F16 (2)     */
 } kvq_config;
 
 typedef struct {

@@ -16,7 +16,7 @@ def to_c(cfg: O.Config):
     k, v = cfg.k, cfg.v
     return K.make_config(cfg.num_q_heads, cfg.num_kv_heads, cfg.head_dim, (k.fmt, k.mode, k.axis, k.group),
                          (v.fmt, v.mode, v.axis, v.group), cfg.residual, cfg.page_size, cfg.rope_pre,
-                         cfg.rope_theta, cfg.src_dtype)
+                         cfg.rope_theta, cfg.src_dtype, cfg.meta_dtype)
 
 
 def torch_src(x: np.ndarray, cfg: O.Config, device="cuda"):

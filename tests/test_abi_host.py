@@ -48,7 +48,8 @@ SPECS = [(O.INT2, O.ASYM, O.PER_CHANNEL, 32), (O.INT8, O.SYM, O.PER_CHANNEL, 64)
 
 @pytest.mark.parametrize("D", [64, 128, 256])
 @pytest.mark.parametrize("P", [16, 64, 256])
-def test_layout_agrees_with_oracle(K, D, P):
+@pytest.mark.parametrize("meta", [O.F32, O.F16])
+def test_layout_agrees_with_oracle(K, D, P, meta):
     for ks in SPECS:
         for vs in SPECS:
             if vs[2] == O.PER_CHANNEL:
@@ -56,8 +57,8 @@ def test_layout_agrees_with_oracle(K, D, P):
             R = 64 if ks[2] == O.PER_CHANNEL else 0
             if ks[2] == O.PER_CHANNEL and (P % ks[3] and ks[3] % P):
                 continue
-            cfg = O.Config(8, 2, D, O.QSpec(*ks), O.QSpec(*vs), R, P)
-            c = K.kvq_config(8, 2, D, K.kvq_qspec(*ks), K.kvq_qspec(*vs), R, P, 0, 1e4, 0)
+            cfg = O.Config(8, 2, D, O.QSpec(*ks), O.QSpec(*vs), R, P, meta_dtype=meta)
+            c = K.kvq_config(8, 2, D, K.kvq_qspec(*ks), K.kvq_qspec(*vs), R, P, 0, 1e4, 0, meta)
             assert K.kvq_validate(c) == 0
             L = O.layout(cfg)
             assert K.kvq_page_bytes(c) == L["page"]
@@ -78,6 +79,8 @@ def test_validation_rejects_bad_configs(K):
     assert K.kvq_validate(_cfg(K, num_q_heads=30)) == E
     assert K.kvq_validate(_cfg(K, head_dim=96)) == U
     assert K.kvq_validate(_cfg(K, residual=60)) == E            # R % G != 0
+    assert K.kvq_validate(_cfg(K, meta_dtype=1)) == E           # scales/minima: F32 or F16 only
+    assert K.kvq_validate(_cfg(K, meta_dtype=2)) == 0
     assert K.kvq_validate(_cfg(K, residual=0)) == E             # per-channel keys need a window
     assert K.kvq_validate(_cfg(K, page_size=24)) == E
     assert K.kvq_validate(_cfg(K, k=K.kvq_qspec(3, 0, 2, 64))) == E

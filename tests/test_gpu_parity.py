@@ -68,6 +68,16 @@ CASES = {
                                     O.BF16), [5, 130, 1500]),
     "fast_rope_i8i4_g128": (O.Config(32, 8, 128, Q(O.INT8, S, CH, 128), Q(O.INT4, A, TOK, 0), 128, 16, 1, 1e4,
                                      O.BF16), [128, 129, 1000, 4100]),
+    # fp16 scale/min storage: the 8B layer's formats, pre-RoPE INT8 keys + INT4 values,
+    # per-channel keys folded through the sub-chunk path (R 512), grouped per-token encodings
+    "m16_int2_kivi": (O.Config(8, 2, 128, Q(O.INT2, A, CH, 32), Q(O.INT2, A, TOK, 32), 128, 256, 0, 1e4, O.BF16,
+                               meta_dtype=O.F16), [0, 1, 127, 128, 129, 300, 1000]),
+    "m16_rope_i8i4": (O.Config(8, 2, 128, Q(O.INT8, S, CH, 64), Q(O.INT4, A, TOK, 128), 64, 16, 1, 5e5, O.BF16,
+                               meta_dtype=O.F16), [1, 63, 64, 65, 700, 2100]),
+    "m16_int4_channel_r512": (O.Config(8, 1, 128, Q(O.INT4, A, CH, 512), Q(O.INT4, A, TOK, 0), 512, 512, 0, 1e4,
+                                       O.F32, meta_dtype=O.F16), [512, 1100]),
+    "m16_d64_grouped": (O.Config(4, 4, 64, Q(O.INT4, S, TOK, 32), Q(O.INT8, A, TOK, 16), 32, 32, 1, 1e4, O.F32,
+                                 meta_dtype=O.F16), [5, 33, 64, 99]),
     # other head sizes and mixed encodings
     "d64_int4sym": (O.Config(4, 4, 64, Q(O.INT4, S, TOK, 32), Q(O.INT8, A, TOK, 16), 32, 32, 1, 1e4, O.F32),
                     [5, 33, 64, 99]),

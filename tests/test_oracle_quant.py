@@ -250,8 +250,8 @@ def test_fp8_formats_quantize_with_their_own_tables():
 
 # ---------------------------------------------------------- fp16 scale/min storage
 
-_HALVES = np.unique(np.arange(0, 0x10000, dtype=np.uint16).view(np.float16).astype(np.float64))
-_HALVES = _HALVES[np.isfinite(_HALVES)]  # every finite binary16 value, increasing
+_H16 = np.arange(0, 0x10000, dtype=np.uint16).view(np.float16)
+_HALVES = np.unique(_H16[np.isfinite(_H16)].astype(np.float64))  # every finite binary16 value, increasing
 
 
 def test_f16_directed_rounding_against_every_half():
