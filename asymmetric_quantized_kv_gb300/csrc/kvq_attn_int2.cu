@@ -22,6 +22,10 @@
 //     32G + 4g .. 32G + 4g + 3), so each 16-row MMA block stays inside one value
 //     group G and B = p * s_t(G) split hi/lo; the minima enter through running
 //     sums of p * m_t(G).
+// Scales and minima stored as binary16 (meta_dtype F16) take a second instance:
+// the codes come with one 2-section tensor copy, the value rows and a group's key
+// scales and minima (256 and 512 bytes) with plain bulk copies, and the readers
+// widen the halves to fp32.
 #include <math.h>
 
 #include "kvq_ptx.cuh"
@@ -48,6 +52,9 @@ constexpr int kOffK = kKMeta2;
 constexpr int kOffV = kOffK + kTI * kRow2;
 constexpr int kOffVM = kOffV + kTI * kRow2;
 constexpr int kTileBytesI = 3 * kTI * kRow2;
+constexpr int kVMetaRow16 = 16;                   // (scale x 4, min x 4) binary16 per token
+constexpr int kKMeta16 = 2 * kD * 2;              // a key group's scales then minima, binary16
+constexpr int kTileBytes16 = 2 * kTI * kRow2 + kTI * kVMetaRow16;
 constexpr int kStageI = 3072;
 constexpr uint32_t kSpinI = 1u << 20;
 constexpr float kLog2eI = 1.4426950408889634f;
@@ -125,6 +132,14 @@ __device__ __forceinline__ void split_sel(float x0, float x1, bool lo, uint32_t&
   out = lo ? nl : hi;
 }
 
+// four binary16 values (two words) widened to fp32
+__device__ __forceinline__ float4 halves4(uint2 w) {
+  const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&w.x));
+  const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&w.y));
+  return make_float4(a.x, a.y, b.x, b.y);
+}
+
+template <bool M16>
 __global__ void __launch_bounds__(kThreadsI, 3)
     split_int2_kernel(KvqView v, const void* q, float scale, float* ws, const __grid_constant__ CUtensorMap tmc,
                       const __grid_constant__ CUtensorMap tmk) {
@@ -261,14 +276,25 @@ __global__ void __launch_bounds__(kThreadsI, 3)
         }
         const int slot = tok & (v.P - 1);
         const bool gstart = (tok & (G - 1)) == 0;
-        mbar_arrive_expect_tx(bar, kTileBytesI + (gstart ? kKMeta2 : 0));
         uint8_t* dst = sm.stage[warp][stage];
         const uint64_t pol = l2_evict_first();
-        tma_load_5d_hint(dst + kOffK, &tmc, 0, slot, 0, h, pid, bar, pol);
-        if (gstart) {
-          const long long byte0 = (long long)pid * v.page_bytes + head_off + v.off_km +
-                                  (long long)(v.P >= G ? slot >> lgG : 0) * kKMeta2;
-          tma_load_2d_hint(dst + kOffKM, &tmk, 0, (int)(byte0 >> 7), bar, pol);
+        if constexpr (M16) {
+          // codes by one 2-section tensor copy; value rows and key meta by bulk copies
+          mbar_arrive_expect_tx(bar, kTileBytes16 + (gstart ? kKMeta16 : 0));
+          tma_load_5d_hint(dst + kOffK, &tmc, 0, slot, 0, h, pid, bar, pol);
+          const uint8_t* hb = v.pages + (long long)pid * v.page_bytes + head_off;
+          bulk_g2s_hint(dst + kOffVM, hb + v.off_vm + slot * kVMetaRow16, kTI * kVMetaRow16, bar, pol);
+          if (gstart)
+            bulk_g2s_hint(dst + kOffKM, hb + v.off_km + (v.P >= G ? slot >> lgG : 0) * kKMeta16, kKMeta16, bar,
+                          pol);
+        } else {
+          mbar_arrive_expect_tx(bar, kTileBytesI + (gstart ? kKMeta2 : 0));
+          tma_load_5d_hint(dst + kOffK, &tmc, 0, slot, 0, h, pid, bar, pol);
+          if (gstart) {
+            const long long byte0 = (long long)pid * v.page_bytes + head_off + v.off_km +
+                                    (long long)(v.P >= G ? slot >> lgG : 0) * kKMeta2;
+            tma_load_2d_hint(dst + kOffKM, &tmk, 0, (int)(byte0 >> 7), bar, pol);
+          }
         }
       };
       int pf = 0;
@@ -311,9 +337,17 @@ __global__ void __launch_bounds__(kThreadsI, 3)
             float sc[16], mn[16];
 #pragma unroll
             for (int k4 = 0; k4 < 4; ++k4) {
-              const int c = 4 * half + k4;
-              const float4 a = *reinterpret_cast<const float4*>(ks + t * 128 + ((c ^ t) << 4));
-              const float4 b = *reinterpret_cast<const float4*>(ks + (4 + t) * 128 + ((c ^ (4 + t)) << 4));
+              float4 a, b;
+              if constexpr (M16) {
+                // linear halves: scales of channels 32t + 16 half + 4 k4 .. at byte 2 * channel, minima after
+                const int off = 64 * t + 32 * half + 8 * k4;
+                a = halves4(*reinterpret_cast<const uint2*>(ks + off));
+                b = halves4(*reinterpret_cast<const uint2*>(ks + 2 * kD + off));
+              } else {
+                const int c = 4 * half + k4;
+                a = *reinterpret_cast<const float4*>(ks + t * 128 + ((c ^ t) << 4));
+                b = *reinterpret_cast<const float4*>(ks + (4 + t) * 128 + ((c ^ (4 + t)) << 4));
+              }
               sc[4 * k4] = a.x; sc[4 * k4 + 1] = a.y; sc[4 * k4 + 2] = a.z; sc[4 * k4 + 3] = a.w;
               mn[4 * k4] = b.x; mn[4 * k4 + 1] = b.y; mn[4 * k4 + 2] = b.z; mn[4 * k4 + 3] = b.w;
             }
@@ -354,10 +388,17 @@ __global__ void __launch_bounds__(kThreadsI, 3)
         softmax(lg0, lg1, p0, p1);
 
         // ---- value minima of tokens g, g+8 (head t) and scales of the B tokens
-        const float* vm = reinterpret_cast<const float*>(buf + kOffVM);
+        // per-token value row: 4 scales then 4 minima (fp32, or binary16 in M16)
+        auto vrow = [&](int tok, int part) -> float4 {
+          if constexpr (M16) {
+            return halves4(*reinterpret_cast<const uint2*>(buf + kOffVM + tok * kVMetaRow16 + 8 * part));
+          } else {
+            return reinterpret_cast<const float4*>(buf + kOffVM + tok * kVMetaRow)[part];
+          }
+        };
         if (valid) {
-          const float4 n0 = reinterpret_cast<const float4*>(vm + g * 8)[1];
-          const float4 n1 = reinterpret_cast<const float4*>(vm + (g + 8) * 8)[1];
+          const float4 n0 = vrow(g, 1);
+          const float4 n1 = vrow(g + 8, 1);
           mb[0] = fmaf(p0, n0.x, fmaf(p1, n1.x, mb[0]));
           mb[1] = fmaf(p0, n0.y, fmaf(p1, n1.y, mb[1]));
           mb[2] = fmaf(p0, n0.z, fmaf(p1, n1.z, mb[2]));
@@ -365,10 +406,10 @@ __global__ void __launch_bounds__(kThreadsI, 3)
         }
         float2 x01, x89;
         exchange(p0, p1, x01, x89);
-        const float4 sa = reinterpret_cast<const float4*>(vm + (2 * t) * 8)[0];
-        const float4 sb = reinterpret_cast<const float4*>(vm + (2 * t + 1) * 8)[0];
-        const float4 sc8 = reinterpret_cast<const float4*>(vm + (2 * t + 8) * 8)[0];
-        const float4 sd = reinterpret_cast<const float4*>(vm + (2 * t + 9) * 8)[0];
+        const float4 sa = vrow(2 * t, 0);
+        const float4 sb = vrow(2 * t + 1, 0);
+        const float4 sc8 = vrow(2 * t + 8, 0);
+        const float4 sd = vrow(2 * t + 9, 0);
         const float sA[4] = {sa.x, sa.y, sa.z, sa.w}, sB[4] = {sb.x, sb.y, sb.z, sb.w};
         const float sC[4] = {sc8.x, sc8.y, sc8.z, sc8.w}, sD[4] = {sd.x, sd.y, sd.z, sd.w};
 
@@ -524,9 +565,12 @@ bool int2_shape_eligible(const KvqView& v) {
   const bool pow2_g = v.kgroup > 0 && (v.kgroup & (v.kgroup - 1)) == 0;
   // the three per-token sections (K codes, V codes, V meta) share 32-byte rows at a
   // uniform section stride, and every offset is a multiple of 128 bytes
-  return !v.meta16 && v.krow == kRow2 && v.vrow == kRow2 && v.v_ng * v.v_nmeta * 4 == kVMetaRow &&
-         v.off_vc == v.P * kRow2 &&
-         v.off_vm == 2 * v.P * kRow2 && v.off_km % 128 == 0 && v.head_bytes % 128 == 0 && v.page_bytes % 128 == 0 &&
+  // (binary16 metadata: 16-byte value rows and 16-byte aligned key meta, read by bulk copies)
+  const int vmeta_row = v.v_ng * v.v_nmeta * v.mb;
+  const bool meta_ok = v.meta16 ? (vmeta_row == kVMetaRow16 && v.off_km % 16 == 0)
+                                : (vmeta_row == kVMetaRow && v.off_km % 128 == 0);
+  return meta_ok && v.krow == kRow2 && v.vrow == kRow2 && v.off_vc == v.P * kRow2 &&
+         v.off_vm == 2 * v.P * kRow2 && v.head_bytes % 128 == 0 && v.page_bytes % 128 == 0 &&
          v.D == kD && v.n_rep == kRepI && v.kfmt == KVQ_INT2 && v.kmode == KVQ_ASYM_MINMAX &&
          v.kaxis == KVQ_PER_CHANNEL && v.vfmt == KVQ_INT2 && v.vmode == KVQ_ASYM_MINMAX &&
          v.vaxis == KVQ_PER_TOKEN && v.vgroup == 32 && v.rope_pre == 0 && pow2_g && v.kgroup >= kTI &&
@@ -542,10 +586,11 @@ kvq_status launch_int2(const KvqView& v, const void* q, float* out, float scale,
   // the per-token sections as a 5-D tensor (row bytes, slot, section, head, page), one tile per box
   CUtensorMap tmc, tmk;
   {
-    const cuuint64_t dims[5] = {(cuuint64_t)kRow2, (cuuint64_t)v.P, 3, (cuuint64_t)v.Hkv, (cuuint64_t)v.n_pages};
+    const cuuint32_t nsec = v.meta16 ? 2 : 3;  // binary16 metadata: codes only (value rows by bulk copies)
+    const cuuint64_t dims[5] = {(cuuint64_t)kRow2, (cuuint64_t)v.P, nsec, (cuuint64_t)v.Hkv, (cuuint64_t)v.n_pages};
     const cuuint64_t strides[4] = {(cuuint64_t)kRow2, (cuuint64_t)v.P * kRow2, (cuuint64_t)v.head_bytes,
                                    (cuuint64_t)v.page_bytes};
-    const cuuint32_t box[5] = {(cuuint32_t)kRow2, (cuuint32_t)kTI, 3, 1, 1};
+    const cuuint32_t box[5] = {(cuuint32_t)kRow2, (cuuint32_t)kTI, nsec, 1, 1};
     const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
     if (tensor_map_encoder()(&tmc, CU_TENSOR_MAP_DATA_TYPE_UINT8, 5, v.pages, dims, strides, box, estr,
                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
@@ -564,23 +609,26 @@ kvq_status launch_int2(const KvqView& v, const void* q, float* out, float scale,
       return KVQ_ERR_UNSUPPORTED;
   }
   const size_t smem = sizeof(SmemI2) + 1024 + sizeof(int) * 3 * (v.batch + 1);
-  static int occ_cache[64] = {0};
+  void (*kern)(KvqView, const void*, float, float*, const CUtensorMap, const CUtensorMap) =
+      v.meta16 ? split_int2_kernel<true> : split_int2_kernel<false>;
+  static int occ_cache[2][64] = {{0}};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64) return KVQ_ERR_UNSUPPORTED;
-  if (!occ_cache[dev]) {
-    if (cudaFuncSetAttribute(split_int2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  int& occ_dev = occ_cache[v.meta16 ? 1 : 0][dev];
+  if (!occ_dev) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)(sizeof(SmemI2) + 1024 + sizeof(int) * 3 * 4097)) != cudaSuccess)
       return KVQ_ERR_CUDA;
     int occ = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, split_int2_kernel, kThreadsI, smem) != cudaSuccess)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kThreadsI, smem) != cudaSuccess)
       return KVQ_ERR_CUDA;
-    occ_cache[dev] = occ > 0 ? occ : 1;
+    occ_dev = occ > 0 ? occ : 1;
   }
-  const int grid = num_sms() * occ_cache[dev];
+  const int grid = num_sms() * occ_dev;
   if (cudaMemsetAsync(static_cast<char*>(ws) + fast_counter_offset(v.batch), 0, 8, st) != cudaSuccess)
     return KVQ_ERR_CUDA;
-  split_int2_kernel<<<grid, kThreadsI, smem, st>>>(v, q, scale, static_cast<float*>(ws), tmc, tmk);
+  kern<<<grid, kThreadsI, smem, st>>>(v, q, scale, static_cast<float*>(ws), tmc, tmk);
   if (cudaGetLastError() != cudaSuccess) return KVQ_ERR_CUDA;
   return launch_split_combine(v, static_cast<float*>(ws), out, st) == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }

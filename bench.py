@@ -63,7 +63,15 @@ SPLIT_TRAFFIC = {5: 1791.3e6, 4: 2193.4e6, 3: 557.3e6}
 SPLIT_KERNEL = {5: "split_rope_i8i4_kernel", 4: "split_fp8_kernel", 3: "split_int2_kernel"}
 
 
-def workload_spec(cid: int, batch: int = 0, fp8: str = "e4m3") -> dict:
+def workload_spec(cid: int, batch: int = 0, fp8: str = "e4m3", meta: str = "f32") -> dict:
+    spec = _workload_spec(cid, batch, fp8)
+    spec["meta"] = meta  # stored scales / minima: "f32" or "f16" (binary16, scale up / minimum down)
+    if meta == "f16":
+        spec["name"] += ", fp16 scales/minima"
+    return spec
+
+
+def _workload_spec(cid: int, batch: int = 0, fp8: str = "e4m3") -> dict:
     w = W.WORKLOADS[cid]
     if batch:  # the first `batch` sequences of the workload (smaller captures for ncu)
         import dataclasses
@@ -102,13 +110,14 @@ def quantized_bytes(spec, n: int) -> int:
     vf, vmode, vaxis, vg = spec["v"]
     nmk = 2 if kmode == ASYM and not _is_fp8(kf) else 1
     nmv = 2 if vmode == ASYM and not _is_fp8(vf) else 1
+    mb = 2 if spec.get("meta") == "f16" else 4  # bytes per stored scale / minimum
     total = n * D * (_bits(kf) + _bits(vf)) // 8
     if kaxis == CH:
-        total += (n // kg) * D * 4 * nmk
+        total += (n // kg) * D * mb * nmk
     elif kaxis == TOK:
-        total += n * (D // (kg or D)) * 4 * nmk
+        total += n * (D // (kg or D)) * mb * nmk
     if vaxis == TOK:
-        total += n * (D // (vg or D)) * 4 * nmv
+        total += n * (D // (vg or D)) * mb * nmv
     return total
 
 
@@ -155,12 +164,13 @@ def append_bytes(spec, lens_before) -> int:
 def _oracle_worker(job):
     """Time the oracle's decode (dequantize + RoPE + attention) on one sampled
     (sequence, kv-head) stream; one BLAS thread per worker process."""
-    cid, b, h, T, steps, fp8 = job
+    cid, b, h, T, steps, fp8, meta = job
     from oracle import kvq_oracle as O
-    spec = workload_spec(cid, 0, fp8)
+    spec = workload_spec(cid, 0, fp8, meta)
     w = spec["w"]
     cfg = O.Config(w.num_q_heads, w.num_kv_heads, w.head_dim, O.QSpec(*spec["k"]), O.QSpec(*spec["v"]),
-                   spec["R"], spec["P"], spec["rope"], spec["theta"], O.BF16 if w.src_dtype == "bf16" else O.F32)
+                   spec["R"], spec["P"], spec["rope"], spec["theta"], O.BF16 if w.src_dtype == "bf16" else O.F32,
+                   meta_dtype=O.F16 if meta == "f16" else O.F32)
     K = W.kv_block(w, b, h, W.KIND_K, 0, T)
     V = W.kv_block(w, b, h, W.KIND_V, 0, T)
     ks = O.calibrate_absmax(K, FP8_MAX[spec["k"][0]]) if _is_fp8(spec["k"][0]) else 0.0
@@ -173,19 +183,19 @@ def _oracle_worker(job):
     return time.perf_counter() - t0
 
 
-def cpu_oracle_throughput(cid: int, n_streams: int, steps: int = 1, fp8: str = "e4m3"):
+def cpu_oracle_throughput(cid: int, n_streams: int, steps: int = 1, fp8: str = "e4m3", meta: str = "f32"):
     """Oracle GB/s on a bounded sample of the workload's streams, timed in a
     spawned process pool (one BLAS thread per process)."""
     import multiprocessing as mp
-    spec = workload_spec(cid, 0, fp8)
+    spec = workload_spec(cid, 0, fp8, meta)
     w = spec["w"]
     lens = W.lengths(w)
     g = np.random.default_rng(1234)
     picks = [(int(g.integers(0, w.batch)), int(g.integers(0, w.num_kv_heads))) for _ in range(n_streams)]
     if cid == 4:  # 131072-token streams: a prefix keeps the sample bounded
-        jobs = [(cid, b, h, 16384, steps, fp8) for b, h in picks]
+        jobs = [(cid, b, h, 16384, steps, fp8, meta) for b, h in picks]
     else:
-        jobs = [(cid, b, h, int(lens[b]), steps, fp8) for b, h in picks]
+        jobs = [(cid, b, h, int(lens[b]), steps, fp8, meta) for b, h in picks]
     try:
         cores = len(os.sched_getaffinity(0))
     except AttributeError:
@@ -210,7 +220,7 @@ def cpu_oracle_throughput(cid: int, n_streams: int, steps: int = 1, fp8: str = "
     # bytes of the sampled streams, as one attention call would move them (per kv-head share)
     src = 2 if w.src_dtype == "bf16" else 4
     nbytes = 0
-    for (_, b, h, T, _, _) in jobs:  # the stream's KV bytes plus its query heads' q and out
+    for (_, b, h, T, _, _, _) in jobs:  # the stream's KV bytes plus its query heads' q and out
         nbytes += (head_bytes(spec, T) + (w.num_q_heads // w.num_kv_heads) * w.head_dim * (src + 4)) * steps
     busy = sum(times)
     return dict(value=nbytes / (busy / procs) / 1e9, unit="GB/s", cores=procs, kind="oracle",
@@ -307,7 +317,8 @@ def build_cache(spec, device, extra_tokens, gen_seed=1):
     Bn, H, D, Hq = w.batch, w.num_kv_heads, w.head_dim, w.num_q_heads
     lens = [int(x) for x in W.lengths(W.WORKLOADS[w.cid])][:w.batch]
     P = spec["P"]
-    cfg = K.make_config(Hq, H, D, spec["k"], spec["v"], spec["R"], P, spec["rope"], spec["theta"], BF16)
+    cfg = K.make_config(Hq, H, D, spec["k"], spec["v"], spec["R"], P, spec["rope"], spec["theta"], BF16,
+                        2 if spec.get("meta") == "f16" else 0)
     need = [(T + extra_tokens + P - 1) // P for T in lens]
     maxp = max(need)
     n_pages = sum(need)
@@ -480,11 +491,12 @@ def main():
     ap.add_argument("--cpu-steps", type=int, default=8)
     ap.add_argument("--batch", type=int, default=0, help="use only the first N sequences (profiling)")
     ap.add_argument("--fp8", default="e4m3", choices=sorted(FP8_FORMATS), help="FP8 format of --config 4")
+    ap.add_argument("--meta", default="f32", choices=["f32", "f16"], help="stored scales / minima (configs 3, 5)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
-    spec = workload_spec(args.config, args.batch, args.fp8)
+    spec = workload_spec(args.config, args.batch, args.fp8, args.meta)
     w = spec["w"]
 
     if args.impl == "reference":
@@ -495,7 +507,8 @@ def main():
         for _ in range(args.warmup):
             pass  # the oracle has no warm state to build
         for _ in range(args.steps):
-            detail = cpu_oracle_throughput(args.config, n_streams=max(2, args.cpu_streams // 4), fp8=args.fp8)
+            detail = cpu_oracle_throughput(args.config, n_streams=max(2, args.cpu_streams // 4), fp8=args.fp8,
+                                           meta=args.meta)
             per_step.append(detail["value"])
         val = statistics.median(per_step)
         detail["value"] = val
@@ -509,7 +522,8 @@ def main():
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_oracle_throughput(args.config, n_streams=args.cpu_streams, steps=args.cpu_steps, fp8=args.fp8)
+        cpu = cpu_oracle_throughput(args.config, n_streams=args.cpu_streams, steps=args.cpu_steps, fp8=args.fp8,
+                                    meta=args.meta)
 
     import torch
     if world > 1:
@@ -538,7 +552,8 @@ def main():
                    "l2": "inputs (%.2f GB per step) larger than the 129 MB L2; no flush" % (att_bytes / 1e9)},
         "pct_of_hbm_peak": 100.0 * value / peak,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": SPLIT_TRAFFIC.get(args.config) if not args.batch and args.fp8 == "e4m3" else None,
+                     "traffic": SPLIT_TRAFFIC.get(args.config)
+                     if not args.batch and args.fp8 == "e4m3" and args.meta == "f32" else None,
                      "kernel": f"kvq_decode_attention: {SPLIT_KERNEL[args.config]} + combine (timed together)",
                      "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)" if peak_kind == "measured"
                      else "fallback 6.8 TB/s", "us_per_launch": att_ms * 1e3,

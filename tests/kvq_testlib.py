@@ -178,17 +178,17 @@ class FullCase:
     absmax taken by torch, so the oracle and the library quantize with the same
     scale without the library computing it."""
 
-    def __init__(self, cid, samples, gen_seed=1, fp8="e4m3"):
+    def __init__(self, cid, samples, gen_seed=1, fp8="e4m3", meta="f32"):
         import bench
         import asymmetric_quantized_kv_gb300 as K
-        spec = bench.workload_spec(cid, 0, fp8)
+        spec = bench.workload_spec(cid, 0, fp8, meta)
         w = spec["w"]
         self.spec, self.w = spec, w
         Bn, H, D, Hq = w.batch, w.num_kv_heads, w.head_dim, w.num_q_heads
         self.lens = [int(x) for x in W.lengths(w)]
         P = spec["P"]
         self.cfg = O.Config(Hq, H, D, O.QSpec(*spec["k"]), O.QSpec(*spec["v"]), spec["R"], P, spec["rope"],
-                            spec["theta"], O.BF16)
+                            spec["theta"], O.BF16, meta_dtype=O.F16 if meta == "f16" else O.F32)
         need = [(T + P - 1) // P for T in self.lens]
         maxp, n_pages = max(need), sum(need)
         perm = W.page_permutation(n_pages, 5)

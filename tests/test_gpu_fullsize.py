@@ -24,10 +24,12 @@ def _samples(cid):
     return [(b_long, 0), (b_short, w.num_kv_heads - 1), ((b_long + 1) % w.batch, 3)]
 
 
-@pytest.mark.parametrize("cid,fp8", [(3, "e4m3"), (4, "e4m3"), (4, "e5m2"), (5, "e4m3")])
-def test_fullsize_sampled_streams(cid, fp8):
-    """(config 4 also in FP8 E5M2: the 70B layer with absmax/57344 scales)"""
-    case = FullCase(cid, _samples(cid), fp8=fp8)
+@pytest.mark.parametrize("cid,fp8,meta", [(3, "e4m3", "f32"), (3, "e4m3", "f16"), (4, "e4m3", "f32"),
+                                          (4, "e5m2", "f32"), (5, "e4m3", "f32")])
+def test_fullsize_sampled_streams(cid, fp8, meta):
+    """(config 4 also in FP8 E5M2 with absmax/57344 scales; config 3 also with
+    binary16 scales and minima)"""
+    case = FullCase(cid, _samples(cid), fp8=fp8, meta=meta)
     case.check_attention()
     case.check_dequantize()
     del case

@@ -72,6 +72,8 @@ CASES = {
     # per-channel keys folded through the sub-chunk path (R 512), grouped per-token encodings
     "m16_int2_kivi": (O.Config(8, 2, 128, Q(O.INT2, A, CH, 32), Q(O.INT2, A, TOK, 32), 128, 256, 0, 1e4, O.BF16,
                                meta_dtype=O.F16), [0, 1, 127, 128, 129, 300, 1000]),
+    "m16_int2_kivi_p16": (O.Config(32, 8, 128, Q(O.INT2, A, CH, 32), Q(O.INT2, A, TOK, 32), 128, 16, 0, 1e4,
+                                   O.BF16, meta_dtype=O.F16), [129, 1000, 2200]),
     "m16_rope_i8i4": (O.Config(8, 2, 128, Q(O.INT8, S, CH, 64), Q(O.INT4, A, TOK, 128), 64, 16, 1, 5e5, O.BF16,
                                meta_dtype=O.F16), [1, 63, 64, 65, 700, 2100]),
     "m16_int4_channel_r512": (O.Config(8, 1, 128, Q(O.INT4, A, CH, 512), Q(O.INT4, A, TOK, 0), 512, 512, 0, 1e4,
