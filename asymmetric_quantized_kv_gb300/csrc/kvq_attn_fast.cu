@@ -220,13 +220,15 @@ __global__ void __launch_bounds__(kThreads, 2)
   SmemRI& sm = *reinterpret_cast<SmemRI*>(dyn);
   int* prefA = reinterpret_cast<int*>(dyn + sizeof(SmemRI));
   int* prefB = prefA + v.batch + 1;
-  __shared__ int s_C, s_NA, s_NB, s_next[2];
+  __shared__ int s_C, s_NA, s_NB, s_NS, s_next[2];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
   const int G = v.kgroup;  // powers of two (checked on the host)
   const int lgG = __ffs(G) - 1, lgP = __ffs(v.P) - 1;
-  fast_plan<kThreads>(v, G, prefA, prefB, &s_C, &s_NA, &s_NB, reinterpret_cast<int*>(&sm.stage[0][0][0]));
-  if (blockIdx.x == 0) store_fast_plan(v, ws, prefA, prefB, s_C, s_NA, s_NB);
+  // one CTA takes all kv-heads of an item: one unit per item, gridDim.x workers
+  fast_plan<kThreads>(v, G, 1, (int)gridDim.x, true, prefA, prefB, &s_C, &s_NA, &s_NB, &s_NS,
+                      reinterpret_cast<int*>(&sm.stage[0][0][0]));
+  if (blockIdx.x == 0) store_fast_plan(v, ws, prefA, prefB, s_C, s_NA, s_NB, s_NS);
   grid_dep_launch();  // the combine kernel may be scheduled; it waits for this grid to complete
   unsigned long long* counter =
       reinterpret_cast<unsigned long long*>(reinterpret_cast<char*>(ws) + fast_counter_offset(v.batch));
@@ -246,7 +248,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   __syncthreads();
 
 
-  const int C = s_C, NA = s_NA, n_items = s_NA + s_NB;
+  const int C = s_C, NA = s_NA, NS = s_NS, n_items = s_NA + s_NB;
   float* part = reinterpret_cast<float*>(reinterpret_cast<char*>(ws) + fast_header_bytes(v.batch));
   const float qscale = scale * kLog2e;
   const int h = warp;
@@ -286,7 +288,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   while (item < n_items) {
     // the CTA's next item, fetched now and read after this item's closing barrier
     if (threadIdx.x == 0) s_next[npar] = (int)gridDim.x + (int)atomicAdd(counter, 1ull);
-    const FastItem it = decode_fast_item(v, prefA, prefB, C, NA, item);
+    const FastItem it = decode_fast_item(v, prefA, prefB, C, NA, NS, G, true, item);
     const int ntiles = (it.t1 - it.t0 + kTile - 1) / kTile;
 
     // B operand: q * scale * log2(e) for query head 4h + g/2, split hi (even g) / lo (odd g);

@@ -67,12 +67,14 @@ __global__ void __launch_bounds__(kThreads8)
   SmemF8& sm = *reinterpret_cast<SmemF8*>(dyn);
   int* prefA = reinterpret_cast<int*>(dyn + sizeof(SmemF8));
   int* prefB = prefA + v.batch + 1;
-  __shared__ int s_C, s_NA, s_NB;
+  __shared__ int s_C, s_NA, s_NB, s_NS;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
   const int lgP = __ffs(v.P) - 1;  // a power of two (checked on the host)
-  fast_plan<kThreads8>(v, kTileT, prefA, prefB, &s_C, &s_NA, &s_NB, reinterpret_cast<int*>(&sm.kv[0][0][0][0]));
-  if (blockIdx.x == 0) store_fast_plan(v, ws, prefA, prefB, s_C, s_NA, s_NB);
+  // a warp takes one kv-head of an item: Hkv units per item, one worker per warp; no cuts
+  fast_plan<kThreads8>(v, kTileT, v.Hkv, (int)gridDim.x * kWarps8, false, prefA, prefB, &s_C, &s_NA, &s_NB, &s_NS,
+                       reinterpret_cast<int*>(&sm.kv[0][0][0][0]));
+  if (blockIdx.x == 0) store_fast_plan(v, ws, prefA, prefB, s_C, s_NA, s_NB, s_NS);
   grid_dep_launch();  // the combine kernel may be scheduled; it waits for this grid to complete
   unsigned long long* counter =
       reinterpret_cast<unsigned long long*>(reinterpret_cast<char*>(ws) + fast_counter_offset(v.batch));
@@ -82,7 +84,7 @@ __global__ void __launch_bounds__(kThreads8)
   }
   __syncthreads();
 
-  const int C = s_C, NA = s_NA;
+  const int C = s_C, NA = s_NA, NS = s_NS;
   const int n_units = (s_NA + s_NB) * v.Hkv;
   float* part = reinterpret_cast<float*>(reinterpret_cast<char*>(ws) + fast_header_bytes(v.batch));
   uint8_t (*ring)[2][kTileB] = sm.kv[warp];
@@ -97,7 +99,7 @@ __global__ void __launch_bounds__(kThreads8)
     unsigned long long nxt = 0;
     if (lane == 0) nxt = atomicAdd(counter, 1ull);
     const int pair = unit / v.Hkv, h = unit - pair * v.Hkv;
-    const FastItem it = decode_fast_item(v, prefA, prefB, C, NA, pair);
+    const FastItem it = decode_fast_item(v, prefA, prefB, C, NA, NS, kTileT, false, pair);
     const int ntiles = (it.t1 - it.t0 + kTileT - 1) / kTileT;
 
     // QK B operand, step s: column block nb holds query heads 4nb .. 4nb+3; column g

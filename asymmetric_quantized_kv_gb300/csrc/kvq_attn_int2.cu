@@ -149,15 +149,17 @@ __global__ void __launch_bounds__(kThreadsI, 3)
   int* prefA = reinterpret_cast<int*>(dyn + sizeof(SmemI2));
   int* prefB = prefA + v.batch + 1;
   int* prefW = prefB + v.batch + 1;
-  __shared__ int s_C, s_NA, s_NB, s_NW;
+  __shared__ int s_C, s_NA, s_NB, s_NS, s_NW;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
   const bool odd = (g & 1) != 0;  // this lane's B columns carry lo halves
   const int G = v.kgroup;  // powers of two (checked on the host)
   const int lgP = __ffs(v.P) - 1, lgG = __ffs(G) - 1;
-  fast_plan<kThreadsI>(v, G, prefA, prefB, &s_C, &s_NA, &s_NB, reinterpret_cast<int*>(&sm.stage[0][0][0]));
+  // a warp takes one kv-head of an item: Hkv units per item, one worker per warp; no cuts
+  fast_plan<kThreadsI>(v, G, v.Hkv, (int)gridDim.x * kWarpsI, false, prefA, prefB, &s_C, &s_NA, &s_NB, &s_NS,
+                       reinterpret_cast<int*>(&sm.stage[0][0][0]));
   window_prefix<kThreadsI>(v, prefW, &s_NW, reinterpret_cast<int*>(&sm.stage[0][0][0]));
-  if (blockIdx.x == 0) store_fast_plan(v, ws, prefA, prefB, s_C, s_NA, s_NB);
+  if (blockIdx.x == 0) store_fast_plan(v, ws, prefA, prefB, s_C, s_NA, s_NB, s_NS);
   grid_dep_launch();  // the combine kernel may be scheduled; it waits for this grid to complete
   unsigned long long* counter =
       reinterpret_cast<unsigned long long*>(reinterpret_cast<char*>(ws) + fast_counter_offset(v.batch));
@@ -167,7 +169,7 @@ __global__ void __launch_bounds__(kThreadsI, 3)
   }
   __syncthreads();
 
-  const int C = s_C, NA = s_NA, NW = s_NW;
+  const int C = s_C, NA = s_NA, NS = s_NS, NW = s_NW;
   // execution order: the residual-window units first (the slowest per token),
   // then every unit of the plan in its long-first order, skipping the windows
   const int n_units = (NW + s_NA + s_NB) * v.Hkv;
@@ -187,13 +189,13 @@ __global__ void __launch_bounds__(kThreadsI, 3)
       const int w = unit / v.Hkv;
       h = unit - w * v.Hkv;
       const int b = seq_of(prefW, v.batch, w);
-      pair = NA + prefB[b] + (n_quantized(seq_tokens(v, b), v.R) % C ? 1 : 0);
+      pair = NA + prefB[b + 1] - 1;  // the window is the sequence's last short item
     } else {
       const int u = unit - NW * v.Hkv;
       pair = u / v.Hkv;
       h = u - pair * v.Hkv;
     }
-    const FastItem it = decode_fast_item(v, prefA, prefB, C, NA, pair);
+    const FastItem it = decode_fast_item(v, prefA, prefB, C, NA, NS, G, false, pair);
     if (it.window && unit >= NW * v.Hkv) {  // done in the first phase
       unit = unit_stride0 + (int)__shfl_sync(0xffffffffu, (unsigned)nxt, 0);
       continue;

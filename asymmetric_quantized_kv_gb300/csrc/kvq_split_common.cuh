@@ -13,27 +13,45 @@ namespace {
 constexpr int kD = 128;
 constexpr int kFastTarget = 1024;
 constexpr int kFastMinChunk = 256;
+constexpr int kTailPieces = 4;   // pieces per chunk of the final round, and per partial chunk at most
+constexpr int kTailMax = 320;    // chunks of the final round that are cut (one round of work at most)
 
 struct FastItem {
   int b, t0, t1, window;
 };
 
 // Work plan of the tensor-core kernels, at the head of the workspace:
-//   int C, NA, NB, pad; int prefA[B+1]; int prefB[B+1]; u64 counter
-// Items d < NA are the full C-token chunks of every sequence (prefA: per-sequence
-// prefix of counts); items d >= NA are the short ones (each sequence's last,
-// partial chunk and its residual window; prefB).  Long items come first, and
-// CTAs take items dynamically from the counter (zeroed by the host before each
-// call), so the last wave holds only short items.
+//   int C, NA, NB, NS; int prefA[B+1]; int prefB[B+1]; u64 counter
+// Workers take items dynamically from the counter (zeroed by the host before each
+// call), in this order:
+//   - whole C-token chunks of every sequence (prefA: per-sequence prefix of chunk
+//     counts), all but the last NS;
+//   - those last NS chunks (about one round of work), each cut into kTailPieces
+//     group-aligned pieces: items up to NA;
+//   - per sequence (prefB: prefix of its short items): its last, partial chunk cut
+//     into pieces of at most piece_tokens(C) tokens, then its residual window.
+// Everything fetched in the final round is then at most a quarter chunk, so the
+// workers, which do not all run at one speed, finish close together.  The cuts
+// are made for kernels whose worker is a whole CTA (two CTAs share an SM and one
+// of them runs markedly slower); kernels whose workers are warps pass cut = false
+// and keep whole chunks and whole partial chunks (NS = 0, one piece per partial).
 __host__ __device__ inline size_t fast_header_ints(int B) { return (size_t)2 * (B + 1) + 4; }
 __host__ __device__ inline size_t fast_counter_offset(int B) { return (fast_header_ints(B) * 4 + 7) & ~(size_t)7; }
 __host__ __device__ inline size_t fast_header_bytes(int B) { return (fast_counter_offset(B) + 8 + 255) / 256 * 256; }
 
+// Tokens of one piece of a partial chunk: a quarter chunk, group-aligned (the
+// whole chunk when the kernel does not cut).
+__host__ __device__ inline int piece_tokens(int C, int align, bool cut) {
+  return cut ? ((C / kTailPieces + align - 1) / align) * align : C;
+}
+__host__ __device__ inline int partial_pieces(int p, int S) { return p ? (p + S - 1) / S : 0; }
+
 // NT threads per block; scratch: 2 * NT ints of shared memory that are free
-// until the caller's main loop
+// until the caller's main loop.  units: work units per item (kv-heads when a
+// worker takes one head of an item, else 1); workers: how many take units at once.
 template <int NT>
-__device__ inline void fast_plan(const KvqView& v, int align, int* sA, int* sB, int* s_C, int* s_NA, int* s_NB,
-                                 int* scratch) {
+__device__ inline void fast_plan(const KvqView& v, int align, int units, int workers, bool cut, int* sA, int* sB,
+                                 int* s_C, int* s_NA, int* s_NB, int* s_NS, int* scratch) {
   __shared__ unsigned long long s_total;
   int* s_pa = scratch;
   int* s_pb = scratch + NT;
@@ -47,13 +65,14 @@ __device__ inline void fast_plan(const KvqView& v, int align, int* sA, int* sB, 
   long long C = (long long)((s_total + kFastTarget - 1) / kFastTarget);
   if (C < kFastMinChunk) C = kFastMinChunk;
   C = (C + align - 1) / align * align;
+  const int S = piece_tokens((int)C, align, cut);
   const int seg = (B + NT - 1) / NT;
   const int b0 = threadIdx.x * seg, b1 = min(B, b0 + seg);
   int la = 0, lb = 0;
   for (int b = b0; b < b1; ++b) {
     const int T = seq_tokens(v, b), nq = n_quantized(T, v.R);
     la += nq / (int)C;
-    lb += (nq % (int)C ? 1 : 0) + (T > nq ? 1 : 0);
+    lb += partial_pieces(nq % (int)C, S) + (T > nq ? 1 : 0);
   }
   s_pa[threadIdx.x] = la;
   s_pb[threadIdx.x] = lb;
@@ -67,9 +86,12 @@ __device__ inline void fast_plan(const KvqView& v, int align, int* sA, int* sB, 
       ra += xa;
       rb += xb;
     }
-    *s_NA = ra;
+    // about one round of work units is cut into pieces
+    int NS = (cut && C / align >= kTailPieces) ? min(min(ra, (workers + units - 1) / units), kTailMax) : 0;
+    *s_NA = ra - NS + NS * kTailPieces;
     *s_NB = rb;
     *s_C = (int)C;
+    *s_NS = NS;
   }
   __syncthreads();
   int ra = s_pa[threadIdx.x], rb = s_pb[threadIdx.x];
@@ -78,22 +100,23 @@ __device__ inline void fast_plan(const KvqView& v, int align, int* sA, int* sB, 
     sA[b] = ra;
     sB[b] = rb;
     ra += nq / (int)C;
-    rb += (nq % (int)C ? 1 : 0) + (T > nq ? 1 : 0);
+    rb += partial_pieces(nq % (int)C, S) + (T > nq ? 1 : 0);
   }
   if (threadIdx.x == 0) {
-    sA[B] = *s_NA;
+    sA[B] = *s_NA - *s_NS * (kTailPieces - 1);  // total full chunks
     sB[B] = *s_NB;
   }
   __syncthreads();
 }
 
 __device__ inline void store_fast_plan(const KvqView& v, float* ws, const int* sA, const int* sB, int C, int NA,
-                                       int NB) {
+                                       int NB, int NS) {
   int* h = reinterpret_cast<int*>(ws);
   if (threadIdx.x == 0) {
     h[0] = C;
     h[1] = NA;
     h[2] = NB;
+    h[3] = NS;
   }
   for (int b = threadIdx.x; b <= v.batch; b += blockDim.x) {
     h[4 + b] = sA[b];
@@ -111,23 +134,36 @@ __device__ inline int seq_of(const int* pref, int B, int x) {
   return lo;
 }
 
+// Item d of the plan (NA: chunk items including the pieces, NS: chunks cut).
 __device__ inline FastItem decode_fast_item(const KvqView& v, const int* sA, const int* sB, int C, int NA,
-                                            int d) {
+                                            int NS, int align, bool cut, int d) {
   FastItem it;
+  const int NU = NA - NS * kTailPieces;  // chunks kept whole
   if (d < NA) {
-    it.b = seq_of(sA, v.batch, d);
+    int c = d, k = -1;
+    if (d >= NU) {  // piece k of chunk c
+      c = NU + (d - NU) / kTailPieces;
+      k = (d - NU) % kTailPieces;
+    }
+    it.b = seq_of(sA, v.batch, c);
     it.window = 0;
-    it.t0 = (d - sA[it.b]) * C;
+    it.t0 = (c - sA[it.b]) * C;
     it.t1 = it.t0 + C;
+    if (k >= 0) {
+      const int groups = C / align, base = it.t0;
+      it.t0 = base + (k * groups / kTailPieces) * align;
+      it.t1 = base + ((k + 1) * groups / kTailPieces) * align;
+    }
     return it;
   }
   const int e = d - NA;
   it.b = seq_of(sB, v.batch, e);
   const int T = seq_tokens(v, it.b), nq = n_quantized(T, v.R);
-  if (e == sB[it.b] && nq % C) {
+  const int S = piece_tokens(C, align, cut), j = e - sB[it.b];
+  if (j < partial_pieces(nq % C, S)) {  // piece j of the partial chunk
     it.window = 0;
-    it.t0 = (nq / C) * C;
-    it.t1 = nq;
+    it.t0 = (nq / C) * C + j * S;
+    it.t1 = min(nq, it.t0 + S);
   } else {
     it.window = 1;
     it.t0 = nq;
@@ -156,15 +192,21 @@ __global__ void __launch_bounds__(kCombineThreads) combine_fast_kernel(KvqView v
   ptx::grid_dep_wait();
   const int hq = blockIdx.x, b = blockIdx.y;
   const int* hdr = reinterpret_cast<const int*>(ws);
-  const int NA = hdr[1];
+  const int NA = hdr[1], NS = hdr[3];
+  const int NU = NA - NS * kTailPieces;
   const int* pA = hdr + 4;
   const int* pB = pA + v.batch + 1;
   const float* part = reinterpret_cast<const float*>(reinterpret_cast<const char*>(ws) + fast_header_bytes(v.batch));
-  // this sequence's items: nA full chunks at pA[b].., then nB short items at NA + pB[b]..
-  const int nA = pA[b + 1] - pA[b], nB = pB[b + 1] - pB[b];
+  // this sequence's records: its whole chunks at item pA[b].., the pieces of its
+  // cut chunks (chunks >= NU), then its nB short items at NA + pB[b]..
+  const int a0 = pA[b], nC = pA[b + 1] - pA[b], nB = pB[b + 1] - pB[b];
+  const int nWhole = max(0, min(nC, NU - a0));
+  const int nA = nWhole + (nC - nWhole) * kTailPieces;
   const int n = nA + nB;
   const long long stride = (long long)v.Hq * kRec;
-  const float* baseA = part + ((long long)pA[b] * v.Hq + hq) * kRec;
+  const long long firstPiece = NU + (long long)(a0 + nWhole - NU) * kTailPieces;  // item of its first piece
+  const float* baseA = part + ((long long)a0 * v.Hq + hq) * kRec;
+  const float* baseP = part + (firstPiece * v.Hq + hq) * kRec;
   const float* baseB = part + ((long long)(NA + pB[b]) * v.Hq + hq) * kRec;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   float m = -INFINITY, l = 0.f;
@@ -179,7 +221,9 @@ __global__ void __launch_bounds__(kCombineThreads) combine_fast_kernel(KvqView v
       rl[j] = 0.f;
       x[j] = make_float4(0.f, 0.f, 0.f, 0.f);
       if (i < n) {
-        const float* r = i < nA ? baseA + (long long)i * stride : baseB + (long long)(i - nA) * stride;
+        const float* r = i < nWhole ? baseA + (long long)i * stride
+                          : i < nA   ? baseP + (long long)(i - nWhole) * stride
+                                     : baseB + (long long)(i - nA) * stride;
         rm[j] = r[0];
         rl[j] = r[1];
         x[j] = reinterpret_cast<const float4*>(r + 4)[lane];
@@ -230,7 +274,9 @@ __global__ void __launch_bounds__(kCombineThreads) combine_fast_kernel(KvqView v
 }
 
 inline size_t split_workspace_bytes(const KvqView& v, int batch) {
-  const long long items = kFastTarget + 2LL * batch;
+  // whole chunks + the pieces of at most kTailMax cut chunks + per sequence up
+  // to kTailPieces + 1 partial-chunk pieces and one window
+  const long long items = kFastTarget + (long long)(kTailPieces - 1) * kTailMax + (kTailPieces + 2LL) * batch;
   return fast_header_bytes(batch) + (size_t)items * v.Hq * (v.D + 4) * sizeof(float);
 }
 
