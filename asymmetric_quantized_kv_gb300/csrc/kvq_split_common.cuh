@@ -11,7 +11,8 @@ namespace kvq {
 namespace {
 
 constexpr int kD = 128;
-constexpr int kFastTarget = 1024;
+constexpr int kFastTarget = 1024;     // chunks per call (about): C = total tokens / target
+constexpr int kFastTargetCut = 768;   // the same for kernels that cut the final round (measured best)
 constexpr int kFastMinChunk = 256;
 constexpr int kTailPieces = 4;   // pieces per chunk of the final round, and per partial chunk at most
 constexpr int kTailMax = 320;    // chunks of the final round that are cut (one round of work at most)
@@ -62,7 +63,8 @@ __device__ inline void fast_plan(const KvqView& v, int align, int units, int wor
   for (int b = threadIdx.x; b < B; b += blockDim.x) sum += (unsigned long long)seq_tokens(v, b);
   atomicAdd(&s_total, sum);
   __syncthreads();
-  long long C = (long long)((s_total + kFastTarget - 1) / kFastTarget);
+  const int target = cut ? kFastTargetCut : kFastTarget;
+  long long C = (long long)((s_total + target - 1) / target);
   if (C < kFastMinChunk) C = kFastMinChunk;
   C = (C + align - 1) / align * align;
   const int S = piece_tokens((int)C, align, cut);
