@@ -13,6 +13,7 @@ namespace {
 constexpr int kD = 128;
 constexpr int kFastTarget = 1024;     // chunks per call (about): C = total tokens / target
 constexpr int kFastTargetCut = 768;   // the same for kernels that cut the final round (measured best)
+constexpr int kMinPiece = 256;        // cut only when a piece keeps at least this many tokens
 constexpr int kFastMinChunk = 256;
 constexpr int kTailPieces = 4;   // pieces per chunk of the final round, and per partial chunk at most
 constexpr int kTailMax = 320;    // chunks of the final round that are cut (one round of work at most)
@@ -40,10 +41,14 @@ __host__ __device__ inline size_t fast_header_ints(int B) { return (size_t)2 * (
 __host__ __device__ inline size_t fast_counter_offset(int B) { return (fast_header_ints(B) * 4 + 7) & ~(size_t)7; }
 __host__ __device__ inline size_t fast_header_bytes(int B) { return (fast_counter_offset(B) + 8 + 255) / 256 * 256; }
 
+// Whether a plan with chunk size C cuts (the kernel asks for cuts and the pieces
+// keep at least kMinPiece tokens; the plan and the item decoder both apply this).
+__host__ __device__ inline bool cuts(int C, bool cut) { return cut && C / kTailPieces >= kMinPiece; }
+
 // Tokens of one piece of a partial chunk: a quarter chunk, group-aligned (the
-// whole chunk when the kernel does not cut).
+// whole chunk when the plan does not cut).
 __host__ __device__ inline int piece_tokens(int C, int align, bool cut) {
-  return cut ? ((C / kTailPieces + align - 1) / align) * align : C;
+  return cuts(C, cut) ? ((C / kTailPieces + align - 1) / align) * align : C;
 }
 __host__ __device__ inline int partial_pieces(int p, int S) { return p ? (p + S - 1) / S : 0; }
 
@@ -63,10 +68,19 @@ __device__ inline void fast_plan(const KvqView& v, int align, int units, int wor
   for (int b = threadIdx.x; b < B; b += blockDim.x) sum += (unsigned long long)seq_tokens(v, b);
   atomicAdd(&s_total, sum);
   __syncthreads();
-  const int target = cut ? kFastTargetCut : kFastTarget;
-  long long C = (long long)((s_total + target - 1) / target);
-  if (C < kFastMinChunk) C = kFastMinChunk;
-  C = (C + align - 1) / align * align;
+  // cutting kernels: chunks for about kFastTargetCut items, cut at the end -- unless
+  // the pieces would fall below kMinPiece tokens (small calls), where the per-item
+  // setup outweighs the balance and the plain plan of kFastTarget chunks is used
+  auto chunk_of = [&](int target) {
+    long long c = (long long)((s_total + target - 1) / target);
+    if (c < kFastMinChunk) c = kFastMinChunk;
+    return (c + align - 1) / align * align;
+  };
+  long long C = chunk_of(cut ? kFastTargetCut : kFastTarget);
+  if (!cuts((int)C, cut)) {
+    cut = false;
+    C = chunk_of(kFastTarget);  // below kMinPiece * kTailPieces as well, so cuts() stays false
+  }
   const int S = piece_tokens((int)C, align, cut);
   const int seg = (B + NT - 1) / NT;
   const int b0 = threadIdx.x * seg, b1 = min(B, b0 + seg);
