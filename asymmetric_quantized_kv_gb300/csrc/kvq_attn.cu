@@ -18,6 +18,7 @@
 #include <math.h>
 
 #include "kvq_attn_plan.cuh"
+#include "kvq_ptx.cuh"
 
 namespace kvq {
 namespace {
@@ -26,39 +27,137 @@ constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
 constexpr float kLog2e = 1.4426950408889634f;
 
-struct TileKeys {
-  const uint8_t* hb;     // head block of the token's page (quantized tokens)
-  const uint8_t* kmeta;  // PER_CHANNEL: group meta; PER_TOKEN: token meta (fp32 or binary16 entries)
-  int slot;
-};
+// Work split: an item (sequence, kv-head, head block, chunk of C tokens) runs on
+// one CTA of 4 warps; each warp takes sub-tiles of kST tokens.  Per sub-tile the
+// warp dequantizes the K rows into shared memory (lanes over 32-bit code words,
+// so each row is one coalesced read), computes the logits with one lane per
+// token, dequantizes the V rows into the same buffer and accumulates P*V with
+// lanes over channels.  Short sub-tiles keep the serial path of a warp short:
+// small calls are latency-bound, and C shrinks to 32 tokens there.
+constexpr int kST = 8;
 
-__device__ __forceinline__ float deq_key(const KvqView& v, const TileKeys& tk, int h, int c) {
-  const unsigned u = get_code(tk.hb + tk.slot * v.krow, c, v.kbits);
-  if (is_fp8(v.kfmt)) return __fmul_rn(fp8_to_float(u, v.kfmt), v.k_scale[h]);
-  if (v.kaxis == KVQ_PER_TENSOR) return dequant_sym(signed_code(u, v.kbits, KVQ_SYM_ABSMAX), v.k_scale[h]);
-  const int code = signed_code(u, v.kbits, v.kmode);
-  float s, mn = 0.f;
-  if (v.kaxis == KVQ_PER_TOKEN) {
-    const int grp = c / v.kgroup;
-    s = load_meta(tk.kmeta, grp, v.meta16);
-    if (v.k_nmeta == 2) mn = load_meta(tk.kmeta, v.k_ng + grp, v.meta16);
-  } else {
-    s = load_meta(tk.kmeta, c, v.meta16);
-    if (v.k_nmeta == 2) mn = load_meta(tk.kmeta, v.D + c, v.meta16);
-  }
-  return v.kmode == KVQ_ASYM_MINMAX ? dequant_asym(code, s, mn) : dequant_sym(code, s);
+// Dequantization rule of one side (K or V) for a call, resolved once.
+struct DeqRule {
+  int kind;        // kFp8, kTensor, kChannel, kToken
+  int bits, fmt;   // code bits; FP8 format
+  bool asym;
+  uint32_t xr;     // code ^ xr - sub = the signed code value (sym INT8: 0x80 / 128)
+  float bias;      // 2^23 + sub
+  int lg, ng;      // PER_TOKEN: log2(group), groups per token
+};
+constexpr int kFp8 = 0, kTensor = 1, kChannel = 2, kToken = 3;
+
+__device__ __forceinline__ DeqRule make_rule(int fmt, int mode, int axis, int group, int bits, int ng) {
+  DeqRule r;
+  r.fmt = fmt;
+  r.bits = bits;
+  r.kind = is_fp8(fmt) ? kFp8 : axis == KVQ_PER_TENSOR ? kTensor : axis == KVQ_PER_CHANNEL ? kChannel : kToken;
+  r.asym = !is_fp8(fmt) && axis != KVQ_PER_TENSOR && mode == KVQ_ASYM_MINMAX;
+  const bool sym = !r.asym;
+  r.xr = (sym && bits == 8) ? 0x80u : 0u;
+  const int sub = !sym ? 0 : bits == 8 ? 128 : (1 << (bits - 1));
+  r.bias = 8388608.f + (float)sub;
+  r.lg = __ffs(group > 0 ? group : 1) - 1;  // group: a power of two (it divides D)
+  r.ng = ng;
+  return r;
 }
 
-__device__ __forceinline__ float deq_value(const KvqView& v, const uint8_t* hb, int slot, int h, int c) {
-  const unsigned u = get_code(hb + v.off_vc + slot * v.vrow, c, v.vbits);
-  if (is_fp8(v.vfmt)) return __fmul_rn(fp8_to_float(u, v.vfmt), v.v_scale[h]);
-  if (v.vaxis == KVQ_PER_TENSOR) return dequant_sym(signed_code(u, v.vbits, KVQ_SYM_ABSMAX), v.v_scale[h]);
-  const uint8_t* meta = hb + v.off_vm + slot * v.v_ng * v.v_nmeta * v.mb;
-  const int grp = c / v.vgroup;
-  const int code = signed_code(u, v.vbits, v.vmode);
-  const float s = load_meta(meta, grp, v.meta16);
-  return v.vmode == KVQ_ASYM_MINMAX ? dequant_asym(code, s, load_meta(meta, v.v_ng + grp, v.meta16))
-                                    : dequant_sym(code, s);
+// Signed code value of the unsigned stored code u, as an exact float.
+__device__ __forceinline__ float code_value(uint32_t u, const DeqRule& r) {
+  return __int_as_float(0x4B000000 | (u ^ r.xr)) - r.bias;
+}
+
+// Entries i..i+3 (i a multiple of 4) of a scale/min array, fp32 or binary16.
+__device__ __forceinline__ float4 load_meta4(const uint8_t* p, int i, int m16) {
+  if (m16) {
+    const uint2 h = *reinterpret_cast<const uint2*>(p + 2 * i);
+    const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&h.x));
+    const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&h.y));
+    return make_float4(a.x, a.y, b.x, b.y);
+  }
+  return *reinterpret_cast<const float4*>(p + 4 * i);
+}
+
+// Dequantize the 32/BITS codes of word w (channels c0..) into dst (fp32).
+// meta: PER_CHANNEL: the key group's entries (D scales, then D minima);
+// PER_TOKEN: the token's entries (ng scales, then ng minima).  ts: per-tensor /
+// FP8 scale.  Every step is the rounding of include/kvq.h: c*s, then + min.
+template <int BITS>
+__device__ __forceinline__ void deq_word(uint32_t w, int c0, const DeqRule& r, const uint8_t* meta, int D, int m16,
+                                         float ts, float* dst) {
+  constexpr int N = 32 / BITS;
+  constexpr uint32_t M = (1u << BITS) - 1u;
+  float x[N];
+  if (r.kind == kFp8) {
+#pragma unroll
+    for (int e = 0; e < N; ++e) x[e] = __fmul_rn(fp8_to_float((w >> (e * BITS)) & M, r.fmt), ts);
+  } else if (r.kind == kTensor) {
+#pragma unroll
+    for (int e = 0; e < N; ++e) x[e] = __fmul_rn(code_value((w >> (e * BITS)) & M, r), ts);
+  } else if (r.kind == kChannel) {
+#pragma unroll
+    for (int e4 = 0; e4 < N; e4 += 4) {
+      const float4 s = load_meta4(meta, c0 + e4, m16);
+      const float4 mn = r.asym ? load_meta4(meta, D + c0 + e4, m16) : make_float4(0.f, 0.f, 0.f, 0.f);
+      const float sv[4] = {s.x, s.y, s.z, s.w}, mv[4] = {mn.x, mn.y, mn.z, mn.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float y = __fmul_rn(code_value((w >> ((e4 + e) * BITS)) & M, r), sv[e]);
+        x[e4 + e] = r.asym ? __fadd_rn(y, mv[e]) : y;
+      }
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < N; ++e) {
+      const int g = (c0 + e) >> r.lg;
+      const float y = __fmul_rn(code_value((w >> (e * BITS)) & M, r), load_meta(meta, g, m16));
+      x[e] = r.asym ? __fadd_rn(y, load_meta(meta, r.ng + g, m16)) : y;
+    }
+  }
+#pragma unroll
+  for (int e = 0; e < N; e += 4) *reinterpret_cast<float4*>(dst + e) = make_float4(x[e], x[e + 1], x[e + 2], x[e + 3]);
+}
+
+// One token's packed row (row_bytes = D*bits/8) -> dst[0..D) fp32, lanes over words.
+template <int BITS>
+__device__ __forceinline__ void deq_row_t(const uint8_t* row, int row_bytes, const DeqRule& r, const uint8_t* meta,
+                                          int D, int m16, float ts, float* dst, int lane) {
+  const int nw = row_bytes >> 2;
+  for (int wi = lane; wi < nw; wi += 32) {
+    const uint32_t w = reinterpret_cast<const uint32_t*>(row)[wi];
+    const int c0 = wi * (32 / BITS);
+    deq_word<BITS>(w, c0, r, meta, D, m16, ts, dst + c0);
+  }
+}
+__device__ __forceinline__ void deq_row(const uint8_t* row, int row_bytes, const DeqRule& r, const uint8_t* meta,
+                                        int D, int m16, float ts, float* dst, int lane) {
+  if (r.bits == 8) deq_row_t<8>(row, row_bytes, r, meta, D, m16, ts, dst, lane);
+  else if (r.bits == 4) deq_row_t<4>(row, row_bytes, r, meta, D, m16, ts, dst, lane);
+  else deq_row_t<2>(row, row_bytes, r, meta, D, m16, ts, dst, lane);
+}
+
+// One window row (source dtype) -> dst[0..D), lanes over channel quads.
+__device__ __forceinline__ void copy_src_row(const void* base, long long row_elem, int D, int bf16, float* dst,
+                                             int lane) {
+  for (int i = lane; i < D / 4; i += 32) {
+    float4 x;
+    if (bf16) {
+      const uint2 h = reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(base) + row_elem)[i];
+      x = make_float4(__uint_as_float(h.x << 16), __uint_as_float(h.x & 0xFFFF0000u), __uint_as_float(h.y << 16),
+                      __uint_as_float(h.y & 0xFFFF0000u));
+    } else {
+      x = reinterpret_cast<const float4*>(static_cast<const float*>(base) + row_elem)[i];
+    }
+    reinterpret_cast<float4*>(dst)[i] = x;
+  }
+}
+
+// Lane src's pointer, to every lane.
+__device__ __forceinline__ const uint8_t* shfl_ptr(const uint8_t* p, int src) {
+  const unsigned long long x = reinterpret_cast<unsigned long long>(p);
+  const unsigned lo = __shfl_sync(0xffffffffu, static_cast<unsigned>(x), src);
+  const unsigned hi = __shfl_sync(0xffffffffu, static_cast<unsigned>(x >> 32), src);
+  return reinterpret_cast<const uint8_t*>((static_cast<unsigned long long>(hi) << 32) | lo);
 }
 
 __device__ __forceinline__ float warp_max(float x) {
@@ -70,37 +169,61 @@ __device__ __forceinline__ float warp_sum(float x) {
   return x;
 }
 
+// Partial record of one (item, query head of the block): running max, sum, two
+// pad words, then D outputs (16-byte aligned).
+__host__ __device__ inline int generic_rec(int D) { return D + 4; }
+
 struct GenericSmem {
-  float qs[kHB][kMaxHeadDim];
-  float ps[kWarps][kHB][32];
+  float qs[kHB][kMaxHeadDim];  // q * scale * log2(e) of the head block
   float wm[kWarps][kHB];
   float wl[kWarps][kHB];
-  float wo[kWarps][kHB][kMaxHeadDim];
   float rope_hi[kMaxHeadDim / 2];
   float rope_lo[kMaxHeadDim / 2];
 };
 
-__global__ void __launch_bounds__(kThreads) split_generic_kernel(KvqView v, const void* q, float scale,
-                                                                  float* ws) {
+// Dynamic shared memory: GenericSmem, pref[B+1], then (16-byte aligned) per warp a
+// sub-tile buffer [kST][D+4] and its probabilities [kHB][kST], then the warps'
+// outputs [kWarps][kHB][D] for the CTA merge.
+__host__ __device__ inline size_t generic_tiles_offset(int batch) {
+  return (sizeof(GenericSmem) + sizeof(int) * (batch + 1) + 15) / 16 * 16;
+}
+__host__ __device__ inline size_t generic_smem_bytes(int batch, int D) {
+  return generic_tiles_offset(batch) +
+         sizeof(float) * ((size_t)kWarps * kST * (D + 4) + (size_t)kWarps * kHB * kST + (size_t)kWarps * kHB * D);
+}
+
+// NH: query heads per item at most (a power of two <= kHB); NJ = D / 32.
+template <int NH, int NJ>
+__global__ void __launch_bounds__(kThreads) split_generic_kernel(KvqView v, const void* q, float scale, float* ws) {
   extern __shared__ __align__(16) unsigned char dyn[];
   GenericSmem& sm = *reinterpret_cast<GenericSmem*>(dyn);
   int* pref = reinterpret_cast<int*>(dyn + sizeof(GenericSmem));
+  constexpr int D = 32 * NJ, DP = D + 4, REC = D + 4;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float* buf = reinterpret_cast<float*>(dyn + generic_tiles_offset(v.batch)) + warp * kST * DP;
+  float* ps = reinterpret_cast<float*>(dyn + generic_tiles_offset(v.batch)) + kWarps * kST * DP + warp * kHB * kST;
+  float* wo = reinterpret_cast<float*>(dyn + generic_tiles_offset(v.batch)) + kWarps * kST * DP + kWarps * kHB * kST;
   const int HB = (v.n_rep + kHB - 1) / kHB;
   __shared__ int s_C, s_items;
   plan_items(v, HB, pref, &s_C, &s_items);
   if (blockIdx.x == 0) store_plan(v, ws, pref, s_C, s_items);
+  ptx::grid_dep_launch();  // the combine's CTAs may be scheduled; they wait for this grid
   const int C = s_C, n_items = s_items;
-  const int D = v.D;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (v.rope_pre) {
     for (int i = threadIdx.x; i < D / 2; i += kThreads) rope_split(v, i, &sm.rope_hi[i], &sm.rope_lo[i]);
   }
+  const DeqRule kr = make_rule(v.kfmt, v.kmode, v.kaxis, v.kgroup, v.kbits, v.k_ng);
+  const DeqRule vr = make_rule(v.vfmt, v.vmode, v.vaxis, v.vgroup, v.vbits, v.v_ng);
+  const int kmeta_tok = v.k_ng * v.k_nmeta * v.mb, vmeta_tok = v.v_ng * v.v_nmeta * v.mb;
+  const int src = v.src_bf16 ? 2 : 4;
   float* part = plan_partials(ws, v.batch);
   for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
     ItemInfo it = decode_item(v, pref, C, HB, item);
     const int nh = min(kHB, v.n_rep - it.hb * kHB);
+    const float kts = (kr.kind == kFp8 || kr.kind == kTensor) ? v.k_scale[it.kvh] : 0.f;
+    const float vts = (vr.kind == kFp8 || vr.kind == kTensor) ? v.v_scale[it.kvh] : 0.f;
     __syncthreads();  // smem of the previous item is free
-    for (int e = threadIdx.x; e < kHB * D; e += kThreads) {
+    for (int e = threadIdx.x; e < NH * D; e += kThreads) {
       const int hh = e / D, c = e % D;
       float x = 0.f;
       if (hh < nh) {
@@ -110,111 +233,151 @@ __global__ void __launch_bounds__(kThreads) split_generic_kernel(KvqView v, cons
       sm.qs[hh][c] = x;
     }
     __syncthreads();
-    float m_run[kHB], l_run[kHB], o[kHB][kMaxHeadDim / 32];
+    float m_run[NH], l_run[NH], o[NH][NJ];
 #pragma unroll
-    for (int hh = 0; hh < kHB; ++hh) {
+    for (int hh = 0; hh < NH; ++hh) {
       m_run[hh] = -INFINITY;
       l_run[hh] = 0.f;
 #pragma unroll
-      for (int j = 0; j < kMaxHeadDim / 32; ++j) o[hh][j] = 0.f;
+      for (int j = 0; j < NJ; ++j) o[hh][j] = 0.f;
     }
-    const int nj = D / 32;
-    for (int tile = it.t0 + warp * 32; tile < it.t1; tile += kWarps * 32) {
-      const int t = tile + lane;
-      bool valid = t < it.t1;
-      TileKeys tk{nullptr, nullptr, 0};
-      long long wrow = 0;
-      if (valid && !it.window) {
-        const uint8_t* page = page_of(v, it.b, t);
-        valid = page != nullptr;
-        if (valid) {
-          tk.hb = page + (long long)it.kvh * v.head_bytes;
-          tk.slot = t % v.P;
-          if (v.kaxis == KVQ_PER_TOKEN) {
-            tk.kmeta = tk.hb + v.off_km + tk.slot * v.k_ng * v.k_nmeta * v.mb;
-          } else if (v.kaxis == KVQ_PER_CHANNEL) {
-            const int g0 = (t / v.kgroup) * v.kgroup;
-            const uint8_t* gp = page_of(v, it.b, g0);
-            valid = gp != nullptr;
-            if (valid)
-              tk.kmeta = gp + (long long)it.kvh * v.head_bytes + v.off_km +
-                         (long long)((g0 % v.P) / v.kgroup) * D * v.k_nmeta * v.mb;
+    const long long wbase = ((long long)it.b * v.R - it.t0) * v.Hkv + it.kvh;  // window row of token t: wbase + t*Hkv
+    for (int tile = it.t0 + warp * kST; tile < it.t1; tile += kWarps * kST) {
+      const int n = min(kST, it.t1 - tile);
+      // lane tt < n: the addresses of token tile + tt's rows (the warp reads them
+      // below, token by token), and the rows requested at once
+      const uint8_t *a_k = nullptr, *a_km = nullptr, *a_v = nullptr, *a_vm = nullptr;
+      bool ok = true;
+      if (lane < n) {
+        const int t = tile + lane;
+        if (it.window) {
+          const long long wrow = (wbase + (long long)t * v.Hkv) * D;
+          ptx::prefetch_l1_range(static_cast<const char*>(v.k_win) + wrow * src, D * src);
+          ptx::prefetch_l1_range(static_cast<const char*>(v.v_win) + wrow * src, D * src);
+        } else {
+          const uint8_t* page = page_of(v, it.b, t);
+          ok = page != nullptr;
+          if (ok) {
+            const uint8_t* hb = page + (long long)it.kvh * v.head_bytes;
+            const int slot = t % v.P;
+            a_k = hb + slot * v.krow;
+            a_v = hb + v.off_vc + slot * v.vrow;
+            a_vm = hb + v.off_vm + slot * vmeta_tok;
+            if (kr.kind == kToken) {
+              a_km = hb + v.off_km + slot * kmeta_tok;
+              ptx::prefetch_l1_range(a_km, kmeta_tok);
+            } else if (kr.kind == kChannel) {  // the key group's entries live in the page of its first token
+              const int g0 = (t / v.kgroup) * v.kgroup;
+              const uint8_t* gp = page_of(v, it.b, g0);
+              ok = gp != nullptr;
+              if (ok)
+                a_km = gp + (long long)it.kvh * v.head_bytes + v.off_km +
+                       (long long)((g0 % v.P) / v.kgroup) * D * v.k_nmeta * v.mb;
+            }
+            ptx::prefetch_l1_range(a_k, v.krow);
+            ptx::prefetch_l1_range(a_v, v.vrow);
+            if (vr.kind == kToken) ptx::prefetch_l1_range(a_vm, vmeta_tok);
           }
         }
-      } else if (valid) {
-        wrow = (((long long)it.b * v.R + (t - it.t0)) * v.Hkv + it.kvh) * D;
       }
-      float acc[kHB];
-#pragma unroll
-      for (int hh = 0; hh < kHB; ++hh) acc[hh] = 0.f;
-      if (valid) {
-        for (int c = 0; c < D; c += 2) {
-          float k0, k1;
-          if (it.window) {
-            k0 = load_src(v.k_win, wrow + c, v.src_bf16);
-            k1 = load_src(v.k_win, wrow + c + 1, v.src_bf16);
-          } else {
-            k0 = deq_key(v, tk, it.kvh, c);
-            k1 = deq_key(v, tk, it.kvh, c + 1);
-          }
-          if (v.rope_pre) {
-            float sn, cs;
-            sincospif(2.f * rope_turns(t, sm.rope_hi[c / 2], sm.rope_lo[c / 2]), &sn, &cs);
-            const float r0 = k0 * cs - k1 * sn;
-            const float r1 = k0 * sn + k1 * cs;
-            k0 = r0;
-            k1 = r1;
-          }
-#pragma unroll
-          for (int hh = 0; hh < kHB; ++hh) acc[hh] += sm.qs[hh][c] * k0 + sm.qs[hh][c + 1] * k1;
+      // tokens whose page (or key group's page) is missing: logits -inf, V rows zero
+      const unsigned bad = __ballot_sync(0xffffffffu, lane < n && !ok);
+      // ---- K rows -> buf
+      for (int tt = 0; tt < n; ++tt) {
+        float* dst = buf + tt * DP;
+        if (it.window) {
+          copy_src_row(v.k_win, (wbase + (long long)(tile + tt) * v.Hkv) * D, D, v.src_bf16, dst, lane);
+        } else if ((bad >> tt) & 1u) {
+          for (int c = lane; c < D; c += 32) dst[c] = 0.f;
+        } else {
+          deq_row(shfl_ptr(a_k, tt), v.krow, kr, shfl_ptr(a_km, tt), D, v.meta16, kts, dst, lane);
         }
-      }
-#pragma unroll
-      for (int hh = 0; hh < kHB; ++hh) {
-        const float lg = valid ? acc[hh] : -INFINITY;
-        const float m_new = fmaxf(m_run[hh], warp_max(lg));
-        const float alpha = m_new == -INFINITY ? 1.f : exp2f(m_run[hh] - m_new);
-        const float p = valid ? exp2f(lg - m_new) : 0.f;
-        l_run[hh] = l_run[hh] * alpha + warp_sum(p);
-        m_run[hh] = m_new;
-#pragma unroll
-        for (int j = 0; j < kMaxHeadDim / 32; ++j) o[hh][j] *= alpha;
-        sm.ps[warp][hh][lane] = p;
       }
       __syncwarp();
-      const int nt = min(32, it.t1 - tile);
-      for (int tt = 0; tt < nt; ++tt) {
-        const int tok = tile + tt;
-        const uint8_t* hb = nullptr;
-        long long vrow = 0;
-        if (!it.window) {
-          const uint8_t* page = page_of(v, it.b, tok);
-          if (!page) continue;
-          hb = page + (long long)it.kvh * v.head_bytes;
-        } else {
-          vrow = (((long long)it.b * v.R + (tok - it.t0)) * v.Hkv + it.kvh) * D;
+      if (v.rope_pre) {  // rotate the pairs in place: lanes over (token, pair)
+        for (int e = lane; e < n * (D / 2); e += 32) {
+          const int tt = e / (D / 2), i = e % (D / 2);
+          float2* pr = reinterpret_cast<float2*>(buf + tt * DP) + i;
+          const float2 k = *pr;
+          float sn, cs;
+          sincospif(2.f * rope_turns(tile + tt, sm.rope_hi[i], sm.rope_lo[i]), &sn, &cs);
+          *pr = make_float2(k.x * cs - k.y * sn, k.x * sn + k.y * cs);
         }
-        for (int j = 0; j < nj; ++j) {
-          const int c = lane + 32 * j;
-          const float vx = it.window ? load_src(v.v_win, vrow + c, v.src_bf16)
-                                     : deq_value(v, hb, tok % v.P, it.kvh, c);
+        __syncwarp();
+      }
+      // ---- logits: lane = token
+      const bool valid = lane < n && !((bad >> lane) & 1u);
+      float acc[NH];
 #pragma unroll
-          for (int hh = 0; hh < kHB; ++hh) o[hh][j] += sm.ps[warp][hh][tt] * vx;
+      for (int hh = 0; hh < NH; ++hh) acc[hh] = 0.f;
+      if (valid) {
+        const float* krow = buf + lane * DP;
+        for (int c = 0; c < D; c += 4) {
+          const float4 k4 = *reinterpret_cast<const float4*>(krow + c);
+#pragma unroll
+          for (int hh = 0; hh < NH; ++hh) {
+            if (hh < nh) {
+              const float4 q4 = *reinterpret_cast<const float4*>(&sm.qs[hh][c]);
+              acc[hh] += q4.x * k4.x + q4.y * k4.y + q4.z * k4.z + q4.w * k4.w;
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int hh = 0; hh < NH; ++hh) {
+        if (hh < nh) {
+          const float lg = valid ? acc[hh] : -INFINITY;
+          const float m_new = fmaxf(m_run[hh], warp_max(lg));
+          const float alpha = m_new == -INFINITY ? 1.f : exp2f(m_run[hh] - m_new);
+          const float p = valid ? exp2f(lg - m_new) : 0.f;
+          l_run[hh] = l_run[hh] * alpha + warp_sum(p);
+          m_run[hh] = m_new;
+#pragma unroll
+          for (int j = 0; j < NJ; ++j) o[hh][j] *= alpha;
+          if (lane < kST) ps[hh * kST + lane] = p;
+        }
+      }
+      __syncwarp();
+      // ---- V rows -> buf (marked tokens: zeros; their p is 0)
+      for (int tt = 0; tt < n; ++tt) {
+        float* dst = buf + tt * DP;
+        if (it.window) {
+          copy_src_row(v.v_win, (wbase + (long long)(tile + tt) * v.Hkv) * D, D, v.src_bf16, dst, lane);
+        } else if ((bad >> tt) & 1u) {
+          for (int c = lane; c < D; c += 32) dst[c] = 0.f;
+        } else {
+          deq_row(shfl_ptr(a_v, tt), v.vrow, vr, shfl_ptr(a_vm, tt), D, v.meta16, vts, dst, lane);
+        }
+      }
+      __syncwarp();
+      // ---- P V: lanes over channels
+      for (int tt = 0; tt < n; ++tt) {
+        float pv[NH];
+#pragma unroll
+        for (int hh = 0; hh < NH; ++hh) pv[hh] = hh < nh ? ps[hh * kST + tt] : 0.f;
+#pragma unroll
+        for (int j = 0; j < NJ; ++j) {
+          const float vx = buf[tt * DP + lane + 32 * j];
+#pragma unroll
+          for (int hh = 0; hh < NH; ++hh) o[hh][j] = fmaf(pv[hh], vx, o[hh][j]);
         }
       }
       __syncwarp();
     }
     // merge the warps of this CTA
 #pragma unroll
-    for (int hh = 0; hh < kHB; ++hh) {
-      if (lane == 0) {
-        sm.wm[warp][hh] = m_run[hh];
-        sm.wl[warp][hh] = l_run[hh];
+    for (int hh = 0; hh < NH; ++hh) {
+      if (hh < nh) {
+        if (lane == 0) {
+          sm.wm[warp][hh] = m_run[hh];
+          sm.wl[warp][hh] = l_run[hh];
+        }
+#pragma unroll
+        for (int j = 0; j < NJ; ++j) wo[(warp * kHB + hh) * D + lane + 32 * j] = o[hh][j];
       }
-      for (int j = 0; j < nj; ++j) sm.wo[warp][hh][lane + 32 * j] = o[hh][j];
     }
     __syncthreads();
-    float* dst = part + (long long)item * kHB * (D + 2);
+    float* dst = part + (long long)item * kHB * REC;
     for (int e = threadIdx.x; e < nh * D; e += kThreads) {
       const int hh = e / D, c = e % D;
       float M = -INFINITY;
@@ -223,50 +386,124 @@ __global__ void __launch_bounds__(kThreads) split_generic_kernel(KvqView v, cons
       for (int w = 0; w < kWarps; ++w) {
         const float f = sm.wm[w][hh] == -INFINITY ? 0.f : exp2f(sm.wm[w][hh] - M);
         L += sm.wl[w][hh] * f;
-        O += sm.wo[w][hh][c] * f;
+        O += wo[(w * kHB + hh) * D + c] * f;
       }
       if (c == 0) {
-        dst[hh * (D + 2) + 0] = M;
-        dst[hh * (D + 2) + 1] = L;
+        dst[hh * REC + 0] = M;
+        dst[hh * REC + 1] = L;
       }
-      dst[hh * (D + 2) + 2 + c] = O;
+      dst[hh * REC + 4 + c] = O;
     }
   }
 }
 
 }  // namespace
 
-__global__ void combine_kernel(KvqView v, float* ws, float* out) {
+// Partials -> out: one CTA of 4 warps per (query head, sequence).  Each warp
+// loads up to 8 of the head's records at once (lanes over channel quads) and
+// merges them online; the warps then merge through shared memory.  Launched as a
+// programmatic dependent of the split kernel: it waits for that grid to complete
+// before reading the workspace.
+__global__ void __launch_bounds__(128) combine_kernel(KvqView v, float* ws, float* out) {
+  constexpr int kCW = 4, kBatch = 8, kQ = kMaxHeadDim / 128;  // channel quads per lane
+  __shared__ float4 o_s[kCW][kMaxHeadDim / 4];
+  __shared__ float m_s[kCW], l_s[kCW];
+  ptx::grid_dep_wait();
   const int hq = blockIdx.x, b = blockIdx.y;
-  const int D = v.D;
+  const int D = v.D, REC = generic_rec(D), nqd = D / 4;
   const int HB = (v.n_rep + kHB - 1) / kHB;
   const int* pref = plan_prefix(ws);
   const float* part = plan_partials(ws, v.batch);
   const int kvh = hq / v.n_rep, hr = hq % v.n_rep, hb = hr / kHB, hh = hr % kHB;
   const int nc = (pref[b + 1] - pref[b]) / (v.Hkv * HB);
-  const long long item0 = pref[b] + (long long)(kvh * HB + hb) * nc;
-  float M = -INFINITY;
-  for (int i = 0; i < nc; ++i) M = fmaxf(M, part[(item0 + i) * kHB * (D + 2) + hh * (D + 2)]);
-  float L = 0.f;
-  for (int i = 0; i < nc; ++i) {
-    const float* p = part + (item0 + i) * kHB * (D + 2) + hh * (D + 2);
-    L += p[0] == -INFINITY ? 0.f : p[1] * exp2f(p[0] - M);
-  }
-  const float invL = L > 0.f ? 1.f / L : 0.f;
-  for (int c = threadIdx.x; c < D; c += blockDim.x) {
-    float O = 0.f;
-    for (int i = 0; i < nc; ++i) {
-      const float* p = part + (item0 + i) * kHB * (D + 2) + hh * (D + 2);
-      if (p[0] != -INFINITY) O += p[2 + c] * exp2f(p[0] - M);
+  const float* base = part + ((long long)pref[b] + (long long)(kvh * HB + hb) * nc) * kHB * REC + hh * REC;
+  const long long stride = (long long)kHB * REC;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  float m = -INFINITY, l = 0.f;
+  float4 o[kQ];
+#pragma unroll
+  for (int k = 0; k < kQ; ++k) o[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int i0 = warp; i0 < nc; i0 += kCW * kBatch) {
+    float rm[kBatch], rl[kBatch];
+    float4 x[kBatch][kQ];
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      const int i = i0 + j * kCW;
+      rm[j] = -INFINITY;
+      rl[j] = 0.f;
+#pragma unroll
+      for (int k = 0; k < kQ; ++k) x[j][k] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (i < nc) {
+        const float* r = base + (long long)i * stride;
+        rm[j] = r[0];
+        rl[j] = r[1];
+#pragma unroll
+        for (int k = 0; k < kQ; ++k)
+          if (lane + 32 * k < nqd) x[j][k] = reinterpret_cast<const float4*>(r + 4)[lane + 32 * k];
+      }
     }
-    out[((long long)b * v.Hq + hq) * D + c] = O * invL;
+    float mn = m;
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) mn = fmaxf(mn, rm[j]);
+    if (mn != -INFINITY) {
+      const float a = exp2f(m - mn);
+      l *= a;
+#pragma unroll
+      for (int k = 0; k < kQ; ++k) {
+        o[k].x *= a; o[k].y *= a; o[k].z *= a; o[k].w *= a;
+      }
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        const float w = rm[j] == -INFINITY ? 0.f : exp2f(rm[j] - mn);
+        l = fmaf(rl[j], w, l);
+#pragma unroll
+        for (int k = 0; k < kQ; ++k) {
+          o[k].x = fmaf(x[j][k].x, w, o[k].x); o[k].y = fmaf(x[j][k].y, w, o[k].y);
+          o[k].z = fmaf(x[j][k].z, w, o[k].z); o[k].w = fmaf(x[j][k].w, w, o[k].w);
+        }
+      }
+      m = mn;
+    }
+  }
+  if (lane == 0) {
+    m_s[warp] = m;
+    l_s[warp] = l;
+  }
+#pragma unroll
+  for (int k = 0; k < kQ; ++k)
+    if (lane + 32 * k < nqd) o_s[warp][lane + 32 * k] = o[k];
+  __syncthreads();
+  if (warp == 0) {
+    float M = m_s[0];
+#pragma unroll
+    for (int w = 1; w < kCW; ++w) M = fmaxf(M, m_s[w]);
+    float L = 0.f;
+#pragma unroll
+    for (int w = 0; w < kCW; ++w) L = fmaf(l_s[w], m_s[w] == -INFINITY ? 0.f : exp2f(m_s[w] - M), L);
+    const float invL = L > 0.f ? 1.f / L : 0.f;
+#pragma unroll
+    for (int k = 0; k < kQ; ++k) {
+      if (lane + 32 * k < nqd) {
+        float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (M != -INFINITY) {
+#pragma unroll
+          for (int w = 0; w < kCW; ++w) {
+            const float a = m_s[w] == -INFINITY ? 0.f : exp2f(m_s[w] - M);
+            const float4 x = o_s[w][lane + 32 * k];
+            r.x = fmaf(x.x, a, r.x); r.y = fmaf(x.y, a, r.y); r.z = fmaf(x.z, a, r.z); r.w = fmaf(x.w, a, r.w);
+          }
+        }
+        r.x *= invL; r.y *= invL; r.z *= invL; r.w *= invL;
+        reinterpret_cast<float4*>(out + ((long long)b * v.Hq + hq) * D)[lane + 32 * k] = r;
+      }
+    }
   }
 }
 
 size_t attention_workspace_bytes(const KvqView& v, int batch) {
   const int HB = (v.n_rep + kHB - 1) / kHB;
   const long long items = kTargetItems + 2LL * batch * v.Hkv * HB;
-  const size_t generic = plan_header_bytes(batch) + (size_t)items * kHB * (v.D + 2) * sizeof(float);
+  const size_t generic = plan_header_bytes(batch) + (size_t)items * kHB * generic_rec(v.D) * sizeof(float);
   KvqView b = v;
   b.batch = batch;
   const size_t split = fast_workspace_bytes(v, batch);  // layout of the tensor-core kernels
@@ -279,19 +516,42 @@ kvq_status launch_attention(const KvqView& v, const void* q, float* out, float s
   if (fast_eligible(v)) return launch_fast(v, q, out, scale, ws, st);
   if (fp8_eligible(v)) return launch_fp8(v, q, out, scale, ws, st);
   if (int2_eligible(v)) return launch_int2(v, q, out, scale, ws, st);
-  const size_t smem = sizeof(GenericSmem) + sizeof(int) * (v.batch + 1);
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(split_generic_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             160 * 1024) != cudaSuccess)
-      return KVQ_ERR_CUDA;
-    attr_set = true;
+  // dynamic shared memory grows with the batch (the plan prefix) and D: raise the
+  // kernel's limit to what this call needs; beyond the device's limit the call
+  // does not fit
+  const int nh = v.n_rep < kHB ? v.n_rep : kHB;
+  const int ih = nh <= 1 ? 0 : nh <= 2 ? 1 : nh <= 4 ? 2 : 3;
+  const int id = v.D == 64 ? 0 : v.D == 128 ? 1 : 2;
+  using Kern = void (*)(KvqView, const void*, float, float*);
+  static const Kern kerns[4][3] = {
+      {split_generic_kernel<1, 2>, split_generic_kernel<1, 4>, split_generic_kernel<1, 8>},
+      {split_generic_kernel<2, 2>, split_generic_kernel<2, 4>, split_generic_kernel<2, 8>},
+      {split_generic_kernel<4, 2>, split_generic_kernel<4, 4>, split_generic_kernel<4, 8>},
+      {split_generic_kernel<8, 2>, split_generic_kernel<8, 4>, split_generic_kernel<8, 8>}};
+  const Kern kern = kerns[ih][id];
+  const size_t smem = generic_smem_bytes(v.batch, v.D);
+  static size_t smem_set[4][3] = {};
+  if (smem > smem_set[ih][id]) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return KVQ_ERR_CAPACITY;
+    }
+    smem_set[ih][id] = smem;
   }
-  if (smem > 160 * 1024) return KVQ_ERR_CAPACITY;
   const int grid = num_sms() * 2;
-  split_generic_kernel<<<grid, kThreads, smem, st>>>(v, q, scale, static_cast<float*>(ws));
-  combine_kernel<<<dim3(v.Hq, v.batch), 128, 0, st>>>(v, static_cast<float*>(ws), out);
-  return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+  kern<<<grid, kThreads, smem, st>>>(v, q, scale, static_cast<float*>(ws));
+  if (cudaGetLastError() != cudaSuccess) return KVQ_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(v.Hq, v.batch);
+  cfg.blockDim = dim3(128);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, combine_kernel, v, static_cast<float*>(ws), out) == cudaSuccess ? KVQ_OK
+                                                                                                 : KVQ_ERR_CUDA;
 }
 
 }  // namespace kvq

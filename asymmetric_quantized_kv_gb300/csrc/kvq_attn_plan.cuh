@@ -16,7 +16,7 @@ namespace kvq {
 constexpr int kHB = 8;              // query heads per work item (head block)
 constexpr int kMaxHeadDim = 256;
 constexpr int kTargetItems = 4096;  // upper bound on quantized chunks per call
-constexpr int kMinChunk = 256;
+constexpr int kMinChunk = 32;      // generic kernel: one 8-token sub-tile for each of its 4 warps
 
 struct ItemInfo {
   int b, kvh, hb, t0, t1, window;
@@ -77,15 +77,26 @@ __device__ inline void plan_items_ex(const KvqView& v, int mult, int align, int 
   for (int b = b0; b < b1; ++b) local += seq_chunks(v, seq_tokens(v, b), (int)C) * mult;
   s_part[threadIdx.x] = local;
   __syncthreads();
-  if (threadIdx.x == 0) {
-    int run = 0;
-    for (int i = 0; i < nt; ++i) {
+  if (threadIdx.x < 32) {  // exclusive scan of s_part[0..nt): lanes over segments, then a shuffle scan
+    const int lane = threadIdx.x, per = (nt + 31) / 32;
+    const int i0 = min(nt, lane * per), i1 = min(nt, i0 + per);
+    int seg = 0;
+    for (int i = i0; i < i1; ++i) seg += s_part[i];
+    int incl = seg;
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    int run = incl - seg;
+    for (int i = i0; i < i1; ++i) {
       const int x = s_part[i];
       s_part[i] = run;
       run += x;
     }
-    *s_items = run;
-    *s_C = (int)C;
+    if (lane == 31) {
+      *s_items = incl;
+      *s_C = (int)C;
+    }
   }
   __syncthreads();
   int run = s_part[threadIdx.x];

@@ -76,6 +76,15 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
 // L2 policy for data read once per call (the packed KV stream): evict first, so
 // the stream does not push small reused data (code, window rows, block tables,
 // partial records) out of L2.
+// Start bringing the 128-byte lines of [p, p + n) into L1 (no data returned, no
+// wait); every address issued lies inside the range.
+__device__ __forceinline__ void prefetch_l1_range(const void* p, int n) {
+  const char* c = static_cast<const char*>(p);
+  for (int o = 0; o < n; o += 128) asm volatile("prefetch.global.L1 [%0];\n" ::"l"(c + o));
+  if (n > 0 && ((reinterpret_cast<uintptr_t>(c) & 127) + (n - 1)) / 128 > (n - 1) / 128)
+    asm volatile("prefetch.global.L1 [%0];\n" ::"l"(c + n - 1));
+}
+
 __device__ __forceinline__ uint64_t l2_evict_first() {
   uint64_t pol;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;\n" : "=l"(pol));

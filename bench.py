@@ -13,13 +13,19 @@ log-uniform in [1024, 65536) tokens (seeded), 32 query / 8 KV heads, head_dim
 INT4 asymmetric per-token values, a 64-token bf16 residual window.
 --config 3 (Llama-3.1-8B-shaped, 2-bit KIVI-style, 32K) and --config 4
 (Llama-3.1-70B-shaped, FP8 E4M3, or E5M2 with --fp8 e5m2, 128K) time the
-decode call alone.  Defaults: 20 warm-up and 200 timed steps; every decode call
+decode call alone.  --config 1 (one fp32 head of 4096 tokens, INT8 keys per
+channel or, with --k-axis tensor, per tensor) and --config 2 (one fp32 kv-head
+of 512 tokens read by 64 query heads, INT4 asymmetric keys per channel or, with
+--k-axis token, per token) are latency-bound: their inputs fit in L2, so L2 is
+flushed (a 256 MiB write) before every decode call, outside its events, and
+the time is the sum of the calls' own event times.  Defaults: 20 warm-up and 200 timed steps; every decode call
 is also bracketed by events, and roofline.us_per_launch (mean) and
 us_per_launch_median come from those.
 
 value = algorithmic bytes per step (packed codes + scale/min metadata + window
 + q + out, plus the append's reads and writes) / device time per step, in
-GB/s; inputs (>1 GB) are larger than L2, so no flush is needed between steps.
+GB/s; the inputs of configs 3-5 (>0.5 GB) are larger than L2, so no flush is
+needed between their steps.
 --impl reference times the CPU oracle (float64 numpy) on a bounded sample of
 the same workload.
 """
@@ -45,10 +51,12 @@ import kvq_inputs as W  # noqa: E402
 METRIC = "quantized-KV decode attention: KV bytes GB/s (% of HBM peak), µs/step"
 INT2, INT4, INT8, FP8, FP8_E5M2 = 2, 4, 8, 9, 10
 FP8_MAX = {FP8: 448.0, FP8_E5M2: 57344.0}  # calibration qmax of each FP8 format
+LATENCY_CONFIGS = (1, 2)  # inputs that fit in L2: flushed before every call
+FLUSH_BYTES = 256 << 20
 FP8_FORMATS = {"e4m3": FP8, "e5m2": FP8_E5M2}
 SYM, ASYM = 0, 1
 TEN, TOK, CH = 0, 1, 2
-BF16 = 1
+F32, BF16 = 0, 1
 
 # kernels this library launches per call (append: fold + window/lengths;
 # attention: split-K + combine)
@@ -60,22 +68,50 @@ LAUNCHES_ATTENTION = 2
 # (profiles/split_rope_i8i4_paged_ragged_b16.md, split_fp8_70b_layer_b2.md,
 # split_int2_8b_layer_b8.md); to be re-captured whenever that kernel changes.
 SPLIT_TRAFFIC = {5: 1790.9e6, 4: 2192.4e6, 3: 556.5e6}
-SPLIT_KERNEL = {5: "split_rope_i8i4_kernel", 4: "split_fp8_kernel", 3: "split_int2_kernel"}
+SPLIT_KERNEL = {5: "split_rope_i8i4_kernel", 4: "split_fp8_kernel", 3: "split_int2_kernel",
+                1: "split_generic_kernel", 2: "split_generic_kernel"}
+K_AXES = {"tensor": 0, "token": 1, "channel": 2}
 
 
-def workload_spec(cid: int, batch: int = 0, fp8: str = "e4m3", meta: str = "f32") -> dict:
-    spec = _workload_spec(cid, batch, fp8)
+def static_qmax(fmt) -> float:
+    """Calibration qmax of a per-tensor format: the FP8 maximum, or 2^(b-1)-1."""
+    return FP8_MAX[fmt] if fmt in FP8_MAX else float((1 << (fmt - 1)) - 1)
+
+
+def workload_spec(cid: int, batch: int = 0, fp8: str = "e4m3", meta: str = "f32", k_axis: str = "channel") -> dict:
+    spec = _workload_spec(cid, batch, fp8, k_axis)
     spec["meta"] = meta  # stored scales / minima: "f32" or "f16" (binary16, scale up / minimum down)
+    spec["flush"] = cid in LATENCY_CONFIGS
     if meta == "f16":
         spec["name"] += ", fp16 scales/minima"
     return spec
 
 
-def _workload_spec(cid: int, batch: int = 0, fp8: str = "e4m3") -> dict:
+def _workload_spec(cid: int, batch: int = 0, fp8: str = "e4m3", k_axis: str = "channel") -> dict:
     w = W.WORKLOADS[cid]
     if batch:  # the first `batch` sequences of the workload (smaller captures for ncu)
         import dataclasses
         w = dataclasses.replace(w, batch=min(batch, w.batch))
+    if cid == 1:
+        if k_axis == "tensor":  # INT8 per-tensor K and V, static scales absmax/127
+            return dict(w=w, k=(INT8, SYM, TEN, 0), v=(INT8, SYM, TEN, 0), R=0, P=256, rope=0, theta=1e4,
+                        append=False, name="single fp32 head, 4096 tokens, Hq1/Hkv1/D128, INT8 per-tensor K and V "
+                                           "(static absmax/127 scales)")
+        if k_axis != "channel":
+            raise SystemExit("--config 1 takes --k-axis channel or tensor")
+        return dict(w=w, k=(INT8, SYM, CH, 4096), v=(INT8, SYM, TOK, 0), R=4096, P=4096, rope=0, theta=1e4,
+                    append=False, name="single fp32 head, 4096 tokens, Hq1/Hkv1/D128, INT8 K per-channel (one "
+                                       "4096-token group) + INT8 V per-token")
+    if cid == 2:
+        if k_axis == "token":
+            return dict(w=w, k=(INT4, ASYM, TOK, 0), v=(INT4, ASYM, TOK, 0), R=0, P=512, rope=0, theta=1e4,
+                        append=False, name="single fp32 kv-head, 512 tokens, 64 query heads, D128, INT4 asym K "
+                                           "per-token + V per-token")
+        if k_axis != "channel":
+            raise SystemExit("--config 2 takes --k-axis channel or token")
+        return dict(w=w, k=(INT4, ASYM, CH, 512), v=(INT4, ASYM, TOK, 0), R=512, P=512, rope=0, theta=1e4,
+                    append=False, name="single fp32 kv-head, 512 tokens, 64 query heads, D128, INT4 asym K "
+                                       "per-channel (one 512-token group) + V per-token")
     if cid == 5:
         return dict(w=w, k=(INT8, SYM, CH, 64), v=(INT4, ASYM, TOK, 128), R=64, P=16, rope=1, theta=500000.0,
                     append=True, name="paged ragged 1K-64K (sum T ~1.0M), Hq32/Hkv8/D128, INT8 per-channel "
@@ -164,17 +200,17 @@ def append_bytes(spec, lens_before) -> int:
 def _oracle_worker(job):
     """Time the oracle's decode (dequantize + RoPE + attention) on one sampled
     (sequence, kv-head) stream; one BLAS thread per worker process."""
-    cid, b, h, T, steps, fp8, meta = job
+    cid, b, h, T, steps, fp8, meta, k_axis = job
     from oracle import kvq_oracle as O
-    spec = workload_spec(cid, 0, fp8, meta)
+    spec = workload_spec(cid, 0, fp8, meta, k_axis)
     w = spec["w"]
     cfg = O.Config(w.num_q_heads, w.num_kv_heads, w.head_dim, O.QSpec(*spec["k"]), O.QSpec(*spec["v"]),
                    spec["R"], spec["P"], spec["rope"], spec["theta"], O.BF16 if w.src_dtype == "bf16" else O.F32,
                    meta_dtype=O.F16 if meta == "f16" else O.F32)
     K = W.kv_block(w, b, h, W.KIND_K, 0, T)
     V = W.kv_block(w, b, h, W.KIND_V, 0, T)
-    ks = O.calibrate_absmax(K, FP8_MAX[spec["k"][0]]) if _is_fp8(spec["k"][0]) else 0.0
-    vs = O.calibrate_absmax(V, FP8_MAX[spec["v"][0]]) if _is_fp8(spec["v"][0]) else 0.0
+    ks = O.calibrate_absmax(K, static_qmax(spec["k"][0])) if spec["k"][2] == TEN else 0.0
+    vs = O.calibrate_absmax(V, static_qmax(spec["v"][0])) if spec["v"][2] == TEN else 0.0
     st = O.quantize_stream(cfg, K, V, ks, vs)
     q = W.queries(w, 0)[b % w.batch, h * cfg.n_rep:(h + 1) * cfg.n_rep].astype(np.float64)
     t0 = time.perf_counter()
@@ -183,19 +219,20 @@ def _oracle_worker(job):
     return time.perf_counter() - t0
 
 
-def cpu_oracle_throughput(cid: int, n_streams: int, steps: int = 1, fp8: str = "e4m3", meta: str = "f32"):
+def cpu_oracle_throughput(cid: int, n_streams: int, steps: int = 1, fp8: str = "e4m3", meta: str = "f32",
+                          k_axis: str = "channel"):
     """Oracle GB/s on a bounded sample of the workload's streams, timed in a
     spawned process pool (one BLAS thread per process)."""
     import multiprocessing as mp
-    spec = workload_spec(cid, 0, fp8, meta)
+    spec = workload_spec(cid, 0, fp8, meta, k_axis)
     w = spec["w"]
     lens = W.lengths(w)
     g = np.random.default_rng(1234)
     picks = [(int(g.integers(0, w.batch)), int(g.integers(0, w.num_kv_heads))) for _ in range(n_streams)]
     if cid == 4:  # 131072-token streams: a prefix keeps the sample bounded
-        jobs = [(cid, b, h, 16384, steps, fp8, meta) for b, h in picks]
+        jobs = [(cid, b, h, 16384, steps, fp8, meta, k_axis) for b, h in picks]
     else:
-        jobs = [(cid, b, h, int(lens[b]), steps, fp8, meta) for b, h in picks]
+        jobs = [(cid, b, h, int(lens[b]), steps, fp8, meta, k_axis) for b, h in picks]
     try:
         cores = len(os.sched_getaffinity(0))
     except AttributeError:
@@ -220,7 +257,7 @@ def cpu_oracle_throughput(cid: int, n_streams: int, steps: int = 1, fp8: str = "
     # bytes of the sampled streams, as one attention call would move them (per kv-head share)
     src = 2 if w.src_dtype == "bf16" else 4
     nbytes = 0
-    for (_, b, h, T, _, _, _) in jobs:  # the stream's KV bytes plus its query heads' q and out
+    for (_, b, h, T, *_rest) in jobs:  # the stream's KV bytes plus its query heads' q and out
         nbytes += (head_bytes(spec, T) + (w.num_q_heads // w.num_kv_heads) * w.head_dim * (src + 4)) * steps
     busy = sum(times)
     return dict(value=nbytes / (busy / procs) / 1e9, unit="GB/s", cores=procs, kind="oracle",
@@ -308,17 +345,19 @@ def load_peaks():
 
 def build_cache(spec, device, extra_tokens, gen_seed=1):
     """Fill a cache with the workload's prefill through kvq_quantize_append.
-    Inputs are drawn on the device with a seeded torch generator (N(0,1), bf16),
-    K outlier channels from kvq_inputs.outliers, static scales (FP8) from
-    kvq_calibrate_absmax."""
+    bf16 workloads are drawn on the device with a seeded torch generator
+    (N(0,1), K outlier channels from kvq_inputs.outliers); the small fp32
+    workloads take the host streams of kvq_inputs.kv_block.  Static per-tensor
+    scales (FP8, per-tensor INT) come from kvq_calibrate_absmax."""
     import torch
     import asymmetric_quantized_kv_gb300 as K
     w = spec["w"]
     Bn, H, D, Hq = w.batch, w.num_kv_heads, w.head_dim, w.num_q_heads
     lens = [int(x) for x in W.lengths(W.WORKLOADS[w.cid])][:w.batch]
     P = spec["P"]
-    cfg = K.make_config(Hq, H, D, spec["k"], spec["v"], spec["R"], P, spec["rope"], spec["theta"], BF16,
-                        2 if spec.get("meta") == "f16" else 0)
+    src_f32 = w.src_dtype == "f32"
+    cfg = K.make_config(Hq, H, D, spec["k"], spec["v"], spec["R"], P, spec["rope"], spec["theta"],
+                        F32 if src_f32 else BF16, 2 if spec.get("meta") == "f16" else 0)
     need = [(T + extra_tokens + P - 1) // P for T in lens]
     maxp = max(need)
     n_pages = sum(need)
@@ -329,6 +368,19 @@ def build_cache(spec, device, extra_tokens, gen_seed=1):
         bt[b, :need[b]] = perm[o:o + need[b]]
         o += need[b]
     cache = K.PagedKVCache(cfg, Bn, maxp, n_pages, bt, device=device)
+    if src_f32:  # small workloads: every stream at once, [B, T, Hkv, D] fp32
+        T = max(lens)
+        kk = torch.from_numpy(np.stack([np.stack([W.kv_block(w, b, h, W.KIND_K, 0, T) for h in range(H)], 1)
+                                        for b in range(Bn)])).to(device)
+        vv = torch.from_numpy(np.stack([np.stack([W.kv_block(w, b, h, W.KIND_V, 0, T) for h in range(H)], 1)
+                                        for b in range(Bn)])).to(device)
+        for kind, src, dst in ((0, kk, cache.k_scale), (1, vv, cache.v_scale)):
+            f = spec["k" if kind == 0 else "v"]
+            if f[2] == TEN:
+                K.kvq_calibrate_absmax(cfg, src.reshape(-1, H, D).contiguous(), Bn * T, static_qmax(f[0]), dst)
+        cache.append(kk, vv, torch.tensor(lens, dtype=torch.int32, device=device))
+        torch.cuda.synchronize(device)
+        return cfg, cache, lens
     scale = W.torch_outlier_scale(w, device)
     g = torch.Generator(device=device)
     g.manual_seed(gen_seed)
@@ -377,9 +429,12 @@ def run_gpu(args, spec, rank, world):
     cfg, cache, lens = build_cache(spec, device, total_steps + 1)
     g = torch.Generator(device=device)
     g.manual_seed(77 + rank)
-    q_all = torch.randn(total_steps, Bn, Hq, D, generator=g, device=device).to(torch.bfloat16)
-    k_all = torch.randn(total_steps, Bn, 1, H, D, generator=g, device=device).to(torch.bfloat16)
-    v_all = torch.randn(total_steps, Bn, 1, H, D, generator=g, device=device).to(torch.bfloat16)
+    sdt = torch.float32 if w.src_dtype == "f32" else torch.bfloat16
+    q_all = torch.randn(total_steps, Bn, Hq, D, generator=g, device=device).to(sdt)
+    k_all = torch.randn(total_steps, Bn, 1, H, D, generator=g, device=device).to(sdt)
+    v_all = torch.randn(total_steps, Bn, 1, H, D, generator=g, device=device).to(sdt)
+    # inputs that fit in L2: a write larger than L2 before every timed call
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device) if spec["flush"] else None
     out = torch.empty(Bn, Hq, D, dtype=torch.float32, device=device)
     stream = torch.cuda.current_stream(device)
     do_append = spec["append"]
@@ -417,6 +472,8 @@ def run_gpu(args, spec, rank, world):
     ev0.record(stream)
     for i in range(steps):
         j = warm + i
+        if flush is not None:
+            flush.fill_(i & 255)
         if do_append:
             K.kvq_quantize_append(cfg, cache.c, k_all[j], v_all[j], 1, None, stream)
         att_ev[i][0].record(stream)
@@ -424,10 +481,11 @@ def run_gpu(args, spec, rank, world):
         att_ev[i][1].record(stream)
     ev1.record(stream)
     torch.cuda.synchronize(device)
-    elapsed_ms = ev0.elapsed_time(ev1)
+    att_ms = [a.elapsed_time(b) for a, b in att_ev]
+    # with flushes in the loop, the step time is the calls' own event times
+    elapsed_ms = ev0.elapsed_time(ev1) if flush is None else sum(att_ms)
     clock_info = clocks.stop()
     elapsed_ms = max_over_ranks(elapsed_ms, world, device)
-    att_ms = [a.elapsed_time(b) for a, b in att_ev]
     status = int(cache.status.item())
     # end to end through the public API: pinned host inputs in, result out, every step
     e2e = None
@@ -462,14 +520,25 @@ def run_gpu(args, spec, rank, world):
         if world > 1:
             dist.barrier()
         torch.cuda.synchronize(device)
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for i in range(steps):
-            e2e_step(warm + i)
-        e1.record(stream)
-        torch.cuda.synchronize(device)
-        e_ms = e0.elapsed_time(e1)
+        if flush is None:
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for i in range(steps):
+                e2e_step(warm + i)
+            e1.record(stream)
+            torch.cuda.synchronize(device)
+            e_ms = e0.elapsed_time(e1)
+        else:
+            pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                     for _ in range(steps)]
+            for i in range(steps):
+                flush.fill_(i & 255)
+                pairs[i][0].record(stream)
+                e2e_step(warm + i)
+                pairs[i][1].record(stream)
+            torch.cuda.synchronize(device)
+            e_ms = sum(a.elapsed_time(b) for a, b in pairs)
         e_ms = max_over_ranks(e_ms, world, device)
         h2d = dq.numel() * dq.element_size() + (2 * dk.numel() * dk.element_size() if do_append else 0)
         e2e = {"value": job_throughput(e2e_bytes, world, e_ms), "unit": "GB/s", "h2d_bytes_per_step": h2d,
@@ -484,7 +553,7 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--config", type=int, default=5, choices=[3, 4, 5])
+    ap.add_argument("--config", type=int, default=5, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", dest="e2e", action="store_false")
     ap.add_argument("--cpu-streams", type=int, default=16)
@@ -492,11 +561,15 @@ def main():
     ap.add_argument("--batch", type=int, default=0, help="use only the first N sequences (profiling)")
     ap.add_argument("--fp8", default="e4m3", choices=sorted(FP8_FORMATS), help="FP8 format of --config 4")
     ap.add_argument("--meta", default="f32", choices=["f32", "f16"], help="stored scales / minima (configs 3, 5)")
+    ap.add_argument("--k-axis", default="channel", choices=sorted(K_AXES),
+                    help="key axis of --config 1 (channel or tensor) and --config 2 (channel or token)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
-    spec = workload_spec(args.config, args.batch, args.fp8, args.meta)
+    if args.k_axis != "channel" and args.config not in LATENCY_CONFIGS:
+        raise SystemExit("--k-axis applies to --config 1 and 2")
+    spec = workload_spec(args.config, args.batch, args.fp8, args.meta, args.k_axis)
     w = spec["w"]
 
     if args.impl == "reference":
@@ -508,7 +581,7 @@ def main():
             pass  # the oracle has no warm state to build
         for _ in range(args.steps):
             detail = cpu_oracle_throughput(args.config, n_streams=max(2, args.cpu_streams // 4), fp8=args.fp8,
-                                           meta=args.meta)
+                                           meta=args.meta, k_axis=args.k_axis)
             per_step.append(detail["value"])
         val = statistics.median(per_step)
         detail["value"] = val
@@ -523,7 +596,7 @@ def main():
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_oracle_throughput(args.config, n_streams=args.cpu_streams, steps=args.cpu_steps, fp8=args.fp8,
-                                    meta=args.meta)
+                                    meta=args.meta, k_axis=args.k_axis)
 
     import torch
     if world > 1:
@@ -549,7 +622,9 @@ def main():
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": spec["name"], "batch": w.batch, "sum_tokens": int(sum(r["lens"])),
                    "parallelism": "replicas" if world > 1 else "single GPU",
-                   "l2": "inputs (%.2f GB per step) larger than the 129 MB L2; no flush" % (att_bytes / 1e9)},
+                   "l2": ("flushed before every decode call (a 256 MiB write outside the call's events); "
+                          "inputs %.2f MB per call" % (att_bytes / 1e6)) if spec["flush"] else
+                         "inputs (%.2f GB per step) larger than the 129 MB L2; no flush" % (att_bytes / 1e9)},
         "pct_of_hbm_peak": 100.0 * value / peak,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": SPLIT_TRAFFIC.get(args.config)

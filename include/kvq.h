@@ -213,7 +213,11 @@ kvq_status kvq_quantize_append(const kvq_config* cfg, const kvq_cache* cache, co
  * (quantized pages and window); a sequence with 0 tokens gets out = 0.
  * Split-K flash decoding: partial (max, sum, output) per token chunk in
  * `workspace` (device, >= kvq_workspace_bytes(cfg, batch, max_pages_per_seq*P)
- * bytes, 256-byte aligned, contents need no initialisation), then a combine. */
+ * bytes, 256-byte aligned, contents need no initialisation), then a combine.
+ * Returns KVQ_ERR_CAPACITY (nothing launched) when the format mix runs on the
+ * generic kernel and its shared memory (the plan's per-sequence prefix grows
+ * with the batch) exceeds the device's per-block limit: above about 46,000
+ * sequences at head_dim 128, 37,000 at 256. */
 kvq_status kvq_decode_attention(const kvq_config* cfg, const kvq_cache* cache, const void* q,
                                 float* out, float softmax_scale, void* workspace,
                                 size_t ws_bytes, void* stream);
