@@ -85,6 +85,12 @@ CASES = {
                     [5, 33, 64, 99]),
     "d256_int8asym": (O.Config(6, 2, 256, Q(O.INT8, A, CH, 16), Q(O.INT2, S, TOK, 64), 48, 16, 0, 1e4, O.BF16),
                       [47, 48, 49, 400]),
+    # the generic kernel's other per-item head counts and encodings: 2 query heads per
+    # kv-head with per-tensor INT4/INT2; 8 with 2-bit asymmetric per-token keys, D 64
+    "int4_tensor_nrep2": (O.Config(4, 2, 128, Q(O.INT4, S, TEN), Q(O.INT2, S, TEN), 0, 32, 0, 1e4, O.BF16),
+                          [1, 31, 32, 33, 250]),
+    "int2_token_nrep8_d64": (O.Config(16, 2, 64, Q(O.INT2, A, TOK, 32), Q(O.INT4, A, TOK, 64), 64, 16, 0, 1e4,
+                                      O.BF16), [0, 7, 64, 65, 190]),
 }
 
 

@@ -1,0 +1,62 @@
+"""Device-side status through every decode kernel: a block-table entry outside
+[0, n_pages) is never dereferenced, sets KVQ_DEV_BAD_PAGE in the caller's status
+word, and leaves the other sequences' attention exact; with the entry restored
+the same cache gives the oracle's attention everywhere again.  (The sequence
+that holds the bad entry has no defined output: which of its tokens drop out
+depends on the kernel.)"""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+from oracle import kvq_oracle as O  # noqa: E402
+
+if not torch.cuda.is_available():  # pragma: no cover
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+from kvq_testlib import ATT_TOL, Case, torch_src  # noqa: E402
+
+Q = O.QSpec
+S, A = O.SYM, O.ASYM
+TEN, TOK, CH = O.PER_TENSOR, O.PER_TOKEN, O.PER_CHANNEL
+BAD_PAGE = 0x1
+
+CASES = {
+    # pre-RoPE INT8 keys + INT4 values (the CTA-level tensor-core kernel)
+    "rope_i8i4": (O.Config(32, 8, 128, Q(O.INT8, S, CH, 64), Q(O.INT4, A, TOK, 128), 64, 16, 1, 5e5, O.BF16),
+                  [700, 2100, 64]),
+    # FP8 (the warp-level tensor-core kernel), 16-token pages
+    "fp8": (O.Config(16, 2, 128, Q(O.FP8_E4M3, S, TEN), Q(O.FP8_E4M3, S, TEN), 0, 16, 0, 1e4, O.F32), [300, 1000, 17]),
+    # 2-bit KIVI (tensor copies of whole page sections)
+    "int2": (O.Config(32, 8, 128, Q(O.INT2, A, CH, 32), Q(O.INT2, A, TOK, 32), 128, 16, 0, 1e4, O.BF16),
+             [1000, 2200, 129]),
+    # the generic kernel
+    "generic": (O.Config(4, 4, 64, Q(O.INT4, S, TOK, 32), Q(O.INT8, A, TOK, 16), 32, 32, 1, 1e4, O.F32),
+                [99, 400, 33]),
+}
+
+
+@pytest.mark.parametrize("name", sorted(CASES))
+def test_bad_block_table_entry(name):
+    cfg, lens = CASES[name]
+    case = Case(cfg, lens, seed=11)
+    q = case.queries(seed=5)
+    b_bad = int(np.argmax(lens))
+    cache = case.cache
+    good = int(cache.block_table[b_bad, 1].item())
+    cache.block_table[b_bad, 1] = cache.n_pages + 7
+    out = cache.attention(torch_src(q, cfg)).cpu().numpy().astype(np.float64)
+    assert int(cache.status.item()) & BAD_PAGE
+    for b in range(len(lens)):
+        if b == b_bad:
+            continue
+        for h in range(cfg.num_kv_heads):
+            heads = slice(h * cfg.n_rep, (h + 1) * cfg.n_rep)
+            ref = O.decode_head(cfg, case.states[b][h], q[b, heads].astype(np.float64), case.k_scale[h],
+                                case.v_scale[h])
+            err = np.linalg.norm(out[b, heads] - ref, axis=1) / np.linalg.norm(ref, axis=1)
+            assert float(err.max()) <= ATT_TOL, (b, h, float(err.max()))
+    cache.block_table[b_bad, 1] = good
+    cache.status.zero_()
+    case.check_attention(q)
