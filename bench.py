@@ -343,6 +343,16 @@ def load_peaks():
     return 6800.0, "fallback"
 
 
+def hold_device(ms: float = 20.0):
+    """Keep the GPU busy for about `ms` before a timed region, so the host queues
+    the region's launches while it waits and no step waits on the host (a host
+    hiccup at the start of the loop would otherwise show up as device time)."""
+    import torch
+    sleep = getattr(torch.cuda, "_sleep", None)
+    if sleep is not None:
+        sleep(int(ms * 1e-3 * 2.0e9))
+
+
 def build_cache(spec, device, extra_tokens, gen_seed=1):
     """Fill a cache with the workload's prefill through kvq_quantize_append.
     bf16 workloads are drawn on the device with a seeded torch generator
@@ -469,6 +479,7 @@ def run_gpu(args, spec, rank, world):
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
     att_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    hold_device()
     ev0.record(stream)
     for i in range(steps):
         j = warm + i
@@ -523,6 +534,7 @@ def run_gpu(args, spec, rank, world):
         if flush is None:
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
+            hold_device()
             e0.record(stream)
             for i in range(steps):
                 e2e_step(warm + i)
