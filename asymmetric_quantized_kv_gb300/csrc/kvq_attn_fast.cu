@@ -33,6 +33,9 @@
 // Residual-window items use the same steps on the source-dtype rows.
 // Partials (max, sum, unnormalised output) per (item, query head) go to the
 // workspace; the combine kernel merges them.
+// Scales and minima stored as binary16 take a second instance (M16): the tile's
+// value (scale, min) rows and a group's key scales arrive in half the bytes and
+// are widened to fp32 where they are read.
 #include <math.h>
 
 #include "kvq_ptx.cuh"
@@ -56,13 +59,19 @@ constexpr int kReseed = 16;  // RoPE table entries are recomputed exactly every 
 constexpr int kNRep = 4;
 
 // Bytes per 16-token tile of one head: K codes, V codes, V meta (scale, min);
-// a tile that starts a key group also carries the group's 128 key scales.
+// a tile that starts a key group also carries the group's 128 key scales.  With
+// binary16 scales and minima (M16) the metadata halves.
 constexpr int kKC = kTile * kD;          // 2048
 constexpr int kVC = kTile * kD / 2;      // 1024
-constexpr int kVM = kTile * 8;           // 128
-constexpr int kStageBytes = kKC + kVC + kVM;
-constexpr int kKMeta = kD * 4;           // per-channel scales of one key group
-constexpr int kStageAlloc = kStageBytes + kKMeta;
+template <bool M16> constexpr int vm_bytes() { return kTile * (M16 ? 4 : 8); }    // 64 / 128
+template <bool M16> constexpr int stage_bytes() { return kKC + kVC + vm_bytes<M16>(); }
+template <bool M16> constexpr int kmeta_bytes() { return kD * (M16 ? 2 : 4); }   // 256 / 512
+constexpr int kStageAlloc = stage_bytes<false>() + kmeta_bytes<false>();
+
+// two binary16 values (low half first) widened to fp32
+__device__ __forceinline__ float2 half2_to_float2(uint32_t w) {
+  return __half22float2(*reinterpret_cast<const __half2*>(&w));
+}
 
 // Shared-memory layouts are chosen so that every 64/128-bit load of a warp
 // meets no bank conflict within the quarter- or half-warp that the hardware
@@ -89,6 +98,9 @@ struct __align__(128) SmemRI {
 };
 static_assert(kStageAlloc % 16 == 0, "bulk-copy destinations must stay 16-byte aligned");
 static_assert(sizeof(SmemRI::stage) >= 2 * kThreads * sizeof(int), "plan scratch lives in the stage ring");
+static_assert(stage_bytes<true>() % 16 == 0 && vm_bytes<true>() % 16 == 0 && kmeta_bytes<true>() % 16 == 0 &&
+                  stage_bytes<true>() + kmeta_bytes<true>() <= kStageAlloc,
+              "binary16 tiles: 16-byte bulk-copy sizes that fit the stage");
 
 __device__ __forceinline__ float2 rope_cs(int p, float w_hi, float w_lo) {
   float s, c;
@@ -214,8 +226,10 @@ __device__ __forceinline__ void softmax_step(Acc& A, float lg0, float lg1, float
   b23 = (g & 1) ? nB : hB;
 }
 
+template <bool M16>
 __global__ void __launch_bounds__(kThreads, 2)
     split_rope_i8i4_kernel(KvqView v, const void* q, float scale, float* ws) {
+  constexpr int kStageBytes = stage_bytes<M16>(), kKMeta = kmeta_bytes<M16>(), kVM = vm_bytes<M16>();
   extern __shared__ __align__(128) unsigned char dyn[];
   SmemRI& sm = *reinterpret_cast<SmemRI*>(dyn);
   int* prefA = reinterpret_cast<int*>(dyn + sizeof(SmemRI));
@@ -348,7 +362,7 @@ __global__ void __launch_bounds__(kThreads, 2)
           const int slot = tok & (v.P - 1);
           bulk_g2s_hint(dst, hbk + slot * kD, kKC, bar, pol);
           bulk_g2s_hint(dst + kKC, hbk + v.off_vc + slot * (kD / 2), kVC, bar, pol);
-          bulk_g2s_hint(dst + kKC + kVC, hbk + v.off_vm + slot * 8, kVM, bar, pol);
+          bulk_g2s_hint(dst + kKC + kVC, hbk + v.off_vm + slot * (kVM / kTile), kVM, bar, pol);
           if (gstart) {
             const int gslot = v.P >= G ? (slot >> lgG) : 0;
             bulk_g2s_hint(dst + kStageBytes, hbk + v.off_km + gslot * kKMeta, kKMeta, bar, pol);
@@ -383,7 +397,14 @@ __global__ void __launch_bounds__(kThreads, 2)
         const uint8_t* buf = sm.stage[warp][stage];
         if (valid && (tok0 & (G - 1)) == 0) {
           // new key group: its scales, quad (c, c+1, c+2, c+3) stored as (c, c+2, c+1, c+3)
-          const float4 raw = reinterpret_cast<const float4*>(buf + kStageBytes)[lane];
+          float4 raw;
+          if constexpr (M16) {
+            const uint2 h = reinterpret_cast<const uint2*>(buf + kStageBytes)[lane];
+            const float2 a = half2_to_float2(h.x), b = half2_to_float2(h.y);
+            raw = make_float4(a.x, a.y, b.x, b.y);
+          } else {
+            raw = reinterpret_cast<const float4*>(buf + kStageBytes)[lane];
+          }
           *reinterpret_cast<float4*>(&sm.kmeta[warp][lane >> 3][4 * (lane & 7)]) =
               make_float4(raw.x, raw.z, raw.y, raw.w);
           __syncwarp();
@@ -431,9 +452,18 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (!valid) lg0 = lg1 = -INFINITY;
 
         // ---- softmax and the PV B operand (P' = p * v_scale, v_min into A.mb)
-        const float2* vm = reinterpret_cast<const float2*>(buf + kKC + kVC);
-        const float2 m0 = valid ? vm[sg] : make_float2(0.f, 0.f);
-        const float2 m1 = valid ? vm[sg + 8] : make_float2(0.f, 0.f);
+        float2 m0 = make_float2(0.f, 0.f), m1 = m0;  // (scale, min) of tokens sg and sg + 8
+        if (valid) {
+          if constexpr (M16) {
+            const uint32_t* vm = reinterpret_cast<const uint32_t*>(buf + kKC + kVC);
+            m0 = half2_to_float2(vm[sg]);
+            m1 = half2_to_float2(vm[sg + 8]);
+          } else {
+            const float2* vm = reinterpret_cast<const float2*>(buf + kKC + kVC);
+            m0 = vm[sg];
+            m1 = vm[sg + 8];
+          }
+        }
         uint32_t b01, b23;
         softmax_step(A, lg0, lg1, m0, m1, g, t, b01, b23);
 
@@ -572,11 +602,12 @@ __global__ void __launch_bounds__(kThreads, 2)
 bool fast_eligible(const KvqView& v) {
   const bool pow2_g = v.kgroup > 0 && (v.kgroup & (v.kgroup - 1)) == 0;
   const bool pow2_p = (v.P & (v.P - 1)) == 0;
-  return !v.meta16 && v.D == kD && v.Hkv == kWarps && v.n_rep == kNRep && v.kfmt == KVQ_INT8 &&
+  const int whole_page = v.meta16 ? stage_bytes<true>() : stage_bytes<false>();
+  return v.D == kD && v.Hkv == kWarps && v.n_rep == kNRep && v.kfmt == KVQ_INT8 &&
          v.kmode == KVQ_SYM_ABSMAX && v.kaxis == KVQ_PER_CHANNEL && v.rope_pre == 1 &&
          v.vfmt == KVQ_INT4 && v.vmode == KVQ_ASYM_MINMAX && v.vaxis == KVQ_PER_TOKEN &&
          v.vgroup == kD && pow2_g && pow2_p && v.kgroup >= kTile * kStages && v.P >= kTile &&
-         (v.P != kTile || v.off_km == kStageBytes) && v.batch <= 4096;
+         (v.P != kTile || v.off_km == whole_page) && v.batch <= 4096;
 }
 
 size_t fast_workspace_bytes(const KvqView& v, int batch) { return split_workspace_bytes(v, batch); }
@@ -584,25 +615,26 @@ size_t fast_workspace_bytes(const KvqView& v, int batch) { return split_workspac
 kvq_status launch_fast(const KvqView& v, const void* q, float* out, float scale, void* ws,
                        cudaStream_t st) {
   const size_t smem = sizeof(SmemRI) + sizeof(int) * 2 * (v.batch + 1);
-  static int occ_cache[64] = {0};
+  static int occ_cache[2][64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64) return KVQ_ERR_UNSUPPORTED;
-  if (!occ_cache[dev]) {
-    if (cudaFuncSetAttribute(split_rope_i8i4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  const int m = v.meta16 ? 1 : 0;
+  auto kern = m ? split_rope_i8i4_kernel<true> : split_rope_i8i4_kernel<false>;
+  if (!occ_cache[m][dev]) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)(sizeof(SmemRI) + sizeof(int) * 2 * 4097)) != cudaSuccess)
       return KVQ_ERR_CUDA;
     int occ = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, split_rope_i8i4_kernel, kThreads, smem) !=
-        cudaSuccess)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kThreads, smem) != cudaSuccess)
       return KVQ_ERR_CUDA;
-    occ_cache[dev] = occ > 0 ? occ : 1;
+    occ_cache[m][dev] = occ > 0 ? occ : 1;
   }
-  const int grid = num_sms() * occ_cache[dev];
+  const int grid = num_sms() * occ_cache[m][dev];
   // the dynamic item counter starts at zero on every call
   if (cudaMemsetAsync(static_cast<char*>(ws) + fast_counter_offset(v.batch), 0, 8, st) != cudaSuccess)
     return KVQ_ERR_CUDA;
-  split_rope_i8i4_kernel<<<grid, kThreads, smem, st>>>(v, q, scale, static_cast<float*>(ws));
+  kern<<<grid, kThreads, smem, st>>>(v, q, scale, static_cast<float*>(ws));
   if (cudaGetLastError() != cudaSuccess) return KVQ_ERR_CUDA;
   return launch_split_combine(v, static_cast<float*>(ws), out, st) == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }

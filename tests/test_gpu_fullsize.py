@@ -25,10 +25,10 @@ def _samples(cid):
 
 
 @pytest.mark.parametrize("cid,fp8,meta", [(3, "e4m3", "f32"), (3, "e4m3", "f16"), (4, "e4m3", "f32"),
-                                          (4, "e5m2", "f32"), (5, "e4m3", "f32")])
+                                          (4, "e5m2", "f32"), (5, "e4m3", "f32"), (5, "e4m3", "f16")])
 def test_fullsize_sampled_streams(cid, fp8, meta):
-    """(config 4 also in FP8 E5M2 with absmax/57344 scales; config 3 also with
-    binary16 scales and minima)"""
+    """(config 4 also in FP8 E5M2 with absmax/57344 scales; configs 3 and 5 also
+    with binary16 scales and minima)"""
     case = FullCase(cid, _samples(cid), fp8=fp8, meta=meta)
     case.check_attention()
     case.check_dequantize()

@@ -76,6 +76,11 @@ CASES = {
                                    O.BF16, meta_dtype=O.F16), [129, 1000, 2200]),
     "m16_rope_i8i4": (O.Config(8, 2, 128, Q(O.INT8, S, CH, 64), Q(O.INT4, A, TOK, 128), 64, 16, 1, 5e5, O.BF16,
                                meta_dtype=O.F16), [1, 63, 64, 65, 700, 2100]),
+    # the pre-RoPE tensor-core kernel's binary16 instance: whole-page and per-section copies
+    "m16_fast_rope_p16": (O.Config(32, 8, 128, Q(O.INT8, S, CH, 64), Q(O.INT4, A, TOK, 128), 64, 16, 1, 5e5,
+                                   O.BF16, meta_dtype=O.F16), [1, 63, 64, 65, 700, 2100, 3000, 777]),
+    "m16_fast_rope_p64": (O.Config(32, 8, 128, Q(O.INT8, S, CH, 64), Q(O.INT4, A, TOK, 128), 64, 64, 1, 5e5,
+                                   O.BF16, meta_dtype=O.F16), [5, 130, 1500]),
     "m16_int4_channel_r512": (O.Config(8, 1, 128, Q(O.INT4, A, CH, 512), Q(O.INT4, A, TOK, 0), 512, 512, 0, 1e4,
                                        O.F32, meta_dtype=O.F16), [512, 1100]),
     "m16_d64_grouped": (O.Config(4, 4, 64, Q(O.INT4, S, TOK, 32), Q(O.INT8, A, TOK, 16), 32, 32, 1, 1e4, O.F32,
