@@ -52,6 +52,7 @@ METRIC = "quantized-KV decode attention: KV bytes GB/s (% of HBM peak), µs/step
 INT2, INT4, INT8, FP8, FP8_E5M2 = 2, 4, 8, 9, 10
 FP8_MAX = {FP8: 448.0, FP8_E5M2: 57344.0}  # calibration qmax of each FP8 format
 LATENCY_CONFIGS = (1, 2)  # inputs that fit in L2: flushed before every call
+REF_MAX_TOKENS = 8192  # the reference arm's streams: prefixes of at most this many tokens
 FLUSH_BYTES = 256 << 20
 FP8_FORMATS = {"e4m3": FP8, "e5m2": FP8_E5M2}
 SYM, ASYM = 0, 1
@@ -197,73 +198,118 @@ def append_bytes(spec, lens_before) -> int:
 
 # ------------------------------------------------------------------ CPU oracle leg
 
+_ORACLE_STATES = {}  # per worker process: quantized streams already built, by job
+
+
+def _oracle_state(cid, b, h, T, fp8, meta, k_axis):
+    """The oracle's quantized stream of one (sequence, kv-head), its queries and
+    static scales (built once per worker process and kept)."""
+    key = (cid, b, h, T, fp8, meta, k_axis)
+    if key not in _ORACLE_STATES:
+        from oracle import kvq_oracle as O
+        spec = workload_spec(cid, 0, fp8, meta, k_axis)
+        w = spec["w"]
+        cfg = O.Config(w.num_q_heads, w.num_kv_heads, w.head_dim, O.QSpec(*spec["k"]), O.QSpec(*spec["v"]),
+                       spec["R"], spec["P"], spec["rope"], spec["theta"],
+                       O.BF16 if w.src_dtype == "bf16" else O.F32, meta_dtype=O.F16 if meta == "f16" else O.F32)
+        K = W.kv_block(w, b, h, W.KIND_K, 0, T)
+        V = W.kv_block(w, b, h, W.KIND_V, 0, T)
+        ks = O.calibrate_absmax(K, static_qmax(spec["k"][0])) if spec["k"][2] == TEN else 0.0
+        vs = O.calibrate_absmax(V, static_qmax(spec["v"][0])) if spec["v"][2] == TEN else 0.0
+        st = O.quantize_stream(cfg, K, V, ks, vs)
+        q = W.queries(w, 0)[b % w.batch, h * cfg.n_rep:(h + 1) * cfg.n_rep].astype(np.float64)
+        _ORACLE_STATES[key] = (O, cfg, st, q, ks, vs)
+    return _ORACLE_STATES[key]
+
+
 def _oracle_worker(job):
     """Time the oracle's decode (dequantize + RoPE + attention) on one sampled
-    (sequence, kv-head) stream; one BLAS thread per worker process."""
+    (sequence, kv-head) stream; one BLAS thread per worker process.  Building
+    the quantized stream is not timed."""
     cid, b, h, T, steps, fp8, meta, k_axis = job
-    from oracle import kvq_oracle as O
-    spec = workload_spec(cid, 0, fp8, meta, k_axis)
-    w = spec["w"]
-    cfg = O.Config(w.num_q_heads, w.num_kv_heads, w.head_dim, O.QSpec(*spec["k"]), O.QSpec(*spec["v"]),
-                   spec["R"], spec["P"], spec["rope"], spec["theta"], O.BF16 if w.src_dtype == "bf16" else O.F32,
-                   meta_dtype=O.F16 if meta == "f16" else O.F32)
-    K = W.kv_block(w, b, h, W.KIND_K, 0, T)
-    V = W.kv_block(w, b, h, W.KIND_V, 0, T)
-    ks = O.calibrate_absmax(K, static_qmax(spec["k"][0])) if spec["k"][2] == TEN else 0.0
-    vs = O.calibrate_absmax(V, static_qmax(spec["v"][0])) if spec["v"][2] == TEN else 0.0
-    st = O.quantize_stream(cfg, K, V, ks, vs)
-    q = W.queries(w, 0)[b % w.batch, h * cfg.n_rep:(h + 1) * cfg.n_rep].astype(np.float64)
+    O, cfg, st, q, ks, vs = _oracle_state(cid, b, h, T, fp8, meta, k_axis)
     t0 = time.perf_counter()
     for _ in range(steps):
         O.decode_head(cfg, st, q, ks, vs)
     return time.perf_counter() - t0
 
 
-def cpu_oracle_throughput(cid: int, n_streams: int, steps: int = 1, fp8: str = "e4m3", meta: str = "f32",
-                          k_axis: str = "channel"):
-    """Oracle GB/s on a bounded sample of the workload's streams, timed in a
-    spawned process pool (one BLAS thread per process)."""
-    import multiprocessing as mp
+def oracle_jobs(cid, n_streams, steps, fp8, meta, k_axis, max_tokens=0):
+    """A seeded sample of the workload's (sequence, kv-head) streams as oracle
+    jobs; streams longer than max_tokens (if set) are cut to that prefix."""
     spec = workload_spec(cid, 0, fp8, meta, k_axis)
     w = spec["w"]
     lens = W.lengths(w)
     g = np.random.default_rng(1234)
     picks = [(int(g.integers(0, w.batch)), int(g.integers(0, w.num_kv_heads))) for _ in range(n_streams)]
-    if cid == 4:  # 131072-token streams: a prefix keeps the sample bounded
-        jobs = [(cid, b, h, 16384, steps, fp8, meta, k_axis) for b, h in picks]
-    else:
-        jobs = [(cid, b, h, int(lens[b]), steps, fp8, meta, k_axis) for b, h in picks]
-    try:
-        cores = len(os.sched_getaffinity(0))
-    except AttributeError:
-        cores = os.cpu_count() or 1
-    procs = max(1, min(cores, len(jobs)))
-    env_keys = ["OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"]
-    old = {k: os.environ.get(k) for k in env_keys}
-    for k in env_keys:
-        os.environ[k] = "1"
-    try:
-        ctx = mp.get_context("spawn")
+    cap = 16384 if cid == 4 else 0  # 131072-token streams: a prefix keeps the sample bounded
+    if max_tokens:
+        cap = min(cap, max_tokens) if cap else max_tokens
+    return [(cid, b, h, min(int(lens[b]), cap) if cap else int(lens[b]), steps, fp8, meta, k_axis)
+            for b, h in picks]
+
+
+def oracle_job_bytes(jobs):
+    """Bytes the sampled streams contribute to decode calls: each stream's KV
+    bytes plus its query heads' q and out, per timed step."""
+    total = 0
+    for (cid, b, h, T, steps, fp8, meta, k_axis) in jobs:
+        spec = workload_spec(cid, 0, fp8, meta, k_axis)
+        w = spec["w"]
+        src = 2 if w.src_dtype == "bf16" else 4
+        total += (head_bytes(spec, T) + (w.num_q_heads // w.num_kv_heads) * w.head_dim * (src + 4)) * steps
+    return total
+
+
+class OraclePool:
+    """A spawned process pool for the oracle leg, one BLAS thread per process."""
+
+    ENV = ["OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"]
+
+    def __init__(self, procs):
+        import multiprocessing as mp
+        try:
+            cores = len(os.sched_getaffinity(0))
+        except AttributeError:
+            cores = os.cpu_count() or 1
+        self.procs = max(1, min(cores, procs))
+        self.old = {k: os.environ.get(k) for k in self.ENV}
+        for k in self.ENV:
+            os.environ[k] = "1"
+        self.pool = mp.get_context("spawn").Pool(self.procs)
+
+    def run(self, jobs):
+        """(per-job decode seconds, wall seconds) of one pass over the jobs."""
         t0 = time.perf_counter()
-        with ctx.Pool(procs) as pool:
-            times = pool.map(_oracle_worker, jobs)
-        wall = time.perf_counter() - t0
-    finally:
-        for k, val in old.items():
+        times = self.pool.map(_oracle_worker, jobs, chunksize=1)
+        return times, time.perf_counter() - t0
+
+    def close(self):
+        self.pool.close()
+        self.pool.join()
+        for k, val in self.old.items():
             if val is None:
                 os.environ.pop(k, None)
             else:
                 os.environ[k] = val
-    # bytes of the sampled streams, as one attention call would move them (per kv-head share)
-    src = 2 if w.src_dtype == "bf16" else 4
-    nbytes = 0
-    for (_, b, h, T, *_rest) in jobs:  # the stream's KV bytes plus its query heads' q and out
-        nbytes += (head_bytes(spec, T) + (w.num_q_heads // w.num_kv_heads) * w.head_dim * (src + 4)) * steps
+
+
+def cpu_oracle_throughput(cid: int, n_streams: int, steps: int = 1, fp8: str = "e4m3", meta: str = "f32",
+                          k_axis: str = "channel"):
+    """Oracle GB/s on a bounded sample of the workload's streams, timed in a
+    spawned process pool (one BLAS thread per process)."""
+    jobs = oracle_jobs(cid, n_streams, steps, fp8, meta, k_axis)
+    pool = OraclePool(len(jobs))
+    try:
+        times, wall = pool.run(jobs)
+    finally:
+        pool.close()
     busy = sum(times)
-    return dict(value=nbytes / (busy / procs) / 1e9, unit="GB/s", cores=procs, kind="oracle",
+    return dict(value=oracle_job_bytes(jobs) / (busy / pool.procs) / 1e9, unit="GB/s", cores=pool.procs,
+                kind="oracle",
                 sample=f"{len(jobs)} (sequence, kv-head) streams of the workload ("
                        f"{sum(j[3] for j in jobs)} tokens), decode = dequantize + RoPE + attention in float64, "
-                       f"{steps} step(s) each, {procs} spawned processes x 1 BLAS thread; "
+                       f"{steps} step(s) each, {pool.procs} spawned processes x 1 BLAS thread; "
                        f"{busy:.1f} s CPU, {wall:.1f} s wall")
 
 
@@ -587,16 +633,30 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return
-        per_step = []
-        detail = None
-        for _ in range(args.warmup):
-            pass  # the oracle has no warm state to build
-        for _ in range(args.steps):
-            detail = cpu_oracle_throughput(args.config, n_streams=max(2, args.cpu_streams // 4), fp8=args.fp8,
-                                           meta=args.meta, k_axis=args.k_axis)
-            per_step.append(detail["value"])
+        # one pool for the whole run; the warm-up passes build each worker's
+        # quantized streams, every timed pass times the decode alone
+        jobs = oracle_jobs(args.config, args.cpu_streams, 1, args.fp8, args.meta, args.k_axis,
+                           max_tokens=REF_MAX_TOKENS)
+        nbytes = oracle_job_bytes(jobs)
+        pool = OraclePool(len(jobs))
+        per_step, busy_all, wall_all = [], 0.0, 0.0
+        try:
+            for _ in range(args.warmup):
+                pool.run(jobs)
+            for _ in range(args.steps):
+                times, wall = pool.run(jobs)
+                busy_all += sum(times)
+                wall_all += wall
+                per_step.append(nbytes / (sum(times) / pool.procs) / 1e9)
+        finally:
+            pool.close()
         val = statistics.median(per_step)
-        detail["value"] = val
+        detail = dict(value=val, unit="GB/s", cores=pool.procs, kind="oracle",
+                      sample=f"{len(jobs)} (sequence, kv-head) streams of the workload (prefixes of at most "
+                             f"{REF_MAX_TOKENS} tokens, {sum(j[3] for j in jobs)} tokens) per step, decode = "
+                             f"dequantize + RoPE + attention in float64, median over {args.steps} steps after "
+                             f"{args.warmup} warm-up passes; {pool.procs} spawned processes x 1 BLAS thread; "
+                             f"{busy_all:.1f} s CPU, {wall_all:.1f} s wall")
         line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "GB/s", "n_gpus": args.gpus,
                 "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "f64", "data": "synthetic",
