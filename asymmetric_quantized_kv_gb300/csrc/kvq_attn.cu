@@ -400,12 +400,12 @@ __global__ void __launch_bounds__(kThreads) split_generic_kernel(KvqView v, cons
 }  // namespace
 
 // Partials -> out: one CTA of 4 warps per (query head, sequence).  Each warp
-// loads up to 8 of the head's records at once (lanes over channel quads) and
+// loads up to 16 of the head's records at once (lanes over channel quads) and
 // merges them online; the warps then merge through shared memory.  Launched as a
 // programmatic dependent of the split kernel: it waits for that grid to complete
 // before reading the workspace.
 __global__ void __launch_bounds__(128) combine_kernel(KvqView v, float* ws, float* out) {
-  constexpr int kCW = 4, kBatch = 8, kQ = kMaxHeadDim / 128;  // channel quads per lane
+  constexpr int kCW = 4, kBatch = 16, kQ = kMaxHeadDim / 128;  // channel quads per lane
   __shared__ float4 o_s[kCW][kMaxHeadDim / 4];
   __shared__ float m_s[kCW], l_s[kCW];
   ptx::grid_dep_wait();
