@@ -132,6 +132,14 @@ __device__ __forceinline__ void split_sel(float x0, float x1, bool lo, uint32_t&
   out = lo ? nl : hi;
 }
 
+// PV k-slot -> tile token: within each group of four slots the tokens are
+// rotated by (slot / 4) % 4, so the four lanes t of a quad, which read slots 2t
+// (or 2t+1, 2t+8, 2t+9) from 32-byte rows, hit four different 128-byte bank
+// offsets; tsig_inv is its inverse.  The p exchange stores each token's p at its
+// slot, so B and the value rows agree.
+__device__ __forceinline__ int tsig(int k) { return (k & ~3) | ((k + (k >> 2)) & 3); }
+__device__ __forceinline__ int tsig_inv(int r) { return (r & ~3) | ((r - (r >> 2)) & 3); }
+
 // four binary16 values (two words) widened to fp32
 __device__ __forceinline__ float4 halves4(uint2 w) {
   const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&w.x));
@@ -153,6 +161,10 @@ __global__ void __launch_bounds__(kThreadsI, 3)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
   const bool odd = (g & 1) != 0;  // this lane's B columns carry lo halves
+  // PV: this lane's k-slots 2t, 2t+1, 2t+8, 2t+9 hold tile tokens T0, T1, T8, T9;
+  // its logits (tokens g, g+8) go to slots X0, X1 + 8
+  const int T0 = tsig(2 * t), T1 = tsig(2 * t + 1), T8 = tsig(2 * t + 8), T9 = tsig(2 * t + 9);
+  const int X0 = tsig_inv(g), X1 = tsig_inv(g + 8) - 8;
   const int G = v.kgroup;  // powers of two (checked on the host)
   const int lgP = __ffs(v.P) - 1, lgG = __ffs(G) - 1;
   // a warp takes one kv-head of an item: Hkv units per item, one worker per warp; no cuts
@@ -252,8 +264,8 @@ __global__ void __launch_bounds__(kThreadsI, 3)
     // p of head g/2 at k-slots 2t, 2t+1 (x01) and 2t+8, 2t+9 (x89)
     auto exchange = [&](float p0, float p1, float2& x01, float2& x89) {
       __syncwarp();
-      pe[t * 8 + g] = p0;
-      pe[32 + t * 8 + g] = p1;
+      pe[t * 8 + X0] = p0;
+      pe[32 + t * 8 + X1] = p1;
       __syncwarp();
       x01 = *reinterpret_cast<const float2*>(pe + (g >> 1) * 8 + 2 * t);
       x89 = *reinterpret_cast<const float2*>(pe + 32 + (g >> 1) * 8 + 2 * t);
@@ -408,14 +420,14 @@ __global__ void __launch_bounds__(kThreadsI, 3)
         }
         float2 x01, x89;
         exchange(p0, p1, x01, x89);
-        const float4 sa = vrow(2 * t, 0);
-        const float4 sb = vrow(2 * t + 1, 0);
-        const float4 sc8 = vrow(2 * t + 8, 0);
-        const float4 sd = vrow(2 * t + 9, 0);
+        const float4 sa = vrow(T0, 0);
+        const float4 sb = vrow(T1, 0);
+        const float4 sc8 = vrow(T8, 0);
+        const float4 sd = vrow(T9, 0);
         const float sA[4] = {sa.x, sa.y, sa.z, sa.w}, sB[4] = {sb.x, sb.y, sb.z, sb.w};
         const float sC[4] = {sc8.x, sc8.y, sc8.z, sc8.w}, sD[4] = {sd.x, sd.y, sd.z, sd.w};
 
-        // ---- PV, value group G: byte 8G + g of tokens 2t, 2t+1 (ya) and 2t+8, 2t+9 (yc)
+        // ---- PV, value group G: byte 8G + g of tokens T0, T1 (ya) and T8, T9 (yc)
         const uint8_t* vc = buf + kOffV;
         const int gb = g & 3;
         const uint32_t sel = gb * 0x0011u + (4 + gb) * 0x1100u;
@@ -426,10 +438,10 @@ __global__ void __launch_bounds__(kThreadsI, 3)
           split_sel(x01.x * sA[G4], x01.y * sB[G4], odd, b01);
           split_sel(x89.x * sC[G4], x89.y * sD[G4], odd, b89);
           const int off = 8 * G4 + woff;
-          const uint32_t wa = *reinterpret_cast<const uint32_t*>(vc + (2 * t) * kRow2 + off);
-          const uint32_t wb = *reinterpret_cast<const uint32_t*>(vc + (2 * t + 1) * kRow2 + off);
-          const uint32_t wc = *reinterpret_cast<const uint32_t*>(vc + (2 * t + 8) * kRow2 + off);
-          const uint32_t wd = *reinterpret_cast<const uint32_t*>(vc + (2 * t + 9) * kRow2 + off);
+          const uint32_t wa = *reinterpret_cast<const uint32_t*>(vc + T0 * kRow2 + off);
+          const uint32_t wb = *reinterpret_cast<const uint32_t*>(vc + T1 * kRow2 + off);
+          const uint32_t wc = *reinterpret_cast<const uint32_t*>(vc + T8 * kRow2 + off);
+          const uint32_t wd = *reinterpret_cast<const uint32_t*>(vc + T9 * kRow2 + off);
           const uint32_t ya = prmt(wa, wb, sel), yc = prmt(wc, wd, sel);
           // m-block 2G4: rows g / g+8 = channels 32G4 + 4g + 0 / + 1 (factors 1, 4)
           mma_16816(O[2 * G4], ya & 0x00030003u, ya & 0x000C000Cu, yc & 0x00030003u, yc & 0x000C000Cu, b01, b89);
@@ -500,7 +512,7 @@ __global__ void __launch_bounds__(kThreadsI, 3)
         split_sel(x01.x, x01.y, odd, b01);
         split_sel(x89.x, x89.y, odd, b89);
         // values as f16, same row -> channel map as the quantized path (32G + 4g + k)
-        const int slots[4] = {2 * t, 2 * t + 1, 2 * t + 8, 2 * t + 9};
+        const int slots[4] = {T0, T1, T8, T9};
 #pragma unroll
         for (int G4 = 0; G4 < 4; ++G4) {
           float vv[4][4];
