@@ -34,3 +34,37 @@ def test_fullsize_sampled_streams(cid, fp8, meta):
     case.check_dequantize()
     del case
     torch.cuda.empty_cache()
+
+
+def test_paged_layer_every_sequence():
+    """Every (sequence, query head) of the paged ragged layer, whose split plan
+    cuts its final round of chunks and its partial chunks into quarter pieces,
+    against attention computed in float64 by torch over the cache's own
+    dequantized keys and values (kvq_dequantize, bit-exact against the oracle on
+    the sampled streams above), the keys rotated by RoPE in float64.  A token
+    the plan dropped or counted twice moves its sequence's output far beyond the
+    tolerance."""
+    case = FullCase(5, [])
+    cfg, w = case.cfg, case.w
+    H, D, n_rep = w.num_kv_heads, w.head_dim, cfg.n_rep
+    out = case.cache.attention(case.q).double()
+    dev = out.device
+    inv = float(cfg.rope_theta) ** (-(2.0 * torch.arange(D // 2, dtype=torch.float64, device=dev)) / D)
+    worst = 0.0
+    for b, T in enumerate(case.lens):
+        k, v = case.cache.dequantize(b, 0, T)
+        k, v = k.double(), v.double()
+        ang = torch.arange(T, dtype=torch.float64, device=dev)[:, None] * inv[None, :]
+        c, s = torch.cos(ang)[:, None, :], torch.sin(ang)[:, None, :]
+        kr = torch.empty_like(k)
+        kr[..., 0::2] = k[..., 0::2] * c - k[..., 1::2] * s
+        kr[..., 1::2] = k[..., 0::2] * s + k[..., 1::2] * c
+        qb = case.q[b].double().view(H, n_rep, D)
+        p = torch.softmax(torch.einsum("hrd,thd->hrt", qb, kr) / D ** 0.5, dim=-1)
+        ref = torch.einsum("hrt,thd->hrd", p, v).reshape(H * n_rep, D)
+        err = (torch.linalg.norm(out[b] - ref, dim=1) / torch.linalg.norm(ref, dim=1)).max().item()
+        worst = max(worst, err)
+    assert worst <= 1e-3, worst
+    assert int(case.cache.status.item()) == 0
+    del case
+    torch.cuda.empty_cache()
