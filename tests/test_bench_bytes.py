@@ -63,3 +63,25 @@ def test_key_axis_is_only_for_the_single_head_workloads():
         bench.workload_spec(1, k_axis="token")
     with pytest.raises(SystemExit):
         bench.workload_spec(2, k_axis="tensor")
+
+
+def test_append_bytes_window_write_and_fold():
+    # paged layer: 8 kv-heads x 128 channels, bf16 sources, 64-token window.
+    # A sequence at 10 tokens reads the new K/V row and writes it to the window; one
+    # at 63 fills the window with it, reads the 63 older rows back and writes 64
+    # tokens' codes (INT8 K, INT4 V, V scale+min per token) and the group's key scales.
+    spec = bench.workload_spec(5)
+    row = 2 * 8 * 128 * 2                        # one token's K and V rows, all heads
+    plain = row + row
+    fold = row + 63 * row + 8 * 64 * (128 + 64 + 8) + 8 * 128 * 4
+    assert bench.append_bytes(spec, [10]) == plain
+    assert bench.append_bytes(spec, [63]) == fold
+    assert bench.append_bytes(spec, [63, 10]) == fold + plain
+
+
+def test_paged_layer_inputs():
+    lens = W.lengths(W.WORKLOADS[5])
+    assert len(lens) == 64 and int(lens.sum()) == 1051067
+    assert lens.min() >= 1024 and lens.max() < 65536
+    perm = W.page_permutation(4099, 5)
+    assert sorted(perm.tolist()) == list(range(4099))
