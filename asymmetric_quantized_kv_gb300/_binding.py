@@ -21,6 +21,7 @@ KVQ_PER_TENSOR, KVQ_PER_TOKEN, KVQ_PER_CHANNEL = 0, 1, 2
 KVQ_F32, KVQ_BF16, KVQ_F16 = 0, 1, 2
 KVQ_DEV_BAD_PAGE, KVQ_DEV_OVERFLOW, KVQ_DEV_TIMEOUT, KVQ_DEV_BAD_LENGTH = 1, 2, 4, 8
 KVQ_NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
+KVQ_KERNEL_GENERIC, KVQ_KERNEL_ROPE_I8I4, KVQ_KERNEL_FP8, KVQ_KERNEL_INT2 = 0, 1, 2, 3
 
 
 class kvq_qspec(ctypes.Structure):
@@ -68,6 +69,7 @@ def _load():
                                                    c_void_p]),
         "kvq_dequantize": (c_int32, [P(kvq_config), P(kvq_cache), c_int32, c_int32, c_int32, c_void_p,
                                      c_void_p, c_void_p]),
+        "kvq_decode_kernel": (c_int32, [P(kvq_config), P(kvq_cache), P(c_int32)]),
         "kvq_status_string": (ctypes.c_char_p, [c_int32]),
     }
     for name, (res, args) in sig.items():
@@ -146,6 +148,13 @@ def kvq_decode_attention_noalloc(cfg, cache: kvq_cache, q, out, softmax_scale, s
     _check("kvq_decode_attention_noalloc",
            LIB.kvq_decode_attention_noalloc(ctypes.byref(cfg), ctypes.byref(cache), _ptr(q), _ptr(out),
                                             float(softmax_scale), _stream(stream)))
+
+
+def kvq_decode_kernel(cfg, cache: kvq_cache) -> int:
+    """The decode kernel (KVQ_KERNEL_*) kvq_decode_attention launches for this cache."""
+    k = c_int32(-1)
+    _check("kvq_decode_kernel", LIB.kvq_decode_kernel(ctypes.byref(cfg), ctypes.byref(cache), ctypes.byref(k)))
+    return k.value
 
 
 def kvq_dequantize(cfg, cache: kvq_cache, seq, tok_begin, tok_end, k_out, v_out, stream=None):

@@ -66,6 +66,10 @@ class PagedKVCache:
         B.kvq_decode_attention(self.cfg, self.c, q, out, softmax_scale, self.workspace, stream)
         return out
 
+    def decode_kernel(self) -> int:
+        """The decode kernel (KVQ_KERNEL_*) attention() launches for this cache."""
+        return B.kvq_decode_kernel(self.cfg, self.c)
+
     def dequantize(self, seq, tok_begin, tok_end, stream=None):
         n = tok_end - tok_begin
         k = torch.empty(n, self.cfg.num_kv_heads, self.cfg.head_dim, dtype=torch.float32, device=self.pages.device)

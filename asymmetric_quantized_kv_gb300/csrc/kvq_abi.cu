@@ -4,6 +4,7 @@
 #include <math.h>
 #include <string.h>
 
+#include "kvq_host.h"
 #include "kvq_internal.cuh"
 
 namespace {
@@ -192,6 +193,7 @@ size_t kvq_workspace_bytes(const kvq_config* c, int32_t batch, int32_t max_seq_l
 
 kvq_status kvq_calibrate_absmax(const kvq_config* c, const void* src, int64_t n_tokens, float qmax,
                                 float* scale_out, void* stream) {
+  const kvq::NvtxRange range("kvq_calibrate_absmax");
   kvq::KvqView v;
   if (!kvq::make_view(c, nullptr, &v)) return kvq_validate(c);
   if (!src || !scale_out || n_tokens < 0 || !(qmax > 0.f) || !isfinite(qmax))
@@ -202,6 +204,7 @@ kvq_status kvq_calibrate_absmax(const kvq_config* c, const void* src, int64_t n_
 kvq_status kvq_quantize_append(const kvq_config* c, const kvq_cache* cache, const void* k_new,
                                const void* v_new, int32_t n_new, const int32_t* n_new_per_seq,
                                void* stream) {
+  const kvq::NvtxRange range("kvq_quantize_append");
   kvq::KvqView v;
   if (!kvq::make_view(c, cache, &v)) return kvq_validate(c);
   kvq_status s = check_cache(c, cache);
@@ -216,6 +219,7 @@ kvq_status kvq_quantize_append(const kvq_config* c, const kvq_cache* cache, cons
 kvq_status kvq_decode_attention(const kvq_config* c, const kvq_cache* cache, const void* q,
                                 float* out, float softmax_scale, void* workspace, size_t ws_bytes,
                                 void* stream) {
+  const kvq::NvtxRange range("kvq_decode_attention");
   kvq::KvqView v;
   if (!kvq::make_view(c, cache, &v)) return kvq_validate(c);
   kvq_status s = check_cache(c, cache);
@@ -230,6 +234,7 @@ kvq_status kvq_decode_attention(const kvq_config* c, const kvq_cache* cache, con
 kvq_status kvq_dequantize(const kvq_config* c, const kvq_cache* cache, int32_t seq,
                           int32_t tok_begin, int32_t tok_end, float* k_out, float* v_out,
                           void* stream) {
+  const kvq::NvtxRange range("kvq_dequantize");
   kvq::KvqView v;
   if (!kvq::make_view(c, cache, &v)) return kvq_validate(c);
   kvq_status s = check_cache(c, cache);
@@ -239,6 +244,16 @@ kvq_status kvq_dequantize(const kvq_config* c, const kvq_cache* cache, int32_t s
   if (tok_end == tok_begin) return KVQ_OK;
   if (!k_out || !v_out) return KVQ_ERR_INVALID_ARG;
   return kvq::launch_dequantize(v, seq, tok_begin, tok_end, k_out, v_out, (cudaStream_t)stream);
+}
+
+kvq_status kvq_decode_kernel(const kvq_config* c, const kvq_cache* cache, int32_t* kernel) {
+  kvq::KvqView v;
+  if (!kernel) return KVQ_ERR_INVALID_ARG;
+  if (!kvq::make_view(c, cache, &v)) return kvq_validate(c);
+  const kvq_status s = check_cache(c, cache);
+  if (s != KVQ_OK) return s;
+  *kernel = kvq::pick_decode_kernel(v);
+  return KVQ_OK;
 }
 
 const char* kvq_status_string(kvq_status s) {

@@ -13,6 +13,7 @@
 // quantizes every window that fills (reading the old window and the new rows);
 // then one CTA per sequence writes the remaining new tokens into the window and
 // advances seq_lens, so window slots are never read and overwritten out of order.
+#include "kvq_host.h"
 #include "kvq_internal.cuh"
 
 namespace kvq {
@@ -816,12 +817,9 @@ kvq_status launch_append(const KvqView& v, const void* k_new, const void* v_new,
   const uintptr_t align_bits = reinterpret_cast<uintptr_t>(k_new) | reinterpret_cast<uintptr_t>(v_new) |
                                reinterpret_cast<uintptr_t>(v.k_win) | reinterpret_cast<uintptr_t>(v.v_win);
   const int stage_ok = stage_bytes > 0 && stage_bytes <= kStageMax && (align_bits & 15) == 0;
-  static bool attr_set = false;
-  if (stage_ok && !attr_set) {
-    if (cudaFuncSetAttribute(append_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kStageMax) !=
-        cudaSuccess)
-      return KVQ_ERR_CUDA;
-    attr_set = true;
+  if (stage_ok) {
+    const kvq_status ss = ensure_dynamic_smem(kSlotAppend, append_kernel, kStageMax);
+    if (ss != KVQ_OK) return ss == KVQ_ERR_CAPACITY ? KVQ_ERR_CUDA : ss;
   }
   append_kernel<<<grid, kThreads, stage_ok ? stage_bytes : 0, st>>>(v, k_new, v_new, n_new, n_new_per_seq,
                                                                     stage_ok);

@@ -510,12 +510,22 @@ size_t attention_workspace_bytes(const KvqView& v, int batch) {
   return (fast_eligible(b) || fp8_shape_eligible(b) || int2_shape_eligible(b)) && split > generic ? split : generic;
 }
 
+int pick_decode_kernel(const KvqView& v) {
+  if (fast_eligible(v)) return KVQ_KERNEL_ROPE_I8I4;
+  if (fp8_eligible(v)) return KVQ_KERNEL_FP8;
+  if (int2_eligible(v)) return KVQ_KERNEL_INT2;
+  return KVQ_KERNEL_GENERIC;
+}
+
 kvq_status launch_attention(const KvqView& v, const void* q, float* out, float scale, void* ws,
                             size_t ws_bytes, cudaStream_t st) {
   (void)ws_bytes;
-  if (fast_eligible(v)) return launch_fast(v, q, out, scale, ws, st);
-  if (fp8_eligible(v)) return launch_fp8(v, q, out, scale, ws, st);
-  if (int2_eligible(v)) return launch_int2(v, q, out, scale, ws, st);
+  switch (pick_decode_kernel(v)) {
+    case KVQ_KERNEL_ROPE_I8I4: return launch_fast(v, q, out, scale, ws, st);
+    case KVQ_KERNEL_FP8: return launch_fp8(v, q, out, scale, ws, st);
+    case KVQ_KERNEL_INT2: return launch_int2(v, q, out, scale, ws, st);
+    default: break;
+  }
   // dynamic shared memory grows with the batch (the plan prefix) and D: raise the
   // kernel's limit to what this call needs; beyond the device's limit the call
   // does not fit
@@ -530,14 +540,8 @@ kvq_status launch_attention(const KvqView& v, const void* q, float* out, float s
       {split_generic_kernel<8, 2>, split_generic_kernel<8, 4>, split_generic_kernel<8, 8>}};
   const Kern kern = kerns[ih][id];
   const size_t smem = generic_smem_bytes(v.batch, v.D);
-  static size_t smem_set[4][3] = {};
-  if (smem > smem_set[ih][id]) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) {
-      (void)cudaGetLastError();
-      return KVQ_ERR_CAPACITY;
-    }
-    smem_set[ih][id] = smem;
-  }
+  const kvq_status ss = ensure_dynamic_smem(kSlotGeneric + 3 * ih + id, kern, smem);
+  if (ss != KVQ_OK) return ss;
   const int grid = num_sms() * 2;
   kern<<<grid, kThreads, smem, st>>>(v, q, scale, static_cast<float*>(ws));
   if (cudaGetLastError() != cudaSuccess) return KVQ_ERR_CUDA;

@@ -615,22 +615,13 @@ size_t fast_workspace_bytes(const KvqView& v, int batch) { return split_workspac
 kvq_status launch_fast(const KvqView& v, const void* q, float* out, float scale, void* ws,
                        cudaStream_t st) {
   const size_t smem = sizeof(SmemRI) + sizeof(int) * 2 * (v.batch + 1);
-  static int occ_cache[2][64] = {};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64) return KVQ_ERR_UNSUPPORTED;
   const int m = v.meta16 ? 1 : 0;
   auto kern = m ? split_rope_i8i4_kernel<true> : split_rope_i8i4_kernel<false>;
-  if (!occ_cache[m][dev]) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)(sizeof(SmemRI) + sizeof(int) * 2 * 4097)) != cudaSuccess)
-      return KVQ_ERR_CUDA;
-    int occ = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kThreads, smem) != cudaSuccess)
-      return KVQ_ERR_CUDA;
-    occ_cache[m][dev] = occ > 0 ? occ : 1;
-  }
-  const int grid = num_sms() * occ_cache[m][dev];
+  int occ = 0;
+  const kvq_status so =
+      occupancy_once(kSlotFast + m, kern, kThreads, smem, sizeof(SmemRI) + sizeof(int) * 2 * 4097, &occ);
+  if (so != KVQ_OK) return so;
+  const int grid = num_sms() * occ;
   // the dynamic item counter starts at zero on every call
   if (cudaMemsetAsync(static_cast<char*>(ws) + fast_counter_offset(v.batch), 0, 8, st) != cudaSuccess)
     return KVQ_ERR_CUDA;

@@ -362,21 +362,11 @@ kvq_status launch_fp8(const KvqView& v, const void* q, float* out, float scale, 
   const bool e5m2 = v.kfmt == KVQ_FP8_E5M2;
   void (*kern)(KvqView, const void*, float, float*, const CUtensorMap) =
       e5m2 ? split_fp8_kernel<true> : split_fp8_kernel<false>;
-  static int occ_cache[2][64] = {{0}};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64) return KVQ_ERR_UNSUPPORTED;
-  int& occ_dev = occ_cache[e5m2 ? 1 : 0][dev];
-  if (!occ_dev) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)(sizeof(SmemF8) + 1024 + sizeof(int) * 2 * 4097)) != cudaSuccess)
-      return KVQ_ERR_CUDA;
-    int occ = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kThreads8, smem) != cudaSuccess)
-      return KVQ_ERR_CUDA;
-    occ_dev = occ > 0 ? occ : 1;
-  }
-  const int grid = num_sms() * occ_dev;
+  int occ = 0;
+  const kvq_status so = occupancy_once(kSlotFp8 + (e5m2 ? 1 : 0), kern, kThreads8, smem,
+                                       sizeof(SmemF8) + 1024 + sizeof(int) * 2 * 4097, &occ);
+  if (so != KVQ_OK) return so;
+  const int grid = num_sms() * occ;
   if (cudaMemsetAsync(static_cast<char*>(ws) + fast_counter_offset(v.batch), 0, 8, st) != cudaSuccess)
     return KVQ_ERR_CUDA;
   kern<<<grid, kThreads8, smem, st>>>(v, q, scale, static_cast<float*>(ws), tmap);

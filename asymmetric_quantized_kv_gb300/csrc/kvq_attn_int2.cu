@@ -1,9 +1,12 @@
 // Tensor-core split-K decode attention for 2-bit asymmetric keys quantized
 // per channel over token groups and 2-bit asymmetric values quantized per token
 // in 32-channel groups, head_dim 128, 4 query heads per kv-head, plus the bf16
-// residual window: the KIVI-style layer ("KIVI: A Tuning-Free Asymmetric 2bit
-// Quantization for KV Cache", section 3: keys per-channel, values per-token,
-// recent tokens kept in full precision).
+// residual window: the KIVI-style layer ("Why Keys Are More Sensitive Than Values
+// in INT8 KV Cache Quantization", section "Computational Paths for Key and
+// Value", and "KV Cache Quantization: Why It's Different from Weight
+// Quantization", section "Why Key and Value Tensors Have Different
+// Distributions": 2-bit keys per channel, values per token, recent tokens kept in
+// full precision).
 //
 // Work: a unit is (sequence, chunk of C tokens, kv-head); every warp takes units
 // from a global counter and streams its 16-token tiles through a private 3-stage
@@ -17,11 +20,18 @@
 //     (mask (3 << 2j) per f16 half: code * 4^j * 2^-24, exact); B = q * s / 4^j
 //     split hi/lo, rebuilt once per key group; the second sum is a per-group,
 //     per-head bias.
-// PV: with v = c * s_t + m_t per (token, 32-channel group), p.v = sum_t (p_t s_t) c
-//     + sum_t p_t m_t.  Lane row g holds byte 8G + g of every token (channels
-//     32G + 4g .. 32G + 4g + 3), so each 16-row MMA block stays inside one value
-//     group G and B = p * s_t(G) split hi/lo; the minima enter through running
-//     sums of p * m_t(G).
+// PV: with v = c * s_t + m_t per (token, 32-channel group), written as
+//     v = (c - 3/2) s_t + (m_t + 3/2 s_t), p.v = sum_t (p_t s_t)(c - 3/2)
+//     + sum_t p_t (m_t + 3/2 s_t).  Lane row g holds byte 8G + g of every token
+//     (channels 32G + 4g .. 32G + 4g + 3), so each 16-row MMA block stays inside
+//     one value group G and B = p * s_t(G) split hi/lo; A = the centred codes
+//     c - 3/2 in f16 (exact), and the group midpoints enter through running sums
+//     of p * (m_t + 3/2 s_t).  Centring matters: the value groups of N(0,1) data
+//     have m ~ -2 and c s in [0, 4], so the uncentred sums sum_t p s c and
+//     sum_t p m are each ~2 sum_t p while a head that spreads its attention has an
+//     output ~50x smaller; every relative error of the tensor-core sum (its
+//     truncating fp32 accumulation, the hi/lo split of B) was magnified by that
+//     ratio.  Centred, both sums are of the order of the output.
 // Scales and minima stored as binary16 (meta_dtype F16) take a second instance:
 // the codes come with one 2-section tensor copy, the value rows and a group's key
 // scales and minima (256 and 512 bytes) with plain bulk copies, and the readers
@@ -140,6 +150,25 @@ __device__ __forceinline__ void split_sel(float x0, float x1, bool lo, uint32_t&
 __device__ __forceinline__ int tsig(int k) { return (k & ~3) | ((k + (k >> 2)) & 3); }
 __device__ __forceinline__ int tsig_inv(int r) { return (r & ~3) | ((r - (r >> 2)) & 3); }
 
+// The 2-bit code fields k (bits 2k, 2k+1 of each 16-bit half) of a packed word,
+// centred: f16x2 (c - 3/2), exact.  OR-ing a field into the mantissa of 1024
+// gives the half 1024 + c * 4^k (the mantissa step at 1024 is 1); for k > 0 one
+// fused multiply-add by 4^-k and -(1024 / 4^k + 3/2) leaves c - 3/2; for k = 0,
+// where 1025.5 is not a half, 1024 and then 3/2 are subtracted in turn.
+template <int K>
+__device__ __forceinline__ uint32_t centred_code(uint32_t w) {
+  const uint32_t x = and_or(w, 0x00030003u << (2 * K), 0x64006400u);
+  if constexpr (K == 0) {
+    return hsub2(hsub2(x, 0x64006400u), 0x3E003E00u);  // - 1024, - 1.5
+  } else if constexpr (K == 1) {
+    return hfma2(x, 0x34003400u, 0xDC06DC06u);  // * 1/4, - 257.5
+  } else if constexpr (K == 2) {
+    return hfma2(x, 0x2C002C00u, 0xD418D418u);  // * 1/16, - 65.5
+  } else {
+    return hfma2(x, 0x24002400u, 0xCC60CC60u);  // * 1/64, - 17.5
+  }
+}
+
 // four binary16 values (two words) widened to fp32
 __device__ __forceinline__ float4 halves4(uint2 w) {
   const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&w.x));
@@ -236,7 +265,7 @@ __global__ void __launch_bounds__(kThreadsI, 3)
 #pragma unroll
     for (int m = 0; m < 8; ++m) O[m][0] = O[m][1] = O[m][2] = O[m][3] = 0.f;
     float m_run = kMinitI, l_loc = 0.f;
-    float mb[4] = {0.f, 0.f, 0.f, 0.f};  // sum of p * v_min per value group (head t)
+    float mb[4] = {0.f, 0.f, 0.f, 0.f};  // sum of p * (v_min + 3/2 v_scale) per value group (head t)
     float* pe = &sm.pex[warp][0][0];
 
     // softmax step for logits of tokens g, g+8 (head t); returns p
@@ -411,12 +440,13 @@ __global__ void __launch_bounds__(kThreadsI, 3)
           }
         };
         if (valid) {
-          const float4 n0 = vrow(g, 1);
-          const float4 n1 = vrow(g + 8, 1);
-          mb[0] = fmaf(p0, n0.x, fmaf(p1, n1.x, mb[0]));
-          mb[1] = fmaf(p0, n0.y, fmaf(p1, n1.y, mb[1]));
-          mb[2] = fmaf(p0, n0.z, fmaf(p1, n1.z, mb[2]));
-          mb[3] = fmaf(p0, n0.w, fmaf(p1, n1.w, mb[3]));
+          // group midpoints m + 3/2 s of tokens g, g+8
+          const float4 n0 = vrow(g, 1), z0 = vrow(g, 0);
+          const float4 n1 = vrow(g + 8, 1), z1 = vrow(g + 8, 0);
+          mb[0] = fmaf(p0, fmaf(1.5f, z0.x, n0.x), fmaf(p1, fmaf(1.5f, z1.x, n1.x), mb[0]));
+          mb[1] = fmaf(p0, fmaf(1.5f, z0.y, n0.y), fmaf(p1, fmaf(1.5f, z1.y, n1.y), mb[1]));
+          mb[2] = fmaf(p0, fmaf(1.5f, z0.z, n0.z), fmaf(p1, fmaf(1.5f, z1.z, n1.z), mb[2]));
+          mb[3] = fmaf(p0, fmaf(1.5f, z0.w, n0.w), fmaf(p1, fmaf(1.5f, z1.w, n1.w), mb[3]));
         }
         float2 x01, x89;
         exchange(p0, p1, x01, x89);
@@ -443,11 +473,12 @@ __global__ void __launch_bounds__(kThreadsI, 3)
           const uint32_t wc = *reinterpret_cast<const uint32_t*>(vc + T8 * kRow2 + off);
           const uint32_t wd = *reinterpret_cast<const uint32_t*>(vc + T9 * kRow2 + off);
           const uint32_t ya = prmt(wa, wb, sel), yc = prmt(wc, wd, sel);
-          // m-block 2G4: rows g / g+8 = channels 32G4 + 4g + 0 / + 1 (factors 1, 4)
-          mma_16816(O[2 * G4], ya & 0x00030003u, ya & 0x000C000Cu, yc & 0x00030003u, yc & 0x000C000Cu, b01, b89);
-          // m-block 2G4+1: channels 32G4 + 4g + 2 / + 3 (factors 16, 64)
-          mma_16816(O[2 * G4 + 1], ya & 0x00300030u, ya & 0x00C000C0u, yc & 0x00300030u, yc & 0x00C000C0u, b01,
-                    b89);
+          // m-block 2G4: rows g / g+8 = channels 32G4 + 4g + 0 / + 1 (code fields 0, 1)
+          mma_16816(O[2 * G4], centred_code<0>(ya), centred_code<1>(ya), centred_code<0>(yc), centred_code<1>(yc),
+                    b01, b89);
+          // m-block 2G4+1: channels 32G4 + 4g + 2 / + 3 (code fields 2, 3)
+          mma_16816(O[2 * G4 + 1], centred_code<2>(ya), centred_code<3>(ya), centred_code<2>(yc),
+                    centred_code<3>(yc), b01, b89);
         }
 
         // ---- release the stage and refill it
@@ -545,15 +576,13 @@ __global__ void __launch_bounds__(kThreadsI, 3)
       rec[0] = m_run;
       rec[1] = l_loc;
     }
-    // quantized codes entered as code * 4^k * 2^-24 (k = channel % 4)
-    const float f0 = it.window ? 1.f : kTwo24, f1 = it.window ? 1.f : kTwo24 / 4.f;
-    const float f2 = it.window ? 1.f : kTwo24 / 16.f, f3 = it.window ? 1.f : kTwo24 / 64.f;
+    // quantized codes entered centred (c - 3/2), window values as they are; the
+    // midpoint sums are zero for window units
 #pragma unroll
     for (int G4 = 0; G4 < 4; ++G4) {
-      const float4 o4 = make_float4(fmaf(O[2 * G4][0] - O[2 * G4][1], f0, mb[G4]),
-                                    fmaf(O[2 * G4][2] - O[2 * G4][3], f1, mb[G4]),
-                                    fmaf(O[2 * G4 + 1][0] - O[2 * G4 + 1][1], f2, mb[G4]),
-                                    fmaf(O[2 * G4 + 1][2] - O[2 * G4 + 1][3], f3, mb[G4]));
+      const float4 o4 = make_float4((O[2 * G4][0] - O[2 * G4][1]) + mb[G4], (O[2 * G4][2] - O[2 * G4][3]) + mb[G4],
+                                    (O[2 * G4 + 1][0] - O[2 * G4 + 1][1]) + mb[G4],
+                                    (O[2 * G4 + 1][2] - O[2 * G4 + 1][3]) + mb[G4]);
       *reinterpret_cast<float4*>(rec + 4 + 32 * G4 + 4 * g) = o4;
     }
     unit = unit_stride0 + (int)__shfl_sync(0xffffffffu, (unsigned)nxt, 0);
@@ -625,21 +654,11 @@ kvq_status launch_int2(const KvqView& v, const void* q, float* out, float scale,
   const size_t smem = sizeof(SmemI2) + 1024 + sizeof(int) * 3 * (v.batch + 1);
   void (*kern)(KvqView, const void*, float, float*, const CUtensorMap, const CUtensorMap) =
       v.meta16 ? split_int2_kernel<true> : split_int2_kernel<false>;
-  static int occ_cache[2][64] = {{0}};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64) return KVQ_ERR_UNSUPPORTED;
-  int& occ_dev = occ_cache[v.meta16 ? 1 : 0][dev];
-  if (!occ_dev) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)(sizeof(SmemI2) + 1024 + sizeof(int) * 3 * 4097)) != cudaSuccess)
-      return KVQ_ERR_CUDA;
-    int occ = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kThreadsI, smem) != cudaSuccess)
-      return KVQ_ERR_CUDA;
-    occ_dev = occ > 0 ? occ : 1;
-  }
-  const int grid = num_sms() * occ_dev;
+  int occ = 0;
+  const kvq_status so = occupancy_once(kSlotInt2 + (v.meta16 ? 1 : 0), kern, kThreadsI, smem,
+                                       sizeof(SmemI2) + 1024 + sizeof(int) * 3 * 4097, &occ);
+  if (so != KVQ_OK) return so;
+  const int grid = num_sms() * occ;
   if (cudaMemsetAsync(static_cast<char*>(ws) + fast_counter_offset(v.batch), 0, 8, st) != cudaSuccess)
     return KVQ_ERR_CUDA;
   kern<<<grid, kThreadsI, smem, st>>>(v, q, scale, static_cast<float*>(ws), tmc, tmk);

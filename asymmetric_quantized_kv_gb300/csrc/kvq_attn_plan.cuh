@@ -9,6 +9,7 @@
 // head of the workspace for the combine kernel.
 #pragma once
 
+#include "kvq_host.h"
 #include "kvq_internal.cuh"
 
 namespace kvq {
@@ -157,18 +158,6 @@ __device__ inline void rope_split(const KvqView& v, int i, float* hi, float* lo)
   const float h = (float)w;
   *hi = h;
   *lo = (float)(w - (double)h);
-}
-
-inline int num_sms() {
-  static int cached[64] = {0};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
-  if (!cached[dev]) {
-    int n = 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
-    cached[dev] = n;
-  }
-  return cached[dev];
 }
 
 }  // namespace kvq

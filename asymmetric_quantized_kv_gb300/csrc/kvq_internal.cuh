@@ -70,6 +70,9 @@ kvq_status launch_fp8(const KvqView& v, const void* q, float* out, float scale, 
 bool int2_shape_eligible(const KvqView& v);  // config only: sizes the workspace
 bool int2_eligible(const KvqView& v);        // config, cache pointers and pool size
 kvq_status launch_int2(const KvqView& v, const void* q, float* out, float scale, void* ws, cudaStream_t st);
+// The decode kernel launch_attention runs for a resolved cache (a kvq_kernel value):
+// the first tensor-core kernel whose shape and pointer tests pass, else the generic one.
+int pick_decode_kernel(const KvqView& v);
 kvq_status launch_attention(const KvqView& v, const void* q, float* out, float scale,
                             void* ws, size_t ws_bytes, cudaStream_t st);
 

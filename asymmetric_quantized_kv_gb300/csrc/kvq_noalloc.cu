@@ -15,18 +15,20 @@
 // per device with cudaGetSymbolAddress, with that device current, and cached.
 // All calls on a device share the array and it keeps the last call's contents;
 // the attention kernels write every workspace byte before they read it, so
-// nothing has to be cleared between calls.
+// nothing has to be cleared between calls.  The cached address belongs to the
+// device's primary context: after a cudaDeviceReset() the library (like its
+// other per-device launch settings) has to be reloaded; a reset is not supported.
 #include <mutex>
 
+#include "kvq_host.h"
 #include "kvq_internal.cuh"
 
 namespace {
 
 static __device__ __align__(256) unsigned char g_scratch[KVQ_NOALLOC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
 std::mutex g_mutex;
-void* g_scratch_addr[kMaxDevices] = {nullptr};
+void* g_scratch_addr[kvq::kMaxDevices] = {nullptr};
 
 // Device address of g_scratch on the calling thread's current device.
 kvq_status scratch_address(void** out) {
@@ -35,7 +37,7 @@ kvq_status scratch_address(void** out) {
     cudaGetLastError();
     return KVQ_ERR_CUDA;
   }
-  if (dev < 0 || dev >= kMaxDevices) return KVQ_ERR_UNSUPPORTED;
+  if (dev < 0 || dev >= kvq::kMaxDevices) return KVQ_ERR_UNSUPPORTED;
   std::lock_guard<std::mutex> lock(g_mutex);
   if (!g_scratch_addr[dev]) {
     void* p = nullptr;
@@ -55,11 +57,15 @@ kvq_status scratch_address(void** out) {
 extern "C" kvq_status kvq_decode_attention_noalloc(const kvq_config* cfg, const kvq_cache* cache,
                                                    const void* q, float* out, float softmax_scale,
                                                    void* stream) {
+  const kvq::NvtxRange range("kvq_decode_attention_noalloc");
   if (!cfg || !cache) return KVQ_ERR_INVALID_ARG;
   const kvq_status valid = kvq_validate(cfg);
   if (valid != KVQ_OK) return valid;
   if (cache->batch < 1 || cache->max_pages_per_seq < 1) return KVQ_ERR_INVALID_ARG;
-  const size_t need = kvq_workspace_bytes(cfg, cache->batch, cache->max_pages_per_seq * cfg->page_size);
+  // the longest sequence the block table can address, in 64-bit arithmetic
+  const long long max_len = (long long)cache->max_pages_per_seq * cfg->page_size;
+  if (max_len > 0x7fffffffLL) return KVQ_ERR_INVALID_ARG;
+  const size_t need = kvq_workspace_bytes(cfg, cache->batch, (int)max_len);
   if (need == 0) return KVQ_ERR_INVALID_ARG;
   if (need > (size_t)KVQ_NOALLOC_SCRATCH_BYTES) return KVQ_ERR_CAPACITY;
   void* scratch = nullptr;

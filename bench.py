@@ -68,7 +68,7 @@ LAUNCHES_ATTENTION = 2
 # capture of a smaller case of the same kernel scaled by algorithmic bytes
 # (profiles/split_rope_i8i4_paged_ragged_b16.md, split_fp8_70b_layer_b2.md,
 # split_int2_8b_layer_b8.md); to be re-captured whenever that kernel changes.
-SPLIT_TRAFFIC = {5: 1790.9e6, 4: 2192.4e6, 3: 557.4e6}
+SPLIT_TRAFFIC = {5: 1790.9e6, 4: 2192.4e6, 3: None}
 SPLIT_KERNEL = {5: "split_rope_i8i4_kernel", 4: "split_fp8_kernel", 3: "split_int2_kernel",
                 1: "split_generic_kernel", 2: "split_generic_kernel"}
 K_AXES = {"tensor": 0, "token": 1, "channel": 2}
@@ -222,16 +222,29 @@ def _oracle_state(cid, b, h, T, fp8, meta, k_axis):
     return _ORACLE_STATES[key]
 
 
-def _oracle_worker(job):
-    """Time the oracle's decode (dequantize + RoPE + attention) on one sampled
-    (sequence, kv-head) stream; one BLAS thread per worker process.  Building
-    the quantized stream is not timed."""
-    cid, b, h, T, steps, fp8, meta, k_axis = job
+def _oracle_decode(job, steps):
+    """Run the oracle's decode (dequantize + RoPE + attention) `steps` times on
+    one sampled (sequence, kv-head) stream; seconds taken."""
+    cid, b, h, T, _, fp8, meta, k_axis = job
     O, cfg, st, q, ks, vs = _oracle_state(cid, b, h, T, fp8, meta, k_axis)
     t0 = time.perf_counter()
     for _ in range(steps):
         O.decode_head(cfg, st, q, ks, vs)
     return time.perf_counter() - t0
+
+
+def _oracle_proc(jobs, inbox, outbox):
+    """One worker process of OraclePool: build the quantized streams of its jobs,
+    report ready, then for every request run each job's decode and report the
+    seconds; one BLAS thread (set by the parent's environment)."""
+    for j in jobs:
+        _oracle_state(*[j[k] for k in (0, 1, 2, 3, 5, 6, 7)])
+    outbox.put(0.0)
+    while True:
+        steps = inbox.get()
+        if steps is None:
+            return
+        outbox.put(sum(_oracle_decode(j, j[4] if steps < 0 else steps) for j in jobs))
 
 
 def oracle_jobs(cid, n_streams, steps, fp8, meta, k_axis, max_tokens=0):
@@ -262,31 +275,48 @@ def oracle_job_bytes(jobs):
 
 
 class OraclePool:
-    """A spawned process pool for the oracle leg, one BLAS thread per process."""
+    """Spawned oracle worker processes, one BLAS thread each, with a fixed share
+    of the jobs (job i goes to process i mod procs).  Each process builds its
+    quantized streams once at start-up (untimed); a pass then starts every
+    process at once and ends when the last one finishes, so the pass's wall time
+    holds decode work only."""
 
     ENV = ["OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"]
 
-    def __init__(self, procs):
+    def __init__(self, procs, jobs):
         import multiprocessing as mp
         try:
             cores = len(os.sched_getaffinity(0))
         except AttributeError:
             cores = os.cpu_count() or 1
-        self.procs = max(1, min(cores, procs))
+        self.procs = max(1, min(cores, procs, len(jobs)))
         self.old = {k: os.environ.get(k) for k in self.ENV}
         for k in self.ENV:
             os.environ[k] = "1"
-        self.pool = mp.get_context("spawn").Pool(self.procs)
+        ctx = mp.get_context("spawn")
+        self.outbox = ctx.Queue()
+        self.inboxes = [ctx.Queue() for _ in range(self.procs)]
+        self.ps = [ctx.Process(target=_oracle_proc, args=(jobs[i::self.procs], self.inboxes[i], self.outbox),
+                               daemon=True) for i in range(self.procs)]
+        for p in self.ps:
+            p.start()
+        for _ in self.ps:  # every stream built
+            self.outbox.get()
 
-    def run(self, jobs):
-        """(per-job decode seconds, wall seconds) of one pass over the jobs."""
+    def run(self, steps=-1):
+        """(summed decode seconds, wall seconds) of one pass: every job's decode
+        `steps` times (-1: each job's own step count)."""
         t0 = time.perf_counter()
-        times = self.pool.map(_oracle_worker, jobs, chunksize=1)
-        return times, time.perf_counter() - t0
+        for q in self.inboxes:
+            q.put(steps)
+        busy = sum(self.outbox.get() for _ in self.ps)
+        return busy, time.perf_counter() - t0
 
     def close(self):
-        self.pool.close()
-        self.pool.join()
+        for q in self.inboxes:
+            q.put(None)
+        for p in self.ps:
+            p.join(timeout=60)
         for k, val in self.old.items():
             if val is None:
                 os.environ.pop(k, None)
@@ -295,22 +325,33 @@ class OraclePool:
 
 
 def cpu_oracle_throughput(cid: int, n_streams: int, steps: int = 1, fp8: str = "e4m3", meta: str = "f32",
-                          k_axis: str = "channel"):
-    """Oracle GB/s on a bounded sample of the workload's streams, timed in a
-    spawned process pool (one BLAS thread per process)."""
+                          k_axis: str = "channel", append: bool = False):
+    """Oracle GB/s on a bounded sample of the workload's streams: bytes of the
+    timed decodes over the wall time of the pass, in a spawned process pool (one
+    BLAS thread per process, one process per available core), and the same
+    sample on one core.  Building the quantized streams happens in an untimed
+    first pass."""
     jobs = oracle_jobs(cid, n_streams, steps, fp8, meta, k_axis)
-    pool = OraclePool(len(jobs))
+    nbytes = oracle_job_bytes(jobs)
+    pool = OraclePool(len(jobs), jobs)
     try:
-        times, wall = pool.run(jobs)
+        busy, wall = pool.run()
     finally:
         pool.close()
-    busy = sum(times)
-    return dict(value=oracle_job_bytes(jobs) / (busy / pool.procs) / 1e9, unit="GB/s", cores=pool.procs,
-                kind="oracle",
+    one = OraclePool(1, jobs)
+    try:
+        one_jobs = [j[:4] + (1,) + j[5:] for j in jobs]  # one step per stream on one core
+        _, wall1 = one.run(1)
+    finally:
+        one.close()
+    return dict(value=nbytes / wall / 1e9, unit="GB/s", cores=pool.procs, kind="oracle",
+                value_1core=oracle_job_bytes(one_jobs) / wall1 / 1e9,
                 sample=f"{len(jobs)} (sequence, kv-head) streams of the workload ("
                        f"{sum(j[3] for j in jobs)} tokens), decode = dequantize + RoPE + attention in float64, "
-                       f"{steps} step(s) each, {pool.procs} spawned processes x 1 BLAS thread; "
-                       f"{busy:.1f} s CPU, {wall:.1f} s wall")
+                       f"{steps} step(s) each; value = bytes / wall time of the pass over {pool.procs} spawned "
+                       f"processes x 1 BLAS thread ({busy:.1f} s CPU, {wall:.1f} s wall); value_1core = one "
+                       f"step per stream in one process ({wall1:.1f} s wall)"
+                       + ("; the append of each step is not timed on the CPU" if append else ""))
 
 
 # ------------------------------------------------------------------ ranks
@@ -605,6 +646,32 @@ def run_gpu(args, spec, rank, world):
                 clocks=clock_info, status=status, e2e=e2e, lens=cur)
 
 
+def layer_line(args, cid, peak, peak_kind):
+    """Decode-only measurement of another headline layer in the same process
+    (the 2-bit 8B layer, the FP8 70B layer): its own cache, events around every
+    decode call over the same number of steps, its roofline against the same
+    HBM peak."""
+    import argparse as _ap
+    import torch
+    spec = workload_spec(cid)
+    sub = _ap.Namespace(**vars(args))
+    sub.e2e = False
+    r = run_gpu(sub, spec, 0, 1)
+    torch.cuda.empty_cache()
+    att_ms = statistics.mean(r["att_ms"])
+    att_bytes = statistics.mean(r["att_bytes"])
+    achieved = att_bytes / (att_ms / 1e3) / 1e9
+    return {"workload": spec["name"], "batch": spec["w"].batch, "sum_tokens": int(sum(r["lens"])),
+            "us_per_call": att_ms * 1e3, "us_per_call_median": statistics.median(r["att_ms"]) * 1e3,
+            "bytes_per_call": att_bytes, "value": achieved, "unit": "GB/s",
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": SPLIT_TRAFFIC.get(cid),
+                         "kernel": f"kvq_decode_attention: {SPLIT_KERNEL[cid]} + combine (timed together)",
+                         "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)" if peak_kind == "measured"
+                         else "fallback 6.8 TB/s"},
+            "gpu_launches": args.steps * LAUNCHES_ATTENTION, "clocks": r["clocks"], "device_status": r["status"]}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -614,6 +681,8 @@ def main():
     ap.add_argument("--config", type=int, default=5, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", dest="e2e", action="store_false")
+    ap.add_argument("--no-layers", dest="layers", action="store_false",
+                    help="skip the 2-bit and FP8 layers that a default (--config 5, one GPU) run adds to its line")
     ap.add_argument("--cpu-streams", type=int, default=16)
     ap.add_argument("--cpu-steps", type=int, default=8)
     ap.add_argument("--batch", type=int, default=0, help="use only the first N sequences (profiling)")
@@ -638,25 +707,25 @@ def main():
         jobs = oracle_jobs(args.config, args.cpu_streams, 1, args.fp8, args.meta, args.k_axis,
                            max_tokens=REF_MAX_TOKENS)
         nbytes = oracle_job_bytes(jobs)
-        pool = OraclePool(len(jobs))
+        pool = OraclePool(len(jobs), jobs)
         per_step, busy_all, wall_all = [], 0.0, 0.0
         try:
             for _ in range(args.warmup):
-                pool.run(jobs)
+                pool.run()
             for _ in range(args.steps):
-                times, wall = pool.run(jobs)
-                busy_all += sum(times)
+                busy, wall = pool.run()
+                busy_all += busy
                 wall_all += wall
-                per_step.append(nbytes / (sum(times) / pool.procs) / 1e9)
+                per_step.append(nbytes / wall / 1e9)
         finally:
             pool.close()
         val = statistics.median(per_step)
         detail = dict(value=val, unit="GB/s", cores=pool.procs, kind="oracle",
                       sample=f"{len(jobs)} (sequence, kv-head) streams of the workload (prefixes of at most "
                              f"{REF_MAX_TOKENS} tokens, {sum(j[3] for j in jobs)} tokens) per step, decode = "
-                             f"dequantize + RoPE + attention in float64, median over {args.steps} steps after "
-                             f"{args.warmup} warm-up passes; {pool.procs} spawned processes x 1 BLAS thread; "
-                             f"{busy_all:.1f} s CPU, {wall_all:.1f} s wall")
+                             f"dequantize + RoPE + attention in float64, bytes / wall time of each pass, median "
+                             f"over {args.steps} steps after {args.warmup} warm-up passes; {pool.procs} spawned "
+                             f"processes x 1 BLAS thread; {busy_all:.1f} s CPU, {wall_all:.1f} s wall")
         line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "GB/s", "n_gpus": args.gpus,
                 "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "f64", "data": "synthetic",
@@ -668,7 +737,7 @@ def main():
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_oracle_throughput(args.config, n_streams=args.cpu_streams, steps=args.cpu_steps, fp8=args.fp8,
-                                    meta=args.meta, k_axis=args.k_axis)
+                                    meta=args.meta, k_axis=args.k_axis, append=spec["append"])
 
     import torch
     if world > 1:
@@ -712,6 +781,9 @@ def main():
         "clocks": r["clocks"],
         "device_status": r["status"],
     }
+    if world == 1 and args.config == 5 and args.layers and not args.batch and args.meta == "f32":
+        # the other two headline layers, decode alone, each against the HBM roofline
+        line["layers"] = {str(cid): layer_line(args, cid, peak, peak_kind) for cid in (3, 4)}
     print(json.dumps(line))
     if world > 1:
         import torch.distributed as dist

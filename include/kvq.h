@@ -42,6 +42,10 @@
  *     that timed out) set bits in the caller's `*status` word with atomicOr
  *     and skip the affected work; kernels never trap and never spin without
  *     an iteration limit.  Read the word when convenient.
+ *   - Every call that enqueues work (calibrate, append, decode, dequantize)
+ *     opens an NVTX range named after itself in the "libkvq" domain, so a
+ *     profiler can attribute the kernels to the call; with no profiler
+ *     attached a range costs a pointer test.
  *
  * Quantization rules (bit-exact; all arithmetic IEEE fp32 round-to-nearest-
  * even, no fused multiply-add, in exactly this order):
@@ -222,6 +226,25 @@ kvq_status kvq_decode_attention(const kvq_config* cfg, const kvq_cache* cache, c
                                 float* out, float softmax_scale, void* workspace,
                                 size_t ws_bytes, void* stream);
 
+/* The decode kernels kvq_decode_attention chooses between (the pages give no
+ * kernel design; these are this library's).  Each tensor-core kernel handles one
+ * format mix at head_dim 128 and takes the call when its shape and pointer tests
+ * pass; every other call runs on the generic kernel. */
+typedef enum {
+  KVQ_KERNEL_GENERIC = 0,   /* any format mix, head_dim 64/128/256, any GQA ratio */
+  KVQ_KERNEL_ROPE_I8I4 = 1, /* sym INT8 per-channel pre-RoPE K + asym INT4 per-token V,
+                               8 kv-heads x 4 query heads, power-of-two G and P */
+  KVQ_KERNEL_FP8 = 2,       /* FP8 (E4M3 or E5M2) K and V, 8 query heads per kv-head */
+  KVQ_KERNEL_INT2 = 3       /* asym 2-bit per-channel K + asym 2-bit per-token V (g = 32),
+                               4 query heads per kv-head, bf16 or fp32 window */
+} kvq_kernel;
+
+/* Which kvq_kernel kvq_decode_attention launches for these arguments.  Host
+ * only: nothing is enqueued and no device memory is read.  Returns the same
+ * argument errors kvq_decode_attention would (before its q/out/workspace
+ * checks); *kernel is written on KVQ_OK. */
+kvq_status kvq_decode_kernel(const kvq_config* cfg, const kvq_cache* cache, int32_t* kernel);
+
 /* Size of the scratch array kvq_decode_attention_noalloc uses (32 MiB). */
 #define KVQ_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
 
@@ -237,8 +260,10 @@ kvq_status kvq_decode_attention(const kvq_config* cfg, const kvq_cache* cache, c
  *   than KVQ_NOALLOC_SCRATCH_BYTES, i.e. when
  *   kvq_workspace_bytes(cfg, batch, max_pages_per_seq * page_size) exceeds it.
  * - The first call on a device (the calling thread's current device, which
- *   must be the cache's) looks up the array's device address; make that first
- *   call before any stream capture.
+ *   must be the cache's) looks up the array's device address and keeps it for
+ *   the process; make that first call before any stream capture.  The address
+ *   belongs to the device's primary context: using the library across a
+ *   cudaDeviceReset() is not supported.
  * - All calls on a device share the one array: calls that overlap on the GPU
  *   (other streams, other host threads) race and corrupt each other's results.
  *   Calls ordered on one stream are safe; nothing needs clearing between them. */

@@ -223,14 +223,18 @@ class FullCase:
             self.cache.k_scale.copy_(torch.tensor(self.k_scale, dtype=torch.float32))
             self.cache.v_scale.copy_(torch.tensor(self.v_scale, dtype=torch.float32))
             g.set_state(state)
-        self.samples = list(samples)
+        self.keep_all = samples == "all"
+        self.samples = [] if self.keep_all else list(samples)
         parts = {s: ([], []) for s in self.samples}
+        self.chunks = []  # keep_all: host bf16 copies of every appended chunk
         done = 0
         while done < T_max:
             n = min(chunk, T_max - done)
             take = [max(0, min(n, T - done)) for T in self.lens]
             kk, vv = W.torch_kv_chunk(w, g, Bn, n, scale, dev)
             self.cache.append(kk, vv, torch.tensor(take, dtype=torch.int32, device=dev))
+            if self.keep_all:
+                self.chunks.append((done, kk.cpu(), vv.cpu()))
             for (b, h) in self.samples:
                 if take[b]:
                     parts[(b, h)][0].append(kk[b, :take[b], h].float().cpu().numpy())
@@ -239,6 +243,48 @@ class FullCase:
         torch.cuda.synchronize()
         self.streams = {s: (np.concatenate(k), np.concatenate(v)) for s, (k, v) in parts.items()}
         self.q = torch.randn(Bn, Hq, D, generator=g, device=dev).to(torch.bfloat16)
+
+    def source_rows(self, b):
+        """keep_all: the source rows of sequence b as float32 [T, Hkv, D] (K, V)."""
+        T = self.lens[b]
+        ks = [kk[b, :max(0, min(kk.shape[1], T - t0))] for t0, kk, _ in self.chunks if t0 < T]
+        vs = [vv[b, :max(0, min(vv.shape[1], T - t0))] for t0, _, vv in self.chunks if t0 < T]
+        return torch.cat(ks).float().numpy(), torch.cat(vs).float().numpy()
+
+    def check_every_stream(self, tol=ATT_TOL, workers=16):
+        """keep_all: every (sequence, kv-head) stream against the oracle in a
+        spawned process pool: kvq_dequantize over the whole stream bit-exact, and
+        the attention of the stream's query heads within `tol`.  Returns the
+        worst relative L2 and the per-(sequence, query head) errors."""
+        import concurrent.futures as cf
+        import multiprocessing as mp
+        from kvq_oracle_pool import check_stream
+        assert self.keep_all
+        out = self.cache.attention(self.q).cpu().numpy()
+        q = self.q.float().cpu().numpy()
+        n_rep, H = self.cfg.n_rep, self.cfg.num_kv_heads
+        errs = np.zeros((len(self.lens), self.cfg.num_q_heads))
+        bad = []
+
+        def tasks():
+            for b, T in enumerate(self.lens):
+                K_, V_ = self.source_rows(b)
+                kd, vd = self.cache.dequantize(b, 0, T)
+                kd, vd = kd.cpu().numpy(), vd.cpu().numpy()
+                for h in range(H):
+                    heads = slice(h * n_rep, (h + 1) * n_rep)
+                    yield ((b, h), self.cfg, K_[:, h], V_[:, h], q[b, heads], kd[:, h], vd[:, h], out[b, heads],
+                           self.k_scale[h], self.v_scale[h])
+
+        with cf.ProcessPoolExecutor(workers, mp_context=mp.get_context("spawn")) as ex:
+            for (b, h), exact, err in ex.map(check_stream, tasks(), chunksize=1):
+                if not exact:
+                    bad.append((b, h))
+                errs[b, h * n_rep:(h + 1) * n_rep] = err
+        assert not bad, f"kvq_dequantize differs from the oracle on streams {bad[:8]}"
+        assert errs.max() <= tol, f"attention rel L2 {errs.max():.3e} > {tol}"
+        assert int(self.cache.status.item()) == 0
+        return float(errs.max()), errs
 
     def state(self, b, h):
         K_, V_ = self.streams[(b, h)]
@@ -258,14 +304,16 @@ class FullCase:
         assert int(self.cache.status.item()) == 0
         return worst
 
-    def check_dequantize(self, span=2048):
-        """Bit-exact kvq_dequantize against the oracle on the first, a middle and
-        the last `span` tokens of each sampled stream."""
+    def check_dequantize(self, span=None):
+        """Bit-exact kvq_dequantize against the oracle on each sampled stream: the
+        whole stream, or (span given) its first, a middle and its last `span`
+        tokens."""
         for (b, h) in self.samples:
             T = self.lens[b]
             ko, vo = O.dequantize_stream(self.cfg, self.state(b, h), self.k_scale[h], self.v_scale[h])
-            for t0 in sorted({0, max(0, T // 2 - span // 2), max(0, T - span)}):
-                t1 = min(T, t0 + span)
+            span_b = T if span is None else span
+            for t0 in sorted({0, max(0, T // 2 - span_b // 2), max(0, T - span_b)}):
+                t1 = min(T, t0 + span_b)
                 k, v = self.cache.dequantize(b, t0, t1)
                 assert np.array_equal(k[:, h].cpu().numpy().astype(np.float64), ko[t0:t1]), (b, h, t0)
                 assert np.array_equal(v[:, h].cpu().numpy().astype(np.float64), vo[t0:t1]), (b, h, t0)

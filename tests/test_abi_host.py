@@ -117,3 +117,23 @@ def test_entry_points_reject_bad_arguments_before_launch(K):
     assert L.kvq_dequantize(by(c), by(fake), 0, 3, 3, None, None, None) == K.KVQ_OK  # empty range: no launch
     assert L.kvq_calibrate_absmax(by(c), None, 10, 448.0, None, None) == K.KVQ_ERR_INVALID_ARG
     assert L.kvq_calibrate_absmax(by(c), 4096, 10, 0.0, 4096, None) == K.KVQ_ERR_INVALID_ARG
+
+
+def test_decode_kernel_query_on_the_host(K):
+    """kvq_decode_kernel answers from the configuration and the cache struct
+    alone (the pointers are never dereferenced): the pre-RoPE INT8/INT4 mix with
+    8 kv-heads x 4 query heads goes to its tensor-core kernel, the same mix with
+    2 kv-heads to the generic kernel; bad arguments give the decode call's errors."""
+    L = K.binding.LIB
+    by = ctypes.byref
+    spec_k = (O.INT8, O.SYM, O.PER_CHANNEL, 64)
+    spec_v = (O.INT4, O.ASYM, O.PER_TOKEN, 0)
+    fast = K.make_config(32, 8, 128, spec_k, spec_v, 64, 16, 1, 5e5, K.KVQ_BF16)
+    small = K.make_config(8, 2, 128, spec_k, spec_v, 64, 16, 1, 5e5, K.KVQ_BF16)
+    fake = K.kvq_cache(4096, 4096, 4096, 4096, 4096, 4096, 4096, 2, 4, 8, 4096)
+    out = ctypes.c_int32(-1)
+    assert L.kvq_decode_kernel(by(fast), by(fake), by(out)) == K.KVQ_OK and out.value == K.KVQ_KERNEL_ROPE_I8I4
+    assert L.kvq_decode_kernel(by(small), by(fake), by(out)) == K.KVQ_OK and out.value == K.KVQ_KERNEL_GENERIC
+    assert L.kvq_decode_kernel(by(fast), by(fake), None) == K.KVQ_ERR_INVALID_ARG
+    empty = K.kvq_cache(None, None, None, None, None, None, None, 1, 1, 1, None)
+    assert L.kvq_decode_kernel(by(fast), by(empty), by(out)) == K.KVQ_ERR_INVALID_ARG

@@ -1,8 +1,12 @@
 """Parity at the benchmark's full sizes, in the launch configuration bench.py
-times: the caches of configs 3, 4 and 5 are filled through the library from the
-same seeded device-side draws as the benchmark, and sampled (sequence, kv-head)
-streams are checked against the oracle: attention within 1e-3 relative L2 per
-query head, kvq_dequantize bit-exact on three token windows per stream."""
+times: the caches of the 2-bit 8B layer, the FP8 70B layer and the paged ragged
+layer are filled through the library from the same seeded device-side draws as
+the benchmark.  Sampled (sequence, kv-head) streams are checked against the
+oracle (attention within 1e-3 relative L2 per query head, kvq_dequantize
+bit-exact over the whole stream); every stream of the 2-bit layer is checked
+against the oracle the same way; every (sequence, query head) of the other two
+layers is checked against float64 attention over the library's dequantized
+cache."""
 import numpy as np
 import pytest
 
@@ -18,10 +22,18 @@ from kvq_testlib import FullCase  # noqa: E402
 
 
 def _samples(cid):
+    """The longest and the shortest sequence, and three more (sequence, kv-head)
+    streams drawn with a fixed seed."""
     w = W.WORKLOADS[cid]
     lens = W.lengths(w)
     b_long, b_short = int(np.argmax(lens)), int(np.argmin(lens))
-    return [(b_long, 0), (b_short, w.num_kv_heads - 1), ((b_long + 1) % w.batch, 3)]
+    out = [(b_long, 0), (b_short, w.num_kv_heads - 1), ((b_long + 1) % w.batch, 3)]
+    g = np.random.default_rng(100 + cid)
+    while len(out) < 6:
+        s = (int(g.integers(w.batch)), int(g.integers(w.num_kv_heads)))
+        if s not in out:
+            out.append(s)
+    return out
 
 
 @pytest.mark.parametrize("cid,fp8,meta", [(3, "e4m3", "f32"), (3, "e4m3", "f16"), (4, "e4m3", "f32"),
@@ -30,21 +42,35 @@ def test_fullsize_sampled_streams(cid, fp8, meta):
     """(config 4 also in FP8 E5M2 with absmax/57344 scales; configs 3 and 5 also
     with binary16 scales and minima)"""
     case = FullCase(cid, _samples(cid), fp8=fp8, meta=meta)
+    import asymmetric_quantized_kv_gb300 as K
+    assert case.cache.decode_kernel() == {3: K.KVQ_KERNEL_INT2, 4: K.KVQ_KERNEL_FP8, 5: K.KVQ_KERNEL_ROPE_I8I4}[cid]
     case.check_attention()
     case.check_dequantize()
     del case
     torch.cuda.empty_cache()
 
 
-@pytest.mark.parametrize("cid", [
-    pytest.param(3, marks=pytest.mark.xfail(
-        reason="2-bit layer: 7 of 512 (sequence, query head) outputs reach 1.24e-3 relative L2 (median 4.3e-5); "
-               "the oracle on that stream agrees with this reference to 1e-15", strict=False)),
-    4, 5])
+@pytest.mark.parametrize("meta", ["f32", "f16"])
+def test_every_stream_of_the_2bit_layer_against_the_oracle(meta):
+    """All 128 (sequence, kv-head) streams of the 2-bit 8B layer (16 x (32768 +
+    127) tokens) through the oracle: kvq_dequantize bit-exact over every whole
+    stream, and all 512 (sequence, query head) outputs within 1e-3 relative L2.
+    The kernel centres the 2-bit value codes (c - 3/2) before the tensor-core
+    product; with uncentred codes the heads that spread their attention lost up
+    to 1.24e-3 to cancellation between the code sum and the minimum sum."""
+    case = FullCase(3, "all", meta=meta)
+    worst, errs = case.check_every_stream()
+    print(f"\n2-bit layer ({meta} scale/min): worst {worst:.3e}, median {np.median(errs):.3e}, "
+          f"above 3e-4: {int((errs > 3e-4).sum())} of {errs.size}")
+    del case
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("cid", [4, 5])
 def test_every_sequence(cid):
     """Every (sequence, query head) of the full layer against attention computed
     in float64 by torch over the cache's own dequantized keys and values
-    (kvq_dequantize, bit-exact against the oracle on the sampled streams above),
+    (kvq_dequantize, bit-exact against the oracle over the whole sampled streams above),
     pre-RoPE keys rotated in float64.  The split plans cover each sequence with
     whole chunks, pieces and the window (the paged layer's plan cuts its final
     round of chunks and its partial chunks into quarter pieces): a token the plan

@@ -99,10 +99,31 @@ CASES = {
 }
 
 
+# The decode kernel each case must run on (kvq_decode_kernel); every other case
+# runs on the generic kernel.  A tensor-core kernel that stopped taking its
+# format mix (a shape test, or the driver's tensor-map encoder missing) would
+# otherwise leave the suite green on the generic kernel.
+TC_KERNEL = {
+    "int2_kivi": "INT2", "int2_kivi_p16": "INT2", "int2_g64_f32": "INT2", "m16_int2_kivi": "INT2",
+    "m16_int2_kivi_p16": "INT2",
+    "fp8": "FP8", "fp8_p16_f32": "FP8", "fp8_64q8kv": "FP8", "fp8_e5m2": "FP8", "fp8_e5m2_p16_f32": "FP8",
+    "fast_rope_i8i4_p16": "ROPE_I8I4", "fast_rope_i8i4_p64": "ROPE_I8I4", "fast_rope_i8i4_g128": "ROPE_I8I4",
+    "m16_fast_rope_p16": "ROPE_I8I4", "m16_fast_rope_p64": "ROPE_I8I4",
+}
+
+
 @pytest.fixture(scope="module", params=sorted(CASES))
 def case(request):
     cfg, lens = CASES[request.param]
-    return Case(cfg, lens, seed=sorted(CASES).index(request.param))
+    c = Case(cfg, lens, seed=sorted(CASES).index(request.param))
+    c.name = request.param
+    return c
+
+
+def test_decode_kernel_choice(case):
+    import asymmetric_quantized_kv_gb300 as K
+    want = getattr(K, "KVQ_KERNEL_" + TC_KERNEL.get(case.name, "GENERIC"))
+    assert case.cache.decode_kernel() == want
 
 
 def test_pages_bit_exact(case):

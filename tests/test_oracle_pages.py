@@ -90,3 +90,61 @@ def test_page_writer_roundtrip(kfmt, kmode, vfmt, vmode):
     # pages never touched stay undefined; every defined byte belongs to a used page
     used = {int(bt[b][t // P]) for b in range(2) for t in range(128)}
     assert set(np.nonzero(defined.any(axis=1))[0].tolist()) == used
+
+
+# Per-token keys and binary16 metadata, worked by hand on a 4-token page, D = 8.
+# K: asymmetric INT4 per token in two groups of 4 channels; V: symmetric INT8 per
+# token (one group).  Every scale is exact (ranges 15 and absmax 127).
+#   K row 0: [0, 15, 1, 2 | -8, 7, 0, 1]  -> group 0: min 0, s 1, codes 0 15 1 2
+#                                            group 1: min -8, s 1, codes 0 15 8 9
+#   packed little-endian, low nibble first: F0 21 F0 98
+#   K row 1: [3, 3, 3, 3 | 1, 16, 2, 3]   -> group 0 constant: d = 1e-8 (fl32), codes 0 0 0 0,
+#                                            min 3; group 1: min 1, s 1, codes 0 15 1 2
+#   packed: 00 00 F0 21
+#   V row 0: [127, -127, 1, 0.5, 2.5, -1.5, 0, 64] -> s 1, codes 127 -127 1 0 2 -2 0 64
+#   bytes (two's complement): 7F 81 01 00 02 FE 00 40
+#   V row 1: [-127, 0, 0, 0, 0, 0, 0, 3.5]  -> s 1, codes -127 0 0 0 0 0 0 4: 81 00 00 00 00 00 00 04
+# Section offsets (16-byte aligned, in the order K codes, V codes, V meta, K meta):
+#   fp32 meta: K codes 4 x 4 = 16 at 0; V codes 4 x 8 = 32 at 16; V meta 4 x 1 x 4 = 16 at 48;
+#              K meta 4 tokens x (2 scales + 2 minima) x 4 = 64 at 64; head block 128
+#   binary16:  V meta 4 x 2 = 8 at 48; K meta 4 x 4 x 2 = 32 at 64 (48 + 8 rounded up); head 96
+_HAND_K = [[0, 15, 1, 2, -8, 7, 0, 1], [3, 3, 3, 3, 1, 16, 2, 3]]
+_HAND_V = [[127, -127, 1, 0.5, 2.5, -1.5, 0, 64], [-127, 0, 0, 0, 0, 0, 0, 3.5]]
+
+
+def _hand_cfg(meta):
+    return O.Config(1, 1, 8, O.QSpec(O.INT4, O.ASYM, O.PER_TOKEN, 4), O.QSpec(O.INT8, O.SYM, O.PER_TOKEN, 8),
+                    residual=0, page_size=4, meta_dtype=meta)
+
+
+@pytest.mark.parametrize("meta", [O.F32, O.F16])
+def test_per_token_key_pages_by_hand(meta):
+    cfg = _hand_cfg(meta)
+    L = O.layout(cfg)
+    want_layout = (0, 16, 48, 64, 128) if meta == O.F32 else (0, 16, 48, 64, 96)
+    assert (L["kc"], L["vc"], L["vm"], L["km"], L["head"]) == want_layout
+    st = O.quantize_stream(cfg, np.array(_HAND_K, float), np.array(_HAND_V, float))
+    pages = np.zeros((3, L["page"]), np.uint8)
+    defined = np.zeros_like(pages, dtype=bool)
+    O.write_head_pages(cfg, pages, defined, np.array([[2]], np.int32), 0, 0, st)
+    pg = pages[2]
+    assert pg[0:8].tolist() == [0xF0, 0x21, 0xF0, 0x98, 0x00, 0x00, 0xF0, 0x21]
+    assert pg[16:32].tolist() == [0x7F, 0x81, 0x01, 0x00, 0x02, 0xFE, 0x00, 0x40,
+                                  0x81, 0x00, 0x00, 0x00, 0x00, 0x00, 0x00, 0x04]
+    tiny = float(np.float32(1e-8) / np.float32(15))  # constant group: max(d, 1e-8) / qmax in fp32
+    if meta == O.F32:
+        # V meta: one fp32 scale per token; K meta: per token (scale g0, scale g1, min g0, min g1)
+        assert pg[48:56].tolist() == [0, 0, 0x80, 0x3F] * 2  # 1.0f
+        assert pg[64:72].tolist() == [0, 0, 0x80, 0x3F, 0, 0, 0x80, 0x3F]  # 1.0f, 1.0f
+        assert pg[72:80].tolist() == [0, 0, 0, 0, 0, 0, 0, 0xC1]  # 0.0f, -8.0f
+        row1 = pg[80:96].view(np.float32)
+        assert row1[0] == np.float32(tiny) and row1[1] == 1.0 and row1[2] == 3.0 and row1[3] == 1.0
+        assert not defined[2, 96:128].any()  # the two unused slots stay undefined
+    else:
+        # binary16: 1.0 = 0x3C00, -8.0 = 0xC800, 3.0 = 0x4200, little-endian; the constant
+        # group's tiny scale rounds up to the smallest subnormal half (2^-24 = 0x0001)
+        assert pg[48:52].tolist() == [0x00, 0x3C, 0x00, 0x3C]
+        assert pg[64:72].tolist() == [0x00, 0x3C, 0x00, 0x3C, 0x00, 0x00, 0x00, 0xC8]
+        assert pg[72:80].tolist() == [0x01, 0x00, 0x00, 0x3C, 0x00, 0x42, 0x00, 0x3C]
+        assert not defined[2, 80:96].any()
+    assert not defined[0].any() and not defined[1].any()

@@ -3,7 +3,7 @@
 Hand-worked examples (tests/golden/quantizer_examples.json), the E4M3 format
 definition (tests/golden/e4m3_points.json and torch's float8_e4m3fn), the
 quantization error bound, exact reconstruction of constant groups, code ranges,
-and a float32 re-implementation of the pages' two listings run through torch.
+and per-tensor codes worked by hand.
 """
 import json
 import os
@@ -52,45 +52,45 @@ def test_asym_hand_examples(case):
     assert O.dequant_asym(c, s, m).tolist() == case["deq"]
 
 
-def _page_qint8_torch(x, axis):
-    """The first page's qint8 listing, in torch float32."""
-    s = (x.abs().amax() if axis is None else x.abs().amax(dim=axis, keepdim=True)) / 127.0
-    return torch.round(x / s).clamp(-127, 127) * s
+# Per-tensor symmetric INT (a static per-head scale, the first page's per-tensor
+# case of its synthetic head): codes = clamp(round_half_even(x / s), -qmax, qmax).
+# Worked by hand with s = 0.5, so every quotient is exact:
+#   x      3.0  -0.25  0.75  1.25  100.0  -100.0  0.2   -3.5
+#   x/s    6    -0.5   1.5   2.5   200    -200    0.4   -7
+#   INT8   6     0     2     2     127    -127    0     -7
+#   INT4   6     0     2     2     7      -7      0     -7
+_PT_X = [3.0, -0.25, 0.75, 1.25, 100.0, -100.0, 0.2, -3.5]
 
 
-def _page_quant_dequant_torch(x, dim, bits):
-    """The fourth page's quant_dequant listing, in torch float32."""
-    qmax = 2 ** bits - 1
-    mn = x.amin(dim=dim, keepdim=True)
-    mx = x.amax(dim=dim, keepdim=True)
-    scale = (mx - mn).clamp(min=1e-8) / qmax
-    q = ((x - mn) / scale).round().clamp(0, qmax)
-    return q * scale + mn
+@pytest.mark.parametrize("fmt,codes", [(O.INT8, [6, 0, 2, 2, 127, -127, 0, -7]),
+                                       (O.INT4, [6, 0, 2, 2, 7, -7, 0, -7]),
+                                       (O.INT2, [1, 0, 1, 1, 1, -1, 0, -1])])
+def test_per_tensor_codes_by_hand(fmt, codes):
+    x = O.fl32(np.array(_PT_X)).reshape(1, 8)
+    c, s, m = O._quant_tokens(x, O.QSpec(fmt, O.SYM, O.PER_TENSOR), 0.5, 8)
+    assert s is None and m is None
+    assert c[0].tolist() == codes
+    assert O._dequant_tokens(c, None, None, O.QSpec(fmt, O.SYM, O.PER_TENSOR), 0.5, 8)[0].tolist() == \
+        [0.5 * k for k in codes]
 
 
-@pytest.mark.parametrize("axis", [None, 0, 1])
-def test_sym_equals_page_listing_in_fp32(axis):
-    torch.manual_seed(3)
-    x = torch.randn(256, 64)
-    x[:, [5, 9]] *= 20.0
-    ref = _page_qint8_torch(x, axis).double().numpy()
-    xn = x.double().numpy()
-    if axis is None:
-        c, s = O.quant_sym(xn, np.max(np.abs(xn)), 8)
-    else:
-        c, s = O.quant_sym(xn, np.max(np.abs(xn), axis=axis, keepdims=True), 8)
-    assert np.array_equal(O.dequant_sym(c, s), ref)
+def test_per_tensor_zero_scale_gives_zero_codes():
+    x = np.zeros((3, 8))
+    c, _, _ = O._quant_tokens(x, O.QSpec(O.INT8, O.SYM, O.PER_TENSOR), 0.0, 8)
+    assert np.all(c == 0)
 
 
-@pytest.mark.parametrize("dim,bits", [(0, 4), (1, 4), (0, 2), (1, 8)])
-def test_asym_equals_page_listing_in_fp32(dim, bits):
-    torch.manual_seed(4)
-    x = torch.randn(512, 128)
-    x[:, [3, 17, 44, 91]] *= 60.0
-    ref = _page_quant_dequant_torch(x, dim, bits).double().numpy()
-    xn = x.double().numpy()
-    c, s, m = O.quant_asym(xn, xn.min(axis=dim, keepdims=True), xn.max(axis=dim, keepdims=True), bits)
-    assert np.array_equal(O.dequant_asym(c, s, m), ref)
+def test_per_tensor_with_the_tensor_absmax_equals_one_group():
+    """With the static scale taken over the whole tensor, the per-tensor branch is
+    the symmetric quantizer applied to the tensor as a single group (pinned above
+    by hand examples and its bound)."""
+    g = np.random.default_rng(12)
+    x = O.fl32(g.standard_normal((300, 64)) * np.where(np.arange(64) % 17 == 3, 25.0, 1.0))
+    for bits in (2, 4, 8):
+        s = O.calibrate_absmax(x, O.sym_qmax(bits))
+        c, _, _ = O._quant_tokens(x, O.QSpec(bits, O.SYM, O.PER_TENSOR), s, 64)
+        c1, s1 = O.quant_sym(x, np.max(np.abs(x)), bits)
+        assert float(s1) == s and np.array_equal(c, c1)
 
 
 @pytest.mark.parametrize("bits", [2, 4, 8])

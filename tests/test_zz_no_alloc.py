@@ -5,8 +5,9 @@ It uses a fixed scratch array inside the library instead of a caller workspace.
 
 Checked through the C ABI against kvq_decode_attention on two calls in a row
 (the second with another query, so leftovers of the first call in the shared
-array cannot leak into it), within the attention tolerance the other tests
-use, and its size limit.  This file sorts last so that a run stopping at the
+array cannot leak into it): within the attention tolerance the other tests use,
+and in fact bit for bit, since both entry points run the same kernels with the
+same split plan.  Also its size limit.  This file sorts last so that a run stopping at the
 first failure has already run every other test.
 """
 import ctypes
@@ -55,6 +56,8 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls():
         torch.cuda.synchronize()
         assert torch.isfinite(out).all(), call
         assert _rel(out, ref) <= TOL, call
+        # same kernels, same split plan, same merge order: the outputs are the same bits
+        assert torch.equal(out, ref), call
     assert int(cache.status.item()) == 0
 
 
