@@ -15,11 +15,15 @@
 // also brings the group's scales and minima with a 2-D tensor copy in 128-byte
 // swizzle, so the per-group reads meet no bank conflict.
 //
-// QK: with k = c * s + m per (group, channel), q.k = sum_c (q_c s_c) c + sum_c q_c m_c.
-//     A = the 2-bit codes, taken as f16 subnormals straight from the packed bytes
-//     (mask (3 << 2j) per f16 half: code * 4^j * 2^-24, exact); B = q * s / 4^j
-//     split hi/lo, rebuilt once per key group; the second sum is a per-group,
-//     per-head bias.
+// QK: with k = c * s + m per (group, channel), written as k = (c - 3/2) s + (m + 3/2 s),
+//     q.k = sum_c (q_c s_c)(c - 3/2) + sum_c q_c (m_c + 3/2 s_c).  A = the centred
+//     codes c - 3/2 in f16 (exact, built from the packed bytes: see centred_code);
+//     B = q * s split hi/lo, rebuilt once per key group; the second sum is a
+//     per-group, per-head bias.  Centring keeps the tensor-core sum of the order
+//     of the logit: with the codes 0..3 as they are, the code sum and the bias
+//     are each several times larger than the logit and cancel, and on the 8B
+//     layer the logits lost enough to put heads at 4.5e-4 relative L2 (2-bit
+//     values centred, keys not) instead of 4.5e-6 (both centred).
 // PV: with v = c * s_t + m_t per (token, 32-channel group), written as
 //     v = (c - 3/2) s_t + (m_t + 3/2 s_t), p.v = sum_t (p_t s_t)(c - 3/2)
 //     + sum_t p_t (m_t + 3/2 s_t).  Lane row g holds byte 8G + g of every token
@@ -70,11 +74,10 @@ constexpr uint32_t kSpinI = 1u << 20;
 constexpr float kLog2eI = 1.4426950408889634f;
 constexpr float kRescaleI = 8.f;
 constexpr float kMinitI = -1e30f;
-constexpr float kTwo24 = 16777216.f;
 
 struct __align__(1024) SmemI2 {
   uint8_t stage[kWarpsI][kStagesI][kStageI];
-  float4 qp[kWarpsI][8][32];  // per warp, step s, lane: q * qscale at the lane's 4 channels of step s
+  float4 qp[kWarpsI][8][32];  // per warp, step s, lane: q * scale * log2(e) at the lane's 4 channels of step s
   float pex[kWarpsI][2][32];  // p exchange: [token / 8][head * 8 + token % 8]
   uint64_t bar[kWarpsI][kStagesI];
   int valid[kWarpsI][kStagesI];
@@ -169,6 +172,12 @@ __device__ __forceinline__ uint32_t centred_code(uint32_t w) {
   }
 }
 
+// centred_code for a field index known only after unrolling
+__device__ __forceinline__ uint32_t centred_field(uint32_t w, int k) {
+  return k == 0 ? centred_code<0>(w) : k == 1 ? centred_code<1>(w) : k == 2 ? centred_code<2>(w)
+                                                                           : centred_code<3>(w);
+}
+
 // four binary16 values (two words) widened to fp32
 __device__ __forceinline__ float4 halves4(uint2 w) {
   const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&w.x));
@@ -243,17 +252,15 @@ __global__ void __launch_bounds__(kThreadsI, 3)
     }
     const int ntiles = (it.t1 - it.t0 + kTI - 1) / kTI;
 
-    // q * scale * log2(e) / 4^(s % 4) of this lane's query head 4h + g/2 at its step
-    // channels (the power of two matches the code field's weight in the f16 subnormal)
+    // q * scale * log2(e) of this lane's query head 4h + g/2 at its step channels
     {
       const long long qb = ((long long)it.b * v.Hq + h * kRepI + (g >> 1)) * kD;
       __syncwarp();
 #pragma unroll
       for (int s = 0; s < 8; ++s) {
-        const float f = qscale / (float)(1 << (2 * (s & 3)));
         float x[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) x[e] = load_src(q, qb + step_channel(t, s, e), v.src_bf16) * f;
+        for (int e = 0; e < 4; ++e) x[e] = load_src(q, qb + step_channel(t, s, e), v.src_bf16) * qscale;
         sm.qp[warp][s][lane] = make_float4(x[0], x[1], x[2], x[3]);
       }
       __syncwarp();
@@ -348,8 +355,8 @@ __global__ void __launch_bounds__(kThreadsI, 3)
       }
       __syncwarp();
 
-      uint32_t bk[8][2];  // QK B: q * s / 4^j of the current key group, hi (even g) / lo (odd g)
-      float bias = 0.f;   // sum_c q_c m_c of the current key group for query head t
+      uint32_t bk[8][2];  // QK B: q * s of the current key group, hi (even g) / lo (odd g)
+      float bias = 0.f;   // sum_c q_c (m_c + 3/2 s_c) of the current key group for query head t
       for (int i = 0; i < ntiles; ++i) {
         const int stage = cstage;
         bool valid = false;
@@ -370,7 +377,7 @@ __global__ void __launch_bounds__(kThreadsI, 3)
         const int tok0 = it.t0 + i * kTI;
 
         if ((tok0 & (G - 1)) == 0) {
-          // ---- new key group: B = q * s / 4^j and the bias sum_c q_c m_c
+          // ---- new key group: B = q * s and the bias sum_c q_c (m_c + 3/2 s_c)
           // rows r < 4: scales of channels 32r .., rows 4 + r: minima; 16-byte chunk c of row r
           // sits at chunk c ^ r
           const uint8_t* ks = buf + kOffKM;
@@ -397,12 +404,14 @@ __global__ void __launch_bounds__(kThreadsI, 3)
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
               const int s = 4 * half + j;
-              // q / 4^j (staged so) at channels j, 8+j, 4+j, 12+j of the half
+              // q at channels j, 8+j, 4+j, 12+j of the half
               const float4 x = qps[32 * s];
               split_sel(x.x * sc[j], x.y * sc[8 + j], odd, bk[s][0]);
               split_sel(x.z * sc[4 + j], x.w * sc[12 + j], odd, bk[s][1]);
-              const float part = fmaf(x.x, mn[j], fmaf(x.y, mn[8 + j], fmaf(x.z, mn[4 + j], x.w * mn[12 + j])));
-              bl = fmaf(part, (float)(1 << (2 * j)), bl);  // undo the exact 4^-j
+              bl = fmaf(x.x, fmaf(1.5f, sc[j], mn[j]), bl);
+              bl = fmaf(x.y, fmaf(1.5f, sc[8 + j], mn[8 + j]), bl);
+              bl = fmaf(x.z, fmaf(1.5f, sc[4 + j], mn[4 + j]), bl);
+              bl = fmaf(x.w, fmaf(1.5f, sc[12 + j], mn[12 + j]), bl);
             }
           }
           // lanes (g, t') of head g/2 hold disjoint channels: sum over t', then the
@@ -412,7 +421,7 @@ __global__ void __launch_bounds__(kThreadsI, 3)
           bias = __shfl_sync(0xffffffffu, bl, 8 * t);
         }
 
-        // ---- QK: rows g / g+8 = tokens g / g+8; codes as f16 subnormals
+        // ---- QK: rows g / g+8 = tokens g / g+8; centred codes
         const uint2 w0 = *reinterpret_cast<const uint2*>(buf + kOffK + g * kRow2 + 8 * t);
         const uint2 w1 = *reinterpret_cast<const uint2*>(buf + kOffK + (g + 8) * kRow2 + 8 * t);
         const uint32_t u0[2] = {w0.x, w0.y}, u1[2] = {w1.x, w1.y};
@@ -420,13 +429,13 @@ __global__ void __launch_bounds__(kThreadsI, 3)
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int s = 0; s < 8; ++s) {
-          const uint32_t msk = 0x00030003u << (2 * (s & 3));
-          const int wd = s >> 2;
-          mma_16816(acc, u0[wd] & msk, u1[wd] & msk, s0[wd] & msk, s1[wd] & msk, bk[s][0], bk[s][1]);
+          const int wd = s >> 2, j = s & 3;
+          mma_16816(acc, centred_field(u0[wd], j), centred_field(u1[wd], j), centred_field(s0[wd], j),
+                    centred_field(s1[wd], j), bk[s][0], bk[s][1]);
         }
         const int nvalid = valid ? min(kTI, it.t1 - tok0) : 0;
-        const float lg0 = g < nvalid ? fmaf(acc[0] - acc[1], kTwo24, bias) : -INFINITY;
-        const float lg1 = g + 8 < nvalid ? fmaf(acc[2] - acc[3], kTwo24, bias) : -INFINITY;
+        const float lg0 = g < nvalid ? (acc[0] - acc[1]) + bias : -INFINITY;
+        const float lg1 = g + 8 < nvalid ? (acc[2] - acc[3]) + bias : -INFINITY;
         float p0, p1;
         softmax(lg0, lg1, p0, p1);
 
@@ -496,9 +505,8 @@ __global__ void __launch_bounds__(kThreadsI, 3)
 #pragma unroll
       for (int s = 0; s < 8; ++s) {
         const float4 x = qps[32 * s];
-        const float f = (float)(1 << (2 * (s & 3)));
-        split_sel(x.x * f, x.y * f, odd, bw[s][0]);
-        split_sel(x.z * f, x.w * f, odd, bw[s][1]);
+        split_sel(x.x, x.y, odd, bw[s][0]);
+        split_sel(x.z, x.w, odd, bw[s][1]);
       }
       const int T = it.t1;
       const long long wrow = ((long long)it.b * v.R) * v.Hkv + h;

@@ -17,6 +17,12 @@
 #include "../../include/kvq.h"
 
 namespace kvq {
+// Internal linkage: every translation unit (and every copy of the library loaded
+// into one process) keeps its own table.  Function-local statics of ordinary
+// inline functions would become process-wide unique symbols, shared between two
+// builds of the library loaded side by side, and one build would then skip a
+// kernel attribute that only its own kernels carry.
+namespace {
 
 constexpr int kMaxDevices = 64;
 
@@ -157,4 +163,5 @@ struct NvtxRange {
   NvtxRange& operator=(const NvtxRange&) = delete;
 };
 
+}  // namespace
 }  // namespace kvq

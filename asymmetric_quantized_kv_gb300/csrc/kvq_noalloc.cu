@@ -28,7 +28,7 @@ namespace {
 static __device__ __align__(256) unsigned char g_scratch[KVQ_NOALLOC_SCRATCH_BYTES];
 
 std::mutex g_mutex;
-void* g_scratch_addr[kvq::kMaxDevices] = {nullptr};
+void* g_scratch_addr[64] = {nullptr};
 
 // Device address of g_scratch on the calling thread's current device.
 kvq_status scratch_address(void** out) {
@@ -37,7 +37,7 @@ kvq_status scratch_address(void** out) {
     cudaGetLastError();
     return KVQ_ERR_CUDA;
   }
-  if (dev < 0 || dev >= kvq::kMaxDevices) return KVQ_ERR_UNSUPPORTED;
+  if (dev < 0 || dev >= 64) return KVQ_ERR_UNSUPPORTED;
   std::lock_guard<std::mutex> lock(g_mutex);
   if (!g_scratch_addr[dev]) {
     void* p = nullptr;

@@ -7,6 +7,7 @@
 #include <cuda_runtime.h>
 
 namespace kvq {
+namespace {  // internal linkage: one lookup per translation unit, never shared across libraries
 
 inline PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   // looked up once per process (a function-local static initialises once, even
@@ -24,4 +25,5 @@ inline PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
+}  // namespace
 }  // namespace kvq

@@ -137,3 +137,19 @@ def test_decode_kernel_query_on_the_host(K):
     assert L.kvq_decode_kernel(by(fast), by(fake), None) == K.KVQ_ERR_INVALID_ARG
     empty = K.kvq_cache(None, None, None, None, None, None, None, 1, 1, 1, None)
     assert L.kvq_decode_kernel(by(fast), by(empty), by(out)) == K.KVQ_ERR_INVALID_ARG
+
+
+def test_no_process_wide_unique_symbols(K):
+    """The library's per-device launch settings live in tables with internal
+    linkage.  A GNU unique symbol (what a function-local static of an ordinary
+    inline function becomes) would be shared by every copy of the library loaded
+    into one process, and a second build would then skip kernel attributes that
+    only its own kernels carry."""
+    import shutil
+    import subprocess
+    nm = shutil.which("nm")
+    if nm is None:
+        pytest.skip("nm not available")
+    out = subprocess.run([nm, "-D", K.binding.LIB_PATH], capture_output=True, text=True, check=True).stdout
+    unique = [line for line in out.splitlines() if " u " in line]
+    assert not unique, unique[:5]

@@ -55,11 +55,13 @@ def test_every_stream_of_the_2bit_layer_against_the_oracle(meta):
     """All 128 (sequence, kv-head) streams of the 2-bit 8B layer (16 x (32768 +
     127) tokens) through the oracle: kvq_dequantize bit-exact over every whole
     stream, and all 512 (sequence, query head) outputs within 1e-3 relative L2.
-    The kernel centres the 2-bit value codes (c - 3/2) before the tensor-core
-    product; with uncentred codes the heads that spread their attention lost up
-    to 1.24e-3 to cancellation between the code sum and the minimum sum."""
+    The kernel centres the 2-bit key and value codes (c - 3/2) before the
+    tensor-core products; with uncentred codes the heads that spread their
+    attention lost up to 1.24e-3 to cancellation between the code sums and the
+    minimum sums.  Centred, the worst head sits near 5e-6, so this test holds it
+    to 1e-4."""
     case = FullCase(3, "all", meta=meta)
-    worst, errs = case.check_every_stream()
+    worst, errs = case.check_every_stream(tol=1e-4)
     print(f"\n2-bit layer ({meta} scale/min): worst {worst:.3e}, median {np.median(errs):.3e}, "
           f"above 3e-4: {int((errs > 3e-4).sum())} of {errs.size}")
     del case
@@ -99,6 +101,7 @@ def test_every_sequence(cid):
         err = (torch.linalg.norm(out[b] - ref, dim=1) / torch.linalg.norm(ref, dim=1)).max().item()
         worst = max(worst, err)
         del k, v, p, ref
+    print(f"\nlayer {cid}: worst relative L2 over every (sequence, query head) {worst:.3e}")
     assert worst <= 1e-3, worst
     assert int(case.cache.status.item()) == 0
     del case
