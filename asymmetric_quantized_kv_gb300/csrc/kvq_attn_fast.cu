@@ -25,11 +25,15 @@
 //   softmax: online in base 2, one running max per head, raised lazily (only
 //       when a logit exceeds it by more than 2^8; the common tile needs no
 //       cross-lane reduction).
-//   PV: A = V^T codes (16 channels x 16 tokens) as f16 subnormals c * 2^-24
-//       (high nibbles as 16c * 2^-24; two PRMT and four LOP per MMA), exact in
-//       the tensor cores; the power-of-two factors come out in the epilogue.
-//       B = p * v_scale split hi/lo; the per-token minimum enters through a
-//       running sum of p * v_min.
+//   PV: with v = c * s + m per token (asymmetric INT4, c in 0..15), written as
+//       v = (c - 8) s + (m + 8 s): A = V^T codes (16 channels x 16 tokens) as the
+//       centred f16 values c - 8 (exact: each nibble OR-ed into the mantissa of
+//       1024, then one f16 subtract or fused multiply-add), B = p * v_scale split
+//       hi/lo, and the per-token midpoints m + 8 s enter through a running sum of
+//       p * (m + 8 s).  Centring keeps the tensor-core sum of the order of the
+//       output: with the codes 0..15 as they are, the code sum and the minimum sum
+//       are each many times larger than the output and cancel (the paged layer's
+//       worst head was at 4.1e-4 relative L2 that way, 1.6e-5 centred).
 // Residual-window items use the same steps on the source-dtype rows.
 // Partials (max, sum, unnormalised output) per (item, query head) go to the
 // workspace; the combine kernel merges them.
@@ -117,6 +121,17 @@ __device__ __forceinline__ float2 magic_bias() { return make_float2(8388736.f, 8
 
 __device__ __forceinline__ int sig(int x) { return x ^ ((x >> 1) & 1); }
 
+// The 4-bit code in the low / high nibble of the low byte of each f16 half of w,
+// centred: f16x2 (c - 8), exact.  OR-ing the nibble into the mantissa of 1024
+// gives 1024 + c (low) or 1024 + 16c (high); subtracting 1032, or multiplying by
+// 1/16 and subtracting 72, leaves c - 8.
+__device__ __forceinline__ uint32_t centred_lo(uint32_t w) {
+  return hsub2(and_or(w, 0x000F000Fu, 0x64006400u), 0x64086408u);
+}
+__device__ __forceinline__ uint32_t centred_hi(uint32_t w) {
+  return hfma2(and_or(w, 0x00F000F0u, 0x64006400u), 0x2C002C00u, 0xD480D480u);
+}
+
 // Bounded wait on an mbarrier phase by every lane; a timeout raises the status
 // flag and this thread's `stalled` flag, after which it attempts no further wait
 // (the kernel then runs to completion on whatever the buffers hold).
@@ -193,6 +208,7 @@ __device__ __forceinline__ void rot_split(float2 X, float2 Y, float4 cs, uint32_
 // Online-softmax step for the two logits of this lane (tokens of MMA rows g and
 // g+8, head t), then the PV B operand: P' = p * pscale for k-slots 2t, 2t+1 and
 // 2t+8, 2t+9 of column g (head g/2, hi half for even g, (hi - x) for odd g).
+// m0, m1 = (scale, minimum) of the two tokens; the midpoint m + 8 s goes to A.mb.
 __device__ __forceinline__ void softmax_step(Acc& A, float lg0, float lg1, float2 m0, float2 m1, int g, int t,
                                              uint32_t& b01, uint32_t& b23) {
   if (__any_sync(0xffffffffu, fmaxf(lg0, lg1) > A.m_run + kRescale)) {
@@ -212,7 +228,7 @@ __device__ __forceinline__ void softmax_step(Acc& A, float lg0, float lg1, float
   }
   const float p0 = ex2(lg0 - A.m_run), p1 = ex2(lg1 - A.m_run);
   A.l_loc += p0 + p1;
-  A.mb = fmaf(p1, m1.y, fmaf(p0, m0.y, A.mb));
+  A.mb = fmaf(p1, fmaf(8.f, m1.x, m1.y), fmaf(p0, fmaf(8.f, m0.x, m0.y), A.mb));
   const float pv0 = p0 * m0.x, pv1 = p1 * m1.x;
   const int src0 = 4 * (2 * t) + (g >> 1), src1 = src0 + 4;
   const float x0 = __shfl_sync(0xffffffffu, pv0, src0);
@@ -468,8 +484,8 @@ __global__ void __launch_bounds__(kThreads, 2)
         softmax_step(A, lg0, lg1, m0, m1, g, t, b01, b23);
 
         // ---- PV: A = V^T (channel rows 16g + 2m (+1); k-slots 2t, 2t+1, 2t+8, 2t+9 =
-        //      tokens sig(2t), sig(2t+1), +8) as f16 subnormals: low nibble c -> c * 2^-24
-        //      (rows g), high nibble -> 16c * 2^-24 (rows g+8)
+        //      tokens sig(2t), sig(2t+1), +8) as centred codes c - 8: low nibbles (rows g),
+        //      high nibbles (rows g+8)
         uint2 vw[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
@@ -485,8 +501,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             // byte j of the two tokens' words into the low bytes of the two f16 halves
             const uint32_t sel = 0x4400u + 0x1111u * j;
             const uint32_t ya = prmt(a0, a1, sel), yc = prmt(c0, c1, sel);
-            mma_16816(A.O[4 * w + j], ya & 0x000F000Fu, ya & 0x00F000F0u, yc & 0x000F000Fu, yc & 0x00F000F0u,
-                      b01, b23);
+            mma_16816(A.O[4 * w + j], centred_lo(ya), centred_hi(ya), centred_lo(yc), centred_hi(yc), b01, b23);
           }
         }
 
@@ -534,7 +549,8 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (tok0 + sg >= T) lg0 = -INFINITY;
         if (tok0 + sg + 8 >= T) lg1 = -INFINITY;
         uint32_t b01, b23;
-        softmax_step(A, lg0, lg1, make_float2(1.f, 0.f), make_float2(1.f, 0.f), g, t, b01, b23);
+        // window values enter as they are: scale 1 and a minimum of -8 make the midpoint term 0
+        softmax_step(A, lg0, lg1, make_float2(1.f, -8.f), make_float2(1.f, -8.f), g, t, b01, b23);
         // values as f16 pairs (k-slots 2t+u, 2t+1+u) per channel 16g + 2m (+1)
         long long vi[4];
         bool vok[4];
@@ -564,8 +580,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       A.l_loc += __shfl_xor_sync(0xffffffffu, A.l_loc, o);
       A.mb += __shfl_xor_sync(0xffffffffu, A.mb, o);
     }
-    // quantized values entered as c * 2^-24 (even channels) and 16c * 2^-24 (odd channels)
-    const float f_even = it.window ? 1.f : 16777216.f, f_odd = it.window ? 1.f : 1048576.f;
+    // values entered as they are (window) or centred (c - 8) with the midpoints in A.mb
     const int hq = h * kNRep + t;
     float* dst = part + ((long long)item * v.Hq + hq) * (kD + 4);
     if (g == 0) {
@@ -574,8 +589,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
 #pragma unroll
     for (int m = 0; m < 8; ++m) {
-      const float2 o2 = make_float2(fmaf(A.O[m][0] - A.O[m][1], f_even, A.mb),
-                                    fmaf(A.O[m][2] - A.O[m][3], f_odd, A.mb));
+      const float2 o2 = make_float2((A.O[m][0] - A.O[m][1]) + A.mb, (A.O[m][2] - A.O[m][3]) + A.mb);
       reinterpret_cast<float2*>(dst + 4 + 16 * g)[m] = o2;  // channels 16g + 2m, 16g + 2m + 1
     }
     named_bar_sync(1, kThreads);

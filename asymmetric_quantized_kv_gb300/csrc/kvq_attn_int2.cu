@@ -51,7 +51,8 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kTI = 16;
+constexpr int kTI = 32;  // tokens per tile of a quantized chunk: two 16-token halves (one MMA row block each)
+constexpr int kHT = 16;  // tokens per half tile, and per tile of a residual window
 constexpr int kWarpsI = 4;
 constexpr int kThreadsI = kWarpsI * 32;
 constexpr int kStagesI = 3;
@@ -59,17 +60,19 @@ constexpr int kRepI = 4;
 constexpr int kRow2 = 32;                         // bytes of one token's 2-bit codes
 constexpr int kVMetaRow = 32;                     // (scale x 4, min x 4) fp32 per token
 constexpr int kKMeta2 = 2 * kD * 4;               // scales then minima of one key group (in the page)
-// stage layout (1024-byte aligned): key scales/minima as 8 swizzled rows of 128
-// bytes, then K codes, V codes and V meta rows of the tile ([3][16][32] bytes)
-constexpr int kOffKM = 0;
-constexpr int kOffK = kKMeta2;
-constexpr int kOffV = kOffK + kTI * kRow2;
-constexpr int kOffVM = kOffV + kTI * kRow2;
-constexpr int kTileBytesI = 3 * kTI * kRow2;
+// stage layout (1024-byte aligned): a key group's scales/minima (fp32: 8 swizzled
+// rows of 128 bytes; binary16: 512 linear bytes), then the two half tiles, each
+// K codes [16][32], V codes [16][32] and the value meta rows [16][32 or 16] bytes
 constexpr int kVMetaRow16 = 16;                   // (scale x 4, min x 4) binary16 per token
 constexpr int kKMeta16 = 2 * kD * 2;              // a key group's scales then minima, binary16
-constexpr int kTileBytes16 = 2 * kTI * kRow2 + kTI * kVMetaRow16;
-constexpr int kStageI = 3072;
+constexpr int kOffKM = 0;
+constexpr int kOffH = kKMeta2;                    // first half tile
+constexpr int kOffV = kHT * kRow2;                // V codes within a half tile
+constexpr int kOffVM32 = 2 * kHT * kRow2;         // value meta rows within a half tile
+constexpr int kOffVM16 = 2 * kHT * kRow2;
+constexpr int kHalf32 = 3 * kHT * kRow2;          // fp32 meta: 1536 bytes per half tile
+constexpr int kHalf16 = 2 * kHT * kRow2 + kHT * kVMetaRow16;  // binary16 meta: 1280
+constexpr int kStageI = 4096;
 constexpr uint32_t kSpinI = 1u << 20;
 constexpr float kLog2eI = 1.4426950408889634f;
 constexpr float kRescaleI = 8.f;
@@ -78,11 +81,13 @@ constexpr float kMinitI = -1e30f;
 struct __align__(1024) SmemI2 {
   uint8_t stage[kWarpsI][kStagesI][kStageI];
   float4 qp[kWarpsI][8][32];  // per warp, step s, lane: q * scale * log2(e) at the lane's 4 channels of step s
-  float pex[kWarpsI][2][32];  // p exchange: [token / 8][head * 8 + token % 8]
+  float pex[kWarpsI][4][32];  // p exchange: [token / 8][head * 8 + token % 8]
   uint64_t bar[kWarpsI][kStagesI];
   int valid[kWarpsI][kStagesI];
 };
-static_assert(kStageI % 1024 == 0 && kOffVM + kTI * kVMetaRow <= kStageI, "stages stay 1024-byte aligned");
+static_assert(kStageI % 1024 == 0 && kOffH + 2 * kHalf32 <= kStageI && kOffH + 2 * kHalf16 <= kStageI &&
+                  kHalf32 % 128 == 0 && kHalf16 % 128 == 0,
+              "stages stay 1024-byte aligned and half tiles 128-byte aligned");
 
 // Lane (g, t), step s: its four channels c0..c3 in k-slot order 2t, 2t+1, 2t+8,
 // 2t+9 are 32t + 16(s/4) + {j, 8+j, 4+j, 12+j} with j = s % 4: the code bit
@@ -203,6 +208,8 @@ __global__ void __launch_bounds__(kThreadsI, 3)
   // its logits (tokens g, g+8) go to slots X0, X1 + 8
   const int T0 = tsig(2 * t), T1 = tsig(2 * t + 1), T8 = tsig(2 * t + 8), T9 = tsig(2 * t + 9);
   const int X0 = tsig_inv(g), X1 = tsig_inv(g + 8) - 8;
+  constexpr int kHalf = M16 ? kHalf16 : kHalf32;
+  const uint64_t pol = l2_evict_first();  // the packed stream is read once: evict it first from L2
   const int G = v.kgroup;  // powers of two (checked on the host)
   const int lgP = __ffs(v.P) - 1, lgG = __ffs(G) - 1;
   // a warp takes one kv-head of an item: Hkv units per item, one worker per warp; no cuts
@@ -250,7 +257,6 @@ __global__ void __launch_bounds__(kThreadsI, 3)
       unit = unit_stride0 + (int)__shfl_sync(0xffffffffu, (unsigned)nxt, 0);
       continue;
     }
-    const int ntiles = (it.t1 - it.t0 + kTI - 1) / kTI;
 
     // q * scale * log2(e) of this lane's query head 4h + g/2 at its step channels
     {
@@ -297,6 +303,28 @@ __global__ void __launch_bounds__(kThreadsI, 3)
       p1 = ex2(lg1 - m_run);
       l_loc += p0 + p1;
     };
+    // softmax step for the logits of tokens g, g+8 of both half tiles (head t)
+    auto softmax4 = [&](const float (&lg)[4], float (&p)[4]) {
+      float mx = fmaxf(fmaxf(lg[0], lg[1]), fmaxf(lg[2], lg[3]));
+      if (__any_sync(0xffffffffu, mx > m_run + kRescaleI)) {
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+        const float mn = fmaxf(m_run, mx);
+        const float alpha = ex2(m_run - mn);
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+          O[m][0] *= alpha; O[m][1] *= alpha; O[m][2] *= alpha; O[m][3] *= alpha;
+        }
+        l_loc *= alpha;
+#pragma unroll
+        for (int G4 = 0; G4 < 4; ++G4) mb[G4] *= alpha;
+        m_run = mn;
+      }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) p[e] = ex2(lg[e] - m_run);
+      l_loc += (p[0] + p[1]) + (p[2] + p[3]);
+    };
     // p of head g/2 at k-slots 2t, 2t+1 (x01) and 2t+8, 2t+9 (x89)
     auto exchange = [&](float p0, float p1, float2& x01, float2& x89) {
       __syncwarp();
@@ -308,50 +336,66 @@ __global__ void __launch_bounds__(kThreadsI, 3)
     };
 
     if (!it.window) {
-      // ======================= quantized chunk
+      // ======================= quantized chunk: 32-token tiles (two 16-token halves)
       const int32_t* bt = v.block_table + (long long)it.b * v.max_pages;
-      const long long head_off = (long long)h * v.head_bytes;
-      auto issue = [&](int i, int pid) {
+      const int ntiles = (it.t1 - it.t0 + kTI - 1) / kTI;
+      const uint8_t* pages_h = v.pages + (long long)h * v.head_bytes;
+      // lane 0: the page ids of the next tile to load (the second half's page when P is 16)
+      int pf0 = 0, pf1 = 0;
+      auto page_pair = [&](int i, int& p0, int& p1) {
+        const int tok = it.t0 + i * kTI;
+        p0 = bt[tok >> lgP];
+        // 16-token pages: the second half sits in the next page, unless it lies past the item's end
+        // (its rows are then masked, and the table entry there need not be a page)
+        p1 = (v.P >= kTI || tok + kHT >= it.t1) ? p0 : bt[(tok + kHT) >> lgP];
+      };
+      auto issue = [&](int i, int pid0, int pid1) {
         const int stage = lstage;
         if (++lstage == kStagesI) lstage = 0;
         ++n_loaded;
         const int tok = it.t0 + i * kTI;
         uint64_t* bar = &sm.bar[warp][stage];
-        const bool ok = pid >= 0 && pid < v.n_pages;
+        const bool ok = pid0 >= 0 && pid0 < v.n_pages && pid1 >= 0 && pid1 < v.n_pages;
         sm.valid[warp][stage] = ok;
         if (!ok) {
           atomicOr(v.status, KVQ_DEV_BAD_PAGE);
           mbar_arrive(bar);
           return;
         }
-        const int slot = tok & (v.P - 1);
+        const int slot0 = tok & (v.P - 1), slot1 = (tok + kHT) & (v.P - 1);
         const bool gstart = (tok & (G - 1)) == 0;
         uint8_t* dst = sm.stage[warp][stage];
-        const uint64_t pol = l2_evict_first();
         if constexpr (M16) {
-          // codes by one 2-section tensor copy; value rows and key meta by bulk copies
-          mbar_arrive_expect_tx(bar, kTileBytes16 + (gstart ? kKMeta16 : 0));
-          tma_load_5d_hint(dst + kOffK, &tmc, 0, slot, 0, h, pid, bar, pol);
-          const uint8_t* hb = v.pages + (long long)pid * v.page_bytes + head_off;
-          bulk_g2s_hint(dst + kOffVM, hb + v.off_vm + slot * kVMetaRow16, kTI * kVMetaRow16, bar, pol);
+          // codes of each half by one 2-section tensor copy, its value rows and the key meta by bulk copies
+          mbar_arrive_expect_tx(bar, 2 * kHalf16 + (gstart ? kKMeta16 : 0));
+          tma_load_5d_hint(dst + kOffH, &tmc, 0, slot0, 0, h, pid0, bar, pol);
+          tma_load_5d_hint(dst + kOffH + kHalf16, &tmc, 0, slot1, 0, h, pid1, bar, pol);
+          bulk_g2s_hint(dst + kOffH + kOffVM16, pages_h + (long long)pid0 * v.page_bytes + v.off_vm +
+                        slot0 * kVMetaRow16, kHT * kVMetaRow16, bar, pol);
+          bulk_g2s_hint(dst + kOffH + kHalf16 + kOffVM16, pages_h + (long long)pid1 * v.page_bytes + v.off_vm +
+                        slot1 * kVMetaRow16, kHT * kVMetaRow16, bar, pol);
           if (gstart)
-            bulk_g2s_hint(dst + kOffKM, hb + v.off_km + (v.P >= G ? slot >> lgG : 0) * kKMeta16, kKMeta16, bar,
-                          pol);
+            bulk_g2s_hint(dst + kOffKM, pages_h + (long long)pid0 * v.page_bytes + v.off_km +
+                          (v.P >= G ? slot0 >> lgG : 0) * kKMeta16, kKMeta16, bar, pol);
         } else {
-          mbar_arrive_expect_tx(bar, kTileBytesI + (gstart ? kKMeta2 : 0));
-          tma_load_5d_hint(dst + kOffK, &tmc, 0, slot, 0, h, pid, bar, pol);
+          mbar_arrive_expect_tx(bar, 2 * kHalf32 + (gstart ? kKMeta2 : 0));
+          tma_load_5d_hint(dst + kOffH, &tmc, 0, slot0, 0, h, pid0, bar, pol);
+          tma_load_5d_hint(dst + kOffH + kHalf32, &tmc, 0, slot1, 0, h, pid1, bar, pol);
           if (gstart) {
-            const long long byte0 = (long long)pid * v.page_bytes + head_off + v.off_km +
-                                    (long long)(v.P >= G ? slot >> lgG : 0) * kKMeta2;
+            const long long byte0 = (long long)pid0 * v.page_bytes + (long long)h * v.head_bytes + v.off_km +
+                                    (long long)(v.P >= G ? slot0 >> lgG : 0) * kKMeta2;
             tma_load_2d_hint(dst + kOffKM, &tmk, 0, (int)(byte0 >> 7), bar, pol);
           }
         }
       };
-      int pf = 0;
       if (lane == 0 && !stalled) {
         fence_proxy_async();
-        for (int i = 0; i < min(kStagesI, ntiles); ++i) issue(i, bt[(it.t0 + i * kTI) >> lgP]);
-        if (kStagesI < ntiles) pf = bt[(it.t0 + kStagesI * kTI) >> lgP];
+        for (int i = 0; i < min(kStagesI, ntiles); ++i) {
+          int p0, p1;
+          page_pair(i, p0, p1);
+          issue(i, p0, p1);
+        }
+        if (kStagesI < ntiles) page_pair(kStagesI, pf0, pf1);
       }
       __syncwarp();
 
@@ -377,125 +421,150 @@ __global__ void __launch_bounds__(kThreadsI, 3)
         const int tok0 = it.t0 + i * kTI;
 
         if ((tok0 & (G - 1)) == 0) {
-          // ---- new key group: B = q * s and the bias sum_c q_c (m_c + 3/2 s_c)
-          // rows r < 4: scales of channels 32r .., rows 4 + r: minima; 16-byte chunk c of row r
-          // sits at chunk c ^ r
+          // ---- new key group: B = q * s and the bias sum_c q_c (m_c + 3/2 s_c).  Lanes g and g ^ 1
+          // (lane ^ 4) hold the same channels for the hi and the (hi - x) column of one query head:
+          // the even lane splits steps 0..3 (channels 32t .. 32t + 15), the odd lane steps 4..7
+          // (32t + 16 .. 32t + 31), and each hands the partner the half of the split it lacks.
           const uint8_t* ks = buf + kOffKM;
+          const int hm = odd ? 1 : 0;
+          float sc[16], mn[16];
+#pragma unroll
+          for (int k4 = 0; k4 < 4; ++k4) {
+            float4 a, b;
+            if constexpr (M16) {
+              // linear halves: scales of channels 32t + 16 hm + 4 k4 .. at byte 2 * channel, minima after
+              const int off = 64 * t + 32 * hm + 8 * k4;
+              a = halves4(*reinterpret_cast<const uint2*>(ks + off));
+              b = halves4(*reinterpret_cast<const uint2*>(ks + 2 * kD + off));
+            } else {
+              // rows r < 4: scales of channels 32r .., rows 4 + r: minima; 16-byte chunk c of row r at c ^ r
+              const int c = 4 * hm + k4;
+              a = *reinterpret_cast<const float4*>(ks + t * 128 + ((c ^ t) << 4));
+              b = *reinterpret_cast<const float4*>(ks + (4 + t) * 128 + ((c ^ (4 + t)) << 4));
+            }
+            sc[4 * k4] = a.x; sc[4 * k4 + 1] = a.y; sc[4 * k4 + 2] = a.z; sc[4 * k4 + 3] = a.w;
+            mn[4 * k4] = b.x; mn[4 * k4 + 1] = b.y; mn[4 * k4 + 2] = b.z; mn[4 * k4 + 3] = b.w;
+          }
           float bl = 0.f;
 #pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            float sc[16], mn[16];
-#pragma unroll
-            for (int k4 = 0; k4 < 4; ++k4) {
-              float4 a, b;
-              if constexpr (M16) {
-                // linear halves: scales of channels 32t + 16 half + 4 k4 .. at byte 2 * channel, minima after
-                const int off = 64 * t + 32 * half + 8 * k4;
-                a = halves4(*reinterpret_cast<const uint2*>(ks + off));
-                b = halves4(*reinterpret_cast<const uint2*>(ks + 2 * kD + off));
-              } else {
-                const int c = 4 * half + k4;
-                a = *reinterpret_cast<const float4*>(ks + t * 128 + ((c ^ t) << 4));
-                b = *reinterpret_cast<const float4*>(ks + (4 + t) * 128 + ((c ^ (4 + t)) << 4));
-              }
-              sc[4 * k4] = a.x; sc[4 * k4 + 1] = a.y; sc[4 * k4 + 2] = a.z; sc[4 * k4 + 3] = a.w;
-              mn[4 * k4] = b.x; mn[4 * k4 + 1] = b.y; mn[4 * k4 + 2] = b.z; mn[4 * k4 + 3] = b.w;
-            }
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const int s = 4 * half + j;
-              // q at channels j, 8+j, 4+j, 12+j of the half
-              const float4 x = qps[32 * s];
-              split_sel(x.x * sc[j], x.y * sc[8 + j], odd, bk[s][0]);
-              split_sel(x.z * sc[4 + j], x.w * sc[12 + j], odd, bk[s][1]);
-              bl = fmaf(x.x, fmaf(1.5f, sc[j], mn[j]), bl);
-              bl = fmaf(x.y, fmaf(1.5f, sc[8 + j], mn[8 + j]), bl);
-              bl = fmaf(x.z, fmaf(1.5f, sc[4 + j], mn[4 + j]), bl);
-              bl = fmaf(x.w, fmaf(1.5f, sc[12 + j], mn[12 + j]), bl);
-            }
+          for (int j = 0; j < 4; ++j) {
+            // q at channels j, 8+j, 4+j, 12+j of this lane's half (step 4 hm + j)
+            const float4 x = qps[32 * (4 * hm + j)];
+            const float2 pa = __fmul2_rn(make_float2(x.x, x.y), make_float2(sc[j], sc[8 + j]));
+            const float2 pb = __fmul2_rn(make_float2(x.z, x.w), make_float2(sc[4 + j], sc[12 + j]));
+            uint32_t ha, na, hb2, nb;
+            split_hi_neglo(pa.x, pa.y, ha, na);
+            split_hi_neglo(pb.x, pb.y, hb2, nb);
+            // the even lane keeps hi and sends (hi - x); the odd lane the other way round
+            const uint32_t ra = __shfl_xor_sync(0xffffffffu, odd ? ha : na, 4);
+            const uint32_t rb = __shfl_xor_sync(0xffffffffu, odd ? hb2 : nb, 4);
+            bk[j][0] = odd ? ra : ha;
+            bk[j][1] = odd ? rb : hb2;
+            bk[4 + j][0] = odd ? na : ra;
+            bk[4 + j][1] = odd ? nb : rb;
+            bl = fmaf(x.x, fmaf(1.5f, sc[j], mn[j]), bl);
+            bl = fmaf(x.y, fmaf(1.5f, sc[8 + j], mn[8 + j]), bl);
+            bl = fmaf(x.z, fmaf(1.5f, sc[4 + j], mn[4 + j]), bl);
+            bl = fmaf(x.w, fmaf(1.5f, sc[12 + j], mn[12 + j]), bl);
           }
-          // lanes (g, t') of head g/2 hold disjoint channels: sum over t', then the
-          // logit lanes (head t) take it from lane 8t
+          // the head's 128 channels: this lane's 16, its partner's 16 (lane ^ 4), the other t (^1, ^2);
+          // the logit lanes (head t) take it from lane 8t
+          bl += __shfl_xor_sync(0xffffffffu, bl, 4);
           bl += __shfl_xor_sync(0xffffffffu, bl, 1);
           bl += __shfl_xor_sync(0xffffffffu, bl, 2);
           bias = __shfl_sync(0xffffffffu, bl, 8 * t);
         }
 
-        // ---- QK: rows g / g+8 = tokens g / g+8; centred codes
-        const uint2 w0 = *reinterpret_cast<const uint2*>(buf + kOffK + g * kRow2 + 8 * t);
-        const uint2 w1 = *reinterpret_cast<const uint2*>(buf + kOffK + (g + 8) * kRow2 + 8 * t);
-        const uint32_t u0[2] = {w0.x, w0.y}, u1[2] = {w1.x, w1.y};
-        const uint32_t s0[2] = {w0.x >> 8, w0.y >> 8}, s1[2] = {w1.x >> 8, w1.y >> 8};
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int s = 0; s < 8; ++s) {
-          const int wd = s >> 2, j = s & 3;
-          mma_16816(acc, centred_field(u0[wd], j), centred_field(u1[wd], j), centred_field(s0[wd], j),
-                    centred_field(s1[wd], j), bk[s][0], bk[s][1]);
-        }
+        // ---- QK per half: rows g / g+8 = tokens 16 hf + g / + 8; centred codes
         const int nvalid = valid ? min(kTI, it.t1 - tok0) : 0;
-        const float lg0 = g < nvalid ? (acc[0] - acc[1]) + bias : -INFINITY;
-        const float lg1 = g + 8 < nvalid ? (acc[2] - acc[3]) + bias : -INFINITY;
-        float p0, p1;
-        softmax(lg0, lg1, p0, p1);
+        float lg[4];
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          const uint8_t* hb = buf + kOffH + hf * kHalf;
+          const uint2 w0 = *reinterpret_cast<const uint2*>(hb + g * kRow2 + 8 * t);
+          const uint2 w1 = *reinterpret_cast<const uint2*>(hb + (g + 8) * kRow2 + 8 * t);
+          const uint32_t u0[2] = {w0.x, w0.y}, u1[2] = {w1.x, w1.y};
+          const uint32_t s0[2] = {w0.x >> 8, w0.y >> 8}, s1[2] = {w1.x >> 8, w1.y >> 8};
+          float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int s = 0; s < 8; ++s) {
+            const int wd = s >> 2, j = s & 3;
+            mma_16816(acc, centred_field(u0[wd], j), centred_field(u1[wd], j), centred_field(s0[wd], j),
+                      centred_field(s1[wd], j), bk[s][0], bk[s][1]);
+          }
+          lg[2 * hf] = kHT * hf + g < nvalid ? (acc[0] - acc[1]) + bias : -INFINITY;
+          lg[2 * hf + 1] = kHT * hf + g + 8 < nvalid ? (acc[2] - acc[3]) + bias : -INFINITY;
+        }
+        float p[4];
+        softmax4(lg, p);
 
-        // ---- value minima of tokens g, g+8 (head t) and scales of the B tokens
-        // per-token value row: 4 scales then 4 minima (fp32, or binary16 in M16)
-        auto vrow = [&](int tok, int part) -> float4 {
+        // ---- value rows: per token 4 scales then 4 minima (fp32, or binary16 in M16)
+        auto vrow = [&](int hf, int tok, int part) -> float4 {
           if constexpr (M16) {
-            return halves4(*reinterpret_cast<const uint2*>(buf + kOffVM + tok * kVMetaRow16 + 8 * part));
+            return halves4(*reinterpret_cast<const uint2*>(buf + kOffH + hf * kHalf16 + kOffVM16 + tok * kVMetaRow16 +
+                                                           8 * part));
           } else {
-            return reinterpret_cast<const float4*>(buf + kOffVM + tok * kVMetaRow)[part];
+            return reinterpret_cast<const float4*>(buf + kOffH + hf * kHalf32 + kOffVM32 + tok * kVMetaRow)[part];
           }
         };
         if (valid) {
-          // group midpoints m + 3/2 s of tokens g, g+8
-          const float4 n0 = vrow(g, 1), z0 = vrow(g, 0);
-          const float4 n1 = vrow(g + 8, 1), z1 = vrow(g + 8, 0);
-          mb[0] = fmaf(p0, fmaf(1.5f, z0.x, n0.x), fmaf(p1, fmaf(1.5f, z1.x, n1.x), mb[0]));
-          mb[1] = fmaf(p0, fmaf(1.5f, z0.y, n0.y), fmaf(p1, fmaf(1.5f, z1.y, n1.y), mb[1]));
-          mb[2] = fmaf(p0, fmaf(1.5f, z0.z, n0.z), fmaf(p1, fmaf(1.5f, z1.z, n1.z), mb[2]));
-          mb[3] = fmaf(p0, fmaf(1.5f, z0.w, n0.w), fmaf(p1, fmaf(1.5f, z1.w, n1.w), mb[3]));
-        }
-        float2 x01, x89;
-        exchange(p0, p1, x01, x89);
-        const float4 sa = vrow(T0, 0);
-        const float4 sb = vrow(T1, 0);
-        const float4 sc8 = vrow(T8, 0);
-        const float4 sd = vrow(T9, 0);
-        const float sA[4] = {sa.x, sa.y, sa.z, sa.w}, sB[4] = {sb.x, sb.y, sb.z, sb.w};
-        const float sC[4] = {sc8.x, sc8.y, sc8.z, sc8.w}, sD[4] = {sd.x, sd.y, sd.z, sd.w};
-
-        // ---- PV, value group G: byte 8G + g of tokens T0, T1 (ya) and T8, T9 (yc)
-        const uint8_t* vc = buf + kOffV;
-        const int gb = g & 3;
-        const uint32_t sel = gb * 0x0011u + (4 + gb) * 0x1100u;
-        const int woff = 4 * (g >> 2);
+          // group midpoints m + 3/2 s of tokens g, g+8 of both halves
 #pragma unroll
-        for (int G4 = 0; G4 < 4; ++G4) {
-          uint32_t b01, b89;
-          split_sel(x01.x * sA[G4], x01.y * sB[G4], odd, b01);
-          split_sel(x89.x * sC[G4], x89.y * sD[G4], odd, b89);
-          const int off = 8 * G4 + woff;
-          const uint32_t wa = *reinterpret_cast<const uint32_t*>(vc + T0 * kRow2 + off);
-          const uint32_t wb = *reinterpret_cast<const uint32_t*>(vc + T1 * kRow2 + off);
-          const uint32_t wc = *reinterpret_cast<const uint32_t*>(vc + T8 * kRow2 + off);
-          const uint32_t wd = *reinterpret_cast<const uint32_t*>(vc + T9 * kRow2 + off);
-          const uint32_t ya = prmt(wa, wb, sel), yc = prmt(wc, wd, sel);
-          // m-block 2G4: rows g / g+8 = channels 32G4 + 4g + 0 / + 1 (code fields 0, 1)
-          mma_16816(O[2 * G4], centred_code<0>(ya), centred_code<1>(ya), centred_code<0>(yc), centred_code<1>(yc),
-                    b01, b89);
-          // m-block 2G4+1: channels 32G4 + 4g + 2 / + 3 (code fields 2, 3)
-          mma_16816(O[2 * G4 + 1], centred_code<2>(ya), centred_code<3>(ya), centred_code<2>(yc),
-                    centred_code<3>(yc), b01, b89);
+          for (int e = 0; e < 4; ++e) {
+            const float4 n = vrow(e >> 1, g + 8 * (e & 1), 1), z = vrow(e >> 1, g + 8 * (e & 1), 0);
+            mb[0] = fmaf(p[e], fmaf(1.5f, z.x, n.x), mb[0]);
+            mb[1] = fmaf(p[e], fmaf(1.5f, z.y, n.y), mb[1]);
+            mb[2] = fmaf(p[e], fmaf(1.5f, z.z, n.z), mb[2]);
+            mb[3] = fmaf(p[e], fmaf(1.5f, z.w, n.w), mb[3]);
+          }
+        }
+        // p of head g/2 at the k-slots of both halves
+        __syncwarp();
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          pe[64 * hf + t * 8 + X0] = p[2 * hf];
+          pe[64 * hf + 32 + t * 8 + X1] = p[2 * hf + 1];
+        }
+        __syncwarp();
+
+        // ---- PV per half (k block of 16 tokens), value group G: byte 8G + g of tokens T0, T1 (ya), T8, T9 (yc)
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          const float2 x01 = *reinterpret_cast<const float2*>(pe + 64 * hf + (g >> 1) * 8 + 2 * t);
+          const float2 x89 = *reinterpret_cast<const float2*>(pe + 64 * hf + 32 + (g >> 1) * 8 + 2 * t);
+          const float4 sa = vrow(hf, T0, 0), sb = vrow(hf, T1, 0), sc8 = vrow(hf, T8, 0), sd = vrow(hf, T9, 0);
+          const float sA[4] = {sa.x, sa.y, sa.z, sa.w}, sB[4] = {sb.x, sb.y, sb.z, sb.w};
+          const float sC[4] = {sc8.x, sc8.y, sc8.z, sc8.w}, sD[4] = {sd.x, sd.y, sd.z, sd.w};
+          const uint8_t* vc = buf + kOffH + hf * kHalf + kOffV;
+          const int gb = g & 3;
+          const uint32_t sel = gb * 0x0011u + (4 + gb) * 0x1100u;
+          const int woff = 4 * (g >> 2);
+#pragma unroll
+          for (int G4 = 0; G4 < 4; ++G4) {
+            uint32_t b01, b89;
+            split_sel(x01.x * sA[G4], x01.y * sB[G4], odd, b01);
+            split_sel(x89.x * sC[G4], x89.y * sD[G4], odd, b89);
+            const int off = 8 * G4 + woff;
+            const uint32_t wa = *reinterpret_cast<const uint32_t*>(vc + T0 * kRow2 + off);
+            const uint32_t wb = *reinterpret_cast<const uint32_t*>(vc + T1 * kRow2 + off);
+            const uint32_t wc = *reinterpret_cast<const uint32_t*>(vc + T8 * kRow2 + off);
+            const uint32_t wd = *reinterpret_cast<const uint32_t*>(vc + T9 * kRow2 + off);
+            const uint32_t ya = prmt(wa, wb, sel), yc = prmt(wc, wd, sel);
+            // m-block 2G4: rows g / g+8 = channels 32G4 + 4g + 0 / + 1 (code fields 0, 1)
+            mma_16816(O[2 * G4], centred_code<0>(ya), centred_code<1>(ya), centred_code<0>(yc),
+                      centred_code<1>(yc), b01, b89);
+            // m-block 2G4+1: channels 32G4 + 4g + 2 / + 3 (code fields 2, 3)
+            mma_16816(O[2 * G4 + 1], centred_code<2>(ya), centred_code<3>(ya), centred_code<2>(yc),
+                      centred_code<3>(yc), b01, b89);
+          }
         }
 
         // ---- release the stage and refill it
         __syncwarp();
         if (lane == 0 && i + kStagesI < ntiles && !stalled) {
           fence_proxy_async();
-          issue(i + kStagesI, pf);
-          if (i + kStagesI + 1 < ntiles) pf = bt[(it.t0 + (i + kStagesI + 1) * kTI) >> lgP];
+          issue(i + kStagesI, pf0, pf1);
+          if (i + kStagesI + 1 < ntiles) page_pair(i + kStagesI + 1, pf0, pf1);
         }
         __syncwarp();
       }
@@ -510,8 +579,9 @@ __global__ void __launch_bounds__(kThreadsI, 3)
       }
       const int T = it.t1;
       const long long wrow = ((long long)it.b * v.R) * v.Hkv + h;
+      const int ntiles = (it.t1 - it.t0 + kHT - 1) / kHT;
       for (int i = 0; i < ntiles; ++i) {
-        const int tok0 = it.t0 + i * kTI;
+        const int tok0 = it.t0 + i * kHT;
         float acc[4] = {0.f, 0.f, 0.f, 0.f}, accn[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
@@ -625,7 +695,7 @@ bool int2_shape_eligible(const KvqView& v) {
          v.D == kD && v.n_rep == kRepI && v.kfmt == KVQ_INT2 && v.kmode == KVQ_ASYM_MINMAX &&
          v.kaxis == KVQ_PER_CHANNEL && v.vfmt == KVQ_INT2 && v.vmode == KVQ_ASYM_MINMAX &&
          v.vaxis == KVQ_PER_TOKEN && v.vgroup == 32 && v.rope_pre == 0 && pow2_g && v.kgroup >= kTI &&
-         v.P >= kTI && (v.P & (v.P - 1)) == 0 && v.batch <= 4096;
+         v.P >= kHT && (v.P & (v.P - 1)) == 0 && v.batch <= 4096;
 }
 
 bool int2_eligible(const KvqView& v) {
@@ -641,7 +711,7 @@ kvq_status launch_int2(const KvqView& v, const void* q, float* out, float scale,
     const cuuint64_t dims[5] = {(cuuint64_t)kRow2, (cuuint64_t)v.P, nsec, (cuuint64_t)v.Hkv, (cuuint64_t)v.n_pages};
     const cuuint64_t strides[4] = {(cuuint64_t)kRow2, (cuuint64_t)v.P * kRow2, (cuuint64_t)v.head_bytes,
                                    (cuuint64_t)v.page_bytes};
-    const cuuint32_t box[5] = {(cuuint32_t)kRow2, (cuuint32_t)kTI, nsec, 1, 1};
+    const cuuint32_t box[5] = {(cuuint32_t)kRow2, (cuuint32_t)kHT, nsec, 1, 1};
     const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
     if (tensor_map_encoder()(&tmc, CU_TENSOR_MAP_DATA_TYPE_UINT8, 5, v.pages, dims, strides, box, estr,
                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,

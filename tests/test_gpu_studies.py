@@ -95,3 +95,111 @@ def test_fp8_unit_scale_clipping_on_the_gpu():
         errs[name] = float(np.mean(e))
     assert errs["e4m3_unit"] > 2.0 * errs["e5m2_unit"], errs
     assert errs["e5m2_unit"] > errs["e4m3_calibrated"], errs
+
+
+# ------------------- attention agreement on caches the library filled (full stream lengths)
+
+def _agreement_caches(cid, specs, seqs, gen_seed=21):
+    """Streams of workload `cid` (its lengths, heads and outlier channels, drawn on
+    the device) for the sequences `seqs`, appended through kvq_quantize_append into
+    one cache per key spec.  Returns (keys [b][T, Hkv, D] float64 as appended,
+    {name: dequantized keys [b][T, Hkv, D] from kvq_dequantize}, q [B, Hq, D])."""
+    import dataclasses
+    import asymmetric_quantized_kv_gb300 as K
+    base = W.WORKLOADS[cid]
+    lens = [int(W.lengths(base)[b]) for b in seqs]
+    w = dataclasses.replace(base, batch=len(seqs))
+    H, D, Hq = w.num_kv_heads, w.head_dim, w.num_q_heads
+    dev = torch.device("cuda")
+    g = torch.Generator(device=dev)
+    g.manual_seed(gen_seed)
+    scale = W.torch_outlier_scale(w, dev)
+    Tm = max(lens)
+    ks, vs = W.torch_kv_chunk(w, g, len(seqs), Tm, scale, dev)
+    per = torch.tensor(lens, dtype=torch.int32, device=dev)
+    deq = {}
+    for name, (kspec, vspec, R, P, rope) in specs.items():
+        cfg = K.make_config(Hq, H, D, kspec, vspec, R, P, rope, THETA, K.KVQ_BF16)
+        maxp = (Tm + P - 1) // P + 1
+        cache = K.PagedKVCache(cfg, len(seqs), maxp)
+        for t0 in range(0, Tm, 4096):
+            n = min(4096, Tm - t0)
+            take = torch.clamp(per - t0, 0, n).to(torch.int32)
+            cache.append(ks[:, t0:t0 + n].contiguous(), vs[:, t0:t0 + n].contiguous(), take)
+        torch.cuda.synchronize()
+        assert int(cache.status.item()) == 0
+        deq[name] = [cache.dequantize(b, 0, T)[0].double() for b, T in enumerate(lens)]
+        del cache
+    keys = [ks[b, :T].double() for b, T in enumerate(lens)]
+    q = torch.randn(len(seqs), Hq, D, generator=g, device=dev).to(torch.bfloat16).double()
+    return keys, deq, q
+
+
+def _rope_t(k):
+    """Rotate keys [T, H, D] (float64, on the device) to their positions."""
+    T, _, D = k.shape
+    inv = THETA ** (-(2.0 * torch.arange(D // 2, dtype=torch.float64, device=k.device)) / D)
+    ang = torch.arange(T, dtype=torch.float64, device=k.device)[:, None] * inv[None, :]
+    c, s = torch.cos(ang)[:, None, :], torch.sin(ang)[:, None, :]
+    out = torch.empty_like(k)
+    out[..., 0::2] = k[..., 0::2] * c - k[..., 1::2] * s
+    out[..., 1::2] = k[..., 0::2] * s + k[..., 1::2] * c
+    return out
+
+
+def _stream_metrics(keys, deq, q, rope, k=32):
+    """Per (sequence, kv-head): mean over its query heads of KL(p_fp || p_q),
+    top-k overlap and top-k rank agreement, p from float64 softmax(q k / sqrt(D))."""
+    from oracle import studies as S
+    H, D, Hq = keys[0].shape[1], keys[0].shape[2], q.shape[1]
+    rep = Hq // H
+    out = []
+    for b, (kf, kq) in enumerate(zip(keys, deq)):
+        if rope:
+            kf, kq = _rope_t(kf), _rope_t(kq)
+        for h in range(H):
+            qh = q[b, h * rep:(h + 1) * rep]
+            pf = torch.softmax(qh @ kf[:, h].T / D ** 0.5, dim=-1).cpu().numpy()
+            pq = torch.softmax(qh @ kq[:, h].T / D ** 0.5, dim=-1).cpu().numpy()
+            out.append((S.kl_rows(pf, pq).mean(), S.topk_overlap(pf, pq, k).mean(),
+                        S.topk_rank_agreement(pf, pq, k).mean()))
+    return np.array(out)
+
+
+@pytest.mark.parametrize("cid", [3, 5])
+def test_attention_agreement_on_the_library_cache_at_full_length(cid):
+    """Per-head attention KL and top-k agreement ("FP8 KV Cache Quantization: Why
+    Keys Break Before Values", section "Why doesn't perplexity catch KV cache
+    quantization damage?") from caches the library filled and dequantized, on the
+    layers' whole streams: the 8B layer's two first sequences (32,895 tokens, all
+    8 kv-heads) and the paged layer's longest, a middle and its shortest sequence
+    (pre-RoPE keys, rotated after dequantization).  The orderings the oracle study
+    pins on 4096-token prefixes hold here: per-channel keys keep the attention
+    closer than per-token keys at 2 and 4 bits (lower KL, higher top-32 overlap),
+    and the per-channel KL falls as the bits grow."""
+    A, S_, CH, TOK = O.ASYM, O.SYM, O.PER_CHANNEL, O.PER_TOKEN
+    if cid == 3:
+        v2 = (O.INT2, A, TOK, 32)
+        specs = {"ch2": ((O.INT2, A, CH, 32), v2, 128, 256, 0), "tok2": ((O.INT2, A, TOK, 32), v2, 128, 256, 0),
+                 "ch4": ((O.INT4, A, CH, 32), v2, 128, 256, 0), "tok4": ((O.INT4, A, TOK, 32), v2, 128, 256, 0),
+                 "ch8": ((O.INT8, S_, CH, 32), v2, 128, 256, 0)}
+        seqs, rope = [0, 1], False
+    else:
+        v4 = (O.INT4, A, TOK, 128)
+        specs = {"ch2": ((O.INT2, A, CH, 64), v4, 64, 16, 1), "tok2": ((O.INT2, A, TOK, 0), v4, 64, 16, 1),
+                 "ch4": ((O.INT4, A, CH, 64), v4, 64, 16, 1), "tok4": ((O.INT4, A, TOK, 0), v4, 64, 16, 1),
+                 "ch8": ((O.INT8, S_, CH, 64), v4, 64, 16, 1)}
+        lens = W.lengths(W.WORKLOADS[5])
+        order = np.argsort(lens)
+        seqs, rope = [int(order[-1]), int(order[len(order) // 2]), int(order[0])], True
+    keys, deq, q = _agreement_caches(cid, specs, seqs)
+    m = {name: _stream_metrics(keys, d, q, rope) for name, d in deq.items()}
+    print(f"\nlayer {cid} (KL, top-32 overlap, rank agreement; mean over streams): " +
+          ", ".join(f"{n} {v[:, 0].mean():.3g}/{v[:, 1].mean():.3f}/{v[:, 2].mean():.3f}" for n, v in m.items()))
+    for bits in ("2", "4"):
+        ch, tok = m["ch" + bits], m["tok" + bits]
+        assert ch[:, 0].mean() < tok[:, 0].mean(), bits  # KL
+        assert ch[:, 1].mean() > tok[:, 1].mean(), bits  # top-32 overlap
+    assert (m["ch2"][:, 0] > m["tok2"][:, 0]).mean() <= 0.25  # per stream, at most a quarter flip at 2 bits
+    assert m["ch2"][:, 0].mean() > m["ch4"][:, 0].mean() > m["ch8"][:, 0].mean() > 0.0
+    assert m["ch8"][:, 1].mean() >= 0.9
