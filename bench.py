@@ -646,6 +646,14 @@ def run_gpu(args, spec, rank, world):
                 clocks=clock_info, status=status, e2e=e2e, lens=cur)
 
 
+def kcycles(us, clocks):
+    """Thousands of SM cycles at the median SM clock sampled during the timed
+    region (time x clock: comparable across runs whose clocks differ)."""
+    if not clocks or not clocks.get("sm_mhz"):
+        return None
+    return us * clocks["sm_mhz"] / 1e3
+
+
 def layer_line(args, cid, peak, peak_kind):
     """Decode-only measurement of another headline layer in the same process
     (the 2-bit 8B layer, the FP8 70B layer): its own cache, events around every
@@ -669,7 +677,8 @@ def layer_line(args, cid, peak, peak_kind):
                          "kernel": f"kvq_decode_attention: {SPLIT_KERNEL[cid]} + combine (timed together)",
                          "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)" if peak_kind == "measured"
                          else "fallback 6.8 TB/s"},
-            "gpu_launches": args.steps * LAUNCHES_ATTENTION, "clocks": r["clocks"], "device_status": r["status"]}
+            "gpu_launches": args.steps * LAUNCHES_ATTENTION, "clocks": r["clocks"], "device_status": r["status"],
+            "kcycles_per_call": kcycles(att_ms * 1e3, r["clocks"])}
 
 
 def main():
@@ -779,6 +788,7 @@ def main():
         "e2e": r["e2e"],
         "gpu_launches": launches,
         "clocks": r["clocks"],
+        "kcycles_per_decode": kcycles(att_ms * 1e3, r["clocks"]),
         "device_status": r["status"],
     }
     if world == 1 and args.config == 5 and args.layers and not args.batch and args.meta == "f32":
