@@ -31,6 +31,14 @@ CASES = {
     # 64-token key groups, fp32 sources
     "int2_g64_f32": (O.Config(8, 2, 128, Q(O.INT2, A, CH, 64), Q(O.INT2, A, TOK, 32), 128, 64, 0, 1e4, O.F32),
                      [63, 64, 65, 700]),
+    # 32-token tiles of the 2-bit kernel across pages: 64-token key groups in 16-token pages (a group
+    # spans two tiles and four pages), 128-token groups in 32-token pages, both metadata types
+    "int2_g64_p16": (O.Config(16, 4, 128, Q(O.INT2, A, CH, 64), Q(O.INT2, A, TOK, 32), 128, 16, 0, 1e4, O.BF16),
+                     [63, 64, 128, 129, 1100]),
+    "m16_int2_g64_p16": (O.Config(16, 4, 128, Q(O.INT2, A, CH, 64), Q(O.INT2, A, TOK, 32), 128, 16, 0, 1e4,
+                                  O.BF16, meta_dtype=O.F16), [63, 64, 128, 129, 1100]),
+    "int2_g128_p32": (O.Config(8, 2, 128, Q(O.INT2, A, CH, 128), Q(O.INT2, A, TOK, 32), 256, 32, 0, 1e4, O.F32),
+                      [255, 256, 257, 900]),
     # INT8 per-channel pre-RoPE keys + INT4 per-token values in 16-token pages
     "int8k_rope_int4v": (O.Config(8, 2, 128, Q(O.INT8, S, CH, 64), Q(O.INT4, A, TOK, 128), 64, 16, 1, 5e5, O.BF16),
                          [1, 63, 64, 65, 700, 2100]),
@@ -105,7 +113,7 @@ CASES = {
 # otherwise leave the suite green on the generic kernel.
 TC_KERNEL = {
     "int2_kivi": "INT2", "int2_kivi_p16": "INT2", "int2_g64_f32": "INT2", "m16_int2_kivi": "INT2",
-    "m16_int2_kivi_p16": "INT2",
+    "m16_int2_kivi_p16": "INT2", "int2_g64_p16": "INT2", "m16_int2_g64_p16": "INT2", "int2_g128_p32": "INT2",
     "fp8": "FP8", "fp8_p16_f32": "FP8", "fp8_64q8kv": "FP8", "fp8_e5m2": "FP8", "fp8_e5m2_p16_f32": "FP8",
     "fast_rope_i8i4_p16": "ROPE_I8I4", "fast_rope_i8i4_p64": "ROPE_I8I4", "fast_rope_i8i4_g128": "ROPE_I8I4",
     "m16_fast_rope_p16": "ROPE_I8I4", "m16_fast_rope_p64": "ROPE_I8I4",
