@@ -82,6 +82,7 @@ struct __align__(1024) SmemI2 {
   uint8_t stage[kWarpsI][kStagesI][kStageI];
   float4 qp[kWarpsI][8][32];  // per warp, step s, lane: q * scale * log2(e) at the lane's 4 channels of step s
   float pex[kWarpsI][4][32];  // p exchange: [token / 8][head * 8 + token % 8]
+  float4 vmw[kWarpsI][2][kHT][2];  // binary16 metadata: the tile's value rows widened to fp32 (scales, minima)
   uint64_t bar[kWarpsI][kStagesI];
   int valid[kWarpsI][kStagesI];
 };
@@ -419,6 +420,14 @@ __global__ void __launch_bounds__(kThreadsI, 3)
         ++n_consumed;
         const uint8_t* buf = sm.stage[warp][stage];
         const int tok0 = it.t0 + i * kTI;
+        if constexpr (M16) {
+          // the tile's 32 value rows (4 scales, 4 minima in binary16) widened once to fp32: lane = (half, token)
+          const int hf = lane >> 4, tk = lane & 15;
+          const uint4 r = *reinterpret_cast<const uint4*>(buf + kOffH + hf * kHalf16 + kOffVM16 + tk * kVMetaRow16);
+          sm.vmw[warp][hf][tk][0] = halves4(make_uint2(r.x, r.y));
+          sm.vmw[warp][hf][tk][1] = halves4(make_uint2(r.z, r.w));
+          __syncwarp();
+        }
 
         if ((tok0 & (G - 1)) == 0) {
           // ---- new key group: B = q * s and the bias sum_c q_c (m_c + 3/2 s_c).  Lanes g and g ^ 1
@@ -501,8 +510,7 @@ __global__ void __launch_bounds__(kThreadsI, 3)
         // ---- value rows: per token 4 scales then 4 minima (fp32, or binary16 in M16)
         auto vrow = [&](int hf, int tok, int part) -> float4 {
           if constexpr (M16) {
-            return halves4(*reinterpret_cast<const uint2*>(buf + kOffH + hf * kHalf16 + kOffVM16 + tok * kVMetaRow16 +
-                                                           8 * part));
+            return sm.vmw[warp][hf][tok][part];
           } else {
             return reinterpret_cast<const float4*>(buf + kOffH + hf * kHalf32 + kOffVM32 + tok * kVMetaRow)[part];
           }
