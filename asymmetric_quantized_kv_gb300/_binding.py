@@ -70,6 +70,7 @@ def _load():
         "kvq_dequantize": (c_int32, [P(kvq_config), P(kvq_cache), c_int32, c_int32, c_int32, c_void_p,
                                      c_void_p, c_void_p]),
         "kvq_decode_kernel": (c_int32, [P(kvq_config), P(kvq_cache), P(c_int32)]),
+        "kvq_selftest_bounded_wait": (c_int32, [c_void_p, c_void_p]),
         "kvq_status_string": (ctypes.c_char_p, [c_int32]),
     }
     for name, (res, args) in sig.items():
@@ -155,6 +156,12 @@ def kvq_decode_kernel(cfg, cache: kvq_cache) -> int:
     k = c_int32(-1)
     _check("kvq_decode_kernel", LIB.kvq_decode_kernel(ctypes.byref(cfg), ctypes.byref(cache), ctypes.byref(k)))
     return k.value
+
+
+def kvq_selftest_bounded_wait(status, stream=None):
+    """Run the bounded-wait self-test: `status` (an int32 device tensor) gets
+    KVQ_DEV_TIMEOUT when the deliberately unfinished wait gives up."""
+    _check("kvq_selftest_bounded_wait", LIB.kvq_selftest_bounded_wait(_ptr(status), _stream(stream)))
 
 
 def kvq_dequantize(cfg, cache: kvq_cache, seq, tok_begin, tok_end, k_out, v_out, stream=None):

@@ -54,7 +54,7 @@ constexpr int kTile = 16;
 constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
 constexpr int kStages = 2;
-constexpr uint32_t kSpin = 1u << 20;  // polls per bounded mbarrier wait
+constexpr uint32_t kSpin = ptx::kWaitPolls;  // polls per bounded mbarrier wait
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescale = 8.f;  // lazy rescale threshold in log2 units
 constexpr float kMinit = -1e30f;  // running max before the first logit (finite: no inf - inf)

@@ -38,7 +38,7 @@ constexpr int kStages8 = 3;
 constexpr int kRep8 = 8;
 constexpr int kRowB = 128;                // bytes of one token's K (or V) codes
 constexpr int kTileB = kTileT * kRowB;    // one TMA box
-constexpr uint32_t kSpin8 = 1u << 20;     // polls per bounded mbarrier wait
+constexpr uint32_t kSpin8 = ptx::kWaitPolls;  // polls per bounded mbarrier wait
 constexpr float kLog2e8 = 1.4426950408889634f;
 constexpr float kRescale8 = 8.f;
 constexpr float kMinit8 = -1e30f;

@@ -73,7 +73,7 @@ constexpr int kOffVM16 = 2 * kHT * kRow2;
 constexpr int kHalf32 = 3 * kHT * kRow2;          // fp32 meta: 1536 bytes per half tile
 constexpr int kHalf16 = 2 * kHT * kRow2 + kHT * kVMetaRow16;  // binary16 meta: 1280
 constexpr int kStageI = 4096;
-constexpr uint32_t kSpinI = 1u << 20;
+constexpr uint32_t kSpinI = ptx::kWaitPolls;  // polls per bounded mbarrier wait
 constexpr float kLog2eI = 1.4426950408889634f;
 constexpr float kRescaleI = 8.f;
 constexpr float kMinitI = -1e30f;

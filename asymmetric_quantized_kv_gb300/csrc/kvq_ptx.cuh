@@ -55,6 +55,11 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Polls of every bounded pipeline wait in the decode kernels (and in their
+// self-test): each poll may suspend the thread briefly, so a wait on a phase that
+// never completes gives up after well under a few seconds.
+constexpr uint32_t kWaitPolls = 1u << 20;
+
 // Bounded wait on an mbarrier phase: gives up after `limit` polls (each poll may
 // itself suspend the warp briefly) and reports false.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint32_t limit) {
@@ -73,9 +78,6 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       : "memory");
 }
 
-// L2 policy for data read once per call (the packed KV stream): evict first, so
-// the stream does not push small reused data (code, window rows, block tables,
-// partial records) out of L2.
 // Start bringing the 128-byte lines of [p, p + n) into L1 (no data returned, no
 // wait); every address issued lies inside the range.
 __device__ __forceinline__ void prefetch_l1_range(const void* p, int n) {
@@ -85,6 +87,9 @@ __device__ __forceinline__ void prefetch_l1_range(const void* p, int n) {
     asm volatile("prefetch.global.L1 [%0];\n" ::"l"(c + n - 1));
 }
 
+// L2 policy for data read once per call (the packed KV stream): evict first, so
+// the stream does not push small reused data (code, window rows, block tables,
+// partial records) out of L2.
 __device__ __forceinline__ uint64_t l2_evict_first() {
   uint64_t pol;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;\n" : "=l"(pol));

@@ -280,6 +280,16 @@ kvq_status kvq_dequantize(const kvq_config* cfg, const kvq_cache* cache, int32_t
                           int32_t tok_begin, int32_t tok_end, float* k_out, float* v_out,
                           void* stream);
 
+/* Self-test of the device-side failure detection (the pages have no
+ * counterpart: it checks this library's own mechanism).  Every pipeline wait of
+ * the decode kernels gives up after a fixed number of polls (well under a few
+ * seconds), sets KVQ_DEV_TIMEOUT in the status word and lets the kernel finish.
+ * This call launches one warp that runs that bounded wait on a barrier phase
+ * that nothing completes, so *status (device int32, OR-ed into) gets
+ * KVQ_DEV_TIMEOUT once the wait gives up; the context stays usable.  Takes up to
+ * about a second of GPU time.  Returns KVQ_ERR_INVALID_ARG for a null status. */
+kvq_status kvq_selftest_bounded_wait(int32_t* status, void* stream);
+
 /* Human-readable name of a status code (static storage). */
 const char* kvq_status_string(kvq_status s);
 

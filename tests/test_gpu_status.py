@@ -60,3 +60,22 @@ def test_bad_block_table_entry(name):
     cache.block_table[b_bad, 1] = good
     cache.status.zero_()
     case.check_attention(q)
+
+
+def test_bounded_wait_gives_up_and_reports_timeout():
+    """A pipeline wait that can never complete (a barrier phase nothing finishes,
+    nothing in flight) gives up after the decode kernels' poll limit and reports
+    KVQ_DEV_TIMEOUT in the status word; the context stays usable: a decode call
+    right after it is exact."""
+    import time
+    import asymmetric_quantized_kv_gb300 as K
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    t0 = time.perf_counter()
+    K.kvq_selftest_bounded_wait(status)
+    torch.cuda.synchronize()
+    waited = time.perf_counter() - t0
+    assert int(status.item()) == K.KVQ_DEV_TIMEOUT
+    assert waited < 30.0, waited
+    cfg, lens = CASES["int2"]
+    c = Case(cfg, lens, seed=4)
+    c.check_attention()
