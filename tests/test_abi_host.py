@@ -153,3 +153,19 @@ def test_no_process_wide_unique_symbols(K):
     out = subprocess.run([nm, "-D", K.binding.LIB_PATH], capture_output=True, text=True, check=True).stdout
     unique = [line for line in out.splitlines() if " u " in line]
     assert not unique, unique[:5]
+
+
+def test_decode_kernel_batch_limit_on_the_host(K):
+    """The tensor-core kernels keep the plan's per-sequence prefix in shared
+    memory and take at most 4096 sequences; a larger batch runs on the generic
+    kernel (the pre-RoPE kernel's shape test needs no device, so the host can
+    check both sides of the limit)."""
+    L = K.binding.LIB
+    by = ctypes.byref
+    cfg = K.make_config(32, 8, 128, (O.INT8, O.SYM, O.PER_CHANNEL, 64), (O.INT4, O.ASYM, O.PER_TOKEN, 0), 64, 16,
+                        1, 5e5, K.KVQ_BF16)
+    out = ctypes.c_int32(-1)
+    for batch, want in ((4096, K.KVQ_KERNEL_ROPE_I8I4), (4097, K.KVQ_KERNEL_GENERIC)):
+        fake = K.kvq_cache(4096, 4096, 4096, 4096, 4096, 4096, 4096, batch, 4, 8 * batch, 4096)
+        assert L.kvq_decode_kernel(by(cfg), by(fake), by(out)) == K.KVQ_OK
+        assert out.value == want, (batch, out.value)
