@@ -81,7 +81,7 @@ constexpr float kMinitI = -1e30f;
 struct __align__(1024) SmemI2 {
   uint8_t stage[kWarpsI][kStagesI][kStageI];
   float4 qp[kWarpsI][8][32];  // per warp, step s, lane: q * scale * log2(e) at the lane's 4 channels of step s
-  float pex[kWarpsI][4][32];  // p exchange: [token / 8][head * 8 + token % 8]
+  float pex[kWarpsI][5][32];  // p exchange (quantized tiles: per half 80 floats, window tiles: 64)
   float4 vmw[kWarpsI][2][kHT][2];  // binary16 metadata: the tile's value rows widened to fp32 (scales, minima)
   uint64_t bar[kWarpsI][kStagesI];
   int valid[kWarpsI][kStagesI];
@@ -178,10 +178,26 @@ __device__ __forceinline__ uint32_t centred_code(uint32_t w) {
   }
 }
 
-// centred_code for a field index known only after unrolling
-__device__ __forceinline__ uint32_t centred_field(uint32_t w, int k) {
-  return k == 0 ? centred_code<0>(w) : k == 1 ? centred_code<1>(w) : k == 2 ? centred_code<2>(w)
-                                                                           : centred_code<3>(w);
+// The 2-bit code fields k + 1 (bits 2k + 2, 2k + 3 of each 16-bit half, k = 0..3),
+// centred: OR-ing the field into the mantissa of 1024 gives 1024 + c * 4^(k+1), and
+// one fused multiply-add by 4^-(k+1) and -(1024 / 4^(k+1) + 3/2) leaves c - 3/2
+// exactly (for the top field, 4 + c - 5.5).
+template <int K>
+__device__ __forceinline__ uint32_t centred_code_up(uint32_t w) {
+  const uint32_t x = and_or(w, 0x000C000Cu << (2 * K), 0x64006400u);
+  if constexpr (K == 0) {
+    return hfma2(x, 0x34003400u, 0xDC06DC06u);  // * 1/4, - 257.5
+  } else if constexpr (K == 1) {
+    return hfma2(x, 0x2C002C00u, 0xD418D418u);  // * 1/16, - 65.5
+  } else if constexpr (K == 2) {
+    return hfma2(x, 0x24002400u, 0xCC60CC60u);  // * 1/64, - 17.5
+  } else {
+    return hfma2(x, 0x1C001C00u, 0xC580C580u);  // * 1/256, - 5.5
+  }
+}
+__device__ __forceinline__ uint32_t centred_field_up(uint32_t w, int k) {
+  return k == 0 ? centred_code_up<0>(w) : k == 1 ? centred_code_up<1>(w) : k == 2 ? centred_code_up<2>(w)
+                                                                                 : centred_code_up<3>(w);
 }
 
 // four binary16 values (two words) widened to fp32
@@ -492,14 +508,16 @@ __global__ void __launch_bounds__(kThreadsI, 3)
           const uint8_t* hb = buf + kOffH + hf * kHalf;
           const uint2 w0 = *reinterpret_cast<const uint2*>(hb + g * kRow2 + 8 * t);
           const uint2 w1 = *reinterpret_cast<const uint2*>(hb + (g + 8) * kRow2 + 8 * t);
-          const uint32_t u0[2] = {w0.x, w0.y}, u1[2] = {w1.x, w1.y};
-          const uint32_t s0[2] = {w0.x >> 8, w0.y >> 8}, s1[2] = {w1.x >> 8, w1.y >> 8};
+          // fields 0..3 of each half moved up to 1..4 (w << 2), fields 4..7 down to 1..4 (w >> 6):
+          // every field then takes one mask and one fused multiply-add (centred_code_up)
+          const uint32_t u0[2] = {w0.x << 2, w0.y << 2}, u1[2] = {w1.x << 2, w1.y << 2};
+          const uint32_t s0[2] = {w0.x >> 6, w0.y >> 6}, s1[2] = {w1.x >> 6, w1.y >> 6};
           float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
           for (int s = 0; s < 8; ++s) {
             const int wd = s >> 2, j = s & 3;
-            mma_16816(acc, centred_field(u0[wd], j), centred_field(u1[wd], j), centred_field(s0[wd], j),
-                      centred_field(s1[wd], j), bk[s][0], bk[s][1]);
+            mma_16816(acc, centred_field_up(u0[wd], j), centred_field_up(u1[wd], j), centred_field_up(s0[wd], j),
+                      centred_field_up(s1[wd], j), bk[s][0], bk[s][1]);
           }
           lg[2 * hf] = kHT * hf + g < nvalid ? (acc[0] - acc[1]) + bias : -INFINITY;
           lg[2 * hf + 1] = kHT * hf + g + 8 < nvalid ? (acc[2] - acc[3]) + bias : -INFINITY;
@@ -520,38 +538,44 @@ __global__ void __launch_bounds__(kThreadsI, 3)
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const float4 n = vrow(e >> 1, g + 8 * (e & 1), 1), z = vrow(e >> 1, g + 8 * (e & 1), 0);
-            mb[0] = fmaf(p[e], fmaf(1.5f, z.x, n.x), mb[0]);
-            mb[1] = fmaf(p[e], fmaf(1.5f, z.y, n.y), mb[1]);
-            mb[2] = fmaf(p[e], fmaf(1.5f, z.z, n.z), mb[2]);
-            mb[3] = fmaf(p[e], fmaf(1.5f, z.w, n.w), mb[3]);
+            const float2 pp = make_float2(p[e], p[e]), h15 = make_float2(1.5f, 1.5f);
+            const float2 m01 = __ffma2_rn(pp, __ffma2_rn(h15, make_float2(z.x, z.y), make_float2(n.x, n.y)),
+                                          make_float2(mb[0], mb[1]));
+            const float2 m23 = __ffma2_rn(pp, __ffma2_rn(h15, make_float2(z.z, z.w), make_float2(n.z, n.w)),
+                                          make_float2(mb[2], mb[3]));
+            mb[0] = m01.x; mb[1] = m01.y; mb[2] = m23.x; mb[3] = m23.y;
           }
         }
         // p of head g/2 at the k-slots of both halves
         __syncwarp();
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
-          pe[64 * hf + t * 8 + X0] = p[2 * hf];
-          pe[64 * hf + 32 + t * 8 + X1] = p[2 * hf + 1];
+          pe[80 * hf + t * 8 + X0] = p[2 * hf];
+          pe[80 * hf + 48 + t * 8 + X1] = p[2 * hf + 1];
         }
         __syncwarp();
 
         // ---- PV per half (k block of 16 tokens), value group G: byte 8G + g of tokens T0, T1 (ya), T8, T9 (yc)
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
-          const float2 x01 = *reinterpret_cast<const float2*>(pe + 64 * hf + (g >> 1) * 8 + 2 * t);
-          const float2 x89 = *reinterpret_cast<const float2*>(pe + 64 * hf + 32 + (g >> 1) * 8 + 2 * t);
-          const float4 sa = vrow(hf, T0, 0), sb = vrow(hf, T1, 0), sc8 = vrow(hf, T8, 0), sd = vrow(hf, T9, 0);
-          const float sA[4] = {sa.x, sa.y, sa.z, sa.w}, sB[4] = {sb.x, sb.y, sb.z, sb.w};
-          const float sC[4] = {sc8.x, sc8.y, sc8.z, sc8.w}, sD[4] = {sd.x, sd.y, sd.z, sd.w};
+          // B = p * s_t(G) of head g/2: the even lane of a pair (lane, lane ^ 4) forms the products of
+          // k-slots 2t, 2t+1 (tokens T0, T1), the odd lane those of 2t+8, 2t+9 (T8, T9); each splits its
+          // pair and hands the partner the half it needs (hi to the even lane, hi - x to the odd lane).
+          // Within a half the slots 8.. sit 48 floats after the slots 0.., so the loads of the two lanes
+          // of a pair fall in different banks.
+          const float2 xo = *reinterpret_cast<const float2*>(pe + 80 * hf + (odd ? 48 : 0) + (g >> 1) * 8 + 2 * t);
+          const float4 sp = vrow(hf, odd ? T8 : T0, 0), sq = vrow(hf, odd ? T9 : T1, 0);
+          const float sP[4] = {sp.x, sp.y, sp.z, sp.w}, sQ[4] = {sq.x, sq.y, sq.z, sq.w};
           const uint8_t* vc = buf + kOffH + hf * kHalf + kOffV;
           const int gb = g & 3;
           const uint32_t sel = gb * 0x0011u + (4 + gb) * 0x1100u;
           const int woff = 4 * (g >> 2);
 #pragma unroll
           for (int G4 = 0; G4 < 4; ++G4) {
-            uint32_t b01, b89;
-            split_sel(x01.x * sA[G4], x01.y * sB[G4], odd, b01);
-            split_sel(x89.x * sC[G4], x89.y * sD[G4], odd, b89);
+            uint32_t hi, nl;
+            split_hi_neglo(xo.x * sP[G4], xo.y * sQ[G4], hi, nl);
+            const uint32_t r = __shfl_xor_sync(0xffffffffu, odd ? hi : nl, 4);
+            const uint32_t b01 = odd ? r : hi, b89 = odd ? nl : r;
             const int off = 8 * G4 + woff;
             const uint32_t wa = *reinterpret_cast<const uint32_t*>(vc + T0 * kRow2 + off);
             const uint32_t wb = *reinterpret_cast<const uint32_t*>(vc + T1 * kRow2 + off);
