@@ -416,7 +416,7 @@ __global__ void __launch_bounds__(kThreadsI, 3)
       }
       __syncwarp();
 
-      uint32_t bk[8][2];  // QK B: q * s of the current key group, hi (even g) / lo (odd g)
+      uint32_t bk[8][2] = {};  // QK B: q * s of the current key group, hi (even g) / lo (odd g)
       float bias = 0.f;   // sum_c q_c (m_c + 3/2 s_c) of the current key group for query head t
       for (int i = 0; i < ntiles; ++i) {
         const int stage = cstage;
@@ -581,9 +581,11 @@ __global__ void __launch_bounds__(kThreadsI, 3)
             const uint32_t wb = *reinterpret_cast<const uint32_t*>(vc + T1 * kRow2 + off);
             const uint32_t wc = *reinterpret_cast<const uint32_t*>(vc + T8 * kRow2 + off);
             const uint32_t wd = *reinterpret_cast<const uint32_t*>(vc + T9 * kRow2 + off);
+            // each half of ya / yc holds the selected byte twice (as its low and its high byte)
             const uint32_t ya = prmt(wa, wb, sel), yc = prmt(wc, wd, sel);
-            // m-block 2G4: rows g / g+8 = channels 32G4 + 4g + 0 / + 1 (code fields 0, 1)
-            mma_16816(O[2 * G4], centred_code<0>(ya), centred_code<1>(ya), centred_code<0>(yc),
+            // m-block 2G4: rows g / g+8 = channels 32G4 + 4g + 0 / + 1 (code fields 0, 1; field 0 read from
+            // the high copy, where it is field 4 of the half and takes one multiply-add)
+            mma_16816(O[2 * G4], centred_code_up<3>(ya), centred_code<1>(ya), centred_code_up<3>(yc),
                       centred_code<1>(yc), b01, b89);
             // m-block 2G4+1: channels 32G4 + 4g + 2 / + 3 (code fields 2, 3)
             mma_16816(O[2 * G4 + 1], centred_code<2>(ya), centred_code<3>(ya), centred_code<2>(yc),
