@@ -39,7 +39,7 @@ class kvq_cache(ctypes.Structure):
     _fields_ = [("pages", c_void_p), ("block_table", c_void_p), ("seq_lens", c_void_p),
                 ("k_win", c_void_p), ("v_win", c_void_p), ("k_scale", c_void_p), ("v_scale", c_void_p),
                 ("batch", c_int32), ("max_pages_per_seq", c_int32), ("n_pages", c_int32),
-                ("status", c_void_p)]
+                ("status", c_void_p), ("rope_table", c_void_p), ("rope_positions", c_int32)]
 
 
 class KvqError(RuntimeError):
@@ -55,6 +55,8 @@ def _load():
     P = ctypes.POINTER
     sig = {
         "kvq_layout_version": (c_int32, []),
+        "kvq_rope_table_bytes": (c_size_t, [P(kvq_config), c_int32]),
+        "kvq_rope_table_init": (c_int32, [P(kvq_config), c_int32, c_void_p, c_void_p]),
         "kvq_validate": (c_int32, [P(kvq_config)]),
         "kvq_head_block_bytes": (c_size_t, [P(kvq_config)]),
         "kvq_page_bytes": (c_size_t, [P(kvq_config)]),
@@ -122,6 +124,15 @@ def kvq_head_block_offsets(cfg: kvq_config) -> list[int]:
 
 def kvq_workspace_bytes(cfg: kvq_config, batch: int, max_seq_len: int) -> int:
     return LIB.kvq_workspace_bytes(ctypes.byref(cfg), batch, max_seq_len)
+
+
+def kvq_rope_table_bytes(cfg: kvq_config, positions: int) -> int:
+    return LIB.kvq_rope_table_bytes(ctypes.byref(cfg), int(positions))
+
+
+def kvq_rope_table_init(cfg, positions, table, stream=None):
+    _check("kvq_rope_table_init",
+           LIB.kvq_rope_table_init(ctypes.byref(cfg), int(positions), _ptr(table), _stream(stream)))
 
 
 def kvq_calibrate_absmax(cfg, src, n_tokens, qmax, scale_out, stream=None):

@@ -28,7 +28,11 @@ class PagedKVCache:
     """Caller-owned buffers of one cache (pages, block table, lengths, window,
     static scales, status word) and the kvq_cache struct pointing at them."""
 
-    def __init__(self, cfg, batch, max_pages_per_seq, n_pages=None, block_table=None, device="cuda"):
+    def __init__(self, cfg, batch, max_pages_per_seq, n_pages=None, block_table=None, device="cuda",
+                 rope_table=True):
+        """rope_table (pre-RoPE keys only): True builds a table for every position the
+        pages can hold, False leaves the decode kernel to compute the cos/sin, and a
+        (tensor, positions) pair shares a table built by kvq_rope_table_init."""
         self.cfg = cfg
         self.batch = batch
         self.max_pages = max_pages_per_seq
@@ -50,10 +54,19 @@ class PagedKVCache:
         self.workspace = torch.empty(
             max(B.kvq_workspace_bytes(cfg, batch, max_pages_per_seq * cfg.page_size), 256),
             dtype=torch.uint8, device=dev)
+        self.rope_table, self.rope_positions = None, 0
+        if cfg.rope_pre and rope_table is not False:
+            if rope_table is True:
+                n = max_pages_per_seq * cfg.page_size
+                self.rope_table = torch.empty(B.kvq_rope_table_bytes(cfg, n), dtype=torch.uint8, device=dev)
+                self.rope_positions = n
+                B.kvq_rope_table_init(cfg, n, self.rope_table)
+            else:
+                self.rope_table, self.rope_positions = rope_table
         p = lambda t: None if t is None else t.data_ptr()
         self.c = B.kvq_cache(p(self.pages), p(self.block_table), p(self.seq_lens), p(self.k_win), p(self.v_win),
                              p(self.k_scale), p(self.v_scale), batch, max_pages_per_seq, self.n_pages,
-                             p(self.status))
+                             p(self.status), p(self.rope_table), self.rope_positions)
 
     # --- thin wrappers over the C ABI
     def append(self, k_new, v_new, n_new_per_seq=None, stream=None):

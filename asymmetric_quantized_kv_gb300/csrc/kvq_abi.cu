@@ -75,6 +75,10 @@ kvq_status check_cache(const kvq_config* c, const kvq_cache* k) {
   if ((c->k.axis == KVQ_PER_TENSOR) && !k->k_scale) return KVQ_ERR_INVALID_ARG;
   if ((c->v.axis == KVQ_PER_TENSOR) && !k->v_scale) return KVQ_ERR_INVALID_ARG;
   if ((long long)k->max_pages_per_seq * c->page_size > (1LL << 30)) return KVQ_ERR_CAPACITY;
+  if (k->rope_table) {
+    if (!c->rope_pre || k->rope_positions < 1 || (reinterpret_cast<uintptr_t>(k->rope_table) & 15))
+      return KVQ_ERR_INVALID_ARG;
+  }
   return KVQ_OK;
 }
 
@@ -131,6 +135,8 @@ bool make_view(const kvq_config* c, const kvq_cache* k, KvqView* v) {
     v->max_pages = k->max_pages_per_seq;
     v->n_pages = k->n_pages;
     v->status = k->status;
+    v->rope_table = k->rope_table;
+    v->rope_positions = k->rope_table ? k->rope_positions : 0;
   }
   return true;
 }
@@ -140,6 +146,20 @@ bool make_view(const kvq_config* c, const kvq_cache* k, KvqView* v) {
 extern "C" {
 
 int32_t kvq_layout_version(void) { return KVQ_LAYOUT_VERSION; }
+
+size_t kvq_rope_table_bytes(const kvq_config* c, int32_t positions) {
+  if (!c || kvq_validate(c) != KVQ_OK || !c->rope_pre || positions < 1) return 0;
+  return (size_t)positions * (size_t)c->head_dim * sizeof(float);
+}
+
+kvq_status kvq_rope_table_init(const kvq_config* c, int32_t positions, void* table, void* stream) {
+  const kvq::NvtxRange range("kvq_rope_table_init");
+  kvq::KvqView v;
+  if (!kvq::make_view(c, nullptr, &v)) return kvq_validate(c);
+  if (!c->rope_pre || positions < 1 || !table || (reinterpret_cast<uintptr_t>(table) & 15))
+    return KVQ_ERR_INVALID_ARG;
+  return kvq::launch_rope_table(v, positions, table, (cudaStream_t)stream);
+}
 
 kvq_status kvq_validate(const kvq_config* c) {
   if (!c) return KVQ_ERR_INVALID_ARG;

@@ -18,10 +18,12 @@
 //       q*scale*log2(e)).  The hi/lo split of both operands keeps the logits to
 //       ~2^-21 relative.  Scaling and rotation run as packed f32x2 arithmetic on
 //       the even channels (x0, x2) and odd channels (x1, x3) of two RoPE pairs.
-//   RoPE table: cos/sin of every (token, pair) of two tiles, built once per CTA
-//       into one of two shared buffers and handed between the 8 warps through
-//       full/empty mbarriers, so warps may drift by up to two tiles instead of
-//       meeting at a CTA barrier every tile.
+//   RoPE table: cos/sin of every (token, pair) of two tiles, in one of two
+//       shared buffers handed between the 8 warps through full/empty mbarriers,
+//       so warps may drift by up to two tiles instead of meeting at a CTA
+//       barrier every tile.  With the caller's table (kvq_cache.rope_table) the
+//       buffer is filled by one bulk copy of its 32 rows; otherwise (or past
+//       the table's end) the CTA computes it.
 //   softmax: online in base 2, one running max per head, raised lazily (only
 //       when a logit exceeds it by more than 2^8; the common tile needs no
 //       cross-lane reduction).
@@ -61,6 +63,7 @@ constexpr float kMinit = -1e30f;  // running max before the first logit (finite:
 constexpr int kSuper = 2;    // tiles per RoPE table (one handoff between the warps per table)
 constexpr int kReseed = 16;  // RoPE table entries are recomputed exactly every kReseed tables
 constexpr int kNRep = 4;
+constexpr uint32_t kTableBytes = kSuper * kTile * 32 * 16;  // one shared RoPE table: 32 rows of 32 float4
 
 // Bytes per 16-token tile of one head: K codes, V codes, V meta (scale, min);
 // a tile that starts a key group also carries the group's 128 key scales.  With
@@ -165,11 +168,21 @@ struct Acc {
 // the thread's own slots of the previous table's buffer) and recomputed exactly
 // at an item's first table and every kReseed tables.
 
-__device__ __forceinline__ float4 trig_entry(const SmemRI& sm, int pos, int u) {
-  const float2 a = rope_cs(pos, sm.w_hi[2 * u], sm.w_lo[2 * u]);
-  const float2 b = rope_cs(pos, sm.w_hi[2 * u + 1], sm.w_lo[2 * u + 1]);
+// (cos A, cos B, sin A, sin B) of pairs A = 2u, B = 2u + 1 at position pos
+__device__ __forceinline__ float4 trig_entry(const float* w_hi, const float* w_lo, int pos, int u) {
+  const float2 a = rope_cs(pos, w_hi[2 * u], w_lo[2 * u]);
+  const float2 b = rope_cs(pos, w_hi[2 * u + 1], w_lo[2 * u + 1]);
   return make_float4(a.x, b.x, a.y, b.y);
 }
+__device__ __forceinline__ float4 trig_entry(const SmemRI& sm, int pos, int u) {
+  return trig_entry(sm.w_hi, sm.w_lo, pos, u);
+}
+
+// Slot of unit u in a table row of token parity `odd`: the bank swizzle of the
+// shared table, also used by the caller's table (whose row p is stored as the
+// shared row of parity p & 1, so a bulk copy of rows from an even position
+// lands in the shared layout).
+__device__ __forceinline__ int trig_slot(int u, int odd) { return u ^ ((((u >> 3) << 1) | odd) & 7); }
 
 __device__ __forceinline__ void trig_produce(SmemRI& sm, uint32_t buf, int ip, int tok0) {
   const int u = threadIdx.x & 31, d0 = threadIdx.x >> 5;
@@ -178,7 +191,7 @@ __device__ __forceinline__ void trig_produce(SmemRI& sm, uint32_t buf, int ip, i
 #pragma unroll
   for (int j = 0; j < 2 * kSuper; ++j) {
     const int d = d0 + 8 * j;
-    const int slot = u ^ ((((u >> 3) << 1) | (d & 1)) & 7);
+    const int slot = trig_slot(u, d & 1);
     float4 e;
     if (ip % kReseed == 0) {
       e = trig_entry(sm, tok0 + d, u);
@@ -242,7 +255,9 @@ __device__ __forceinline__ void softmax_step(Acc& A, float lg0, float lg1, float
   b23 = (g & 1) ? nB : hB;
 }
 
-template <bool M16>
+// TAB: the RoPE tables come from the caller's table (which covers every position
+// the cache can hold); otherwise the CTA computes them.
+template <bool M16, bool TAB>
 __global__ void __launch_bounds__(kThreads, 2)
     split_rope_i8i4_kernel(KvqView v, const void* q, float scale, float* ws) {
   constexpr int kStageBytes = stage_bytes<M16>(), kKMeta = kmeta_bytes<M16>(), kVM = vm_bytes<M16>();
@@ -272,9 +287,11 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
   }
   if (lane == 0) fence_mbar_init();
-  if (threadIdx.x < kD / 2) rope_split(v, threadIdx.x, &sm.w_hi[threadIdx.x], &sm.w_lo[threadIdx.x]);
-  __syncthreads();
-  if (threadIdx.x < 32) sm.rstep[threadIdx.x] = trig_entry(sm, kSuper * kTile, threadIdx.x);
+  if constexpr (!TAB) {
+    if (threadIdx.x < kD / 2) rope_split(v, threadIdx.x, &sm.w_hi[threadIdx.x], &sm.w_lo[threadIdx.x]);
+    __syncthreads();
+    if (threadIdx.x < 32) sm.rstep[threadIdx.x] = trig_entry(sm, kSuper * kTile, threadIdx.x);
+  }
   __syncthreads();
 
 
@@ -291,25 +308,63 @@ __global__ void __launch_bounds__(kThreads, 2)
   bool stalled = false;  // set by a timed-out wait: no further waits
   uint32_t tc = 0;  // RoPE tables used by this CTA: table tc in buffer tc & 1, its use tc >> 1
 
-  // produce CTA table tcp (item table ip, first token tok0) once the warps are
-  // done with the buffer's previous use
-  auto produce = [&](uint32_t tcp, int ip, int tok0) {
+  const float4* rope_tab = static_cast<const float4*>(v.rope_table);
+  // thread 0: copy CTA table tcp (first token tok0) into its buffer once the
+  // warps are done with the buffer's previous use; this arrival carries the
+  // byte count (a timed-out wait leaves the buffer as it is)
+  auto issue_copy = [&](uint32_t tcp, int tok0) {
     const uint32_t b = tcp & 1;
     if (tcp >= 2) bounded_wait(&sm.tempty[b], ((tcp >> 1) - 1) & 1, stalled, v.status);
-    trig_produce(sm, b, ip, tok0);
-    warp_arrive(&sm.tfull[b]);
+    if (!stalled) {
+      fence_proxy_async();  // the buffer may last have been written through the generic proxy
+      mbar_arrive_expect_tx(&sm.tfull[b], kTableBytes);
+      bulk_g2s_hint(&sm.trig[b][0][0], rope_tab + (long long)tok0 * 32, kTableBytes, &sm.tfull[b],
+                    l2_evict_last());
+    } else {
+      mbar_arrive(&sm.tfull[b]);
+    }
   };
-  // before the K loop of item tile i: wait for its table and point at its rows
-  auto table_rows = [&](int i) {
-    if ((i & (kSuper - 1)) == 0) bounded_wait(&sm.tfull[tc & 1], (tc >> 1) & 1, stalled, v.status);
+  // every warp: make CTA table tcp (item table ip, first token tok0) ready.  A
+  // copied table's bytes were requested by thread 0 (at the item's start for its
+  // first table, else one table ahead), whose arrival that was; the other warps
+  // arrive.  A computed table: wait for the buffer, compute this thread's
+  // entries, arrive.
+  auto produce = [&](uint32_t tcp, int ip, int tok0, bool first) {
+    const uint32_t b = tcp & 1;
+    if constexpr (TAB) {
+      if (warp != 0) {
+        warp_arrive(&sm.tfull[b]);
+      } else if (first) {
+        __syncwarp();
+        if (lane == 0) issue_copy(tcp, tok0);
+      }
+    } else {
+      if (tcp >= 2) bounded_wait(&sm.tempty[b], ((tcp >> 1) - 1) & 1, stalled, v.status);
+      trig_produce(sm, b, ip, tok0);
+      warp_arrive(&sm.tfull[b]);
+    }
+  };
+  // before the K loop of item tile i (item from token t0, ntiles tiles): at a
+  // table's first tile, thread 0 requests the next table's copy (TAB), then
+  // every warp waits for this table; returns this thread's rows
+  auto table_rows = [&](int i, int ntiles, int t0) {
+    if ((i & (kSuper - 1)) == 0) {
+      if constexpr (TAB) {
+        if (warp == 0 && i + kSuper < ntiles) {
+          __syncwarp();
+          if (lane == 0) issue_copy(tc + 1, t0 + (i + kSuper) * kTile);
+        }
+      }
+      bounded_wait(&sm.tfull[tc & 1], (tc >> 1) & 1, stalled, v.status);
+    }
     return &sm.trig[tc & 1][kTile * (i & (kSuper - 1)) + sg][0];
   };
   // after the K loop of item tile i: release the table after its last tile and
-  // produce the next one
+  // make the next one ready
   auto table_done = [&](int i, int ntiles, int tok0) {
     if ((i & (kSuper - 1)) == kSuper - 1 || i + 1 == ntiles) {
       warp_arrive(&sm.tempty[tc & 1]);
-      if (i + 1 < ntiles) produce(tc + 1, (i + 1) / kSuper, tok0 + kTile);
+      if (i + 1 < ntiles) produce(tc + 1, (i + 1) / kSuper, tok0 + kTile, false);
       ++tc;
     }
   };
@@ -347,7 +402,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     A.l_loc = 0.f;
     A.mb = 0.f;
 
-    produce(tc, 0, it.t0);
+    produce(tc, 0, it.t0, true);
     const float4* trow0 = &sm.trig[0][sg][0];  // re-pointed per tile
     if (!it.window) {
       // ======================= quantized chunk: tiles through the TMA ring
@@ -425,7 +480,7 @@ __global__ void __launch_bounds__(kThreads, 2)
               make_float4(raw.x, raw.z, raw.y, raw.w);
           __syncwarp();
         }
-        trow0 = table_rows(i);
+        trow0 = table_rows(i, ntiles, it.t0);
         const float4* trow1 = trow0 + 8 * 32;
 
         // ---- QK: MMA rows g / g+8 = tile tokens sg / sg+8, channels 32t .. 32t+31
@@ -520,7 +575,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       const long long wrow = ((long long)it.b * v.R) * v.Hkv + h;  // (b, slot 0, h) row index
       for (int i = 0; i < ntiles; ++i) {
         const int tok0 = it.t0 + i * kTile;
-        trow0 = table_rows(i);
+        trow0 = table_rows(i, ntiles, it.t0);
         const float4* trow1 = trow0 + 8 * 32;
         float acc[4] = {0.f, 0.f, 0.f, 0.f}, accn[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -611,7 +666,28 @@ __global__ void __launch_bounds__(kThreads, 2)
 }
 
 
+// Caller's RoPE table: row p (D/4 float4) holds trig_entry(p, u) at trig_slot(u, p & 1).
+__global__ void __launch_bounds__(256) rope_table_kernel(KvqView v, int positions, float4* table) {
+  __shared__ float w_hi[kMaxHeadDim / 2], w_lo[kMaxHeadDim / 2];
+  for (int i = threadIdx.x; i < v.D / 2; i += blockDim.x) rope_split(v, i, &w_hi[i], &w_lo[i]);
+  __syncthreads();
+  const int U = v.D / 4;
+  const long long n = (long long)positions * U;
+  for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < n; e += (long long)gridDim.x * blockDim.x) {
+    const int p = (int)(e / U), u = (int)(e - (long long)p * U);
+    table[(long long)p * U + trig_slot(u, p & 1)] = trig_entry(w_hi, w_lo, p, u);
+  }
+}
+
 }  // namespace
+
+kvq_status launch_rope_table(const KvqView& v, int positions, void* table, cudaStream_t st) {
+  const long long n = (long long)positions * (v.D / 4);
+  const long long blocks = (n + 255) / 256, cap = (long long)num_sms() * 8;
+  const int grid = (int)(blocks < cap ? blocks : cap);
+  rope_table_kernel<<<grid, 256, 0, st>>>(v, positions, static_cast<float4*>(table));
+  return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+}
 
 bool fast_eligible(const KvqView& v) {
   const bool pow2_g = v.kgroup > 0 && (v.kgroup & (v.kgroup - 1)) == 0;
@@ -629,8 +705,13 @@ size_t fast_workspace_bytes(const KvqView& v, int batch) { return split_workspac
 kvq_status launch_fast(const KvqView& v, const void* q, float* out, float scale, void* ws,
                        cudaStream_t st) {
   const size_t smem = sizeof(SmemRI) + sizeof(int) * 2 * (v.batch + 1);
-  const int m = v.meta16 ? 1 : 0;
-  auto kern = m ? split_rope_i8i4_kernel<true> : split_rope_i8i4_kernel<false>;
+  // the caller's RoPE table when it covers every position the cache can hold
+  const bool tab = v.rope_table != nullptr && (long long)v.rope_positions >= (long long)v.max_pages * v.P;
+  const int m = (v.meta16 ? 1 : 0) + (tab ? 2 : 0);
+  auto kern = m == 3   ? split_rope_i8i4_kernel<true, true>
+              : m == 2 ? split_rope_i8i4_kernel<false, true>
+              : m == 1 ? split_rope_i8i4_kernel<true, false>
+                       : split_rope_i8i4_kernel<false, false>;
   int occ = 0;
   const kvq_status so =
       occupancy_once(kSlotFast + m, kern, kThreads, smem, sizeof(SmemRI) + sizeof(int) * 2 * 4097, &occ);

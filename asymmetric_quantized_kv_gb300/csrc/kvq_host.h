@@ -30,8 +30,8 @@ enum SetupSlot {
   kSlotSms = 0,        // multiprocessor count
   kSlotAppend,         // append kernel: dynamic shared-memory limit raised
   kSlotGeneric,        // generic decode kernels (12 instances): shared-memory limit set so far
-  kSlotFast = kSlotGeneric + 12,  // pre-RoPE tensor-core kernel, 2 instances: CTAs per SM
-  kSlotFp8 = kSlotFast + 2,       // FP8 tensor-core kernel, 2 instances
+  kSlotFast = kSlotGeneric + 12,  // pre-RoPE tensor-core kernel, 4 instances: CTAs per SM
+  kSlotFp8 = kSlotFast + 4,       // FP8 tensor-core kernel, 2 instances
   kSlotInt2 = kSlotFp8 + 2,       // 2-bit tensor-core kernel, 2 instances
   kSlotCount = kSlotInt2 + 2
 };

@@ -44,6 +44,8 @@ struct KvqView {
   const float* v_scale;
   int batch, max_pages, n_pages;
   int32_t* status;
+  const void* rope_table;  // optional: kvq_rope_table_init output for positions [0, rope_positions)
+  int rope_positions;
 };
 
 // Host: resolve a validated config + cache into a view (false when invalid).
@@ -57,6 +59,8 @@ kvq_status launch_dequantize(const KvqView& v, int seq, int t0, int t1, float* k
 kvq_status launch_calibrate(const KvqView& v, const void* src, long long n_tokens, float qmax,
                             float* scale_out, cudaStream_t st);
 size_t attention_workspace_bytes(const KvqView& v, int batch);
+// Fill a RoPE table (kvq_rope_table_init): positions rows of D/4 float4.
+kvq_status launch_rope_table(const KvqView& v, int positions, void* table, cudaStream_t st);
 // Tensor-core decode kernel for INT8 per-channel pre-RoPE keys + INT4 per-token values.
 bool fast_eligible(const KvqView& v);
 size_t fast_workspace_bytes(const KvqView& v, int batch);

@@ -96,6 +96,13 @@ __device__ __forceinline__ uint64_t l2_evict_first() {
   return pol;
 }
 
+// L2 policy for small data that many CTAs read (a RoPE table): evict last.
+__device__ __forceinline__ uint64_t l2_evict_last() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;\n" : "=l"(pol));
+  return pol;
+}
+
 // bulk_g2s with an L2 cache policy
 __device__ __forceinline__ void bulk_g2s_hint(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
                                               uint64_t pol) {

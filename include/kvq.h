@@ -170,10 +170,39 @@ typedef struct {
   int32_t max_pages_per_seq;
   int32_t n_pages;
   int32_t* status;            /* one device int32; error bits are OR-ed in            */
+  /* Optional RoPE table, pre-RoPE keys only (NULL otherwise, and then
+   * rope_positions is ignored): the output of kvq_rope_table_init for this
+   * config, covering positions [0, rope_positions), rope_positions >= 1.
+   * Device, 16-byte aligned, owned by the caller, read only, and shareable by
+   * every cache with the same head_dim and rope_theta.  When it covers every
+   * position the pages can hold (rope_positions >= max_pages_per_seq *
+   * page_size), the pre-RoPE tensor-core decode kernel copies the cos/sin from
+   * it instead of computing them; otherwise the kernel computes them (same
+   * results to ~1e-6 relative).  KVQ_ERR_INVALID_ARG for a table that is
+   * misaligned, set for a config without pre-RoPE keys, or with
+   * rope_positions < 1. */
+  const void* rope_table;
+  int32_t rope_positions;
 } kvq_cache;
 
 /* Library layout version (KVQ_LAYOUT_VERSION). */
 int32_t kvq_layout_version(void);
+
+/* Bytes of a RoPE table for `positions` positions: positions * head_dim * 4
+ * (the cos and sin of every (position, pair) in fp32); 0 when cfg is invalid,
+ * does not hold pre-RoPE keys, or positions < 1. */
+size_t kvq_rope_table_bytes(const kvq_config* cfg, int32_t positions);
+
+/* Fill a RoPE table (kvq_cache.rope_table): the rotation of pair i at position
+ * p, angle p * theta^(-2i/D) ("KV Cache Quantization: Why Keys and Values Need
+ * Different Axes", "Where does RoPE break this?"; interleaved pairs (2i, 2i+1)),
+ * for p in [0, positions).  The values are those the decode kernel computes
+ * itself (the same angle reduction and sincospi); the arrangement inside the
+ * table is private to the library.  table: device, kvq_rope_table_bytes bytes,
+ * 16-byte aligned, overwritten.  Enqueued on `stream`; no synchronisation.
+ * KVQ_ERR_INVALID_ARG for a null or misaligned table, positions < 1, or a
+ * config without pre-RoPE keys. */
+kvq_status kvq_rope_table_init(const kvq_config* cfg, int32_t positions, void* table, void* stream);
 
 /* KVQ_OK when the configuration is consistent and supported, else the reason. */
 kvq_status kvq_validate(const kvq_config* cfg);

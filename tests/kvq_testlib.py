@@ -32,7 +32,10 @@ class Case:
     the oracle states."""
 
     def __init__(self, cfg: O.Config, lens, seed=0, outliers=(3, 17), factor=30.0, chunking="random",
-                 permute_pages=True, extra_pages=1, streams=None, static_scales=None):
+                 permute_pages=True, extra_pages=1, streams=None, static_scales=None, rope_table=True):
+        """rope_table (pre-RoPE keys): True, a table for every position the pages hold;
+        False, none (the decode kernel computes the cos/sin); an int n, a table of
+        the first n positions only."""
         import asymmetric_quantized_kv_gb300 as K
         self.cfg, self.lens, self.seed = cfg, list(lens), seed
         Bn, H, D, P = len(lens), cfg.num_kv_heads, cfg.head_dim, cfg.page_size
@@ -57,7 +60,12 @@ class Case:
             bt = W.page_permutation(n_pages, seed + 17)
         self.block_table = bt.reshape(Bn, self.maxp)
         self.c_cfg = to_c(cfg)
-        self.cache = K.PagedKVCache(self.c_cfg, Bn, self.maxp, n_pages, self.block_table)
+        if cfg.rope_pre and not isinstance(rope_table, bool):
+            n = int(rope_table)
+            table = torch.empty(K.kvq_rope_table_bytes(self.c_cfg, n), dtype=torch.uint8, device="cuda")
+            K.kvq_rope_table_init(self.c_cfg, n, table)
+            rope_table = (table, n)
+        self.cache = K.PagedKVCache(self.c_cfg, Bn, self.maxp, n_pages, self.block_table, rope_table=rope_table)
         if static_scales is not None:  # given per-head scales (e.g. the uncalibrated unit scale)
             self.k_scale = [float(O.fl32(x)) for x in static_scales[0]]
             self.v_scale = [float(O.fl32(x)) for x in static_scales[1]]

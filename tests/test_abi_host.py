@@ -169,3 +169,32 @@ def test_decode_kernel_batch_limit_on_the_host(K):
         fake = K.kvq_cache(4096, 4096, 4096, 4096, 4096, 4096, 4096, batch, 4, 8 * batch, 4096)
         assert L.kvq_decode_kernel(by(cfg), by(fake), by(out)) == K.KVQ_OK
         assert out.value == want, (batch, out.value)
+
+
+def test_rope_table_arguments_on_the_host(K):
+    """kvq_rope_table_bytes / kvq_rope_table_init argument checks, and the cache
+    struct's optional table (checked before anything is launched: a misaligned
+    table, a table on a config without pre-RoPE keys, or no positions)."""
+    L = K.binding.LIB
+    by = ctypes.byref
+    rope = _cfg(K)
+    plain = _cfg(K, rope_pre=0)
+    assert K.kvq_rope_table_bytes(rope, 100) == 100 * 128 * 4
+    assert K.kvq_rope_table_bytes(_cfg(K, head_dim=64, k=K.kvq_qspec(8, 0, 2, 64)), 3) == 3 * 64 * 4
+    assert K.kvq_rope_table_bytes(rope, 0) == 0
+    assert K.kvq_rope_table_bytes(plain, 100) == 0
+    assert L.kvq_rope_table_init(by(rope), 100, None, None) == K.KVQ_ERR_INVALID_ARG
+    assert L.kvq_rope_table_init(by(rope), 100, 4100, None) == K.KVQ_ERR_INVALID_ARG   # not 16-byte aligned
+    assert L.kvq_rope_table_init(by(rope), 0, 4096, None) == K.KVQ_ERR_INVALID_ARG
+    assert L.kvq_rope_table_init(by(plain), 100, 4096, None) == K.KVQ_ERR_INVALID_ARG
+    out = ctypes.c_int32(-1)
+    ok = K.kvq_cache(4096, 4096, 4096, 4096, 4096, 4096, 4096, 2, 4, 8, 4096, 8192, 64)
+    assert L.kvq_decode_kernel(by(rope), by(ok), by(out)) == K.KVQ_OK and out.value == K.KVQ_KERNEL_ROPE_I8I4
+    for table, n, cfg in ((8200, 64, rope), (8192, 0, rope), (8192, 64, plain)):
+        bad = K.kvq_cache(4096, 4096, 4096, 4096, 4096, 4096, 4096, 2, 4, 8, 4096, table, n)
+        assert L.kvq_decode_kernel(by(cfg), by(bad), by(out)) == K.KVQ_ERR_INVALID_ARG, (table, n)
+        assert L.kvq_decode_attention(by(cfg), by(bad), 4096, 4096, 0.0, 4096, 1 << 30, None) == \
+            K.KVQ_ERR_INVALID_ARG
+    # no table: rope_positions is ignored
+    none = K.kvq_cache(4096, 4096, 4096, 4096, 4096, 4096, 4096, 2, 4, 8, 4096, None, -5)
+    assert L.kvq_decode_kernel(by(rope), by(none), by(out)) == K.KVQ_OK

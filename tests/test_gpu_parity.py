@@ -15,7 +15,7 @@ from oracle import kvq_oracle as O  # noqa: E402
 if not torch.cuda.is_available():  # pragma: no cover
     pytest.skip("needs a CUDA GPU", allow_module_level=True)
 
-from kvq_testlib import Case  # noqa: E402
+from kvq_testlib import Case, to_c, torch_src  # noqa: E402
 
 Q = O.QSpec
 A, S = O.ASYM, O.SYM
@@ -153,6 +153,50 @@ def test_attention_within_tolerance(case):
 
 def test_attention_custom_scale(case):
     case.check_attention(scale=0.05)
+
+
+@pytest.mark.parametrize("name", ["fast_rope_i8i4_p16", "m16_fast_rope_p16", "fast_rope_i8i4_g128"])
+def test_rope_table_paths(name):
+    """The pre-RoPE tensor-core kernel with the cos/sin computed in the kernel
+    (no table, and a table too short for the cache, which the kernel then does
+    not use) and copied from a table of every position: each within the
+    tolerance of the oracle, and the outputs within 5e-5 of each other (the
+    kernel's own cos/sin follow a recurrence reseeded every 512 tokens; the
+    table's are computed per position)."""
+    import asymmetric_quantized_kv_gb300 as K
+    cfg, lens = CASES[name]
+    outs = []
+    for rope_table in (False, 200, True):
+        c = Case(cfg, lens, seed=5, rope_table=rope_table)
+        assert c.cache.decode_kernel() == K.KVQ_KERNEL_ROPE_I8I4
+        c.check_attention()
+        q = c.queries()
+        outs.append(c.cache.attention(torch_src(q, cfg)).cpu().numpy().astype(np.float64))
+    for o in outs[:2]:
+        err = np.linalg.norm(o - outs[2], axis=-1) / np.maximum(np.linalg.norm(outs[2], axis=-1), 1e-30)
+        assert float(err.max()) <= 5e-5, float(err.max())
+
+
+def test_rope_table_values():
+    """kvq_rope_table_init against the oracle's rotation angles (float64 cos and
+    sin of p * theta^(-2i/D)): every (position, pair) of 70,000 positions to
+    2e-6, read through the table's private arrangement (row p holds pairs
+    (2u, 2u+1) as (cos, cos, sin, sin) at slot u ^ ((2 (u / 8) + p % 2) % 8))."""
+    import asymmetric_quantized_kv_gb300 as K
+    for D, theta in ((128, 5e5), (64, 1e4)):
+        cfg = to_c(O.Config(8, 2, D, Q(O.INT8, S, CH, 64), Q(O.INT4, A, TOK, 0), 64, 16, 1, theta, O.BF16))
+        n = 70000
+        table = torch.empty(K.kvq_rope_table_bytes(cfg, n), dtype=torch.uint8, device="cuda")
+        K.kvq_rope_table_init(cfg, n, table)
+        t = table.view(torch.float32).view(n, D // 4, 4).cpu().numpy().astype(np.float64)
+        U = D // 4
+        p = np.arange(n)[:, None]
+        u = np.arange(U)[None, :]
+        slot = u ^ (((2 * (u >> 3)) | (p & 1)) & 7)
+        got = np.take_along_axis(t, np.broadcast_to(slot[..., None], (n, U, 4)), axis=1)
+        ang = O.rope_angles(np.arange(n), D, theta)  # [n, D/2]
+        want = np.stack([np.cos(ang[:, 0::2]), np.cos(ang[:, 1::2]), np.sin(ang[:, 0::2]), np.sin(ang[:, 1::2])], -1)
+        assert float(np.abs(got - want).max()) <= 2e-6, (D, float(np.abs(got - want).max()))
 
 
 @pytest.mark.parametrize("chunking", ["all", "one"])
