@@ -186,7 +186,7 @@ class FullCase:
     absmax taken by torch, so the oracle and the library quantize with the same
     scale without the library computing it."""
 
-    def __init__(self, cid, samples, gen_seed=1, fp8="e4m3", meta="f32"):
+    def __init__(self, cid, samples, gen_seed=1, fp8="e4m3", meta="f32", rope_table=True):
         import bench
         import asymmetric_quantized_kv_gb300 as K
         spec = bench.workload_spec(cid, 0, fp8, meta)
@@ -205,7 +205,7 @@ class FullCase:
         for b in range(Bn):
             bt[b, :need[b]] = perm[o:o + need[b]]
             o += need[b]
-        self.cache = K.PagedKVCache(to_c(self.cfg), Bn, maxp, n_pages, bt)
+        self.cache = K.PagedKVCache(to_c(self.cfg), Bn, maxp, n_pages, bt, rope_table=rope_table)
         dev = torch.device("cuda")
         scale = W.torch_outlier_scale(w, dev)
         g = torch.Generator(device=dev)

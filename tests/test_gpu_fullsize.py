@@ -68,8 +68,8 @@ def test_every_stream_of_the_2bit_layer_against_the_oracle(meta):
     torch.cuda.empty_cache()
 
 
-@pytest.mark.parametrize("cid", [4, 5])
-def test_every_sequence(cid):
+@pytest.mark.parametrize("cid,rope_table", [(4, True), (5, True), (5, False)])
+def test_every_sequence(cid, rope_table):
     """Every (sequence, query head) of the full layer against attention computed
     in float64 by torch over the cache's own dequantized keys and values
     (kvq_dequantize, bit-exact against the oracle over the whole sampled streams above),
@@ -77,8 +77,9 @@ def test_every_sequence(cid):
     whole chunks, pieces and the window (the paged layer's plan cuts its final
     round of chunks and its partial chunks into quarter pieces): a token the plan
     dropped or counted twice moves its sequence's output far beyond the
-    tolerance."""
-    case = FullCase(cid, [])
+    tolerance.  The paged layer runs both pre-RoPE kernel instances: RoPE
+    tables copied from the cache's table, and computed by the kernel."""
+    case = FullCase(cid, [], rope_table=rope_table)
     cfg, w = case.cfg, case.w
     H, D, n_rep = w.num_kv_heads, w.head_dim, cfg.n_rep
     out = case.cache.attention(case.q).double()
@@ -101,7 +102,8 @@ def test_every_sequence(cid):
         err = (torch.linalg.norm(out[b] - ref, dim=1) / torch.linalg.norm(ref, dim=1)).max().item()
         worst = max(worst, err)
         del k, v, p, ref
-    print(f"\nlayer {cid}: worst relative L2 over every (sequence, query head) {worst:.3e}")
+    print(f"\nlayer {cid} (RoPE table {rope_table}): worst relative L2 over every (sequence, query head) "
+          f"{worst:.3e}")
     assert worst <= 1e-3, worst
     assert int(case.cache.status.item()) == 0
     del case
