@@ -158,6 +158,7 @@ kvq_status kvq_rope_table_init(const kvq_config* c, int32_t positions, void* tab
   if (!kvq::make_view(c, nullptr, &v)) return kvq_validate(c);
   if (!c->rope_pre || positions < 1 || !table || (reinterpret_cast<uintptr_t>(table) & 15))
     return KVQ_ERR_INVALID_ARG;
+  if (positions > (1 << 24)) return KVQ_ERR_CAPACITY;
   return kvq::launch_rope_table(v, positions, table, (cudaStream_t)stream);
 }
 

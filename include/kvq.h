@@ -201,7 +201,8 @@ size_t kvq_rope_table_bytes(const kvq_config* cfg, int32_t positions);
  * table is private to the library.  table: device, kvq_rope_table_bytes bytes,
  * 16-byte aligned, overwritten.  Enqueued on `stream`; no synchronisation.
  * KVQ_ERR_INVALID_ARG for a null or misaligned table, positions < 1, or a
- * config without pre-RoPE keys. */
+ * config without pre-RoPE keys; KVQ_ERR_CAPACITY above 2^24 positions (the
+ * angle reduction, here and in the kernel, is exact below that). */
 kvq_status kvq_rope_table_init(const kvq_config* cfg, int32_t positions, void* table, void* stream);
 
 /* KVQ_OK when the configuration is consistent and supported, else the reason. */

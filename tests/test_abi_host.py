@@ -187,6 +187,7 @@ def test_rope_table_arguments_on_the_host(K):
     assert L.kvq_rope_table_init(by(rope), 100, 4100, None) == K.KVQ_ERR_INVALID_ARG   # not 16-byte aligned
     assert L.kvq_rope_table_init(by(rope), 0, 4096, None) == K.KVQ_ERR_INVALID_ARG
     assert L.kvq_rope_table_init(by(plain), 100, 4096, None) == K.KVQ_ERR_INVALID_ARG
+    assert L.kvq_rope_table_init(by(rope), (1 << 24) + 1, 4096, None) == K.KVQ_ERR_CAPACITY
     out = ctypes.c_int32(-1)
     ok = K.kvq_cache(4096, 4096, 4096, 4096, 4096, 4096, 4096, 2, 4, 8, 4096, 8192, 64)
     assert L.kvq_decode_kernel(by(rope), by(ok), by(out)) == K.KVQ_OK and out.value == K.KVQ_KERNEL_ROPE_I8I4
