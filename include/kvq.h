@@ -46,6 +46,11 @@
  *     opens an NVTX range named after itself in the "libkvq" domain, so a
  *     profiler can attribute the kernels to the call; with no profiler
  *     attached a range costs a pointer test.
+ *   - Those calls can be captured into a CUDA graph (stream capture) once the
+ *     same call has run uncaptured on the device: the first call of a kernel
+ *     on a device sets its launch attributes.  A replay re-reads the cache
+ *     struct's device buffers (lengths, block table), so replaying an append
+ *     and a decode advances the cache exactly as eager calls do.
  *
  * Quantization rules (bit-exact; all arithmetic IEEE fp32 round-to-nearest-
  * even, no fused multiply-add, in exactly this order):
