@@ -31,8 +31,9 @@ class PagedKVCache:
     def __init__(self, cfg, batch, max_pages_per_seq, n_pages=None, block_table=None, device="cuda",
                  rope_table=True):
         """rope_table (pre-RoPE keys only): True builds a table for every position the
-        pages can hold, False leaves the decode kernel to compute the cos/sin, and a
-        (tensor, positions) pair shares a table built by kvq_rope_table_init."""
+        pages can hold (rounded up to a multiple of 32, as the kernel reads whole
+        32-position tables), False leaves the decode kernel to compute the cos/sin,
+        and a (tensor, positions) pair shares a table built by kvq_rope_table_init."""
         self.cfg = cfg
         self.batch = batch
         self.max_pages = max_pages_per_seq
@@ -57,7 +58,7 @@ class PagedKVCache:
         self.rope_table, self.rope_positions = None, 0
         if cfg.rope_pre and rope_table is not False:
             if rope_table is True:
-                n = max_pages_per_seq * cfg.page_size
+                n = (max_pages_per_seq * cfg.page_size + 31) // 32 * 32  # whole 32-position tables
                 self.rope_table = torch.empty(B.kvq_rope_table_bytes(cfg, n), dtype=torch.uint8, device=dev)
                 self.rope_positions = n
                 B.kvq_rope_table_init(cfg, n, self.rope_table)

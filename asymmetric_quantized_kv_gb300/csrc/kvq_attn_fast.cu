@@ -21,9 +21,10 @@
 //   RoPE table: cos/sin of every (token, pair) of two tiles, in one of two
 //       shared buffers handed between the 8 warps through full/empty mbarriers,
 //       so warps may drift by up to two tiles instead of meeting at a CTA
-//       barrier every tile.  With the caller's table (kvq_cache.rope_table) the
-//       buffer is filled by one bulk copy of its 32 rows; otherwise (or past
-//       the table's end) the CTA computes it.
+//       barrier every tile.  With the caller's table (kvq_cache.rope_table,
+//       covering every position the pages hold, rounded up to a whole table) a
+//       second instance fills the buffer with one bulk copy of its 32 rows,
+//       requested one table ahead; otherwise the CTA computes it.
 //   softmax: online in base 2, one running max per head, raised lazily (only
 //       when a logit exceeds it by more than 2^8; the common tile needs no
 //       cross-lane reduction).
@@ -311,7 +312,10 @@ __global__ void __launch_bounds__(kThreads, 2)
   const float4* rope_tab = static_cast<const float4*>(v.rope_table);
   // thread 0: copy CTA table tcp (first token tok0) into its buffer once the
   // warps are done with the buffer's previous use; this arrival carries the
-  // byte count (a timed-out wait leaves the buffer as it is)
+  // byte count (a timed-out wait leaves the buffer as it is).  tok0 is a
+  // multiple of 32 (items start on key-group boundaries, G >= 32), so the rows
+  // have the shared table's parity, and tok0 + 32 <= rope_positions (the host
+  // takes this instance only then)
   auto issue_copy = [&](uint32_t tcp, int tok0) {
     const uint32_t b = tcp & 1;
     if (tcp >= 2) bounded_wait(&sm.tempty[b], ((tcp >> 1) - 1) & 1, stalled, v.status);
@@ -705,8 +709,10 @@ size_t fast_workspace_bytes(const KvqView& v, int batch) { return split_workspac
 kvq_status launch_fast(const KvqView& v, const void* q, float* out, float scale, void* ws,
                        cudaStream_t st) {
   const size_t smem = sizeof(SmemRI) + sizeof(int) * 2 * (v.batch + 1);
-  // the caller's RoPE table when it covers every position the cache can hold
-  const bool tab = v.rope_table != nullptr && (long long)v.rope_positions >= (long long)v.max_pages * v.P;
+  // the caller's RoPE table when it covers every position the cache can hold,
+  // rounded up to a whole table (the last table's copy reads all 32 rows)
+  const long long span = ((long long)v.max_pages * v.P + kSuper * kTile - 1) / (kSuper * kTile) * (kSuper * kTile);
+  const bool tab = v.rope_table != nullptr && (long long)v.rope_positions >= span;
   const int m = (v.meta16 ? 1 : 0) + (tab ? 2 : 0);
   auto kern = m == 3   ? split_rope_i8i4_kernel<true, true>
               : m == 2 ? split_rope_i8i4_kernel<false, true>

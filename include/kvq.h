@@ -180,9 +180,10 @@ typedef struct {
    * config, covering positions [0, rope_positions), rope_positions >= 1.
    * Device, 16-byte aligned, owned by the caller, read only, and shareable by
    * every cache with the same head_dim and rope_theta.  When it covers every
-   * position the pages can hold (rope_positions >= max_pages_per_seq *
-   * page_size), the pre-RoPE tensor-core decode kernel copies the cos/sin from
-   * it instead of computing them; otherwise the kernel computes them (same
+   * position the pages can hold, rounded up to a multiple of 32
+   * (rope_positions >= max_pages_per_seq * page_size rounded up), the pre-RoPE
+   * tensor-core decode kernel copies the cos/sin from it, 32 positions at a
+   * time, instead of computing them; otherwise the kernel computes them (same
    * results to ~1e-6 relative).  KVQ_ERR_INVALID_ARG for a table that is
    * misaligned, set for a config without pre-RoPE keys, or with
    * rope_positions < 1. */

@@ -177,6 +177,21 @@ def test_rope_table_paths(name):
         assert float(err.max()) <= 5e-5, float(err.max())
 
 
+@pytest.mark.parametrize("rope_table", [80, 96, True])
+def test_rope_table_on_a_full_cache_of_80_positions(rope_table):
+    """A cache of 5 pages of 16 tokens (80 positions, not a whole number of the
+    kernel's 32-position tables) filled to capacity: a table of exactly 80
+    positions is not used (the last table's copy would read past its end), one
+    of 96 is, and the cache wrapper rounds its own table up to 96; all within
+    tolerance of the oracle."""
+    cfg, _ = CASES["fast_rope_i8i4_p16"]
+    c = Case(cfg, [80, 33, 64], seed=6, extra_pages=0, rope_table=rope_table)
+    assert c.maxp * cfg.page_size == 80
+    if rope_table is True:
+        assert c.cache.rope_positions == 96
+    c.check_attention()
+
+
 def test_rope_table_values():
     """kvq_rope_table_init against the oracle's rotation angles (float64 cos and
     sin of p * theta^(-2i/D)): every (position, pair) of 70,000 positions to
