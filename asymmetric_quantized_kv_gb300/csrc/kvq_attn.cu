@@ -29,12 +29,20 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 // Work split: an item (sequence, kv-head, head block, chunk of C tokens) runs on
 // one CTA of 4 warps; each warp takes sub-tiles of kST tokens.  Per sub-tile the
-// warp dequantizes the K rows into shared memory (lanes over 32-bit code words,
-// so each row is one coalesced read), computes the logits with one lane per
-// token, dequantizes the V rows into the same buffer and accumulates P*V with
-// lanes over channels.  Short sub-tiles keep the serial path of a warp short:
+// warp dequantizes the K rows into shared memory (lanes over 32-bit code words;
+// rows of fewer than 32 words share a pass), computes the logits with the lanes
+// over (token, head group or channel part), dequantizes the V rows into the same
+// buffer and accumulates P*V with lanes over channels.  Short sub-tiles keep the serial path of a warp short:
 // small calls are latency-bound, and C shrinks to 32 tokens there.
 constexpr int kST = 8;
+// The sub-tile's packed K and V rows (with per-token scale/min entries of up to
+// kMetaStage bytes a token, and the key group's per-channel entries when the
+// sub-tile lies in one group) are copied to shared memory with cp.async before
+// any is dequantized: all the sub-tile's reads are in flight at once.  A warp's
+// first sub-tile is requested before the query is loaded, each later one as soon
+// as the previous sub-tile's V rows are dequantized (its P*V and the next logits
+// overlap the copies).
+constexpr int kMetaStage = 64;
 
 // Dequantization rule of one side (K or V) for a call, resolved once.
 struct DeqRule {
@@ -118,24 +126,6 @@ __device__ __forceinline__ void deq_word(uint32_t w, int c0, const DeqRule& r, c
   for (int e = 0; e < N; e += 4) *reinterpret_cast<float4*>(dst + e) = make_float4(x[e], x[e + 1], x[e + 2], x[e + 3]);
 }
 
-// One token's packed row (row_bytes = D*bits/8) -> dst[0..D) fp32, lanes over words.
-template <int BITS>
-__device__ __forceinline__ void deq_row_t(const uint8_t* row, int row_bytes, const DeqRule& r, const uint8_t* meta,
-                                          int D, int m16, float ts, float* dst, int lane) {
-  const int nw = row_bytes >> 2;
-  for (int wi = lane; wi < nw; wi += 32) {
-    const uint32_t w = reinterpret_cast<const uint32_t*>(row)[wi];
-    const int c0 = wi * (32 / BITS);
-    deq_word<BITS>(w, c0, r, meta, D, m16, ts, dst + c0);
-  }
-}
-__device__ __forceinline__ void deq_row(const uint8_t* row, int row_bytes, const DeqRule& r, const uint8_t* meta,
-                                        int D, int m16, float ts, float* dst, int lane) {
-  if (r.bits == 8) deq_row_t<8>(row, row_bytes, r, meta, D, m16, ts, dst, lane);
-  else if (r.bits == 4) deq_row_t<4>(row, row_bytes, r, meta, D, m16, ts, dst, lane);
-  else deq_row_t<2>(row, row_bytes, r, meta, D, m16, ts, dst, lane);
-}
-
 // One window row (source dtype) -> dst[0..D), lanes over channel quads.
 __device__ __forceinline__ void copy_src_row(const void* base, long long row_elem, int D, int bf16, float* dst,
                                              int lane) {
@@ -152,6 +142,73 @@ __device__ __forceinline__ void copy_src_row(const void* base, long long row_ele
   }
 }
 
+// 4-byte asynchronous copy global -> shared (both 4-byte aligned), and its groups.
+__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(ptx::smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+
+// n staged rows (row tt at stage + tt*D) -> buf rows (stride DP floats), lanes
+// over (row, 32-bit word): a row of nw < 32 words takes nw lanes, so 32/nw rows
+// go per pass.  meta_of(tt) gives row tt's scale/min entries (every lane calls
+// it: it may shuffle); rows marked in `bad` are written as zeros.
+template <int BITS, typename MetaOf>
+__device__ __forceinline__ void deq_staged_t(const uint8_t* stage, int D, int DP, int n, unsigned bad, int row_bytes,
+                                             const DeqRule& r, MetaOf meta_of, int m16, float ts, float* buf,
+                                             int lane) {
+  constexpr int N = 32 / BITS;
+  const int nw = row_bytes >> 2;  // a power of two, 4..64
+  const int rpp = nw >= 32 ? 1 : 32 / nw;
+  const int sub = nw >= 32 ? 0 : lane / nw, wl = nw >= 32 ? lane : lane % nw;
+  for (int t0 = 0; t0 < n; t0 += rpp) {
+    const int tt = t0 + sub;
+    const uint8_t* meta = meta_of(tt);
+    if (tt < n) {
+      float* dst = buf + tt * DP;
+      const uint32_t* row = reinterpret_cast<const uint32_t*>(stage + tt * D);
+      for (int wi = wl; wi < nw; wi += 32) {
+        if ((bad >> tt) & 1u) {
+#pragma unroll
+          for (int e = 0; e < N; e += 4) *reinterpret_cast<float4*>(dst + wi * N + e) = make_float4(0.f, 0.f, 0.f, 0.f);
+        } else {
+          deq_word<BITS>(row[wi], wi * N, r, meta, D, m16, ts, dst + wi * N);
+        }
+      }
+    }
+  }
+}
+template <typename MetaOf>
+__device__ __forceinline__ void deq_staged(const uint8_t* stage, int D, int DP, int n, unsigned bad, int row_bytes,
+                                           const DeqRule& r, MetaOf meta_of, int m16, float ts, float* buf, int lane) {
+  if (r.bits == 8) deq_staged_t<8>(stage, D, DP, n, bad, row_bytes, r, meta_of, m16, ts, buf, lane);
+  else if (r.bits == 4) deq_staged_t<4>(stage, D, DP, n, bad, row_bytes, r, meta_of, m16, ts, buf, lane);
+  else deq_staged_t<2>(stage, D, DP, n, bad, row_bytes, r, meta_of, m16, ts, buf, lane);
+}
+
+// Max and sum over the 8 lanes of a lane's group of 8 (lanes 8g .. 8g+7).
+__device__ __forceinline__ float max8(float x) {
+  for (int o = 1; o < 8; o <<= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+  return x;
+}
+__device__ __forceinline__ float sum8(float x) {
+  for (int o = 1; o < 8; o <<= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
+
+// What a staged sub-tile's dequantization reads besides the staging: lane tt's
+// K and V entry pointers (used where they are not staged), the missing-page mask,
+// and whether the key group's per-channel entries were staged.
+struct TileRefs {
+  const uint8_t* km;
+  const uint8_t* vm;
+  unsigned bad;
+  bool kc;
+};
+
 // Lane src's pointer, to every lane.
 __device__ __forceinline__ const uint8_t* shfl_ptr(const uint8_t* p, int src) {
   const unsigned long long x = reinterpret_cast<unsigned long long>(p);
@@ -160,14 +217,6 @@ __device__ __forceinline__ const uint8_t* shfl_ptr(const uint8_t* p, int src) {
   return reinterpret_cast<const uint8_t*>((static_cast<unsigned long long>(hi) << 32) | lo);
 }
 
-__device__ __forceinline__ float warp_max(float x) {
-  for (int o = 16; o; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
-  return x;
-}
-__device__ __forceinline__ float warp_sum(float x) {
-  for (int o = 16; o; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-  return x;
-}
 
 // Partial record of one (item, query head of the block): running max, sum, two
 // pad words, then D outputs (16-byte aligned).
@@ -183,13 +232,16 @@ struct GenericSmem {
 
 // Dynamic shared memory: GenericSmem, pref[B+1], then (16-byte aligned) per warp a
 // sub-tile buffer [kST][D+4] and its probabilities [kHB][kST], then the warps'
-// outputs [kWarps][kHB][D] for the CTA merge.
+// outputs [kWarps][kHB][D] for the CTA merge, then per warp the packed staging of
+// a sub-tile: K rows [kST][D bytes], K entries [kST][kMetaStage], the same for V,
+// and one key group's per-channel entries [8 D bytes].
 __host__ __device__ inline size_t generic_tiles_offset(int batch) {
   return (sizeof(GenericSmem) + sizeof(int) * (batch + 1) + 15) / 16 * 16;
 }
 __host__ __device__ inline size_t generic_smem_bytes(int batch, int D) {
   return generic_tiles_offset(batch) +
-         sizeof(float) * ((size_t)kWarps * kST * (D + 4) + (size_t)kWarps * kHB * kST + (size_t)kWarps * kHB * D);
+         sizeof(float) * ((size_t)kWarps * kST * (D + 4) + (size_t)kWarps * kHB * kST + (size_t)kWarps * kHB * D) +
+         (size_t)kWarps * (2 * kST * (D + kMetaStage) + 8 * D);
 }
 
 // NH: query heads per item at most (a power of two <= kHB); NJ = D / 32.
@@ -203,6 +255,11 @@ __global__ void __launch_bounds__(kThreads) split_generic_kernel(KvqView v, cons
   float* buf = reinterpret_cast<float*>(dyn + generic_tiles_offset(v.batch)) + warp * kST * DP;
   float* ps = reinterpret_cast<float*>(dyn + generic_tiles_offset(v.batch)) + kWarps * kST * DP + warp * kHB * kST;
   float* wo = reinterpret_cast<float*>(dyn + generic_tiles_offset(v.batch)) + kWarps * kST * DP + kWarps * kHB * kST;
+  uint8_t* sk = reinterpret_cast<uint8_t*>(wo + kWarps * kHB * D) + warp * (2 * kST * (D + kMetaStage) + 8 * D);
+  uint8_t* skm = sk + kST * D;
+  uint8_t* sv = skm + kST * kMetaStage;
+  uint8_t* svm = sv + kST * D;
+  uint8_t* skc = svm + kST * kMetaStage;
   const int HB = (v.n_rep + kHB - 1) / kHB;
   __shared__ int s_C, s_items;
   plan_items(v, HB, pref, &s_C, &s_items);
@@ -215,6 +272,10 @@ __global__ void __launch_bounds__(kThreads) split_generic_kernel(KvqView v, cons
   const DeqRule kr = make_rule(v.kfmt, v.kmode, v.kaxis, v.kgroup, v.kbits, v.k_ng);
   const DeqRule vr = make_rule(v.vfmt, v.vmode, v.vaxis, v.vgroup, v.vbits, v.v_ng);
   const int kmeta_tok = v.k_ng * v.k_nmeta * v.mb, vmeta_tok = v.v_ng * v.v_nmeta * v.mb;
+  // per-token entries that are staged with the rows (whole 4-byte words that fit)
+  const bool stage_km = kr.kind == kToken && kmeta_tok <= kMetaStage && (kmeta_tok & 3) == 0;
+  const bool stage_vm = vr.kind == kToken && vmeta_tok <= kMetaStage && (vmeta_tok & 3) == 0;
+  const int kmeta_ch = D * v.k_nmeta * v.mb;  // one key group's per-channel entries (<= 8 D bytes)
   const int src = v.src_bf16 ? 2 : 4;
   float* part = plan_partials(ws, v.batch);
   for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
@@ -222,30 +283,12 @@ __global__ void __launch_bounds__(kThreads) split_generic_kernel(KvqView v, cons
     const int nh = min(kHB, v.n_rep - it.hb * kHB);
     const float kts = (kr.kind == kFp8 || kr.kind == kTensor) ? v.k_scale[it.kvh] : 0.f;
     const float vts = (vr.kind == kFp8 || vr.kind == kTensor) ? v.v_scale[it.kvh] : 0.f;
-    __syncthreads();  // smem of the previous item is free
-    for (int e = threadIdx.x; e < NH * D; e += kThreads) {
-      const int hh = e / D, c = e % D;
-      float x = 0.f;
-      if (hh < nh) {
-        const int hq = it.kvh * v.n_rep + it.hb * kHB + hh;
-        x = load_src(q, ((long long)it.b * v.Hq + hq) * D + c, v.src_bf16) * scale * kLog2e;
-      }
-      sm.qs[hh][c] = x;
-    }
-    __syncthreads();
-    float m_run[NH], l_run[NH], o[NH][NJ];
-#pragma unroll
-    for (int hh = 0; hh < NH; ++hh) {
-      m_run[hh] = -INFINITY;
-      l_run[hh] = 0.f;
-#pragma unroll
-      for (int j = 0; j < NJ; ++j) o[hh][j] = 0.f;
-    }
     const long long wbase = ((long long)it.b * v.R - it.t0) * v.Hkv + it.kvh;  // window row of token t: wbase + t*Hkv
-    for (int tile = it.t0 + warp * kST; tile < it.t1; tile += kWarps * kST) {
+    // Sub-tile at token `tile` (warp-uniform): lane tt < n looks up token tile +
+    // tt's rows; the packed rows go to the warp's staging, K (copy group 1) then V
+    // (group 2).  Returns what the dequantization needs besides the staging.
+    auto stage_tile = [&](int tile) -> TileRefs {
       const int n = min(kST, it.t1 - tile);
-      // lane tt < n: the addresses of token tile + tt's rows (the warp reads them
-      // below, token by token), and the rows requested at once
       const uint8_t *a_k = nullptr, *a_km = nullptr, *a_v = nullptr, *a_vm = nullptr;
       bool ok = true;
       if (lane < n) {
@@ -265,7 +308,7 @@ __global__ void __launch_bounds__(kThreads) split_generic_kernel(KvqView v, cons
             a_vm = hb + v.off_vm + slot * vmeta_tok;
             if (kr.kind == kToken) {
               a_km = hb + v.off_km + slot * kmeta_tok;
-              ptx::prefetch_l1_range(a_km, kmeta_tok);
+              if (!stage_km) ptx::prefetch_l1_range(a_km, kmeta_tok);
             } else if (kr.kind == kChannel) {  // the key group's entries live in the page of its first token
               const int g0 = (t / v.kgroup) * v.kgroup;
               const uint8_t* gp = page_of(v, it.b, g0);
@@ -274,24 +317,92 @@ __global__ void __launch_bounds__(kThreads) split_generic_kernel(KvqView v, cons
                 a_km = gp + (long long)it.kvh * v.head_bytes + v.off_km +
                        (long long)((g0 % v.P) / v.kgroup) * D * v.k_nmeta * v.mb;
             }
-            ptx::prefetch_l1_range(a_k, v.krow);
-            ptx::prefetch_l1_range(a_v, v.vrow);
-            if (vr.kind == kToken) ptx::prefetch_l1_range(a_vm, vmeta_tok);
+            if (vr.kind == kToken && !stage_vm) ptx::prefetch_l1_range(a_vm, vmeta_tok);
           }
         }
       }
+      TileRefs r;
+      r.km = a_km;
+      r.vm = a_vm;
       // tokens whose page (or key group's page) is missing: logits -inf, V rows zero
-      const unsigned bad = __ballot_sync(0xffffffffu, lane < n && !ok);
-      // ---- K rows -> buf
-      for (int tt = 0; tt < n; ++tt) {
-        float* dst = buf + tt * DP;
-        if (it.window) {
-          copy_src_row(v.k_win, (wbase + (long long)(tile + tt) * v.Hkv) * D, D, v.src_bf16, dst, lane);
-        } else if ((bad >> tt) & 1u) {
-          for (int c = lane; c < D; c += 32) dst[c] = 0.f;
-        } else {
-          deq_row(shfl_ptr(a_k, tt), v.krow, kr, shfl_ptr(a_km, tt), D, v.meta16, kts, dst, lane);
+      r.bad = __ballot_sync(0xffffffffu, lane < n && !ok);
+      r.kc = false;
+      if (!it.window) {
+        for (int tt = 0; tt < n; ++tt) {
+          if ((r.bad >> tt) & 1u) continue;
+          const uint8_t* pk = shfl_ptr(a_k, tt);
+          for (int w = lane; w < (v.krow >> 2); w += 32) cp_async4(sk + tt * D + 4 * w, pk + 4 * w);
+          if (stage_km) {
+            const uint8_t* pm = shfl_ptr(a_km, tt);
+            if (lane < (kmeta_tok >> 2)) cp_async4(skm + tt * kMetaStage + 4 * lane, pm + 4 * lane);
+          }
         }
+        r.kc = kr.kind == kChannel && !(r.bad & 1u) && tile / v.kgroup == (tile + n - 1) / v.kgroup;
+        if (r.kc) {
+          const uint8_t* pm = shfl_ptr(a_km, 0);
+          for (int w = lane; w < (kmeta_ch >> 2); w += 32) cp_async4(skc + 4 * w, pm + 4 * w);
+        }
+        cp_async_commit();
+        for (int tt = 0; tt < n; ++tt) {
+          if ((r.bad >> tt) & 1u) continue;
+          const uint8_t* pv = shfl_ptr(a_v, tt);
+          for (int w = lane; w < (v.vrow >> 2); w += 32) cp_async4(sv + tt * D + 4 * w, pv + 4 * w);
+          if (stage_vm) {
+            const uint8_t* pm = shfl_ptr(a_vm, tt);
+            if (lane < (vmeta_tok >> 2)) cp_async4(svm + tt * kMetaStage + 4 * lane, pm + 4 * lane);
+          }
+        }
+        cp_async_commit();
+      }
+      return r;
+    };
+    // the query's loads go out first, then the first sub-tile's lookups and copies
+    constexpr int QPT = (NH * D + kThreads - 1) / kThreads;
+    float qv[QPT];
+#pragma unroll
+    for (int i = 0; i < QPT; ++i) {
+      const int e = threadIdx.x + i * kThreads, hh = e / D, c = e % D;
+      qv[i] = 0.f;
+      if (e < NH * D && hh < nh) {
+        const int hq = it.kvh * v.n_rep + it.hb * kHB + hh;
+        qv[i] = load_src(q, ((long long)it.b * v.Hq + hq) * D + c, v.src_bf16) * scale * kLog2e;
+      }
+    }
+    __syncthreads();  // smem of the previous item is free
+    int tile = it.t0 + warp * kST;
+    TileRefs tr{nullptr, nullptr, 0u, false};
+    if (tile < it.t1) tr = stage_tile(tile);
+#pragma unroll
+    for (int i = 0; i < QPT; ++i) {
+      const int e = threadIdx.x + i * kThreads;
+      if (e < NH * D) sm.qs[e / D][e % D] = qv[i];
+    }
+    __syncthreads();
+    float m_run[NH], l_run[NH], o[NH][NJ];
+#pragma unroll
+    for (int hh = 0; hh < NH; ++hh) {
+      m_run[hh] = -INFINITY;
+      l_run[hh] = 0.f;
+#pragma unroll
+      for (int j = 0; j < NJ; ++j) o[hh][j] = 0.f;
+    }
+    for (; tile < it.t1; tile += kWarps * kST) {
+      const int n = min(kST, it.t1 - tile);
+      const unsigned bad = tr.bad;
+      if (!it.window) {
+        cp_async_wait<1>();
+        __syncwarp();
+      }
+      // ---- K rows -> buf
+      if (it.window) {
+        for (int tt = 0; tt < n; ++tt)
+          copy_src_row(v.k_win, (wbase + (long long)(tile + tt) * v.Hkv) * D, D, v.src_bf16, buf + tt * DP, lane);
+      } else {
+        const TileRefs& rf = tr;
+        auto km_of = [&](int tt) -> const uint8_t* {
+          return rf.kc ? skc : stage_km ? skm + tt * kMetaStage : shfl_ptr(rf.km, tt);
+        };
+        deq_staged(sk, D, DP, n, bad, v.krow, kr, km_of, v.meta16, kts, buf, lane);
       }
       __syncwarp();
       if (v.rope_pre) {  // rotate the pairs in place: lanes over (token, pair)
@@ -305,51 +416,85 @@ __global__ void __launch_bounds__(kThreads) split_generic_kernel(KvqView v, cons
         }
         __syncwarp();
       }
-      // ---- logits: lane = token
-      const bool valid = lane < n && !((bad >> lane) & 1u);
-      float acc[NH];
+      // ---- logits: lane = token tt + 8 g.  With 4 or more heads, lane group g
+      // takes heads g*HPG .. g*HPG+HPG-1 over all channels; with 1 or 2 heads,
+      // CPG groups share a head, each over D/CPG channels, and add their parts.
+      constexpr int HPG = NH >= 4 ? NH / 4 : 1, CPG = NH >= 4 ? 1 : 4 / NH;
+      const int tt = lane & 7, g = lane >> 3;
+      const int h0 = NH >= 4 ? g * HPG : g / CPG, cb = NH >= 4 ? 0 : (g % CPG) * (D / CPG);
+      const bool valid = tt < n && !((bad >> tt) & 1u);
+      float acc[HPG];
 #pragma unroll
-      for (int hh = 0; hh < NH; ++hh) acc[hh] = 0.f;
+      for (int j = 0; j < HPG; ++j) acc[j] = 0.f;
       if (valid) {
-        const float* krow = buf + lane * DP;
-        for (int c = 0; c < D; c += 4) {
+        const float* krow = buf + tt * DP + cb;
+#pragma unroll 4
+        for (int c = 0; c < D / CPG; c += 4) {
           const float4 k4 = *reinterpret_cast<const float4*>(krow + c);
 #pragma unroll
-          for (int hh = 0; hh < NH; ++hh) {
-            if (hh < nh) {
-              const float4 q4 = *reinterpret_cast<const float4*>(&sm.qs[hh][c]);
-              acc[hh] += q4.x * k4.x + q4.y * k4.y + q4.z * k4.z + q4.w * k4.w;
-            }
+          for (int j = 0; j < HPG; ++j) {
+            const float4 q4 = *reinterpret_cast<const float4*>(&sm.qs[h0 + j][cb + c]);
+            acc[j] += q4.x * k4.x + q4.y * k4.y + q4.z * k4.z + q4.w * k4.w;
           }
         }
       }
+      if (CPG >= 2) acc[0] += __shfl_xor_sync(0xffffffffu, acc[0], 8);
+      if (CPG >= 4) acc[0] += __shfl_xor_sync(0xffffffffu, acc[0], 16);
+      float lg[HPG], mx[HPG];
+#pragma unroll
+      for (int j = 0; j < HPG; ++j) {
+        lg[j] = valid && h0 + j < nh ? acc[j] : -INFINITY;
+        mx[j] = max8(lg[j]);
+      }
+      // every lane updates every head's running max, sum and output; the group
+      // holding head hh supplies its max and probability sum
+      float mine[HPG];
+#pragma unroll
+      for (int j = 0; j < HPG; ++j) mine[j] = -INFINITY;
+      float alpha[NH];
 #pragma unroll
       for (int hh = 0; hh < NH; ++hh) {
-        if (hh < nh) {
-          const float lg = valid ? acc[hh] : -INFINITY;
-          const float m_new = fmaxf(m_run[hh], warp_max(lg));
-          const float alpha = m_new == -INFINITY ? 1.f : exp2f(m_run[hh] - m_new);
-          const float p = valid ? exp2f(lg - m_new) : 0.f;
-          l_run[hh] = l_run[hh] * alpha + warp_sum(p);
-          m_run[hh] = m_new;
+        const int src_lane = (NH >= 4 ? hh / HPG : hh * CPG) * 8;
+        const float m_new = fmaxf(m_run[hh], __shfl_sync(0xffffffffu, mx[hh % HPG], src_lane));
+        alpha[hh] = m_new == -INFINITY ? 1.f : exp2f(m_run[hh] - m_new);
+        m_run[hh] = m_new;
+        if (h0 + hh % HPG == hh) mine[hh % HPG] = m_new;
+      }
+      float psum[HPG];
 #pragma unroll
-          for (int j = 0; j < NJ; ++j) o[hh][j] *= alpha;
-          if (lane < kST) ps[hh * kST + lane] = p;
+      for (int j = 0; j < HPG; ++j) {
+        const float p = valid && h0 + j < nh ? exp2f(lg[j] - mine[j]) : 0.f;
+        if (cb == 0 && h0 + j < nh) ps[(h0 + j) * kST + tt] = p;
+        psum[j] = sum8(p);
+      }
+#pragma unroll
+      for (int hh = 0; hh < NH; ++hh) {
+        const int src_lane = (NH >= 4 ? hh / HPG : hh * CPG) * 8;
+        const float ls = __shfl_sync(0xffffffffu, psum[hh % HPG], src_lane);
+        if (hh < nh) {
+          l_run[hh] = l_run[hh] * alpha[hh] + ls;
+#pragma unroll
+          for (int j = 0; j < NJ; ++j) o[hh][j] *= alpha[hh];
         }
       }
       __syncwarp();
       // ---- V rows -> buf (marked tokens: zeros; their p is 0)
-      for (int tt = 0; tt < n; ++tt) {
-        float* dst = buf + tt * DP;
-        if (it.window) {
-          copy_src_row(v.v_win, (wbase + (long long)(tile + tt) * v.Hkv) * D, D, v.src_bf16, dst, lane);
-        } else if ((bad >> tt) & 1u) {
-          for (int c = lane; c < D; c += 32) dst[c] = 0.f;
-        } else {
-          deq_row(shfl_ptr(a_v, tt), v.vrow, vr, shfl_ptr(a_vm, tt), D, v.meta16, vts, dst, lane);
-        }
+      if (!it.window) {
+        cp_async_wait<0>();
+        __syncwarp();
+      }
+      if (it.window) {
+        for (int tt = 0; tt < n; ++tt)
+          copy_src_row(v.v_win, (wbase + (long long)(tile + tt) * v.Hkv) * D, D, v.src_bf16, buf + tt * DP, lane);
+      } else {
+        const TileRefs& rf = tr;
+        auto vm_of = [&](int tt) -> const uint8_t* {
+          return stage_vm ? svm + tt * kMetaStage : shfl_ptr(rf.vm, tt);
+        };
+        deq_staged(sv, D, DP, n, bad, v.vrow, vr, vm_of, v.meta16, vts, buf, lane);
       }
       __syncwarp();
+      if (tile + kWarps * kST < it.t1) tr = stage_tile(tile + kWarps * kST);  // the staging is free again
       // ---- P V: lanes over channels
       for (int tt = 0; tt < n; ++tt) {
         float pv[NH];
