@@ -104,6 +104,13 @@ CASES = {
                           [1, 31, 32, 33, 250]),
     "int2_token_nrep8_d64": (O.Config(16, 2, 64, Q(O.INT2, A, TOK, 32), Q(O.INT4, A, TOK, 64), 64, 16, 0, 1e4,
                                       O.BF16), [0, 7, 64, 65, 190]),
+    # per-token scale/min entries the generic kernel reads from the pages instead of
+    # staging them: 128 bytes a token (D 256, 16-channel groups, asymmetric fp32),
+    # and 2 bytes a token (one binary16 scale per row)
+    "d256_token_g16": (O.Config(4, 2, 256, Q(O.INT4, A, TOK, 16), Q(O.INT8, A, TOK, 16), 32, 32, 0, 1e4, O.F32),
+                       [1, 31, 32, 33, 150]),
+    "m16_int8_token_row": (O.Config(4, 4, 128, Q(O.INT8, S, TOK, 0), Q(O.INT4, S, TOK, 0), 0, 16, 0, 1e4, O.BF16,
+                                    meta_dtype=O.F16), [1, 17, 200]),
 }
 
 

@@ -34,6 +34,10 @@ CASES = {
     # the generic kernel
     "generic": (O.Config(4, 4, 64, Q(O.INT4, S, TOK, 32), Q(O.INT8, A, TOK, 16), 32, 32, 1, 1e4, O.F32),
                 [99, 400, 33]),
+    # the generic kernel with per-channel keys: 32-token key groups over 16-token pages
+    # (the tokens of the bad page lose their rows, their group's scales are elsewhere)
+    "generic_channel": (O.Config(8, 2, 128, Q(O.INT8, A, CH, 32), Q(O.INT4, A, TOK, 0), 32, 16, 0, 1e4, O.BF16),
+                        [99, 400, 33]),
 }
 
 
