@@ -111,6 +111,18 @@ CASES = {
                        [1, 31, 32, 33, 150]),
     "m16_int8_token_row": (O.Config(4, 4, 128, Q(O.INT8, S, TOK, 0), Q(O.INT4, S, TOK, 0), 0, 16, 0, 1e4, O.BF16,
                                     meta_dtype=O.F16), [1, 17, 200]),
+    # the generic kernel's remaining (query heads per item, D) instances: 8 heads at D 256,
+    # 1 head at D 256, 2 and 4 heads at D 64 (pre-RoPE), and 12 query heads per kv-head
+    # (a full block of 8, then a block of 4)
+    "nrep8_d256": (O.Config(16, 2, 256, Q(O.INT4, A, CH, 32), Q(O.INT4, A, TOK, 64), 32, 32, 0, 1e4, O.BF16),
+                   [1, 40, 300]),
+    "nrep1_d256": (O.Config(2, 2, 256, Q(O.INT8, S, TOK, 0), Q(O.INT8, A, TOK, 128), 0, 64, 0, 1e4, O.F32),
+                   [5, 200]),
+    "nrep2_d64_int2": (O.Config(4, 2, 64, Q(O.INT2, A, CH, 16), Q(O.INT2, A, TOK, 32), 32, 16, 0, 1e4, O.BF16),
+                       [3, 77]),
+    "nrep4_d64_rope": (O.Config(8, 2, 64, Q(O.INT8, S, CH, 16), Q(O.INT4, S, TOK, 0), 16, 16, 1, 1e4, O.BF16),
+                       [17, 150]),
+    "nrep12": (O.Config(12, 1, 128, Q(O.INT4, A, CH, 16), Q(O.INT8, S, TOK, 0), 16, 32, 0, 1e4, O.F32), [33, 100]),
 }
 
 
