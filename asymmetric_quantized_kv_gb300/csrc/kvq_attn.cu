@@ -32,16 +32,18 @@ constexpr float kLog2e = 1.4426950408889634f;
 // warp dequantizes the K rows into shared memory (lanes over 32-bit code words;
 // rows of fewer than 32 words share a pass), computes the logits with the lanes
 // over (token, head group or channel part), dequantizes the V rows into the same
-// buffer and accumulates P*V with lanes over channels.  Short sub-tiles keep the serial path of a warp short:
-// small calls are latency-bound, and C shrinks to 32 tokens there.
+// buffer and accumulates P*V with lanes over channels.  Short sub-tiles keep the
+// serial path of a warp short: small calls are latency-bound, and C shrinks to 32
+// tokens there.
 constexpr int kST = 8;
 // The sub-tile's packed K and V rows (with per-token scale/min entries of up to
 // kMetaStage bytes a token, and the key group's per-channel entries when the
 // sub-tile lies in one group) are copied to shared memory with cp.async before
 // any is dequantized: all the sub-tile's reads are in flight at once.  A warp's
-// first sub-tile is requested before the query is loaded, each later one as soon
-// as the previous sub-tile's V rows are dequantized (its P*V and the next logits
-// overlap the copies).
+// first sub-tile is requested right after the query's loads are issued (q goes
+// to shared memory after the requests), each later one as soon as the previous
+// sub-tile's V rows are dequantized (its P*V and the next logits overlap the
+// copies).
 constexpr int kMetaStage = 64;
 
 // Dequantization rule of one side (K or V) for a call, resolved once.
