@@ -256,8 +256,8 @@ kvq_status kvq_quantize_append(const kvq_config* cfg, const kvq_cache* cache, co
  * bytes, 256-byte aligned, contents need no initialisation), then a combine.
  * Returns KVQ_ERR_CAPACITY (nothing launched) when the format mix runs on the
  * generic kernel and its shared memory (the plan's per-sequence prefix grows
- * with the batch) exceeds the device's per-block limit: above about 46,000
- * sequences at head_dim 128, 37,000 at 256. */
+ * with the batch) exceeds the device's per-block limit: above about 42,000
+ * sequences at head_dim 128, 30,000 at 256. */
 kvq_status kvq_decode_attention(const kvq_config* cfg, const kvq_cache* cache, const void* q,
                                 float* out, float softmax_scale, void* workspace,
                                 size_t ws_bytes, void* stream);

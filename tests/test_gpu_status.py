@@ -83,3 +83,32 @@ def test_bounded_wait_gives_up_and_reports_timeout():
     cfg, lens = CASES["int2"]
     c = Case(cfg, lens, seed=4)
     c.check_attention()
+
+
+@pytest.mark.parametrize("D,fits,too_many", [(128, 41_000, 43_000), (256, 30_000, 32_000)])
+def test_generic_kernel_batch_limit(D, fits, too_many):
+    """The generic kernel's shared memory grows with the batch (the plan's
+    per-sequence prefix): the header gives about 42,000 sequences at head_dim
+    128 and 30,000 at 256.  A batch below that runs (every sequence empty: out is
+    0); one above returns KVQ_ERR_CAPACITY with nothing launched (out untouched)."""
+    import asymmetric_quantized_kv_gb300 as K
+    from kvq_testlib import to_c
+    cfg = to_c(O.Config(4, 4, D, Q(O.INT8, S, TOK, 0), Q(O.INT8, S, TOK, 0), 0, 16, 0, 1e4, O.F32))
+    for batch, ok in ((fits, True), (too_many, False)):
+        cache = K.PagedKVCache(cfg, batch, 1, n_pages=1, block_table=torch.zeros(batch, 1, dtype=torch.int32))
+        assert cache.decode_kernel() == K.KVQ_KERNEL_GENERIC
+        q = torch.randn(batch, 4, D, device="cuda")
+        out = torch.full((batch, 4, D), 7.0, device="cuda")
+        if ok:
+            cache.attention(q, out)
+            torch.cuda.synchronize()
+            assert float(out.abs().max()) == 0.0
+        else:
+            with pytest.raises(K.KvqError) as e:
+                cache.attention(q, out)
+            assert e.value.code == K.KVQ_ERR_CAPACITY
+            torch.cuda.synchronize()
+            assert bool((out == 7.0).all())
+        assert int(cache.status.item()) == 0
+        del cache, q, out
+        torch.cuda.empty_cache()
