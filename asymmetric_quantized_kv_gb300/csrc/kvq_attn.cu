@@ -117,11 +117,15 @@ __device__ __forceinline__ void deq_word(uint32_t w, int c0, const DeqRule& r, c
       }
     }
   } else {
+    // a word's N codes lie in one channel group (groups are multiples of 16
+    // channels, N <= 16 divides them): one scale and one minimum per word
+    const int g = c0 >> r.lg;
+    const float sc = load_meta(meta, g, m16);
+    const float mn = r.asym ? load_meta(meta, r.ng + g, m16) : 0.f;
 #pragma unroll
     for (int e = 0; e < N; ++e) {
-      const int g = (c0 + e) >> r.lg;
-      const float y = __fmul_rn(code_value((w >> (e * BITS)) & M, r), load_meta(meta, g, m16));
-      x[e] = r.asym ? __fadd_rn(y, load_meta(meta, r.ng + g, m16)) : y;
+      const float y = __fmul_rn(code_value((w >> (e * BITS)) & M, r), sc);
+      x[e] = r.asym ? __fadd_rn(y, mn) : y;
     }
   }
 #pragma unroll
@@ -689,7 +693,12 @@ kvq_status launch_attention(const KvqView& v, const void* q, float* out, float s
   const size_t smem = generic_smem_bytes(v.batch, v.D);
   const kvq_status ss = ensure_dynamic_smem(kSlotGeneric + 3 * ih + id, kern, smem);
   if (ss != KVQ_OK) return ss;
-  const int grid = num_sms() * 2;
+  // as many CTAs as fit on the SMs at once (registers and shared memory): the
+  // warps' dependent chains need company on each scheduler
+  int occ = 0;
+  const kvq_status so = occupancy_at(kSlotGenericOcc + 3 * ih + id, kern, kThreads, smem, &occ);
+  if (so != KVQ_OK) return so;
+  const int grid = num_sms() * occ;
   kern<<<grid, kThreads, smem, st>>>(v, q, scale, static_cast<float*>(ws));
   if (cudaGetLastError() != cudaSuccess) return KVQ_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};

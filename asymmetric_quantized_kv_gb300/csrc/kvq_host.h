@@ -30,7 +30,8 @@ enum SetupSlot {
   kSlotSms = 0,        // multiprocessor count
   kSlotAppend,         // append kernel: dynamic shared-memory limit raised
   kSlotGeneric,        // generic decode kernels (12 instances): shared-memory limit set so far
-  kSlotFast = kSlotGeneric + 12,  // pre-RoPE tensor-core kernel, 4 instances: CTAs per SM
+  kSlotGenericOcc = kSlotGeneric + 12,  // the same instances: last (shared memory, CTAs per SM)
+  kSlotFast = kSlotGenericOcc + 12,     // pre-RoPE tensor-core kernel, 4 instances: CTAs per SM
   kSlotFp8 = kSlotFast + 4,       // FP8 tensor-core kernel, 2 instances
   kSlotInt2 = kSlotFp8 + 2,       // 2-bit tensor-core kernel, 2 instances
   kSlotCount = kSlotInt2 + 2
@@ -138,6 +139,33 @@ kvq_status occupancy_once(int slot, Kern kern, int threads, size_t smem, size_t 
       &occ);
   *ctas = (int)occ;
   return s;
+}
+
+// CTAs per SM of `kern` at `threads` threads and `smem` dynamic bytes (its
+// shared-memory limit already raised that far).  The last answer per device is
+// kept in `slot` with its byte count: consecutive calls of one workload ask for
+// the same bytes and skip the query.
+template <class Kern>
+kvq_status occupancy_at(int slot, Kern kern, int threads, size_t smem, int* ctas) {
+  const int dev = current_device();
+  if (dev < 0) return KVQ_ERR_CUDA;
+  if (dev >= kMaxDevices) return KVQ_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(setup_mutex());
+  long long& v = setup_value(dev, slot);
+  if (v > 0 && (v >> 16) == (long long)smem) {
+    *ctas = (int)(v & 0xFFFF);
+    return KVQ_OK;
+  }
+  int o = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, kern, threads, smem) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return KVQ_ERR_CUDA;
+  }
+  if (o < 1) o = 1;
+  if (o > 0xFFFF) o = 0xFFFF;
+  v = ((long long)smem << 16) | o;
+  *ctas = o;
+  return KVQ_OK;
 }
 
 // NVTX range around one public call, in the "libkvq" domain: profilers show the
