@@ -51,7 +51,7 @@ struct DeqRule {
   int kind;        // kFp8, kTensor, kChannel, kToken
   int bits, fmt;   // code bits; FP8 format
   bool asym;
-  uint32_t xr;     // code ^ xr - sub = the signed code value (sym INT8: 0x80 / 128)
+  uint32_t xw;     // word ^ xw, then code - sub = the signed code value (sym INT8: 0x80 per byte / 128)
   float bias;      // 2^23 + sub
   int lg, ng;      // PER_TOKEN: log2(group), groups per token
 };
@@ -64,7 +64,7 @@ __device__ __forceinline__ DeqRule make_rule(int fmt, int mode, int axis, int gr
   r.kind = is_fp8(fmt) ? kFp8 : axis == KVQ_PER_TENSOR ? kTensor : axis == KVQ_PER_CHANNEL ? kChannel : kToken;
   r.asym = !is_fp8(fmt) && axis != KVQ_PER_TENSOR && mode == KVQ_ASYM_MINMAX;
   const bool sym = !r.asym;
-  r.xr = (sym && bits == 8) ? 0x80u : 0u;
+  r.xw = (sym && bits == 8) ? 0x80808080u : 0u;
   const int sub = !sym ? 0 : bits == 8 ? 128 : (1 << (bits - 1));
   r.bias = 8388608.f + (float)sub;
   r.lg = __ffs(group > 0 ? group : 1) - 1;  // group: a power of two (it divides D)
@@ -72,9 +72,10 @@ __device__ __forceinline__ DeqRule make_rule(int fmt, int mode, int axis, int gr
   return r;
 }
 
-// Signed code value of the unsigned stored code u, as an exact float.
+// Signed code value of code field u (of a word already XOR-ed with r.xw), as an
+// exact float: the field in the mantissa of 2^23, minus 2^23 + sub.
 __device__ __forceinline__ float code_value(uint32_t u, const DeqRule& r) {
-  return __int_as_float(0x4B000000 | (u ^ r.xr)) - r.bias;
+  return __int_as_float(0x4B000000 | u) - r.bias;
 }
 
 // Entries i..i+3 (i a multiple of 4) of a scale/min array, fp32 or binary16.
@@ -98,6 +99,7 @@ __device__ __forceinline__ void deq_word(uint32_t w, int c0, const DeqRule& r, c
   constexpr int N = 32 / BITS;
   constexpr uint32_t M = (1u << BITS) - 1u;
   float x[N];
+  if (r.kind != kFp8) w ^= r.xw;
   if (r.kind == kFp8) {
 #pragma unroll
     for (int e = 0; e < N; ++e) x[e] = __fmul_rn(fp8_to_float((w >> (e * BITS)) & M, r.fmt), ts);
@@ -148,9 +150,21 @@ __device__ __forceinline__ void copy_src_row(const void* base, long long row_ele
   }
 }
 
-// 4-byte asynchronous copy global -> shared (both 4-byte aligned), and its groups.
+// Lane src's pointer, to every lane.
+__device__ __forceinline__ const uint8_t* shfl_ptr(const uint8_t* p, int src) {
+  const unsigned long long x = reinterpret_cast<unsigned long long>(p);
+  const unsigned lo = __shfl_sync(0xffffffffu, static_cast<unsigned>(x), src);
+  const unsigned hi = __shfl_sync(0xffffffffu, static_cast<unsigned>(x >> 32), src);
+  return reinterpret_cast<const uint8_t*>((static_cast<unsigned long long>(hi) << 32) | lo);
+}
+
+// 4- and 16-byte asynchronous copies global -> shared (both sides aligned to the
+// size), and their groups.
 __device__ __forceinline__ void cp_async4(void* dst, const void* src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(ptx::smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(ptx::smem_u32(dst)), "l"(src) : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
 template <int N>
@@ -158,41 +172,65 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
 }
 
-// n staged rows (row tt at stage + tt*D) -> buf rows (stride DP floats), lanes
-// over (row, 32-bit word): a row of nw < 32 words takes nw lanes, so 32/nw rows
-// go per pass.  meta_of(tt) gives row tt's scale/min entries (every lane calls
-// it: it may shuffle); rows marked in `bad` are written as zeros.
-template <int BITS, typename MetaOf>
-__device__ __forceinline__ void deq_staged_t(const uint8_t* stage, int D, int DP, int n, unsigned bad, int row_bytes,
-                                             const DeqRule& r, MetaOf meta_of, int m16, float ts, float* buf,
-                                             int lane) {
-  constexpr int N = 32 / BITS;
-  const int nw = row_bytes >> 2;  // a power of two, 4..64
-  const int rpp = nw >= 32 ? 1 : 32 / nw;
-  const int sub = nw >= 32 ? 0 : lane / nw, wl = nw >= 32 ? lane : lane % nw;
-  for (int t0 = 0; t0 < n; t0 += rpp) {
-    const int tt = t0 + sub;
-    const uint8_t* meta = meta_of(tt);
-    if (tt < n) {
-      float* dst = buf + tt * DP;
-      const uint32_t* row = reinterpret_cast<const uint32_t*>(stage + tt * D);
-      for (int wi = wl; wi < nw; wi += 32) {
-        if ((bad >> tt) & 1u) {
+// Staged row pitch in bytes: a row plus 16, so that the 8 rows' words at one
+// offset fall in 8 different 4-bank groups.
+template <int D>
+constexpr int stage_pitch() { return D + 16; }
+
+// n <= 8 staged rows (row tt at stage + tt * pitch) -> buf rows (stride DP
+// floats) in one pass: lane = (token lane/4, part lane%4), part p taking words
+// p, p + 4, p + 8, ... of the row's NW (so a quarter-warp's four parts read and
+// write adjacent words: no bank conflicts).  meta_of(tt) gives row tt's
+// scale/min entries (every lane calls it: it may shuffle); rows marked in `bad`
+// are written as zeros.  The word loop stays rolled: the kernel's code size
+// decides the latency-bound calls, whose code is fetched cold from DRAM.
+template <int BITS, int D, typename MetaOf>
+__device__ __forceinline__ void deq_staged_t(const uint8_t* stage, int DP, int n, unsigned bad, const DeqRule& r,
+                                             MetaOf meta_of, int m16, float ts, float* buf, int lane) {
+  constexpr int N = 32 / BITS, NW = D * BITS / 32, CW = NW / 4;  // CW: 1..16 words per lane
+  static_assert(kST == 8 && NW % 4 == 0, "one pass covers 8 rows in quarters");
+  const int tt = lane >> 2, part = lane & 3;
+  const uint8_t* meta = meta_of(tt);
+  if (tt < n) {
+    float* dst = buf + tt * DP + part * N;
+    const uint32_t* row = reinterpret_cast<const uint32_t*>(stage + tt * stage_pitch<D>()) + part;
+    if ((bad >> tt) & 1u) {
+#pragma unroll 1
+      for (int i = 0; i < CW; ++i) {
 #pragma unroll
-          for (int e = 0; e < N; e += 4) *reinterpret_cast<float4*>(dst + wi * N + e) = make_float4(0.f, 0.f, 0.f, 0.f);
-        } else {
-          deq_word<BITS>(row[wi], wi * N, r, meta, D, m16, ts, dst + wi * N);
-        }
+        for (int e = 0; e < N; e += 4)
+          *reinterpret_cast<float4*>(dst + 4 * i * N + e) = make_float4(0.f, 0.f, 0.f, 0.f);
       }
+    } else {
+#pragma unroll 1
+      for (int i = 0; i < CW; ++i) deq_word<BITS>(row[4 * i], (part + 4 * i) * N, r, meta, D, m16, ts, dst + 4 * i * N);
     }
   }
 }
-template <typename MetaOf>
-__device__ __forceinline__ void deq_staged(const uint8_t* stage, int D, int DP, int n, unsigned bad, int row_bytes,
-                                           const DeqRule& r, MetaOf meta_of, int m16, float ts, float* buf, int lane) {
-  if (r.bits == 8) deq_staged_t<8>(stage, D, DP, n, bad, row_bytes, r, meta_of, m16, ts, buf, lane);
-  else if (r.bits == 4) deq_staged_t<4>(stage, D, DP, n, bad, row_bytes, r, meta_of, m16, ts, buf, lane);
-  else deq_staged_t<2>(stage, D, DP, n, bad, row_bytes, r, meta_of, m16, ts, buf, lane);
+template <int D, typename MetaOf>
+__device__ __forceinline__ void deq_staged(const uint8_t* stage, int DP, int n, unsigned bad, const DeqRule& r,
+                                           MetaOf meta_of, int m16, float ts, float* buf, int lane) {
+  if (r.bits == 8) deq_staged_t<8, D>(stage, DP, n, bad, r, meta_of, m16, ts, buf, lane);
+  else if (r.bits == 4) deq_staged_t<4, D>(stage, DP, n, bad, r, meta_of, m16, ts, buf, lane);
+  else deq_staged_t<2, D>(stage, DP, n, bad, r, meta_of, m16, ts, buf, lane);
+}
+
+// Asynchronous copy of the n <= 8 rows of `bytes` bytes (a power of two, >= 4)
+// that lane tt's `src` points at, to dst + tt * pitch, as 16-byte chunks when
+// both sides allow (q16) else 4-byte words: lanes over (row, chunk).  Rows
+// marked in `bad` are skipped.  Every lane takes part (shuffles).
+__device__ __forceinline__ void stage_rows(uint8_t* dst, int pitch, const uint8_t* src, int bytes, int n, unsigned bad,
+                                           bool q16, int lane) {
+  const int lg = q16 && bytes >= 16 ? 4 : 2;
+  const int per = bytes >> lg, lper = __ffs(per) - 1;  // chunks per row, a power of two
+  for (int k0 = 0; k0 < n * per; k0 += 32) {
+    const int k = k0 + lane, tt = min(k >> lper, kST - 1), c = (k & (per - 1)) << lg;
+    const uint8_t* p = shfl_ptr(src, tt);
+    if (k < n * per && !((bad >> tt) & 1u)) {
+      if (lg == 4) cp_async16(dst + tt * pitch + c, p + c);
+      else cp_async4(dst + tt * pitch + c, p + c);
+    }
+  }
 }
 
 // Max and sum over the 8 lanes of a lane's group of 8 (lanes 8g .. 8g+7).
@@ -215,13 +253,6 @@ struct TileRefs {
   bool kc;
 };
 
-// Lane src's pointer, to every lane.
-__device__ __forceinline__ const uint8_t* shfl_ptr(const uint8_t* p, int src) {
-  const unsigned long long x = reinterpret_cast<unsigned long long>(p);
-  const unsigned lo = __shfl_sync(0xffffffffu, static_cast<unsigned>(x), src);
-  const unsigned hi = __shfl_sync(0xffffffffu, static_cast<unsigned>(x >> 32), src);
-  return reinterpret_cast<const uint8_t*>((static_cast<unsigned long long>(hi) << 32) | lo);
-}
 
 
 // Partial record of one (item, query head of the block): running max, sum, two
@@ -239,15 +270,15 @@ struct GenericSmem {
 // Dynamic shared memory: GenericSmem, pref[B+1], then (16-byte aligned) per warp a
 // sub-tile buffer [kST][D+4] and its probabilities [kHB][kST], then the warps'
 // outputs [kWarps][kHB][D] for the CTA merge, then per warp the packed staging of
-// a sub-tile: K rows [kST][D bytes], K entries [kST][kMetaStage], the same for V,
-// and one key group's per-channel entries [8 D bytes].
+// a sub-tile: K rows [kST][D + 16 bytes], K entries [kST][kMetaStage], the same
+// for V, and one key group's per-channel entries [8 D bytes].
 __host__ __device__ inline size_t generic_tiles_offset(int batch) {
   return (sizeof(GenericSmem) + sizeof(int) * (batch + 1) + 15) / 16 * 16;
 }
 __host__ __device__ inline size_t generic_smem_bytes(int batch, int D) {
   return generic_tiles_offset(batch) +
          sizeof(float) * ((size_t)kWarps * kST * (D + 4) + (size_t)kWarps * kHB * kST + (size_t)kWarps * kHB * D) +
-         (size_t)kWarps * (2 * kST * (D + kMetaStage) + 8 * D);
+         (size_t)kWarps * (2 * kST * (D + 16 + kMetaStage) + 8 * D);
 }
 
 // NH: query heads per item at most (a power of two <= kHB); NJ = D / 32.
@@ -261,10 +292,11 @@ __global__ void __launch_bounds__(kThreads) split_generic_kernel(KvqView v, cons
   float* buf = reinterpret_cast<float*>(dyn + generic_tiles_offset(v.batch)) + warp * kST * DP;
   float* ps = reinterpret_cast<float*>(dyn + generic_tiles_offset(v.batch)) + kWarps * kST * DP + warp * kHB * kST;
   float* wo = reinterpret_cast<float*>(dyn + generic_tiles_offset(v.batch)) + kWarps * kST * DP + kWarps * kHB * kST;
-  uint8_t* sk = reinterpret_cast<uint8_t*>(wo + kWarps * kHB * D) + warp * (2 * kST * (D + kMetaStage) + 8 * D);
-  uint8_t* skm = sk + kST * D;
+  constexpr int SP = stage_pitch<D>();
+  uint8_t* sk = reinterpret_cast<uint8_t*>(wo + kWarps * kHB * D) + warp * (2 * kST * (SP + kMetaStage) + 8 * D);
+  uint8_t* skm = sk + kST * SP;
   uint8_t* sv = skm + kST * kMetaStage;
-  uint8_t* svm = sv + kST * D;
+  uint8_t* svm = sv + kST * SP;
   uint8_t* skc = svm + kST * kMetaStage;
   const int HB = (v.n_rep + kHB - 1) / kHB;
   __shared__ int s_C, s_items;
@@ -282,6 +314,9 @@ __global__ void __launch_bounds__(kThreads) split_generic_kernel(KvqView v, cons
   const bool stage_km = kr.kind == kToken && kmeta_tok <= kMetaStage && (kmeta_tok & 3) == 0;
   const bool stage_vm = vr.kind == kToken && vmeta_tok <= kMetaStage && (vmeta_tok & 3) == 0;
   const int kmeta_ch = D * v.k_nmeta * v.mb;  // one key group's per-channel entries (<= 8 D bytes)
+  // every page section starts on a 16-byte boundary of its page and rows are
+  // multiples of 16 bytes: whole 16-byte copies when the pool is 16-byte aligned
+  const bool q16 = (reinterpret_cast<uintptr_t>(v.pages) & 15) == 0;
   const int src = v.src_bf16 ? 2 : 4;
   float* part = plan_partials(ws, v.batch);
   for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
@@ -334,30 +369,22 @@ __global__ void __launch_bounds__(kThreads) split_generic_kernel(KvqView v, cons
       r.bad = __ballot_sync(0xffffffffu, lane < n && !ok);
       r.kc = false;
       if (!it.window) {
-        for (int tt = 0; tt < n; ++tt) {
-          if ((r.bad >> tt) & 1u) continue;
-          const uint8_t* pk = shfl_ptr(a_k, tt);
-          for (int w = lane; w < (v.krow >> 2); w += 32) cp_async4(sk + tt * D + 4 * w, pk + 4 * w);
-          if (stage_km) {
-            const uint8_t* pm = shfl_ptr(a_km, tt);
-            if (lane < (kmeta_tok >> 2)) cp_async4(skm + tt * kMetaStage + 4 * lane, pm + 4 * lane);
-          }
-        }
+        stage_rows(sk, SP, a_k, v.krow, n, r.bad, q16, lane);
+        if (stage_km) stage_rows(skm, kMetaStage, a_km, kmeta_tok, n, r.bad, false, lane);
         r.kc = kr.kind == kChannel && !(r.bad & 1u) && tile / v.kgroup == (tile + n - 1) / v.kgroup;
         if (r.kc) {
           const uint8_t* pm = shfl_ptr(a_km, 0);
-          for (int w = lane; w < (kmeta_ch >> 2); w += 32) cp_async4(skc + 4 * w, pm + 4 * w);
-        }
-        cp_async_commit();
-        for (int tt = 0; tt < n; ++tt) {
-          if ((r.bad >> tt) & 1u) continue;
-          const uint8_t* pv = shfl_ptr(a_v, tt);
-          for (int w = lane; w < (v.vrow >> 2); w += 32) cp_async4(sv + tt * D + 4 * w, pv + 4 * w);
-          if (stage_vm) {
-            const uint8_t* pm = shfl_ptr(a_vm, tt);
-            if (lane < (vmeta_tok >> 2)) cp_async4(svm + tt * kMetaStage + 4 * lane, pm + 4 * lane);
+          for (int c = 16 * lane; c < kmeta_ch; c += 512) {
+            if (q16) {
+              cp_async16(skc + c, pm + c);
+            } else {
+              for (int j = 0; j < 16; j += 4) cp_async4(skc + c + j, pm + c + j);
+            }
           }
         }
+        cp_async_commit();
+        stage_rows(sv, SP, a_v, v.vrow, n, r.bad, q16, lane);
+        if (stage_vm) stage_rows(svm, kMetaStage, a_vm, vmeta_tok, n, r.bad, false, lane);
         cp_async_commit();
       }
       return r;
@@ -408,7 +435,7 @@ __global__ void __launch_bounds__(kThreads) split_generic_kernel(KvqView v, cons
         auto km_of = [&](int tt) -> const uint8_t* {
           return rf.kc ? skc : stage_km ? skm + tt * kMetaStage : shfl_ptr(rf.km, tt);
         };
-        deq_staged(sk, D, DP, n, bad, v.krow, kr, km_of, v.meta16, kts, buf, lane);
+        deq_staged<D>(sk, DP, n, bad, kr, km_of, v.meta16, kts, buf, lane);
       }
       __syncwarp();
       if (v.rope_pre) {  // rotate the pairs in place: lanes over (token, pair)
@@ -497,7 +524,7 @@ __global__ void __launch_bounds__(kThreads) split_generic_kernel(KvqView v, cons
         auto vm_of = [&](int tt) -> const uint8_t* {
           return stage_vm ? svm + tt * kMetaStage : shfl_ptr(rf.vm, tt);
         };
-        deq_staged(sv, D, DP, n, bad, v.vrow, vr, vm_of, v.meta16, vts, buf, lane);
+        deq_staged<D>(sv, DP, n, bad, vr, vm_of, v.meta16, vts, buf, lane);
       }
       __syncwarp();
       if (tile + kWarps * kST < it.t1) tr = stage_tile(tile + kWarps * kST);  // the staging is free again
