@@ -215,19 +215,21 @@ __device__ __forceinline__ void deq_staged(const uint8_t* stage, int DP, int n, 
   else deq_staged_t<2, D>(stage, DP, n, bad, r, meta_of, m16, ts, buf, lane);
 }
 
-// Asynchronous copy of the n <= 8 rows of `bytes` bytes (a power of two, >= 4)
-// that lane tt's `src` points at, to dst + tt * pitch, as 16-byte chunks when
-// both sides allow (q16) else 4-byte words: lanes over (row, chunk).  Rows
-// marked in `bad` are skipped.  Every lane takes part (shuffles).
+// Asynchronous copy of the n <= 8 rows of `bytes` bytes (a power of two, a
+// multiple of CHUNK) that lane tt's `src` points at, to dst + tt * pitch, in
+// CHUNK-byte copies (16 for code rows: the pool is 16-byte aligned and every row
+// a multiple of 16 bytes; 4 for per-token entries): lanes over (row, chunk).
+// Rows marked in `bad` are skipped.  Every lane takes part (shuffles).
+template <int CHUNK>
 __device__ __forceinline__ void stage_rows(uint8_t* dst, int pitch, const uint8_t* src, int bytes, int n, unsigned bad,
-                                           bool q16, int lane) {
-  const int lg = q16 && bytes >= 16 ? 4 : 2;
-  const int per = bytes >> lg, lper = __ffs(per) - 1;  // chunks per row, a power of two
+                                           int lane) {
+  constexpr int LG = CHUNK == 16 ? 4 : 2;
+  const int per = bytes >> LG, lper = __ffs(per) - 1;  // chunks per row, a power of two
   for (int k0 = 0; k0 < n * per; k0 += 32) {
-    const int k = k0 + lane, tt = min(k >> lper, kST - 1), c = (k & (per - 1)) << lg;
+    const int k = k0 + lane, tt = min(k >> lper, kST - 1), c = (k & (per - 1)) << LG;
     const uint8_t* p = shfl_ptr(src, tt);
     if (k < n * per && !((bad >> tt) & 1u)) {
-      if (lg == 4) cp_async16(dst + tt * pitch + c, p + c);
+      if constexpr (CHUNK == 16) cp_async16(dst + tt * pitch + c, p + c);
       else cp_async4(dst + tt * pitch + c, p + c);
     }
   }
@@ -314,9 +316,6 @@ __global__ void __launch_bounds__(kThreads) split_generic_kernel(KvqView v, cons
   const bool stage_km = kr.kind == kToken && kmeta_tok <= kMetaStage && (kmeta_tok & 3) == 0;
   const bool stage_vm = vr.kind == kToken && vmeta_tok <= kMetaStage && (vmeta_tok & 3) == 0;
   const int kmeta_ch = D * v.k_nmeta * v.mb;  // one key group's per-channel entries (<= 8 D bytes)
-  // every page section starts on a 16-byte boundary of its page and rows are
-  // multiples of 16 bytes: whole 16-byte copies when the pool is 16-byte aligned
-  const bool q16 = (reinterpret_cast<uintptr_t>(v.pages) & 15) == 0;
   const int src = v.src_bf16 ? 2 : 4;
   float* part = plan_partials(ws, v.batch);
   for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
@@ -369,22 +368,16 @@ __global__ void __launch_bounds__(kThreads) split_generic_kernel(KvqView v, cons
       r.bad = __ballot_sync(0xffffffffu, lane < n && !ok);
       r.kc = false;
       if (!it.window) {
-        stage_rows(sk, SP, a_k, v.krow, n, r.bad, q16, lane);
-        if (stage_km) stage_rows(skm, kMetaStage, a_km, kmeta_tok, n, r.bad, false, lane);
+        stage_rows<16>(sk, SP, a_k, v.krow, n, r.bad, lane);
+        if (stage_km) stage_rows<4>(skm, kMetaStage, a_km, kmeta_tok, n, r.bad, lane);
         r.kc = kr.kind == kChannel && !(r.bad & 1u) && tile / v.kgroup == (tile + n - 1) / v.kgroup;
         if (r.kc) {
           const uint8_t* pm = shfl_ptr(a_km, 0);
-          for (int c = 16 * lane; c < kmeta_ch; c += 512) {
-            if (q16) {
-              cp_async16(skc + c, pm + c);
-            } else {
-              for (int j = 0; j < 16; j += 4) cp_async4(skc + c + j, pm + c + j);
-            }
-          }
+          for (int c = 16 * lane; c < kmeta_ch; c += 512) cp_async16(skc + c, pm + c);
         }
         cp_async_commit();
-        stage_rows(sv, SP, a_v, v.vrow, n, r.bad, q16, lane);
-        if (stage_vm) stage_rows(svm, kMetaStage, a_vm, vmeta_tok, n, r.bad, false, lane);
+        stage_rows<16>(sv, SP, a_v, v.vrow, n, r.bad, lane);
+        if (stage_vm) stage_rows<4>(svm, kMetaStage, a_vm, vmeta_tok, n, r.bad, lane);
         cp_async_commit();
       }
       return r;
