@@ -255,8 +255,6 @@ struct TileRefs {
   bool kc;
 };
 
-
-
 // Partial record of one (item, query head of the block): running max, sum, two
 // pad words, then D outputs (16-byte aligned).
 __host__ __device__ inline int generic_rec(int D) { return D + 4; }
